@@ -1,0 +1,177 @@
+"""Python binding of libditattn (include/ditattn.h): argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels; this module turns torch
+tensors into pointers and sizes, allocates workspace with torch when the caller gives none,
+and raises ``DitAttnError`` for any non-OK status. There is no fallback: if the compiled
+library is missing, importing the binding's functions raises.
+
+Modes follow the pages ("TRTLLM Attention" user guide): dense BF16; SAGE with INT8 or FP8 E4M3
+Q/K per token block (block sizes 1, 4, 16) and per-channel FP8 V; Skip-Softmax with
+threshold = threshold_scale_factor / Skv.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+MODE_DENSE, MODE_SAGE, MODE_SKIP = 0, 1, 2
+QK_BF16, QK_INT8, QK_FP8_E4M3 = 0, 1, 2
+HEAD_DIM = 128
+TILE = 128
+STATUS_NAMES = {0: "DIT_OK", 1: "DIT_E_INVALID_ARG", 2: "DIT_E_UNSUPPORTED", 3: "DIT_E_CUDA", 4: "DIT_E_TIMEOUT",
+                5: "DIT_E_WORKSPACE"}
+QK_DTYPES = {"bf16": QK_BF16, "int8": QK_INT8, "fp8_e4m3": QK_FP8_E4M3}
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libditattn.so")
+
+# Every symbol include/ditattn.h declares, with its ctypes signature.
+_c_int, _c_float, _c_size, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_void_p
+SIGNATURES = {
+    "dit_abi_version": (_c_int, []),
+    "dit_status_string": (ctypes.c_char_p, [_c_int]),
+    "dit_attn_workspace_bytes": (_c_size, [_c_int] * 9),
+    "dit_attn_fwd": (_c_int, [_vp, _vp, _vp, _vp] + [_c_int] * 9 + [_c_float, _vp, _vp, _c_size, _vp]),
+    "sage_quantize_workspace_bytes": (_c_size, [_c_int] * 3),
+    "sage_quantize_qkv": (_c_int, [_vp, _vp, _vp] + [_c_int] * 8 + [_vp] * 8 + [_c_size, _vp]),
+    "dit_attn_quantized_workspace_bytes": (_c_size, [_c_int] * 6),
+    "dit_attn_fwd_quantized": (_c_int, [_vp] * 7 + [_c_int] * 9 + [_c_float, _vp, _vp, _c_size, _vp]),
+    "dit_attn_check_errors": (_c_int, [_vp]),
+}
+
+
+class DitAttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} ({_lib().dit_status_string(status).decode()})")
+
+
+_LIB = None
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"libditattn.so is not built ({LIB_PATH}); run "
+                              "`python -m diffusion_transformer_attention_gb300.build_lib`")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = lib
+    return _LIB
+
+
+def library():
+    """The loaded ctypes library (loads it on first use)."""
+    return _lib()
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise DitAttnError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _qk(qk_dtype) -> int:
+    return QK_DTYPES[qk_dtype] if isinstance(qk_dtype, str) else int(qk_dtype)
+
+
+def _shape(q, k):
+    B, Sq, Hq, D = q.shape
+    Bk, Skv, Hkv, Dk = k.shape
+    if D != HEAD_DIM or Dk != HEAD_DIM or Bk != B:
+        raise ValueError("q, k, v must be [B, S, H, 128] with the same B")
+    return B, Hq, Hkv, Sq, Skv
+
+
+def dit_attn_workspace_bytes(B, Hq, Hkv, Sq, Skv, mode, qk_dtype, q_block=1, k_block=16) -> int:
+    return int(_lib().dit_attn_workspace_bytes(B, Hq, Hkv, Sq, Skv, mode, _qk(qk_dtype), q_block, k_block))
+
+
+def dit_attn_fwd(q, k, v, out=None, *, mode=MODE_DENSE, qk_dtype="bf16", q_block=1, k_block=16,
+                 threshold_scale_factor=0.0, stream=None, workspace=None, skip_counts=None):
+    """O = softmax(Q K^T / sqrt(128)) V on the GPU; q [B,Sq,Hq,128], k/v [B,Skv,Hkv,128] bf16."""
+    B, Hq, Hkv, Sq, Skv = _shape(q, k)
+    if out is None:
+        out = torch.empty_like(q)
+    qk = _qk(qk_dtype)
+    need = _lib().dit_attn_workspace_bytes(B, Hq, Hkv, Sq, Skv, mode, qk, q_block, k_block)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = _lib().dit_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, Sq, Skv, mode, qk, q_block, k_block,
+                             float(threshold_scale_factor), _stream(stream), _ptr(workspace), ws_bytes,
+                             _ptr(skip_counts))
+    _check(st, "dit_attn_fwd")
+    return out
+
+
+def sage_quantize_workspace_bytes(B, Hkv, Skv) -> int:
+    return int(_lib().sage_quantize_workspace_bytes(B, Hkv, Skv))
+
+
+def sage_quantize_qkv(q, k, v, *, qk_dtype="int8", q_block=1, k_block=16, stream=None, workspace=None):
+    """The SAGE prepass alone; returns a dict of codes (uint8 views of the 1-byte codes) and scales."""
+    B, Hq, Hkv, Sq, Skv = _shape(q, k)
+    dev = q.device
+    code_t = torch.int8 if _qk(qk_dtype) == QK_INT8 else torch.uint8
+    res = dict(
+        q_codes=torch.empty(q.shape, dtype=code_t, device=dev),
+        k_codes=torch.empty(k.shape, dtype=code_t, device=dev),
+        v_codes=torch.empty(v.shape, dtype=torch.uint8, device=dev),
+        q_scale=torch.empty((B, Hq, math.ceil(Sq / q_block)), dtype=torch.float32, device=dev),
+        k_scale=torch.empty((B, Hkv, math.ceil(Skv / k_block)), dtype=torch.float32, device=dev),
+        v_scale=torch.empty((B, Hkv, HEAD_DIM), dtype=torch.float32, device=dev),
+        k_mean=torch.empty((B, Hkv, HEAD_DIM), dtype=torch.float32, device=dev),
+    )
+    need = _lib().sage_quantize_workspace_bytes(B, Hkv, Skv)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    st = _lib().sage_quantize_qkv(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Sq, Skv, _qk(qk_dtype), q_block, k_block,
+                                  _ptr(res["q_codes"]), _ptr(res["k_codes"]), _ptr(res["v_codes"]),
+                                  _ptr(res["q_scale"]), _ptr(res["k_scale"]), _ptr(res["v_scale"]),
+                                  _ptr(res["k_mean"]), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "sage_quantize_qkv")
+    return res
+
+
+def dit_attn_fwd_quantized(quant: dict, out, *, mode=MODE_SAGE, qk_dtype="int8", q_block=1, k_block=16,
+                           threshold_scale_factor=0.0, stream=None, workspace=None, skip_counts=None):
+    """Attention over the codes and scales that ``sage_quantize_qkv`` returned."""
+    qc, kc = quant["q_codes"], quant["k_codes"]
+    B, Sq, Hq, _ = qc.shape
+    _, Skv, Hkv, _ = kc.shape
+    qk = _qk(qk_dtype)
+    need = _lib().dit_attn_quantized_workspace_bytes(B, Hq, Hkv, Sq, Skv, qk)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=qc.device)
+    ws_bytes = 0 if workspace is None else workspace.numel()
+    st = _lib().dit_attn_fwd_quantized(_ptr(qc), _ptr(kc), _ptr(quant["v_codes"]), _ptr(quant["q_scale"]),
+                                       _ptr(quant["k_scale"]), _ptr(quant["v_scale"]), _ptr(out), B, Hq, Hkv, Sq,
+                                       Skv, mode, qk, q_block, k_block, float(threshold_scale_factor),
+                                       _stream(stream), _ptr(workspace), ws_bytes, _ptr(skip_counts))
+    _check(st, "dit_attn_fwd_quantized")
+    return out
+
+
+def dit_attn_check_errors(stream=None):
+    _check(_lib().dit_attn_check_errors(_stream(stream)), "dit_attn_check_errors")
+
+
+def dit_status_string(status: int) -> str:
+    return _lib().dit_status_string(status).decode()

@@ -1,0 +1,353 @@
+// C-ABI entry points (include/ditattn.h): argument validation, workspace layout, TMA tensor-map
+// encoding and the launch sequence. Arguments are validated on the host before any CUDA call,
+// so a rejected call has no side effects and needs no GPU.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/ditattn.h"
+#include "ditattn_internal.h"
+
+using namespace ditattn;
+
+namespace {
+
+constexpr int kAbiVersion = 1;
+constexpr unsigned long long kWaitBudgetNs = 4000000000ull;  // far beyond any legitimate wait
+
+__device__ int g_device_error = 0;
+
+bool is_block(int x) { return x == 1 || x == 4 || x == 16; }
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+// Shapes shared by every entry point. Empty problems (B == 0 or Sq == 0) are valid no-ops.
+bool valid_shape(int B, int Hq, int Hkv, int Sq, int Skv) {
+  if (B < 0 || Sq < 0 || Hq < 1 || Hkv < 1 || Skv < 1) return false;
+  if (Hq % Hkv != 0) return false;
+  if (Hq > 65535 || B > 65535) return false;  // grid y / z limits
+  // every element index must fit the 64-bit offsets and TMA's 2^40-byte stride limit
+  const double q_bytes = (double)B * Sq * Hq * kHeadDim * 2.0;
+  const double kv_bytes = (double)B * Skv * Hkv * kHeadDim * 2.0;
+  return q_bytes < 1e12 && kv_bytes < 1e12;
+}
+
+bool valid_mode(int mode, int qk_dtype, int q_block, int k_block, float factor) {
+  if (mode < 0 || mode > (DIT_MODE_SAGE | DIT_MODE_SKIP)) return false;
+  if (mode & DIT_MODE_SAGE) {
+    if (qk_dtype != DIT_QK_INT8 && qk_dtype != DIT_QK_FP8_E4M3) return false;
+    if (!is_block(q_block) || !is_block(k_block)) return false;
+  } else if (qk_dtype != DIT_QK_BF16) {
+    return false;  // a quantized dtype without SAGE is a contradictory request
+  }
+  if (mode & DIT_MODE_SKIP) {
+    if (!std::isfinite(factor) || factor < 0.0f) return false;
+  }
+  return true;
+}
+
+struct SageLayout {
+  size_t q_codes, k_codes, v_codes, q_scale, k_scale, v_scale, k_mean, psum, pmax, total;
+};
+
+SageLayout sage_layout(int B, int Hq, int Hkv, int Sq, int Skv, int qk_dtype, int q_block, int k_block) {
+  SageLayout L{};
+  const size_t code_bytes = (qk_dtype == DIT_QK_INT8) ? 2 : 1;  // INT8 codes are held as exact fp16
+  size_t off = 0;
+  L.q_codes = off; off = align256(off + (size_t)B * Sq * Hq * kHeadDim * code_bytes);
+  L.k_codes = off; off = align256(off + (size_t)B * Skv * Hkv * kHeadDim * code_bytes);
+  L.v_codes = off; off = align256(off + (size_t)B * Skv * Hkv * kHeadDim);
+  L.q_scale = off; off = align256(off + (size_t)B * Hq * ceil_div(Sq, q_block) * 4);
+  L.k_scale = off; off = align256(off + (size_t)B * Hkv * ceil_div(Skv, k_block) * 4);
+  L.v_scale = off; off = align256(off + (size_t)B * Hkv * kHeadDim * 4);
+  L.k_mean = off;  off = align256(off + (size_t)B * Hkv * kHeadDim * 4);
+  L.psum = off;    off = align256(off + (size_t)B * Hkv * stats_chunks(Skv) * kHeadDim * 8);
+  L.pmax = off;    off = align256(off + (size_t)B * Hkv * stats_chunks(Skv) * kHeadDim * 4);
+  L.total = off;
+  return L;
+}
+
+size_t stats_bytes(int B, int Hkv, int Skv) {
+  const size_t n = (size_t)B * Hkv * stats_chunks(Skv) * kHeadDim;
+  return align256(n * 8) + align256(n * 4);
+}
+
+// ------------------------------------------------------------------ device checks and state
+struct DeviceState {
+  bool checked = false;
+  bool supported = false;
+  int* err = nullptr;
+};
+DeviceState g_dev[64];
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+dit_status prepare_device(int** err_out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return DIT_E_UNSUPPORTED;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& st = g_dev[dev];
+  if (!st.checked) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return DIT_E_UNSUPPORTED;
+    }
+    st.checked = true;
+    st.supported = (prop.major == 10 && prop.minor == 3);
+    if (st.supported) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) {
+        cudaGetLastError();
+        st.supported = false;
+      }
+      st.err = static_cast<int*>(p);
+    }
+    if (st.supported && g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr) {
+        cudaGetLastError();
+        st.supported = false;
+      } else {
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+      }
+    }
+  }
+  if (!st.supported) return DIT_E_UNSUPPORTED;
+  *err_out = st.err;
+  return DIT_OK;
+}
+
+// [B, S, H, 128] tensor as a 4-D map {128, S, H, B} with boxes of {box_inner, 128, 1, 1}
+// (box_inner * element size = 128 bytes) and 128-byte swizzling.
+bool encode_map(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int esize, int B, int S, int H) {
+  const cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)S, (cuuint64_t)H, (cuuint64_t)B};
+  const cuuint64_t row = (cuuint64_t)kHeadDim * esize;
+  const cuuint64_t strides[3] = {row * (cuuint64_t)H, row, row * (cuuint64_t)H * (cuuint64_t)S};
+  const cuuint32_t box[4] = {(cuuint32_t)(128 / esize), 128, 1, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  const CUresult r = g_encode(m, dt, 4, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+dit_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return DIT_OK;
+  cudaGetLastError();
+  return DIT_E_CUDA;
+}
+
+// Launch the attention kernel over prepared operands.
+dit_status run_attention(const void* q, const void* k, const void* v, void* out, CUtensorMapDataType qk_dt,
+                         int qk_esize, int qk_format, int pv_format, int B, int Hq, int Hkv, int Sq, int Skv,
+                         int mode, int q_block, int k_block, float factor, const float* q_scale,
+                         const float* k_scale, const float* v_scale, int32_t* skip_counts, int* err,
+                         cudaStream_t stream) {
+  CUtensorMap tq, tk, tv, to;
+  const CUtensorMapDataType pv_dt =
+      (pv_format == PV_BF16) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const int pv_esize = (pv_format == PV_BF16) ? 2 : 1;
+  if (!encode_map(&tq, q, qk_dt, qk_esize, B, Sq, Hq) || !encode_map(&tk, k, qk_dt, qk_esize, B, Skv, Hkv) ||
+      !encode_map(&tv, v, pv_dt, pv_esize, B, Skv, Hkv) ||
+      !encode_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, Sq, Hq))
+    return DIT_E_CUDA;
+  FmhaParams p{};
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Sq = Sq; p.Skv = Skv;
+  p.group = Hq / Hkv;
+  p.n_q_tiles = ceil_div(Sq, kTile);
+  p.n_kv_tiles = ceil_div(Skv, kTile);
+  p.c_scale = (float)(1.4426950408889634 / std::sqrt(128.0));  // softmax scale * log2(e)
+  const bool skip = (mode & DIT_MODE_SKIP) != 0;
+  p.log2_thr = (skip && factor > 0.0f) ? (float)std::log2((double)factor / (double)Skv) : -INFINITY;
+  p.q_scale = q_scale; p.q_block = q_block; p.nqb = ceil_div(Sq, q_block);
+  p.k_scale = k_scale; p.k_block = k_block; p.nkb = ceil_div(Skv, k_block);
+  p.v_scale = v_scale;
+  p.skip_counts = skip_counts;
+  p.err = err;
+  p.wait_budget_ns = kWaitBudgetNs;
+  return from_cuda(launch_fmha(qk_format, pv_format, skip, tq, tk, tv, to, p, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int dit_abi_version(void) { return kAbiVersion; }
+
+const char* dit_status_string(dit_status s) {
+  switch (s) {
+    case DIT_OK: return "ok";
+    case DIT_E_INVALID_ARG: return "invalid argument";
+    case DIT_E_UNSUPPORTED: return "unsupported device (needs an sm_103 GPU)";
+    case DIT_E_CUDA: return "CUDA error";
+    case DIT_E_TIMEOUT: return "kernel wait timed out";
+    case DIT_E_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+size_t dit_attn_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int mode, int qk_dtype, int q_block,
+                                int k_block) {
+  if (!valid_shape(B, Hq, Hkv, Sq, Skv) || !valid_mode(mode, qk_dtype, q_block, k_block, 0.0f)) return 0;
+  if (!(mode & DIT_MODE_SAGE)) return 0;
+  return sage_layout(B, Hq, Hkv, Sq, Skv, qk_dtype, q_block, k_block).total;
+}
+
+dit_status dit_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv, int Sq,
+                        int Skv, int mode, int qk_dtype, int q_block, int k_block, float threshold_scale_factor,
+                        void* stream, void* workspace, size_t workspace_bytes, int32_t* skip_counts) {
+  if (!valid_shape(B, Hq, Hkv, Sq, Skv) || !valid_mode(mode, qk_dtype, q_block, k_block, threshold_scale_factor))
+    return DIT_E_INVALID_ARG;
+  if (B == 0 || Sq == 0) return DIT_OK;
+  if (!q || !k || !v || !out || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      !aligned16(skip_counts))
+    return DIT_E_INVALID_ARG;
+  const bool sage = (mode & DIT_MODE_SAGE) != 0;
+  SageLayout L{};
+  if (sage) {
+    L = sage_layout(B, Hq, Hkv, Sq, Skv, qk_dtype, q_block, k_block);
+    if (workspace == nullptr || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+      return DIT_E_WORKSPACE;
+  }
+  int* err = nullptr;
+  const dit_status ds = prepare_device(&err);
+  if (ds != DIT_OK) return ds;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (!sage)
+    return run_attention(q, k, v, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, QK_BF16, PV_BF16, B, Hq, Hkv, Sq, Skv,
+                         mode, 1, 1, threshold_scale_factor, nullptr, nullptr, nullptr, skip_counts, err, st);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* q_scale = reinterpret_cast<float*>(ws + L.q_scale);
+  float* k_scale = reinterpret_cast<float*>(ws + L.k_scale);
+  float* v_scale = reinterpret_cast<float*>(ws + L.v_scale);
+  float* k_mean = reinterpret_cast<float*>(ws + L.k_mean);
+  const int code_out = (qk_dtype == DIT_QK_INT8) ? CODE_I8_AS_F16 : CODE_E4M3;
+  cudaError_t e = launch_kv_stats(k, v, B, Hkv, Skv, reinterpret_cast<double*>(ws + L.psum),
+                                  reinterpret_cast<float*>(ws + L.pmax), k_mean, v_scale, st);
+  if (e == cudaSuccess) e = launch_quant_q(q, B, Hq, Sq, q_block, code_out, ws + L.q_codes, q_scale, st);
+  if (e == cudaSuccess)
+    e = launch_quant_kv(k, v, B, Hkv, Skv, k_block, code_out, k_mean, v_scale, ws + L.k_codes, k_scale,
+                        ws + L.v_codes, st);
+  if (e != cudaSuccess) return from_cuda(e);
+  const bool i8 = (qk_dtype == DIT_QK_INT8);
+  return run_attention(ws + L.q_codes, ws + L.k_codes, ws + L.v_codes, out,
+                       i8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, i8 ? 2 : 1,
+                       i8 ? QK_F16 : QK_E4M3, PV_E4M3, B, Hq, Hkv, Sq, Skv, mode, q_block, k_block,
+                       threshold_scale_factor, q_scale, k_scale, v_scale, skip_counts, err, st);
+}
+
+size_t sage_quantize_workspace_bytes(int B, int Hkv, int Skv) {
+  if (B < 0 || Hkv < 1 || Skv < 1) return 0;
+  return stats_bytes(B, Hkv, Skv);
+}
+
+dit_status sage_quantize_qkv(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int Sq, int Skv,
+                             int qk_dtype, int q_block, int k_block, void* q_codes, void* k_codes, void* v_codes,
+                             float* q_scale, float* k_scale, float* v_scale, float* k_mean, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  if (!valid_shape(B, Hq, Hkv, Sq, Skv) || !valid_mode(DIT_MODE_SAGE, qk_dtype, q_block, k_block, 0.0f))
+    return DIT_E_INVALID_ARG;
+  if (B == 0) return DIT_OK;
+  const void* ptrs[] = {k, v, k_codes, v_codes, k_scale, v_scale, k_mean};
+  for (const void* ptr : ptrs)
+    if (!ptr || !aligned16(ptr)) return DIT_E_INVALID_ARG;
+  if (Sq > 0 && (!q || !q_codes || !q_scale || !aligned16(q) || !aligned16(q_codes))) return DIT_E_INVALID_ARG;
+  const size_t need = stats_bytes(B, Hkv, Skv);
+  if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return DIT_E_WORKSPACE;
+  int* err = nullptr;
+  const dit_status ds = prepare_device(&err);
+  if (ds != DIT_OK) return ds;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t n = (size_t)B * Hkv * stats_chunks(Skv) * kHeadDim;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int code_out = (qk_dtype == DIT_QK_INT8) ? CODE_I8 : CODE_E4M3;
+  cudaError_t e = launch_kv_stats(k, v, B, Hkv, Skv, reinterpret_cast<double*>(ws),
+                                  reinterpret_cast<float*>(ws + align256(n * 8)), k_mean, v_scale, st);
+  if (e == cudaSuccess && Sq > 0) e = launch_quant_q(q, B, Hq, Sq, q_block, code_out, q_codes, q_scale, st);
+  if (e == cudaSuccess)
+    e = launch_quant_kv(k, v, B, Hkv, Skv, k_block, code_out, k_mean, v_scale, k_codes, k_scale, v_codes, st);
+  return from_cuda(e);
+}
+
+size_t dit_attn_quantized_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int qk_dtype) {
+  if (!valid_shape(B, Hq, Hkv, Sq, Skv)) return 0;
+  if (qk_dtype == DIT_QK_FP8_E4M3) return 0;
+  if (qk_dtype != DIT_QK_INT8) return 0;
+  return align256((size_t)B * Sq * Hq * kHeadDim * 2) + align256((size_t)B * Skv * Hkv * kHeadDim * 2);
+}
+
+dit_status dit_attn_fwd_quantized(const void* q_codes, const void* k_codes, const void* v_codes,
+                                  const float* q_scale, const float* k_scale, const float* v_scale, void* out, int B,
+                                  int Hq, int Hkv, int Sq, int Skv, int mode, int qk_dtype, int q_block, int k_block,
+                                  float threshold_scale_factor, void* stream, void* workspace,
+                                  size_t workspace_bytes, int32_t* skip_counts) {
+  if (!valid_shape(B, Hq, Hkv, Sq, Skv) || !(mode & DIT_MODE_SAGE) ||
+      !valid_mode(mode, qk_dtype, q_block, k_block, threshold_scale_factor))
+    return DIT_E_INVALID_ARG;
+  if (B == 0 || Sq == 0) return DIT_OK;
+  const void* ptrs[] = {q_codes, k_codes, v_codes, q_scale, k_scale, v_scale, out};
+  for (const void* ptr : ptrs)
+    if (!ptr) return DIT_E_INVALID_ARG;
+  if (!aligned16(q_codes) || !aligned16(k_codes) || !aligned16(v_codes) || !aligned16(out) ||
+      !aligned16(skip_counts))
+    return DIT_E_INVALID_ARG;
+  const bool i8 = (qk_dtype == DIT_QK_INT8);
+  const size_t need = dit_attn_quantized_workspace_bytes(B, Hq, Hkv, Sq, Skv, qk_dtype);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+    return DIT_E_WORKSPACE;
+  int* err = nullptr;
+  const dit_status ds = prepare_device(&err);
+  if (ds != DIT_OK) return ds;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const void* qa = q_codes;
+  const void* ka = k_codes;
+  if (i8) {
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const size_t nq = (size_t)B * Sq * Hq * kHeadDim, nk = (size_t)B * Skv * Hkv * kHeadDim;
+    void* q16 = ws;
+    void* k16 = ws + align256(nq * 2);
+    cudaError_t e = launch_widen_i8(static_cast<const int8_t*>(q_codes), nq, q16, st);
+    if (e == cudaSuccess) e = launch_widen_i8(static_cast<const int8_t*>(k_codes), nk, k16, st);
+    if (e != cudaSuccess) return from_cuda(e);
+    qa = q16;
+    ka = k16;
+  }
+  return run_attention(qa, ka, v_codes, out, i8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                       i8 ? 2 : 1, i8 ? QK_F16 : QK_E4M3, PV_E4M3, B, Hq, Hkv, Sq, Skv, mode, q_block, k_block,
+                       threshold_scale_factor, q_scale, k_scale, v_scale, skip_counts, err,
+                       static_cast<cudaStream_t>(stream));
+}
+
+dit_status dit_attn_check_errors(void* stream) {
+  int* err = nullptr;
+  const dit_status ds = prepare_device(&err);
+  if (ds != DIT_OK) return ds;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return DIT_E_CUDA;
+  }
+  int h = 0;
+  if (cudaMemcpy(&h, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return from_cuda(cudaErrorUnknown);
+  if (h != 0) {
+    const int zero = 0;
+    cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    return (dit_status)h;
+  }
+  return DIT_OK;
+}
+
+}  // extern "C"

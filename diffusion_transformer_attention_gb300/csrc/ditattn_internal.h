@@ -1,0 +1,60 @@
+// Declarations shared by the library's translation units (not part of the public ABI).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace ditattn {
+
+constexpr int kHeadDim = 128;
+constexpr int kTile = 128;
+constexpr int kStatsChunk = 256;  // tokens per CTA in the K-mean / V-absmax partial pass
+
+// Storage formats of the Q/K operands of BMM1 and the V operand of BMM2.
+enum QKFormat { QK_BF16 = 0, QK_F16 = 1, QK_E4M3 = 2 };  // QK_F16: INT8 codes held exactly as fp16
+enum PVFormat { PV_BF16 = 0, PV_E4M3 = 1 };
+
+// Output formats of the Q/K quantizer.
+enum CodeOut { CODE_I8 = 0, CODE_I8_AS_F16 = 1, CODE_E4M3 = 2 };
+
+// Device error word codes (match dit_status).
+constexpr int kErrTimeout = 4;
+
+struct FmhaParams {
+  int B, Hq, Hkv, Sq, Skv;
+  int group;          // Hq / Hkv
+  int n_q_tiles;      // ceil(Sq / 128)
+  int n_kv_tiles;     // ceil(Skv / 128)
+  float c_scale;      // softmax scale * log2(e)
+  float log2_thr;     // log2(threshold_scale_factor / Skv); -inf when the factor is 0
+  const float* q_scale;  // SAGE: [B, Hq, nqb]
+  int q_block, nqb;
+  const float* k_scale;  // SAGE: [B, Hkv, nkb]
+  int k_block, nkb;
+  const float* v_scale;  // SAGE: [B, Hkv, 128]
+  int32_t* skip_counts;  // optional [B, Hq, n_q_tiles]
+  int* err;              // device error word
+  unsigned long long wait_budget_ns;
+};
+
+// Attention kernel launcher (fmha_sm103.cu). Tensor maps describe q, k, v, out as 4-D
+// {128, S, H, B} tensors with 128-byte swizzled boxes.
+cudaError_t launch_fmha(int qk_format, int pv_format, bool skip, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                        const CUtensorMap& tm_v, const CUtensorMap& tm_o, const FmhaParams& p, cudaStream_t stream);
+size_t fmha_smem_bytes();
+
+// Quantize-prepass launchers (prepass.cu).
+cudaError_t launch_kv_stats(const void* k, const void* v, int B, int Hkv, int Skv, double* psum, float* pmax,
+                            float* k_mean, float* v_scale, cudaStream_t stream);
+cudaError_t launch_quant_q(const void* q, int B, int Hq, int Sq, int q_block, int code_out, void* q_codes,
+                           float* q_scale, cudaStream_t stream);
+cudaError_t launch_quant_kv(const void* k, const void* v, int B, int Hkv, int Skv, int k_block, int code_out,
+                            const float* k_mean, const float* v_scale, void* k_codes, float* k_scale, void* v_codes,
+                            cudaStream_t stream);
+cudaError_t launch_widen_i8(const int8_t* codes, size_t n, void* out_f16, cudaStream_t stream);
+cudaError_t launch_zero_i32(int32_t* p, size_t n, cudaStream_t stream);
+
+inline int stats_chunks(int Skv) { return (Skv + kStatsChunk - 1) / kStatsChunk; }
+
+}  // namespace ditattn

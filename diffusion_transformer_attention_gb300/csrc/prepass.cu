@@ -1,0 +1,349 @@
+// SAGE quantize prepass: memory-bound kernels that read bf16 Q/K/V once or twice and write
+// 1-byte (or exactly-widened 2-byte) codes plus float32 scales.
+//
+// What they compute follows "VisualGen Quantized Attention", section "SageAttention in the
+// TRTLLM backend" (one scale per token block per head for Q and K; V per head per channel in
+// FP8 E4M3) and the "TRTLLM Attention" user guide, section "SAGE quantization" (K-smoothing is
+// internal). Where the pages are silent the kernels take these readings, which the oracle
+// shares and the parity tests check bit for bit:
+//   * the K mean is over all Skv tokens: float64 partial sums in a fixed order, divided by Skv
+//     in float64, rounded once to float32; smoothed K = float32(K) - mean (float32 subtract);
+//   * scale = absmax / QMAX (QMAX 127 or 448) and code = f(x / scale), both IEEE float32
+//     divisions (true division, round to nearest); INT8 rounds half to even and clamps to
+//     +-127; E4M3 rounds to nearest even and saturates; an all-zero block has scale 0 and
+//     zero codes.
+//
+// Access pattern: a row of one head is 128 bf16 = 256 contiguous bytes; 16 lanes read it with
+// 16-byte vector loads, so a warp covers two rows per instruction. Results are written with
+// 8-byte (codes) or 16-byte (widened codes) stores at the same positions.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "ditattn_internal.h"
+
+namespace ditattn {
+namespace {
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return (uint32_t)r;
+}
+
+__device__ __forceinline__ int int8_code(float q) {
+  int c = __float2int_rn(q);  // round half to even
+  return max(-127, min(127, c));
+}
+
+// ------------------------------------------------------------------ K mean / V absmax
+// Pass 1: each CTA reduces kStatsChunk tokens of one (batch, kv head): float64 sums of K
+// and float32 max |V| per channel. Thread t handles channels 8*(t%16).. and tokens t/16 + 16i.
+// The 16 partial rows are then combined in a fixed order, so the result is deterministic.
+__global__ void __launch_bounds__(256) kv_stats_partial_kernel(const __nv_bfloat16* __restrict__ k,
+                                                               const __nv_bfloat16* __restrict__ v, int Skv, int Hkv,
+                                                               int nchunk, double* __restrict__ psum,
+                                                               float* __restrict__ pmax) {
+  __shared__ double ssum[16][kHeadDim];
+  __shared__ float smax[16][kHeadDim];
+  const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int cg = threadIdx.x & 15, tr = threadIdx.x >> 4;
+  double s[8];
+  float m[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    s[e] = 0.0;
+    m[e] = 0.0f;
+  }
+  const int j0 = chunk * kStatsChunk;
+  const int j1 = min(Skv, j0 + kStatsChunk);
+  for (int j = j0 + tr; j < j1; j += 16) {
+    const size_t off = (((size_t)b * Skv + j) * Hkv + h) * kHeadDim + cg * 8;
+    float kf[8], vf[8];
+    bf16x8_to_f32(ld_stream_v4(k + off), kf);
+    bf16x8_to_f32(ld_stream_v4(v + off), vf);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      s[e] += (double)kf[e];
+      m[e] = fmaxf(m[e], fabsf(vf[e]));
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    ssum[tr][cg * 8 + e] = s[e];
+    smax[tr][cg * 8 + e] = m[e];
+  }
+  __syncthreads();
+  if (threadIdx.x < kHeadDim) {
+    double a = 0.0;
+    float mx = 0.0f;
+    for (int r = 0; r < 16; ++r) {
+      a += ssum[r][threadIdx.x];
+      mx = fmaxf(mx, smax[r][threadIdx.x]);
+    }
+    const size_t o = (((size_t)b * Hkv + h) * nchunk + chunk) * kHeadDim + threadIdx.x;
+    psum[o] = a;
+    pmax[o] = mx;
+  }
+}
+
+// Pass 2: combine the chunks of one (batch, kv head) in chunk order.
+__global__ void __launch_bounds__(128) kv_stats_final_kernel(const double* __restrict__ psum,
+                                                             const float* __restrict__ pmax, int Skv, int Hkv,
+                                                             int nchunk, float* __restrict__ k_mean,
+                                                             float* __restrict__ v_scale) {
+  const int h = blockIdx.x, b = blockIdx.y, c = threadIdx.x;
+  const size_t base = ((size_t)b * Hkv + h) * nchunk * kHeadDim + c;
+  double a = 0.0;
+  float mx = 0.0f;
+  for (int i = 0; i < nchunk; ++i) {
+    a += psum[base + (size_t)i * kHeadDim];
+    mx = fmaxf(mx, pmax[base + (size_t)i * kHeadDim]);
+  }
+  const size_t o = ((size_t)b * Hkv + h) * kHeadDim + c;
+  k_mean[o] = __double2float_rn(__ddiv_rn(a, (double)Skv));
+  v_scale[o] = __fdiv_rn(mx, 448.0f);
+}
+
+// ------------------------------------------------------------------ token-block quantizer
+// One warp unit covers ROWS = max(QB, 2) consecutive tokens of one (batch, head): two rows per
+// iteration, 16 lanes per row. For QB == 1 each half-warp is its own block; otherwise the whole
+// unit is one block. WITH_V also quantizes V (same rows) with the per-channel v_scale.
+template <int QB, int OUT, bool SMOOTH, bool WITH_V>
+__global__ void __launch_bounds__(256) quant_tokens_kernel(const __nv_bfloat16* __restrict__ x, int B, int S, int H,
+                                                           const float* __restrict__ mean, void* __restrict__ codes,
+                                                           float* __restrict__ scales, int nblk,
+                                                           const __nv_bfloat16* __restrict__ v,
+                                                           const float* __restrict__ v_scale,
+                                                           uint8_t* __restrict__ v_codes) {
+  constexpr int ROWS = QB < 2 ? 2 : QB;
+  constexpr int IT = ROWS / 2;
+  constexpr float QMAX = (OUT == CODE_E4M3) ? 448.0f : 127.0f;
+  const int lane = threadIdx.x & 31;
+  const int half = lane >> 4, cg = lane & 15;
+  const int warps_per_cta = blockDim.x >> 5;
+  const long long nrb = (S + ROWS - 1) / ROWS;
+  const long long nunits = (long long)B * nrb * H;
+  for (long long unit = (long long)blockIdx.x * warps_per_cta + (threadIdx.x >> 5); unit < nunits;
+       unit += (long long)gridDim.x * warps_per_cta) {
+    const int h = (int)(unit % H);
+    const long long rest = unit / H;
+    const int rb = (int)(rest % nrb);
+    const int b = (int)(rest / nrb);
+    float mu[8];
+    if constexpr (SMOOTH) {
+      const float4* mp = reinterpret_cast<const float4*>(mean + ((size_t)b * H + h) * kHeadDim + cg * 8);
+      const float4 m0 = mp[0], m1 = mp[1];
+      mu[0] = m0.x; mu[1] = m0.y; mu[2] = m0.z; mu[3] = m0.w;
+      mu[4] = m1.x; mu[5] = m1.y; mu[6] = m1.z; mu[7] = m1.w;
+    }
+    float val[IT][8];
+    float amax = 0.0f;
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+      const int row = rb * ROWS + 2 * it + half;
+      if (row < S) {
+        const size_t off = (((size_t)b * S + row) * H + h) * kHeadDim + cg * 8;
+        bf16x8_to_f32(ld_stream_v4(x + off), val[it]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          if constexpr (SMOOTH) val[it][e] = __fsub_rn(val[it][e], mu[e]);
+          amax = fmaxf(amax, fabsf(val[it][e]));
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) val[it][e] = 0.0f;
+      }
+    }
+    // block absmax: over 16 lanes (QB == 1, one row per half-warp) or the whole warp
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if constexpr (QB > 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
+    const float scale = __fdiv_rn(amax, QMAX);
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+      const int row = rb * ROWS + 2 * it + half;
+      if (row >= S) continue;
+      const size_t off = (((size_t)b * S + row) * H + h) * kHeadDim + cg * 8;
+      float q[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) q[e] = (scale == 0.0f) ? 0.0f : __fdiv_rn(val[it][e], scale);
+      if constexpr (OUT == CODE_E4M3) {
+        uint2 w;
+        w.x = e4m3x2(q[0], q[1]) | (e4m3x2(q[2], q[3]) << 16);
+        w.y = e4m3x2(q[4], q[5]) | (e4m3x2(q[6], q[7]) << 16);
+        *reinterpret_cast<uint2*>(static_cast<uint8_t*>(codes) + off) = w;
+      } else if constexpr (OUT == CODE_I8) {
+        uint2 w;
+        w.x = (uint32_t)(int8_code(q[0]) & 0xFF) | ((uint32_t)(int8_code(q[1]) & 0xFF) << 8) |
+              ((uint32_t)(int8_code(q[2]) & 0xFF) << 16) | ((uint32_t)(int8_code(q[3]) & 0xFF) << 24);
+        w.y = (uint32_t)(int8_code(q[4]) & 0xFF) | ((uint32_t)(int8_code(q[5]) & 0xFF) << 8) |
+              ((uint32_t)(int8_code(q[6]) & 0xFF) << 16) | ((uint32_t)(int8_code(q[7]) & 0xFF) << 24);
+        *reinterpret_cast<uint2*>(static_cast<uint8_t*>(codes) + off) = w;
+      } else {  // CODE_I8_AS_F16: the same integer codes, held exactly in fp16
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const __half lo = __int2half_rn(int8_code(q[2 * e]));
+          const __half hi = __int2half_rn(int8_code(q[2 * e + 1]));
+          w[e] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+        }
+        *reinterpret_cast<uint4*>(static_cast<__half*>(codes) + off) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      if constexpr (WITH_V) {
+        const float4* sp = reinterpret_cast<const float4*>(v_scale + ((size_t)b * H + h) * kHeadDim + cg * 8);
+        const float4 s0 = sp[0], s1 = sp[1];
+        const float vs[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+        float vf[8];
+        bf16x8_to_f32(ld_stream_v4(v + off), vf);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) vf[e] = (vs[e] == 0.0f) ? 0.0f : __fdiv_rn(vf[e], vs[e]);
+        uint2 w;
+        w.x = e4m3x2(vf[0], vf[1]) | (e4m3x2(vf[2], vf[3]) << 16);
+        w.y = e4m3x2(vf[4], vf[5]) | (e4m3x2(vf[6], vf[7]) << 16);
+        *reinterpret_cast<uint2*>(v_codes + off) = w;
+      }
+    }
+    // scales: one per block; for QB == 1 lane 0 and lane 16 each own a row (= a block)
+    if (QB == 1) {
+      const int row = rb * 2 + half;
+      if (cg == 0 && row < S) scales[((size_t)b * H + h) * nblk + row] = scale;
+    } else if (lane == 0) {
+      scales[((size_t)b * H + h) * nblk + rb] = scale;
+    }
+  }
+}
+
+__global__ void widen_i8_kernel(const int8_t* __restrict__ in, size_t n8, __half* __restrict__ out) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+    const uint2 w = *reinterpret_cast<const uint2*>(in + i * 8);
+    const int8_t* c = reinterpret_cast<const int8_t*>(&w);
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      o[e] = (uint32_t)__half_as_ushort(__int2half_rn(c[2 * e])) |
+             ((uint32_t)__half_as_ushort(__int2half_rn(c[2 * e + 1])) << 16);
+    *reinterpret_cast<uint4*>(out + i * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+__global__ void zero_i32_kernel(int32_t* p, size_t n) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) p[i] = 0;
+}
+
+int grid_for(long long work_items, int per_cta) {
+  long long g = (work_items + per_cta - 1) / per_cta;
+  const long long cap = 152LL * 32;  // a few waves over 152 SMs; the kernels loop beyond that
+  if (g > cap) g = cap;
+  if (g < 1) g = 1;
+  return (int)g;
+}
+
+template <int OUT, bool SMOOTH, bool WITH_V>
+cudaError_t launch_quant_tokens(const void* x, int B, int S, int H, int block, const float* mean, void* codes,
+                                float* scales, const void* v, const float* v_scale, void* v_codes,
+                                cudaStream_t stream) {
+  const int nblk = (S + block - 1) / block;
+  const int rows = block < 2 ? 2 : block;
+  const long long units = (long long)B * ((S + rows - 1) / rows) * H;
+  const int grid = grid_for(units, 8);
+  auto xb = static_cast<const __nv_bfloat16*>(x);
+  auto vb = static_cast<const __nv_bfloat16*>(v);
+  auto vc = static_cast<uint8_t*>(v_codes);
+  switch (block) {
+    case 1:
+      quant_tokens_kernel<1, OUT, SMOOTH, WITH_V>
+          <<<grid, 256, 0, stream>>>(xb, B, S, H, mean, codes, scales, nblk, vb, v_scale, vc);
+      break;
+    case 4:
+      quant_tokens_kernel<4, OUT, SMOOTH, WITH_V>
+          <<<grid, 256, 0, stream>>>(xb, B, S, H, mean, codes, scales, nblk, vb, v_scale, vc);
+      break;
+    case 16:
+      quant_tokens_kernel<16, OUT, SMOOTH, WITH_V>
+          <<<grid, 256, 0, stream>>>(xb, B, S, H, mean, codes, scales, nblk, vb, v_scale, vc);
+      break;
+    default:
+      return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_kv_stats(const void* k, const void* v, int B, int Hkv, int Skv, double* psum, float* pmax,
+                            float* k_mean, float* v_scale, cudaStream_t stream) {
+  const int nchunk = stats_chunks(Skv);
+  kv_stats_partial_kernel<<<dim3(nchunk, Hkv, B), 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(k),
+                                                                    static_cast<const __nv_bfloat16*>(v), Skv, Hkv,
+                                                                    nchunk, psum, pmax);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  kv_stats_final_kernel<<<dim3(Hkv, B), kHeadDim, 0, stream>>>(psum, pmax, Skv, Hkv, nchunk, k_mean, v_scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_q(const void* q, int B, int Hq, int Sq, int q_block, int code_out, void* q_codes,
+                           float* q_scale, cudaStream_t stream) {
+  switch (code_out) {
+    case CODE_I8:
+      return launch_quant_tokens<CODE_I8, false, false>(q, B, Sq, Hq, q_block, nullptr, q_codes, q_scale, nullptr,
+                                                        nullptr, nullptr, stream);
+    case CODE_I8_AS_F16:
+      return launch_quant_tokens<CODE_I8_AS_F16, false, false>(q, B, Sq, Hq, q_block, nullptr, q_codes, q_scale,
+                                                               nullptr, nullptr, nullptr, stream);
+    case CODE_E4M3:
+      return launch_quant_tokens<CODE_E4M3, false, false>(q, B, Sq, Hq, q_block, nullptr, q_codes, q_scale, nullptr,
+                                                          nullptr, nullptr, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_quant_kv(const void* k, const void* v, int B, int Hkv, int Skv, int k_block, int code_out,
+                            const float* k_mean, const float* v_scale, void* k_codes, float* k_scale, void* v_codes,
+                            cudaStream_t stream) {
+  switch (code_out) {
+    case CODE_I8:
+      return launch_quant_tokens<CODE_I8, true, true>(k, B, Skv, Hkv, k_block, k_mean, k_codes, k_scale, v, v_scale,
+                                                      v_codes, stream);
+    case CODE_I8_AS_F16:
+      return launch_quant_tokens<CODE_I8_AS_F16, true, true>(k, B, Skv, Hkv, k_block, k_mean, k_codes, k_scale, v,
+                                                             v_scale, v_codes, stream);
+    case CODE_E4M3:
+      return launch_quant_tokens<CODE_E4M3, true, true>(k, B, Skv, Hkv, k_block, k_mean, k_codes, k_scale, v,
+                                                        v_scale, v_codes, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_widen_i8(const int8_t* codes, size_t n, void* out_f16, cudaStream_t stream) {
+  const size_t n8 = n / 8;  // n is a multiple of 128
+  widen_i8_kernel<<<grid_for((long long)n8, 256), 256, 0, stream>>>(codes, n8, static_cast<__half*>(out_f16));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_zero_i32(int32_t* p, size_t n, cudaStream_t stream) {
+  zero_i32_kernel<<<grid_for((long long)n, 256), 256, 0, stream>>>(p, n);
+  return cudaGetLastError();
+}
+
+}  // namespace ditattn

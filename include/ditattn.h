@@ -1,0 +1,152 @@
+/*
+ * ditattn -- diffusion-transformer attention forward pass on GB300 (sm_103a).
+ *
+ * The operation is full-context, non-causal multi-head attention with head_dim 128 and GQA,
+ * O = softmax(Q K^T / sqrt(128)) V, in three modes that combine:
+ *
+ *   DENSE  BF16 Q/K/V/O ("TRTLLM Attention" user guide, section "Dense mode").
+ *   SAGE   Q and K quantized per token block (INT8 or FP8 E4M3, one scale per block per head),
+ *          K-smoothed (its per-channel mean over tokens subtracted) inside the routine, V
+ *          quantized per channel to FP8 E4M3, and both matrix products run on low-precision
+ *          tensor cores with dequantization scales ("TRTLLM Attention" user guide, section
+ *          "SAGE quantization"; "VisualGen Quantized Attention", section "SageAttention in the
+ *          TRTLLM backend").
+ *   SKIP   Skip-Softmax: a 128-column KV tile's exp and P.V work is skipped for a 128-row Q
+ *          tile when every valid row has exp(m_tile - m_run) < threshold, with
+ *          threshold = threshold_scale_factor / Skv ("SAGE + Skip-Softmax -- API Design & Test
+ *          Plan", Part 1 §4, table mapping knobs to kernel arguments).
+ *
+ * Conventions shared by every call:
+ *   - Tensors are row-major [B, S, H, 128]; Q and O have Hq heads, K and V have Hkv heads,
+ *     Hq % Hkv == 0, and query head h reads kv head h / (Hq / Hkv).
+ *   - All pointers named as device pointers are device memory owned by the caller; the library
+ *     allocates nothing and keeps no pointer after a call returns. Tensor pointers must be
+ *     16-byte aligned.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL = legacy default
+ *     stream). Argument errors are detected on the host before anything is launched and are
+ *     returned synchronously. Launch failures return DIT_E_CUDA. A kernel that finds itself
+ *     waiting far longer than any correct run could take records DIT_E_TIMEOUT in a device
+ *     error word and exits; dit_attn_check_errors() reports it.
+ *   - The library never switches mode, dtype or backend on its own: an unsupported request is
+ *     an error ("TRTLLM Attention" user guide, section "Requirements": an incompatible selection
+ *     raises instead of silently changing the backend).
+ *   - Only sm_103 devices (GB300 / B300) are accepted; anything else returns DIT_E_UNSUPPORTED.
+ */
+#ifndef DITATTN_H_
+#define DITATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum dit_status {
+  DIT_OK = 0,
+  DIT_E_INVALID_ARG = 1, /* bad shape, mode, dtype, block size, factor, or pointer alignment */
+  DIT_E_UNSUPPORTED = 2, /* no CUDA device, or the current device is not sm_103 */
+  DIT_E_CUDA = 3,        /* a CUDA runtime/driver call or a kernel launch failed */
+  DIT_E_TIMEOUT = 4,     /* a kernel gave up waiting (reported by dit_attn_check_errors) */
+  DIT_E_WORKSPACE = 5    /* workspace missing or smaller than the *_workspace_bytes query */
+} dit_status;
+
+/* Mode bits (or-able): DIT_MODE_SAGE | DIT_MODE_SKIP is SAGE with Skip-Softmax. */
+enum { DIT_MODE_DENSE = 0, DIT_MODE_SAGE = 1, DIT_MODE_SKIP = 2 };
+
+/* Q/K element type. DENSE uses BF16; SAGE takes INT8 or FP8 E4M3 ("TRTLLM Attention" user guide,
+ * SAGE table: dtype_qk in {int8, fp8_e4m3}). */
+enum { DIT_QK_BF16 = 0, DIT_QK_INT8 = 1, DIT_QK_FP8_E4M3 = 2 };
+
+/* Rows and columns of one attention tile; skip counts are kept per 128-row Q tile. */
+enum { DIT_HEAD_DIM = 128, DIT_TILE = 128 };
+
+/* Version of this interface. */
+int dit_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* dit_status_string(dit_status status);
+
+/*
+ * Bytes of device workspace dit_attn_fwd needs for these arguments: 0 for DENSE (with or without
+ * SKIP), otherwise room for the quantized codes, their scales and the K-mean partial sums.
+ * Returns 0 for arguments dit_attn_fwd would reject.
+ */
+size_t dit_attn_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int mode, int qk_dtype, int q_block,
+                                int k_block);
+
+/*
+ * The whole forward pass: (SAGE) quantize prepass, then the fused attention kernel.
+ *
+ *   q          device bf16 [B, Sq, Hq, 128]
+ *   k, v       device bf16 [B, Skv, Hkv, 128]
+ *   out        device bf16 [B, Sq, Hq, 128], written completely
+ *   mode       DIT_MODE_* bits
+ *   qk_dtype   DIT_QK_BF16 without SAGE; DIT_QK_INT8 or DIT_QK_FP8_E4M3 with SAGE
+ *   q_block, k_block   SAGE tokens per Q / K scale block, each in {1, 4, 16}
+ *              ("TRTLLM Attention" user guide, SAGE table); ignored without SAGE
+ *   threshold_scale_factor   with SKIP: finite and >= 0, threshold = factor / Skv (0 never
+ *              skips and gives the same output as the mode without SKIP); ignored without SKIP
+ *   workspace  device scratch of at least dit_attn_workspace_bytes(...) bytes, 256-byte
+ *              aligned; may be NULL when that query returns 0. Its contents on entry do not
+ *              matter and are garbage afterwards.
+ *   skip_counts  optional device int32 [B, Hq, ceil(Sq/128)]: number of KV tiles skipped per
+ *              Q tile (written as 0 without SKIP); NULL to not report
+ *
+ * Sq == 0 or B == 0 is a no-op. Skv must be >= 1.
+ */
+dit_status dit_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv, int Sq,
+                        int Skv, int mode, int qk_dtype, int q_block, int k_block, float threshold_scale_factor,
+                        void* stream, void* workspace, size_t workspace_bytes, int32_t* skip_counts);
+
+/* Bytes of device scratch sage_quantize_qkv needs (the K-mean / V-absmax partials). */
+size_t sage_quantize_workspace_bytes(int B, int Hkv, int Skv);
+
+/*
+ * The SAGE quantize prepass alone ("VisualGen Quantized Attention", section "SageAttention in
+ * the TRTLLM backend": one scale per token block per head for Q/K, per head per channel for V).
+ *
+ *   q, k, v    device bf16 inputs as for dit_attn_fwd
+ *   qk_dtype   DIT_QK_INT8 (codes are int8, |code| <= 127, round half to even) or
+ *              DIT_QK_FP8_E4M3 (codes are E4M3 bit patterns, round to nearest even, saturating)
+ *   q_codes    device [B, Sq, Hq, 128], 1 byte per element
+ *   k_codes    device [B, Skv, Hkv, 128], codes of K minus its per-channel mean
+ *   v_codes    device [B, Skv, Hkv, 128], E4M3 bit patterns
+ *   q_scale    device float [B, Hq, ceil(Sq/q_block)]   = block absmax / QMAX
+ *   k_scale    device float [B, Hkv, ceil(Skv/k_block)] (of the smoothed K)
+ *   v_scale    device float [B, Hkv, 128]               = channel absmax / 448
+ *   k_mean     device float [B, Hkv, 128]               = mean of K over all Skv tokens
+ *   workspace  device scratch of sage_quantize_workspace_bytes(B, Hkv, Skv) bytes
+ * QMAX is 127 for INT8 and 448 for E4M3; a block or channel whose absmax is 0 gets scale 0 and
+ * zero codes. Results are bit-for-bit deterministic.
+ */
+dit_status sage_quantize_qkv(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int Sq, int Skv,
+                             int qk_dtype, int q_block, int k_block, void* q_codes, void* k_codes, void* v_codes,
+                             float* q_scale, float* k_scale, float* v_scale, float* k_mean, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/* Bytes of device workspace dit_attn_fwd_quantized needs (INT8 codes are widened there). */
+size_t dit_attn_quantized_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int qk_dtype);
+
+/*
+ * Attention over codes and scales produced by sage_quantize_qkv (same layouts and meanings).
+ * mode must include DIT_MODE_SAGE; the other arguments are as for dit_attn_fwd.
+ */
+dit_status dit_attn_fwd_quantized(const void* q_codes, const void* k_codes, const void* v_codes,
+                                  const float* q_scale, const float* k_scale, const float* v_scale, void* out, int B,
+                                  int Hq, int Hkv, int Sq, int Skv, int mode, int qk_dtype, int q_block, int k_block,
+                                  float threshold_scale_factor, void* stream, void* workspace,
+                                  size_t workspace_bytes, int32_t* skip_counts);
+
+/*
+ * Synchronizes `stream`, then reports and clears the device error word: DIT_OK, or
+ * DIT_E_TIMEOUT if a kernel since the last check gave up waiting, or DIT_E_CUDA if the
+ * synchronization itself failed.
+ */
+dit_status dit_attn_check_errors(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DITATTN_H_ */

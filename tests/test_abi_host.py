@@ -1,0 +1,135 @@
+"""Host-side tests of the C-ABI library (CPU only; no kernel is launched).
+
+The library must load without a GPU, export every function include/ditattn.h declares, and
+reject invalid arguments on the host before any CUDA call ("TRTLLM Attention" user guide,
+section "Requirements": an incompatible request raises instead of silently changing backend).
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import diffusion_transformer_attention_gb300 as dit
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ditattn.h")
+INVALID, UNSUPPORTED, WORKSPACE = 1, 2, 5
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(dit.LIB_PATH):
+        from diffusion_transformer_attention_gb300 import build_lib
+        build_lib.build()
+    return dit.library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^(?:const\s+)?(?:size_t|dit_status|int|char)\s*\*?\s*(\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ["dit_attn_fwd", "sage_quantize_qkv", "dit_attn_workspace_bytes", "dit_attn_fwd_quantized",
+                     "dit_attn_check_errors", "dit_status_string"]:
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+        assert name in dit.SIGNATURES, f"binding lacks a signature for {name}"
+
+
+def test_status_strings(lib):
+    assert dit.dit_status_string(0) == "ok"
+    for s in range(6):
+        assert dit.dit_status_string(s)
+    assert lib.dit_abi_version() == 1
+
+
+FAKE = ctypes.c_void_p(1 << 20)           # a 16-byte aligned, never-dereferenced address
+MISALIGNED = ctypes.c_void_p((1 << 20) + 8)
+
+
+def _fwd(lib, q=FAKE, B=1, Hq=4, Hkv=2, Sq=256, Skv=256, mode=0, qk=0, qb=1, kb=16, factor=0.0, ws=None,
+         ws_bytes=0, skip=None):
+    return lib.dit_attn_fwd(q, FAKE, FAKE, FAKE, B, Hq, Hkv, Sq, Skv, mode, qk, qb, kb, factor, None, ws, ws_bytes,
+                            skip)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(Hq=5, Hkv=2),                      # Hq not a multiple of Hkv
+    dict(Hkv=0), dict(Hq=0), dict(Skv=0), dict(B=-1), dict(Sq=-1),
+    dict(mode=4), dict(mode=-1),
+    dict(mode=0, qk=1),                     # a quantized dtype without SAGE
+    dict(mode=1, qk=0),                     # SAGE without a quantized dtype
+    dict(mode=1, qk=3),
+    dict(mode=1, qk=1, qb=2), dict(mode=1, qk=2, kb=8), dict(mode=1, qk=1, kb=0),
+    dict(mode=2, factor=-1.0), dict(mode=2, factor=float("nan")), dict(mode=3, qk=1, factor=float("inf")),
+    dict(q=MISALIGNED), dict(q=None),
+    dict(skip=MISALIGNED),
+])
+def test_invalid_arguments_rejected_on_host(lib, kw):
+    assert _fwd(lib, **kw) == INVALID
+
+
+def test_empty_problem_is_a_noop(lib):
+    assert _fwd(lib, B=0) == 0
+    assert _fwd(lib, Sq=0) == 0
+
+
+def test_sage_without_workspace_is_rejected(lib):
+    assert _fwd(lib, mode=1, qk=1, ws=None, ws_bytes=0) == WORKSPACE
+    need = lib.dit_attn_workspace_bytes(1, 4, 2, 256, 256, 1, 1, 1, 16)
+    assert need > 0
+    assert _fwd(lib, mode=1, qk=1, ws=FAKE, ws_bytes=need - 1) == WORKSPACE
+
+
+def test_valid_call_without_gpu_reports_unsupported(lib):
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present: a valid call would launch on these placeholder pointers")
+    assert _fwd(lib) == UNSUPPORTED
+    assert lib.dit_attn_check_errors(None) == UNSUPPORTED
+
+
+def _recipes():
+    rows = []
+    for line in open(os.path.join(ROOT, "tests", "golden", "recipes.txt")):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            src, dt, qb, kb, vb = line.split()
+            rows.append((src, dt, int(qb), int(kb), int(vb)))
+    return rows
+
+
+@pytest.mark.parametrize("recipe", _recipes())
+def test_every_printed_recipe_is_accepted(lib, recipe):
+    _, dt, qb, kb, vb = recipe
+    assert vb == 1  # V is always per channel
+    qk = dit.QK_DTYPES[dt]
+    assert lib.dit_attn_workspace_bytes(2, 32, 8, 1000, 1000, 1, qk, qb, kb) > 0
+    assert lib.dit_attn_workspace_bytes(2, 32, 8, 1000, 1000, 3, qk, qb, kb) > 0
+
+
+@pytest.mark.parametrize("bad", [0, 2, 3, 8, 32])
+def test_block_sizes_outside_the_pages_set_are_rejected(lib, bad):
+    assert lib.dit_attn_workspace_bytes(1, 4, 4, 512, 512, 1, 1, bad, 16) == 0
+    assert lib.dit_attn_workspace_bytes(1, 4, 4, 512, 512, 1, 1, 1, bad) == 0
+
+
+def test_workspace_layout_size():
+    # INT8 codes are held as exact fp16 (2 bytes), FP8 codes as 1 byte; V codes 1 byte.
+    B, Hq, Hkv, S = 1, 40, 40, 32768
+    n = B * S * Hq * 128
+    i8 = dit.dit_attn_workspace_bytes(B, Hq, Hkv, S, S, 1, "int8", 1, 16)
+    f8 = dit.dit_attn_workspace_bytes(B, Hq, Hkv, S, S, 1, "fp8_e4m3", 1, 16)
+    assert 5 * n <= i8 < 5 * n + 16 * 2**20
+    assert 3 * n <= f8 < 3 * n + 16 * 2**20
+    assert dit.dit_attn_workspace_bytes(B, Hq, Hkv, S, S, 0, "bf16") == 0
+    assert dit.dit_attn_workspace_bytes(B, Hq, Hkv, S, S, 2, "bf16") == 0
