@@ -37,6 +37,9 @@ namespace ditattn {
 namespace {
 
 constexpr int kThreads = 384;
+constexpr int kLaunchRegs = 168;          // 65536 / 384, rounded down to a multiple of 8
+constexpr int kRegsWG0 = 72, kRegsSoftmax = 216;  // 128 * 72 + 256 * 216 == 384 * 168
+static_assert(128 * kRegsWG0 + 256 * kRegsSoftmax == kThreads * kLaunchRegs, "register hand-over must balance");
 constexpr int kSlots = 4;
 constexpr uint32_t kSlotBytes = 32768;
 constexpr uint32_t kQRegionBytes = 2 * 32768;
@@ -139,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // allocator, scale stager) gives registers to the two softmax warpgroups, which hold a
   // 128-float score row each: 128 x 72 + 256 x 216 = 64512.
   if (warp < 4) {
-  regs_dec<72>();
+  regs_dec<kRegsWG0>();
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -277,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   } else {
     // ------------------------------------------------------------ softmax groups
-    regs_inc<216>();
+    regs_inc<kRegsSoftmax>();
     const int i = (warp - 4) >> 2;                 // Q tile within the CTA
     const int r = ((warp & 3) << 5) + lane;        // row within the tile == TMEM lane
     const uint32_t lane_base = (uint32_t)((warp & 3) << 5) << 16;
@@ -495,6 +498,12 @@ cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !attr_set[dev]) {
+    // The register hand-over in the kernel (setmaxnreg) assumes exactly kLaunchRegs per thread at
+    // launch; with fewer, the softmax warpgroups' increase could never be granted.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, fmha_fwd_kernel<QKF, PVF, SKIP>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidKernelImage;
     e = cudaFuncSetAttribute(fmha_fwd_kernel<QKF, PVF, SKIP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes);
     if (e != cudaSuccess) return e;

@@ -1,0 +1,226 @@
+"""GPU parity: the CUDA path through the C-ABI against the CPU oracle, element by element.
+
+Bars: quantized codes and scales bit-exact; dense BF16 output rel-L2 <= 5e-3 and max-abs <= 2e-2;
+SAGE and SAGE+skip output rel-L2 <= 1e-2 against the quantization-emulating oracle; skipped-tile
+counts within 0.5% of the oracle's (at least one tile of slack for tiny totals, since a vote
+whose margin is below float32 rounding may flip).
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import diffusion_transformer_attention_gb300 as dit
+import workloads
+from oracle import attention as oatt
+from oracle import formats, sage_quant
+
+pytestmark = pytest.mark.gpu
+
+DENSE_REL, DENSE_ABS, SAGE_REL = 5e-3, 2e-2, 1e-2
+
+
+def _np(t):
+    return t.float().cpu().numpy()
+
+
+def _rel(a, b):
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+def _inputs(w, seed=0):
+    q, k, v = workloads.generate(w, seed)
+    return (q, k, v), dict(q=_np(q), k=_np(k), v=_np(v))
+
+
+def _gpu(*ts):
+    return [t.cuda() for t in ts]
+
+
+def _poisoned_like(q):
+    return torch.full_like(q, float("nan"), device="cuda")
+
+
+SMALL = workloads.Workload("small", 1, 2, 2, 256, 256)
+
+
+# ---------------------------------------------------------------- prepass: bit-exact codes and scales
+@pytest.mark.parametrize("dtype", ["int8", "fp8_e4m3"])
+@pytest.mark.parametrize("qb,kb", [(1, 16), (4, 4), (16, 1), (1, 1), (16, 16)])
+@pytest.mark.parametrize("kind", ["koffset", "outlier"])
+def test_prepass_bit_exact(dtype, qb, kb, kind):
+    w = workloads.Workload("pp", 2, 4, 2, 300, 333, kind=kind)
+    (q, k, v), inp = _inputs(w, seed=3)
+    got = dit.sage_quantize_qkv(*_gpu(q, k, v), qk_dtype=dtype, q_block=qb, k_block=kb)
+    torch.cuda.synchronize()
+    want = sage_quant.sage_quantize(inp["q"], inp["k"], inp["v"], dtype, qb, kb)
+    for name in ["k_mean", "v_scale", "q_scale", "k_scale"]:
+        g = got[name].cpu().numpy()
+        assert g.shape == want[name].shape, name
+        assert np.array_equal(g.view(np.uint32), want[name].view(np.uint32)), name
+    for name in ["q_codes", "k_codes", "v_codes"]:
+        g = got[name].cpu().numpy().view(np.uint8)
+        wv = want[name].view(np.uint8)
+        bad = np.count_nonzero(g != wv)
+        assert bad == 0, f"{name}: {bad} of {g.size} codes differ"
+
+
+def test_prepass_is_deterministic():
+    w = workloads.Workload("pp", 1, 8, 8, 1000, 1000, kind="koffset")
+    (q, k, v), _ = _inputs(w, seed=4)
+    qd, kd, vd = _gpu(q, k, v)
+    a = dit.sage_quantize_qkv(qd, kd, vd, qk_dtype="int8")
+    b = dit.sage_quantize_qkv(qd, kd, vd, qk_dtype="int8")
+    for name in a:
+        assert torch.equal(a[name], b[name]), name
+
+
+# ---------------------------------------------------------------- dense BF16
+@pytest.mark.parametrize("shape", [
+    (1, 2, 2, 256, 256),        # the tiny workload: one CTA per head
+    (1, 2, 2, 300, 300),        # ragged Q and KV tails
+    (2, 4, 2, 200, 520),        # GQA, Sq != Skv
+    (1, 3, 1, 130, 1000),       # MQA, cross-attention shape
+    (1, 1, 1, 1, 1),            # a single query and key
+    (1, 2, 1, 513, 129),        # one full KV tile plus one key
+])
+def test_dense_matches_oracle(shape):
+    B, Hq, Hkv, Sq, Skv = shape
+    w = workloads.Workload("d", B, Hq, Hkv, Sq, Skv)
+    (q, k, v), inp = _inputs(w, seed=1)
+    qd, kd, vd = _gpu(q, k, v)
+    out = _poisoned_like(qd)
+    counts = torch.full((B, Hq, math.ceil(Sq / 128)), -1, dtype=torch.int32, device="cuda")
+    dit.dit_attn_fwd(qd, kd, vd, out, skip_counts=counts)
+    dit.dit_attn_check_errors()
+    got = _np(out)
+    want = oatt.dense_attention(inp["q"], inp["k"], inp["v"])
+    assert np.isfinite(got).all()
+    assert _rel(got, want) <= DENSE_REL
+    assert np.abs(got - want).max() <= DENSE_ABS
+    assert (counts == 0).all()
+
+
+def test_dense_koffset_large_logits():
+    # per-channel K offsets of std 2 make logits large; softmax must stay exact in shift
+    w = workloads.Workload("d", 1, 2, 2, 384, 700, kind="koffset")
+    (q, k, v), inp = _inputs(w, seed=2)
+    out = dit.dit_attn_fwd(*_gpu(q, k, v))
+    got, want = _np(out), oatt.dense_attention(inp["q"], inp["k"], inp["v"])
+    assert _rel(got, want) <= DENSE_REL and np.abs(got - want).max() <= DENSE_ABS
+
+
+# ---------------------------------------------------------------- SAGE
+def _sage_reference(inp, w, dtype, qb, kb, factor=None):
+    quant = sage_quant.sage_quantize(inp["q"], inp["k"], inp["v"], dtype, qb, kb)
+    B, Sq, Hq = inp["q"].shape[:3]
+    out = np.zeros(inp["q"].shape)
+    counts = np.zeros((B, Hq, math.ceil(Sq / 128)), np.int64)
+    for b in range(B):
+        for h in range(Hq):
+            for t in range(math.ceil(Sq / 128)):
+                o, n, rows = oatt.attention_q_tile(inp, b, h, t, mode="sage", qk_dtype=dtype, q_block=qb,
+                                                   k_block=kb, factor=factor, quant=quant)
+                out[b, rows, h] = o
+                counts[b, h, t] = n
+    return out, counts
+
+
+@pytest.mark.parametrize("dtype", ["int8", "fp8_e4m3"])
+@pytest.mark.parametrize("qb,kb", [(1, 16), (1, 4), (4, 1), (16, 16)])
+def test_sage_matches_oracle(dtype, qb, kb):
+    w = workloads.Workload("s", 2, 4, 2, 300, 400, kind="koffset")
+    (q, k, v), inp = _inputs(w, seed=5)
+    out = _poisoned_like(q.cuda())
+    dit.dit_attn_fwd(*_gpu(q, k, v), out, mode=dit.MODE_SAGE, qk_dtype=dtype, q_block=qb, k_block=kb)
+    dit.dit_attn_check_errors()
+    got = _np(out)
+    want, _ = _sage_reference(inp, w, dtype, qb, kb)
+    assert np.isfinite(got).all()
+    assert _rel(got, want) <= SAGE_REL
+
+
+@pytest.mark.parametrize("dtype", ["int8", "fp8_e4m3"])
+def test_quantized_entry_equals_fused_path(dtype):
+    w = workloads.Workload("s", 1, 4, 4, 260, 390, kind="outlier")
+    (q, k, v), _ = _inputs(w, seed=6)
+    qd, kd, vd = _gpu(q, k, v)
+    fused = dit.dit_attn_fwd(qd, kd, vd, mode=dit.MODE_SAGE, qk_dtype=dtype, q_block=1, k_block=16)
+    quant = dit.sage_quantize_qkv(qd, kd, vd, qk_dtype=dtype, q_block=1, k_block=16)
+    sep = dit.dit_attn_fwd_quantized(quant, torch.empty_like(qd), qk_dtype=dtype, q_block=1, k_block=16)
+    dit.dit_attn_check_errors()
+    assert torch.equal(fused, sep)
+
+
+# ---------------------------------------------------------------- Skip-Softmax
+VIDEO_SMALL = workloads.Workload("v", 1, 2, 2, 3 * 16 * 24, 3 * 16 * 24, kind="video", grid=(3, 16, 24))
+
+
+@pytest.mark.parametrize("sage", [False, True])
+@pytest.mark.parametrize("factor", [0.0, 5.0, 50.0, 400.0])
+def test_skip_matches_oracle(sage, factor):
+    w = VIDEO_SMALL
+    (q, k, v), inp = _inputs(w, seed=7)
+    B, Hq, Sq = w.B, w.Hq, w.Sq
+    nqt = math.ceil(Sq / 128)
+    counts = torch.full((B, Hq, nqt), -1, dtype=torch.int32, device="cuda")
+    mode = dit.MODE_SKIP | (dit.MODE_SAGE if sage else 0)
+    out = dit.dit_attn_fwd(*_gpu(q, k, v), mode=mode, qk_dtype="int8" if sage else "bf16", q_block=1, k_block=16,
+                           threshold_scale_factor=factor, skip_counts=counts)
+    dit.dit_attn_check_errors()
+    got = _np(out)
+    if sage:
+        want, wcounts = _sage_reference(inp, w, "int8", 1, 16, factor=factor)
+        tol_ok = _rel(got, want) <= SAGE_REL
+    else:
+        want = np.zeros(got.shape)
+        wcounts = np.zeros((B, Hq, nqt), np.int64)
+        for h in range(Hq):
+            for t in range(nqt):
+                o, n, rows = oatt.attention_q_tile(inp, 0, h, t, mode="dense", factor=factor)
+                want[0, rows, h] = o
+                wcounts[0, h, t] = n
+        tol_ok = _rel(got, want) <= DENSE_REL and np.abs(got - want).max() <= DENSE_ABS
+    gc = counts.cpu().numpy()
+    assert (gc >= 0).all()
+    assert abs(int(gc.sum()) - int(wcounts.sum())) <= max(1, 0.005 * wcounts.sum())
+    assert tol_ok, _rel(got, want)
+    if factor == 0.0:
+        assert gc.sum() == 0
+
+
+@pytest.mark.parametrize("sage", [False, True])
+def test_skip_factor_zero_is_bit_identical_to_no_skip(sage):
+    (q, k, v), _ = _inputs(VIDEO_SMALL, seed=8)
+    qd, kd, vd = _gpu(q, k, v)
+    base = dit.MODE_SAGE if sage else dit.MODE_DENSE
+    dt = "int8" if sage else "bf16"
+    a = dit.dit_attn_fwd(qd, kd, vd, mode=base, qk_dtype=dt)
+    b = dit.dit_attn_fwd(qd, kd, vd, mode=base | dit.MODE_SKIP, qk_dtype=dt, threshold_scale_factor=0.0)
+    assert torch.equal(a, b)
+
+
+def test_skip_counts_monotone_in_factor():
+    (q, k, v), _ = _inputs(VIDEO_SMALL, seed=9)
+    qd, kd, vd = _gpu(q, k, v)
+    prev = -1
+    for factor in [0.0, 1.0, 10.0, 100.0, 1000.0]:
+        counts = torch.zeros((1, 2, math.ceil(VIDEO_SMALL.Sq / 128)), dtype=torch.int32, device="cuda")
+        dit.dit_attn_fwd(qd, kd, vd, mode=dit.MODE_SKIP, threshold_scale_factor=factor, skip_counts=counts)
+        total = int(counts.sum())
+        assert total >= prev
+        prev = total
+    assert prev > 0
+
+
+def test_check_errors_reports_ok_after_runs():
+    dit.dit_attn_check_errors()
+
+
+def test_python_binding_raises_on_invalid_arguments():
+    q = torch.zeros((1, 128, 3, 128), dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros((1, 128, 2, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(dit.DitAttnError):
+        dit.dit_attn_fwd(q, k, k)  # 3 query heads over 2 kv heads
