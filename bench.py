@@ -1,0 +1,373 @@
+"""Benchmark: dense-equivalent attention TFLOP/s of the DiT attention forward pass on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {ours,reference}] [--no-modes]
+
+One step is one call of the hot path on the headline workload: dense BF16 attention with
+B=1, Hq=Hkv=40, Sq=Skv=32768, head_dim 128 (the DiT-shaped workload; K carries a per-channel
+offset). Dense-equivalent FLOP per call = 4*B*Hq*Sq*Skv*128. Prints one JSON line.
+
+* value        device-timed throughput: inputs resident in HBM, CUDA events on the launching
+               stream around K back-to-back steps (inputs of 1 GiB exceed the 126 MB L2, so no
+               flush is needed), max over ranks.
+* e2e          the same metric through the public API with pinned host buffers: every step
+               copies Q, K, V host->device, runs the call and copies O back.
+* roofline     the attention kernel against the measured dense BF16 tensor peak.
+* cpu_baseline the CPU oracle (float64 NumPy) timed on this host on a bounded sample.
+* modes        the other workloads (SAGE INT8, SAGE FP8 with GQA, SAGE INT8 + Skip-Softmax sweep
+               on the 75600-token video grid), each against its own instruction peak.
+* --impl reference times the oracle (there is no reference implementation to install: the
+  pages give no code); it prints the same metric with "impl": "reference".
+
+Multi-GPU (torchrun): every rank runs its own copy of the workload (weak scaling, no
+collective on the data path); value = total FLOP of all ranks / the slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+HEADLINE = "dit_dense_32k"
+METRIC = "dense-equiv attention TFLOPS at B=1,H=40,S=32768,d=128; % of tensor-core peak"
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), \
+            float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, 1700.0, FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------------ clocks during the timed region
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        load = [r for r in rows if (num(r[3]) or 0) > 300] or rows  # samples under load
+        sm = [num(r[1]) for r in load if num(r[1]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in load:
+            for name, val in zip(names, r[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(rows[0][2]),
+                "reasons": sorted(reasons), "samples": len(load)}
+
+
+# ------------------------------------------------------------------ distributed helpers
+def dist_setup(n_gpus):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle sample
+def oracle_sample(w: workloads.Workload, budget_s: float = 15.0, max_tiles: int = 64, warmup: int = 0,
+                  steps: int | None = None):
+    """Time the CPU oracle on whole 128-row query tiles of one head of the workload's recipe.
+
+    One sample (a "step") is one query tile against all Skv keys. With ``steps`` given, runs
+    ``warmup`` untimed tiles and then exactly ``steps`` timed tiles; otherwise runs tiles until
+    ``budget_s`` seconds or ``max_tiles``. Returns (dense-equiv TFLOP/s, seconds per tile, tiles,
+    threads, description)."""
+    from oracle import attention as oatt
+    from oracle import sage_quant
+    one = w.scaled(B=1, Hq=1, Hkv=1)
+    q, k, v = workloads.generate(one, seed=0)
+    inp = dict(q=q.float().numpy(), k=k.float().numpy(), v=v.float().numpy())
+    quant = None
+    if w.mode == "sage":
+        quant = sage_quant.sage_quantize(inp["q"], inp["k"], inp["v"], w.qk_dtype, w.q_block, w.k_block)
+    factor = w.factors[len(w.factors) // 2] if w.factors else None
+    ntiles = math.ceil(w.Sq / 128)
+    order = np.random.default_rng(0).permutation(ntiles)
+
+    def tile(n):
+        oatt.attention_q_tile(inp, 0, 0, int(order[n % ntiles]), mode=w.mode, qk_dtype=w.qk_dtype,
+                              q_block=w.q_block, k_block=w.k_block, factor=factor, quant=quant)
+    for n in range(warmup):
+        tile(n)
+    t0 = time.perf_counter()
+    tiles = 0
+    while (tiles < steps) if steps is not None else (tiles < max_tiles and time.perf_counter() - t0 < budget_s):
+        tile(warmup + tiles)
+        tiles += 1
+    dt = time.perf_counter() - t0
+    flop = 4.0 * tiles * 128 * w.Skv * 128
+    try:
+        threads = len(os.sched_getaffinity(0))
+    except AttributeError:
+        threads = os.cpu_count()
+    desc = (f"{tiles} query tiles x 128 rows of one head against all {w.Skv} keys, float64 NumPy "
+            f"({w.name} recipe)")
+    return flop / dt / 1e12, dt / max(tiles, 1), tiles, threads, desc
+
+
+# ------------------------------------------------------------------ timing helpers
+def time_steps(fn, steps, warmup, world, stream):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)  # ms on this rank
+
+
+def run_modes(dit, steps, warmup, world, stream, peak16):
+    """The other workloads, each as one call of the whole path (prepass + attention)."""
+    res = {}
+    peak8 = 2.0 * peak16                               # FP8 dense = 2 x BF16 (nominal ratio)
+    peak_i8 = 2.0 * peak16 * peak8 / (peak16 + peak8)  # BMM1 on fp16 codes, BMM2 on FP8
+    for name, peak, peak_desc in [("dit_sage_int8_32k", peak_i8, "BMM1 f16 + BMM2 e4m3 harmonic peak"),
+                                  ("gqa_sage_fp8_16k", peak8, "2 x measured bf16 (e4m3 nominal ratio)")]:
+        w = workloads.WORKLOADS[name]
+        q, k, v = workloads.generate(w, seed=1, device="cuda")
+        ws = torch.empty(dit.dit_attn_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, dit.MODE_SAGE, w.qk_dtype,
+                                                      w.q_block, w.k_block), dtype=torch.uint8, device="cuda")
+        out = torch.empty_like(q)
+
+        def step():
+            dit.dit_attn_fwd(q, k, v, out, mode=dit.MODE_SAGE, qk_dtype=w.qk_dtype, q_block=w.q_block,
+                             k_block=w.k_block, workspace=ws, stream=stream)
+        ms = max_over_ranks(time_steps(step, steps, warmup, world, stream), world) / steps
+        tf = w.dense_equiv_flop / (ms * 1e-3) / 1e12
+        res[name] = {"ms": round(ms, 3), "tflops": round(tf, 1), "peak_tflops": round(peak, 1),
+                     "frac": round(tf / peak, 3), "peak": peak_desc, "launches_per_step": 5}
+        del q, k, v, ws, out
+    # Skip-Softmax sweep on the video grid, against dense BF16 on the same shape
+    w = workloads.WORKLOADS["video_skip_int8_75600"]
+    q, k, v = workloads.generate(w, seed=1, device="cuda")
+    out = torch.empty_like(q)
+    nqt = math.ceil(w.Sq / 128)
+    counts = torch.zeros((w.B, w.Hq, nqt), dtype=torch.int32, device="cuda")
+    ws = torch.empty(dit.dit_attn_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, dit.MODE_SAGE, w.qk_dtype,
+                                                  w.q_block, w.k_block), dtype=torch.uint8, device="cuda")
+    s = max(2, steps // 4)
+
+    def dense():
+        dit.dit_attn_fwd(q, k, v, out, stream=stream)
+    dense_ms = max_over_ranks(time_steps(dense, s, min(warmup, 3), world, stream), world) / s
+    sweep = {}
+    nkt = math.ceil(w.Skv / 128)
+    for factor in w.factors:
+        def step():
+            dit.dit_attn_fwd(q, k, v, out, mode=dit.MODE_SAGE | dit.MODE_SKIP, qk_dtype=w.qk_dtype,
+                             q_block=w.q_block, k_block=w.k_block, threshold_scale_factor=factor, workspace=ws,
+                             skip_counts=counts, stream=stream)
+        ms = max_over_ranks(time_steps(step, s, min(warmup, 3), world, stream), world) / s
+        frac = float(counts.sum().item()) / (w.B * w.Hq * nqt * nkt)
+        sweep[str(factor)] = {"ms": round(ms, 3), "skip_fraction": round(frac, 4),
+                              "speedup_vs_dense_bf16": round(dense_ms / ms, 3),
+                              "dense_equiv_tflops": round(w.dense_equiv_flop / (ms * 1e-3) / 1e12, 1)}
+    res["video_skip_int8_75600"] = {"dense_bf16_ms": round(dense_ms, 3),
+                                    "dense_bf16_tflops": round(w.dense_equiv_flop / (dense_ms * 1e-3) / 1e12, 1),
+                                    "sweep": sweep}
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-modes", action="store_true", help="skip the SAGE / Skip-Softmax workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    warmup = max(3, args.warmup)
+    w = workloads.WORKLOADS[HEADLINE]
+    flop = w.dense_equiv_flop
+    config = {"workload": HEADLINE, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Skv": w.Skv, "head_dim": 128,
+              "mode": "dense bf16", "l2": "inputs 1.0 GiB > 126 MB L2, no flush"}
+
+    rank, world, local = dist_setup(args.gpus) if args.impl == "ours" else (
+        int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), 0)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        tf, per_tile, tiles, threads, desc = oracle_sample(w, warmup=warmup, steps=args.steps)
+        line = {"metric": METRIC, "value": round(tf, 6), "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+                "warmup": warmup, "ms_per_step": round(per_tile * 1e3, 3), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+                "impl": "reference",
+                "cpu_baseline": {"value": round(tf, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                                 "sample": desc},
+                "e2e": {"value": round(tf, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import diffusion_transformer_attention_gb300 as dit
+    dit.library()  # raises if the CUDA library is missing: no fallback
+    torch.cuda.set_device(local)
+    stream = torch.cuda.current_stream()
+    peak16, peak16_sus, hbm, peak_src = peaks()
+
+    q, k, v = workloads.generate(w, seed=rank, device="cuda")
+    out = torch.empty_like(q)
+
+    def step():
+        dit.dit_attn_fwd(q, k, v, out, stream=stream)
+
+    props = torch.cuda.get_device_properties(local)
+    gpu_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) is not None else str(local)
+    with ClockSampler(gpu_id) as clk:
+        elapsed = time_steps(step, args.steps, warmup, world, stream)
+    clocks = clk.summary()
+    dit.dit_attn_check_errors(stream)
+    tmax = max_over_ranks(elapsed, world)
+    ms = tmax / args.steps
+    value = world * flop * args.steps / (tmax * 1e-3) / 1e12
+    kernel_tflops = flop / (elapsed / args.steps * 1e-3) / 1e12  # this rank's launch average
+
+    # end to end through the public API with pinned host buffers
+    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        dit.dit_attn_fwd(q, k, v, out, stream=stream)
+        hout.copy_(out, non_blocking=True)
+    e2e_steps = max(2, args.steps // 2)
+    e2e_ms = max_over_ranks(time_steps(e2e_step, e2e_steps, warmup, world, stream), world) / e2e_steps
+    e2e_value = world * flop / (e2e_ms * 1e-3) / 1e12
+    h2d = 3 * q.numel() * q.element_size()
+    d2h = out.numel() * out.element_size()
+    del hq, hk, hv, hout
+
+    modes = None
+    if not args.no_modes:
+        del q, k, v, out
+        torch.cuda.empty_cache()
+        modes = run_modes(dit, args.steps, warmup, world, stream, peak16)
+
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline:
+        tf, _, tiles, threads, desc = oracle_sample(w)
+        cpu = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc}
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "fmha_dense_bf16_dit32k.json")
+    if os.path.exists(prof):
+        with open(prof) as f:
+            traffic = json.load(f).get("dram_bytes_per_launch")
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": warmup, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) Q/V, K + per-channel offset)",
+        "config": config,
+        "pct_of_peak": round(100.0 * kernel_tflops / peak16, 1),
+        "roofline": {"bound": "tensor", "achieved": round(kernel_tflops, 1), "peak": peak16, "unit": "TFLOP/s",
+                     "frac": round(kernel_tflops / peak16, 3), "traffic": traffic,
+                     "peak_source": f"{peak_src} dense bf16 burst (MEASURED_PEAKS.json bf16_tflops)",
+                     "kernel": "fmha_fwd_kernel<bf16,bf16,noskip>", "flop_per_launch": flop},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 1), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if modes is not None:
+        line["modes"] = modes
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

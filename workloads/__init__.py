@@ -73,7 +73,7 @@ WORKLOADS = {
 
 
 def _randn(gen: torch.Generator, shape, std: float = 1.0) -> torch.Tensor:
-    x = torch.randn(*shape, generator=gen, dtype=torch.float32)
+    x = torch.randn(*shape, generator=gen, dtype=torch.float32, device=gen.device)
     return x * std if std != 1.0 else x
 
 
@@ -81,17 +81,23 @@ def video_embedding(gen: torch.Generator, grid, n_freq: int = 64, std: float = 0
     """The fixed random Fourier embedding f(p) of the grid coordinates: [T*H*W, 2*n_freq]."""
     T, H, W = grid
     omega = _randn(gen, (n_freq, 3), std).double()
-    t = torch.arange(T, dtype=torch.float64)
-    h = torch.arange(H, dtype=torch.float64)
-    w = torch.arange(W, dtype=torch.float64)
+    dev = gen.device
+    t = torch.arange(T, dtype=torch.float64, device=dev)
+    h = torch.arange(H, dtype=torch.float64, device=dev)
+    w = torch.arange(W, dtype=torch.float64, device=dev)
     p = torch.stack(torch.meshgrid(t, h, w, indexing="ij"), dim=-1).reshape(-1, 3)  # raster order
     ang = p @ omega.T
     return torch.cat([torch.cos(ang), torch.sin(ang)], dim=1).float()
 
 
-def generate(w: Workload, seed: int = 0):
-    """(q, k, v) as CPU bf16 tensors of shape [B, Sq, Hq, 128] / [B, Skv, Hkv, 128]."""
-    gen = torch.Generator("cpu").manual_seed(seed)
+def generate(w: Workload, seed: int = 0, device: str = "cpu"):
+    """(q, k, v) as bf16 tensors of shape [B, Sq, Hq, 128] / [B, Skv, Hkv, 128].
+
+    The CPU generator is the canonical one (parity tests and the oracle use it). With
+    device='cuda' the same recipe is drawn by the device generator: a different random stream
+    with the same distribution, used where only timing matters.
+    """
+    gen = torch.Generator(device).manual_seed(seed)
     D = HEAD_DIM
     if w.kind == "video":
         assert w.Sq == w.Skv == math.prod(w.grid), "video workloads are self-attention over the grid"
@@ -110,7 +116,7 @@ def generate(w: Workload, seed: int = 0):
         k.add_(c[None, None])
     elif w.kind == "outlier":
         n = round(0.01 * w.Hkv * D)
-        pick = torch.randperm(w.Hkv * D, generator=gen)[:n]
+        pick = torch.randperm(w.Hkv * D, generator=gen, device=gen.device)[:n]
         kv = k.view(w.B, w.Skv, w.Hkv * D)
         kv[:, :, pick] *= 8.0
     elif w.kind != "iid":
