@@ -37,6 +37,7 @@ SIGNATURES = {
     "dit_attn_fwd": (_c_int, [_vp, _vp, _vp, _vp] + [_c_int] * 9 + [_c_float, _vp, _vp, _c_size, _vp]),
     "sage_quantize_workspace_bytes": (_c_size, [_c_int] * 3),
     "sage_quantize_qkv": (_c_int, [_vp, _vp, _vp] + [_c_int] * 8 + [_vp] * 8 + [_c_size, _vp]),
+    "sage_quantize_qkv_noalloc": (_c_int, [_vp, _vp, _vp] + [_c_int] * 8 + [_vp] * 7 + [_vp]),
     "dit_attn_quantized_workspace_bytes": (_c_size, [_c_int] * 6),
     "dit_attn_fwd_quantized": (_c_int, [_vp] * 7 + [_c_int] * 9 + [_c_float, _vp, _vp, _c_size, _vp]),
     "dit_attn_check_errors": (_c_int, [_vp]),
@@ -148,6 +149,19 @@ def sage_quantize_qkv(q, k, v, *, qk_dtype="int8", q_block=1, k_block=16, stream
                                   _ptr(res["k_mean"]), _ptr(workspace), workspace.numel(), _stream(stream))
     _check(st, "sage_quantize_qkv")
     return res
+
+
+def sage_quantize_qkv_noalloc(q, k, v, out: dict, *, qk_dtype="int8", q_block=1, k_block=16, stream=None):
+    """``sage_quantize_qkv`` into caller-provided outputs, with the scratch the library keeps in
+    its own fixed 32 MiB device array (for callers that cannot allocate at call time). ``out``
+    holds preallocated tensors with the keys and shapes ``sage_quantize_qkv`` returns."""
+    B, Hq, Hkv, Sq, Skv = _shape(q, k)
+    st = _lib().sage_quantize_qkv_noalloc(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Sq, Skv, _qk(qk_dtype), q_block,
+                                          k_block, _ptr(out["q_codes"]), _ptr(out["k_codes"]),
+                                          _ptr(out["v_codes"]), _ptr(out["q_scale"]), _ptr(out["k_scale"]),
+                                          _ptr(out["v_scale"]), _ptr(out["k_mean"]), _stream(stream))
+    _check(st, "sage_quantize_qkv_noalloc")
+    return out
 
 
 def dit_attn_fwd_quantized(quant: dict, out, *, mode=MODE_SAGE, qk_dtype="int8", q_block=1, k_block=16,

@@ -125,6 +125,29 @@ dit_status sage_quantize_qkv(const void* q, const void* k, const void* v, int B,
                              float* q_scale, float* k_scale, float* v_scale, float* k_mean, void* workspace,
                              size_t workspace_bytes, void* stream);
 
+/*
+ * sage_quantize_qkv without a workspace argument, for callers that cannot allocate device memory
+ * when they call: for example a plugin whose host framework owns the whole device memory pool and
+ * gives it no allocator, or a latency-critical loop where cudaMalloc (which may synchronize the
+ * device) is not allowed. The pages have no counterpart; this is a library convenience.
+ *
+ * Inputs, outputs and results are exactly those of sage_quantize_qkv. The scratch for the K-mean
+ * and V-absmax partial sums lives in a fixed 32 MiB device array inside the library, which every
+ * GPU that loads the library reserves until the process exits. It holds B * Hkv * ceil(Skv/256)
+ * chunks of 128 channels at 12 bytes per channel (each of its two parts rounded up to 256 bytes);
+ * larger problems return DIT_E_WORKSPACE (e.g. B * Hkv = 40 allows Skv up to about 140,000).
+ * Nothing here calls cudaMalloc, cudaFree or any allocating routine.
+ *
+ * The first call on each device looks up the array's device address (a one-time set-up); make
+ * that first call before any stream capture. Every call shares the one array and the kernels
+ * write each scratch value before reading it, so nothing needs clearing between calls; but two
+ * calls whose kernels overlap on the GPU (e.g. on different streams) race on it.
+ */
+dit_status sage_quantize_qkv_noalloc(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int Sq,
+                                     int Skv, int qk_dtype, int q_block, int k_block, void* q_codes, void* k_codes,
+                                     void* v_codes, float* q_scale, float* k_scale, float* v_scale, float* k_mean,
+                                     void* stream);
+
 /* Bytes of device workspace dit_attn_fwd_quantized needs (INT8 codes are widened there). */
 size_t dit_attn_quantized_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int qk_dtype);
 
