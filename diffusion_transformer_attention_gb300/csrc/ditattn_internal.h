@@ -42,7 +42,12 @@ struct FmhaParams {
 // {128, S, H, B} tensors with 128-byte swizzled boxes.
 cudaError_t launch_fmha(int qk_format, int pv_format, bool skip, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                         const CUtensorMap& tm_v, const CUtensorMap& tm_o, const FmhaParams& p, cudaStream_t stream);
-size_t fmha_smem_bytes();
+cudaError_t launch_fmha_dense(bool skip, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const CUtensorMap& to, const FmhaParams& p, cudaStream_t stream);
+cudaError_t launch_fmha_sage_i8(bool skip, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                const CUtensorMap& to, const FmhaParams& p, cudaStream_t stream);
+cudaError_t launch_fmha_sage_f8(bool skip, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                const CUtensorMap& to, const FmhaParams& p, cudaStream_t stream);
 
 // Quantize-prepass launchers (prepass.cu).
 cudaError_t launch_kv_stats(const void* k, const void* v, int B, int Hkv, int Skv, double* psum, float* pmax,

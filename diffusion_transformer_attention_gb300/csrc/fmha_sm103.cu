@@ -1,534 +1,15 @@
-// Fused attention forward kernel for sm_103a: TMA-staged Q/K/V tiles, tcgen05 MMAs accumulating
-// S = Q K^T and O += P V in tensor memory, online softmax with exp2, optional SAGE dequantization
-// and P re-quantization to FP8, and the Skip-Softmax tile test.
-//
-// The method is fixed by the pages ("TRTLLM Attention" user guide: dense BF16, SAGE, Skip-Softmax;
-// "SAGE + Skip-Softmax -- API Design & Test Plan", Part 1 §4: bmm1/bmm2 scales and
-// threshold = factor / seqlen). The pages give no kernel design; this one is built for GB300:
-//
-// CTA = 2 query tiles of 128 rows of one (batch, query head); 384 threads in 12 warps.
-//   warp 0       TMA producer: Q0, Q1 once, then K_j / V_j into a ring of 4 x 32 KB slots.
-//   warp 1       MMA issuer (one thread): BMM1 S_i = Q_i K_j^T (SS), BMM2 O_i += P_i V_j (TS:
-//                P from tensor memory, V from shared memory, V is MN-major so no transpose).
-//   warp 2       tensor-memory allocator (512 columns: S0 | S1 | O0 | O1).
-//   warp 3       SAGE only: stages the per-column K scales of each KV tile and the V scales.
-//   warps 4-7    softmax for Q tile 0 (thread = row = TMEM lane);  warps 8-11: Q tile 1.
-// The MMA issue order is S0(j) S1(j) | O0 += P0(j) V_j, S0(j+1) | O1 += P1(j) V_j, S1(j+1) ...
-// so while one softmax group turns S_i into P_i, the tensor cores work on the other tile.
-// P_i overwrites the first columns of S_i (bf16: 64 columns; e4m3: 32 columns).
-//
-// Numerics: logits are kept in log2 units (scaled by softmax_scale * log2 e). Dense mode rescales
-// O lazily (only when the running max grows by more than 8, P then stays below 2^8); SAGE rescales
-// eagerly so P = exp2(s - m_run) lies in [0, 1] and P * 448 re-quantizes on the same grid as the
-// definition. The row sum uses the unquantized P. Skip-Softmax compares the tile max against
-// the exact running max.
-//
-// Every wait is bounded; on expiry the kernel records a timeout in the device error word, tells
-// the other roles to stop, drains its own copies and MMAs, frees tensor memory and exits.
-#include <cuda_runtime.h>
-
-#include <cmath>
-#include <cstdint>
-
+// Attention-kernel dispatch: picks the instantiation for the operand formats, the K scale block
+// size and Skip-Softmax. The instantiations live in fmha_dense.cu, fmha_sage_i8.cu and
+// fmha_sage_f8.cu so that they compile in parallel.
 #include "ditattn_internal.h"
-#include "sm103_ptx.cuh"
 
 namespace ditattn {
-namespace {
-
-constexpr int kThreads = 384;
-constexpr int kLaunchRegs = 168;          // 65536 / 384, rounded down to a multiple of 8
-constexpr int kRegsWG0 = 72, kRegsSoftmax = 216;  // 128 * 72 + 256 * 216 == 384 * 168
-static_assert(128 * kRegsWG0 + 256 * kRegsSoftmax == kThreads * kLaunchRegs, "register hand-over must balance");
-constexpr int kSlots = 4;
-constexpr uint32_t kSlotBytes = 32768;
-constexpr uint32_t kQRegionBytes = 2 * 32768;
-constexpr uint32_t kRingOff = kQRegionBytes;
-constexpr uint32_t kKsOff = kRingOff + kSlots * kSlotBytes;  // 4 x 128 floats
-constexpr uint32_t kVsOff = kKsOff + kSlots * 512;           // 128 floats
-constexpr uint32_t kBarOff = kVsOff + 512;
-constexpr uint32_t kSmemBytes = kBarOff + 512 + 1024;        // + alignment slack
-constexpr float kLazyRescale = 8.0f;                         // log2 units
-constexpr float kLog2_448 = 8.807354922057604f;
-
-struct Bars {
-  uint64_t q_full;
-  uint64_t kv_full[kSlots];
-  uint64_t kv_empty[kSlots];
-  uint64_t s_full[2];
-  uint64_t p_full[2];
-  uint64_t o_full[2];
-  uint64_t ks_full[kSlots];
-  uint64_t ks_empty[kSlots];
-  uint64_t vs_full;
-  uint64_t drain;
-  uint32_t tmem_base;
-  int abort_flag;
-  int skip_flag[2];
-};
-static_assert(sizeof(Bars) <= 512, "barrier block too large");
-
-__device__ __forceinline__ void record_timeout(const FmhaParams& p, Bars* bars) {
-  atomicExch(p.err, kErrTimeout);
-  *reinterpret_cast<volatile int*>(&bars->abort_flag) = 1;
-}
-
-template <int QKF, int PVF, bool SKIP>
-__global__ void __launch_bounds__(kThreads, 1)
-    fmha_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                    const FmhaParams p) {
-  constexpr bool kSage = (QKF != QK_BF16);
-  constexpr int kQKBytes = (QKF == QK_E4M3) ? 1 : 2;
-  constexpr int kPVBytes = (PVF == PV_E4M3) ? 1 : 2;
-  constexpr uint32_t kQTileBytes = 128u * 128u * kQKBytes;
-  constexpr uint32_t kVTileBytes = 128u * 128u * kPVBytes;
-  constexpr int kMma1Kind = (QKF == QK_E4M3) ? KIND_F8F6F4 : KIND_F16;
-  constexpr int kMma2Kind = (PVF == PV_E4M3) ? KIND_F8F6F4 : KIND_F16;
-  constexpr int kK1Steps = (QKF == QK_E4M3) ? 4 : 8;  // K = 128 in steps of 32 (8-bit) or 16
-  constexpr int kK2Steps = (PVF == PV_E4M3) ? 4 : 8;
-  constexpr uint32_t kIdesc1 = (QKF == QK_BF16)  ? make_idesc(1, 1, 0, 0, 128, 128)
-                               : (QKF == QK_F16) ? make_idesc(0, 0, 0, 0, 128, 128)
-                                                 : make_idesc(0, 0, 0, 0, 128, 128);
-  constexpr uint32_t kIdesc2 = (PVF == PV_BF16) ? make_idesc(1, 1, 0, 1, 128, 128) : make_idesc(0, 0, 0, 1, 128, 128);
-
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Bars* bars = reinterpret_cast<Bars*>(smem + kBarOff);
-  float* s_ks = reinterpret_cast<float*>(smem + kKsOff);
-  float* s_vs = reinterpret_cast<float*>(smem + kVsOff);
-  const volatile int* abort_flag = &bars->abort_flag;
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int hq = blockIdx.y, b = blockIdx.z;
-  const int hkv = hq / p.group;
-  const int q0 = blockIdx.x * 256;
-  const int nt = p.n_kv_tiles;
-  const uint64_t budget = p.wait_budget_ns;
-
-  if (threadIdx.x == 0) {
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_v);
-    tma_prefetch_desc(&tm_o);
-    mbar_init(&bars->q_full, 1);
-    for (int s = 0; s < kSlots; ++s) {
-      mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
-      mbar_init(&bars->ks_full[s], 32);
-      mbar_init(&bars->ks_empty[s], 256);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->p_full[i], 128);
-      mbar_init(&bars->o_full[i], 1);
-    }
-    mbar_init(&bars->vs_full, 32);
-    mbar_init(&bars->drain, 1);
-    bars->abort_flag = 0;
-    bars->skip_flag[0] = bars->skip_flag[1] = 0;
-    fence_mbar_init();
-  }
-  if (warp == 2) {
-    tmem_alloc(&bars->tmem_base, 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tbase = bars->tmem_base;
-
-  // Launched at 168 registers per thread (384 x 168 = 64512): warpgroup 0 (producer, MMA,
-  // allocator, scale stager) gives registers to the two softmax warpgroups, which hold a
-  // 128-float score row each: 128 x 72 + 256 x 216 = 64512.
-  if (warp < 4) {
-  regs_dec<kRegsWG0>();
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      const uint64_t pol_q = l2_policy_evict_first();
-      const uint64_t pol_kv = l2_policy_evict_last();
-      int issued[kSlots] = {0, 0, 0, 0};
-      bool ok = true;
-      mbar_arrive_expect_tx(&bars->q_full, 2 * kQTileBytes);
-      for (int i = 0; i < 2; ++i) {
-        uint8_t* dst = smem + i * 32768;
-        if (kQKBytes == 2) {
-          tma_load_4d(dst, &tm_q, &bars->q_full, 0, q0 + 128 * i, hq, b, pol_q);
-          tma_load_4d(dst + 16384, &tm_q, &bars->q_full, 64, q0 + 128 * i, hq, b, pol_q);
-        } else {
-          tma_load_4d(dst, &tm_q, &bars->q_full, 0, q0 + 128 * i, hq, b, pol_q);
-        }
-      }
-      for (int j = 0; j < nt && ok; ++j) {
-        for (int kv = 0; kv < 2; ++kv) {
-          const int t = 2 * j + kv, s = t & (kSlots - 1), u = t / kSlots;
-          if (!mbar_wait_bounded(&bars->kv_empty[s], (u & 1) ^ 1, budget, abort_flag)) {
-            record_timeout(p, bars);
-            ok = false;
-            break;
-          }
-          uint8_t* dst = smem + kRingOff + s * kSlotBytes;
-          const CUtensorMap* map = kv ? &tm_v : &tm_k;
-          const int bytes = kv ? kVTileBytes : kQTileBytes;
-          const int eb = kv ? kPVBytes : kQKBytes;
-          mbar_arrive_expect_tx(&bars->kv_full[s], bytes);
-          if (eb == 2) {
-            tma_load_4d(dst, map, &bars->kv_full[s], 0, 128 * j, hkv, b, pol_kv);
-            tma_load_4d(dst + 16384, map, &bars->kv_full[s], 64, 128 * j, hkv, b, pol_kv);
-          } else {
-            tma_load_4d(dst, map, &bars->kv_full[s], 0, 128 * j, hkv, b, pol_kv);
-          }
-          ++issued[s];
-        }
-      }
-      if (!ok) {
-        // drain: wait (bounded) for every copy this thread started before shared memory goes away
-        mbar_wait_bounded(&bars->q_full, 0, budget, nullptr);
-        for (int s = 0; s < kSlots; ++s)
-          if (issued[s] > 0) mbar_wait_bounded(&bars->kv_full[s], (issued[s] - 1) & 1, budget, nullptr);
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      bool ok = mbar_wait_bounded(&bars->q_full, 0, budget, abort_flag);
-      if (!ok) record_timeout(p, bars);
-      tc_fence_after();
-      const uint32_t sbase = smem_u32(smem);
-      uint64_t dq[2], dk[kSlots], dv[kSlots];
-      for (int i = 0; i < 2; ++i) dq[i] = make_sdesc_sw128(sbase + i * 32768, 16, 1024);
-      for (int s = 0; s < kSlots; ++s) {
-        dk[s] = make_sdesc_sw128(sbase + kRingOff + s * kSlotBytes, 16, 1024);
-        dv[s] = make_sdesc_sw128(sbase + kRingOff + s * kSlotBytes, kPVBytes == 2 ? 16384 : 8192, 1024);
-      }
-      volatile int* skip_flag = bars->skip_flag;
-      for (int j = 0; j <= nt && ok; ++j) {
-        const int tk = 2 * j, tv = 2 * j - 1;
-        if (j < nt) {
-          if (!mbar_wait_bounded(&bars->kv_full[tk & 3], (tk >> 2) & 1, budget, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-        }
-        if (j >= 1) {
-          if (!mbar_wait_bounded(&bars->kv_full[tv & 3], (tv >> 2) & 1, budget, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-        }
-        for (int i = 0; i < 2; ++i) {
-          if (j >= 1) {
-            if (!mbar_wait_bounded(&bars->p_full[i], (j - 1) & 1, budget, abort_flag)) { ok = false; break; }
-            tc_fence_after();
-            if (!SKIP || skip_flag[i] == 0) {
-              const uint64_t bv = dv[tv & 3];
-              const uint32_t d = tbase + 256 + 128 * i;
-              const uint32_t a = tbase + 128 * i;
-#pragma unroll
-              for (int kk = 0; kk < kK2Steps; ++kk) {
-                const uint32_t off = (kPVBytes == 2) ? kk * 2048 : kk * 4096;
-                mma_ts<kMma2Kind>(d, a + 8 * kk, bv + (off >> 4), kIdesc2, (j > 1 || kk > 0) ? 1u : 0u);
-              }
-            }
-          }
-          if (j < nt) {
-            const uint64_t aq = dq[i], bk = dk[tk & 3];
-            const uint32_t d = tbase + 128 * i;
-#pragma unroll
-            for (int kk = 0; kk < kK1Steps; ++kk) {
-              const uint32_t off = (kQKBytes == 2) ? (kk >> 2) * 16384 + (kk & 3) * 32 : kk * 32;
-              mma_ss<kMma1Kind>(d, aq + (off >> 4), bk + (off >> 4), kIdesc1, kk > 0 ? 1u : 0u);
-            }
-            mma_commit(&bars->s_full[i]);
-          }
-        }
-        if (!ok) break;
-        if (j >= 1) mma_commit(&bars->kv_empty[tv & 3]);
-        if (j < nt) mma_commit(&bars->kv_empty[tk & 3]);
-      }
-      if (ok) {
-        mma_commit(&bars->o_full[0]);
-        mma_commit(&bars->o_full[1]);
-      } else {
-        record_timeout(p, bars);
-      }
-      // drain: no MMA may still be running when tensor memory is freed
-      mma_commit(&bars->drain);
-      mbar_wait_bounded(&bars->drain, 0, budget, nullptr);
-    }
-  } else if (warp == 3) {
-    // ------------------------------------------------------------ SAGE scale stager
-    if constexpr (kSage) {
-      bool ok = true;
-      const float* vs = p.v_scale + ((size_t)b * p.Hkv + hkv) * kHeadDim;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) s_vs[lane * 4 + e] = vs[lane * 4 + e];
-      mbar_arrive(&bars->vs_full);
-      const float* ks = p.k_scale + ((size_t)b * p.Hkv + hkv) * p.nkb;
-      for (int j = 0; j < nt; ++j) {
-        const int e = j & 3, u = j >> 2;
-        ok = mbar_wait_bounded(&bars->ks_empty[e], (u & 1) ^ 1, budget, abort_flag);
-        if (!__all_sync(0xffffffffu, ok)) {
-          if (lane == 0) record_timeout(p, bars);
-          break;
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int col = 128 * j + lane * 4 + q;
-          s_ks[e * 128 + lane * 4 + q] = (col < p.Skv) ? __ldg(ks + col / p.k_block) : 0.0f;
-        }
-        mbar_arrive(&bars->ks_full[e]);
-      }
-    }
-  }
-  } else {
-    // ------------------------------------------------------------ softmax groups
-    regs_inc<kRegsSoftmax>();
-    const int i = (warp - 4) >> 2;                 // Q tile within the CTA
-    const int r = ((warp & 3) << 5) + lane;        // row within the tile == TMEM lane
-    const uint32_t lane_base = (uint32_t)((warp & 3) << 5) << 16;
-    const uint32_t t_s = tbase + lane_base + 128 * i;
-    const uint32_t t_o = tbase + lane_base + 256 + 128 * i;
-    const int qrow = q0 + 128 * i + r;
-    const bool row_valid = qrow < p.Sq;
-    const int bar_id = 1 + i;
-    float c = p.c_scale;
-    if constexpr (kSage) {
-      const float qs = row_valid ? __ldg(p.q_scale + ((size_t)b * p.Hq + hq) * p.nqb + qrow / p.q_block) : 0.0f;
-      c = qs * p.c_scale;
-    }
-    float m_ex = -INFINITY, m_ref = -INFINITY, l = 0.0f;
-    int nskip = 0;
-    bool ok = true;
-    volatile int* skip_flag = bars->skip_flag;
-
-    for (int j = 0; j < nt; ++j) {
-      if (ok) {
-        ok = mbar_wait_bounded(&bars->s_full[i], j & 1, budget, abort_flag);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok && lane == 0) record_timeout(p, bars);
-      }
-      if (!ok) {
-        if (SKIP && j > 0) named_bar_and(bar_id, 128, true);  // keep the group's barrier count in step
-        continue;
-      }
-      tc_fence_after();
-      float s[128];
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) tmem_ld32(t_s + 32 * cc, s + 32 * cc);
-      tmem_ld_wait();
-      if constexpr (kSage) {
-        const int e = j & 3;
-        bool ks_ok = mbar_wait_bounded(&bars->ks_full[e], (j >> 2) & 1, budget, abort_flag);
-        ks_ok = __all_sync(0xffffffffu, ks_ok);
-        if (ks_ok) {
-          const float4* ksv = reinterpret_cast<const float4*>(s_ks + e * 128);
-#pragma unroll
-          for (int q = 0; q < 32; ++q) {
-            const float4 w = ksv[q];
-            s[4 * q] *= w.x;
-            s[4 * q + 1] *= w.y;
-            s[4 * q + 2] *= w.z;
-            s[4 * q + 3] *= w.w;
-          }
-        } else {
-          if (lane == 0) record_timeout(p, bars);
-          ok = false;
-        }
-        mbar_arrive(&bars->ks_empty[e]);
-      }
-      const int nvalid = min(128, p.Skv - 128 * j);
-      const bool tail = nvalid < 128;
-      float mx = -INFINITY;
-      if (!tail) {
-#pragma unroll
-        for (int k = 0; k < 128; ++k) mx = fmaxf(mx, s[k]);
-      } else {
-#pragma unroll
-        for (int k = 0; k < 128; ++k) mx = (k < nvalid) ? fmaxf(mx, s[k]) : mx;
-      }
-      const float mt = mx * c;  // c >= 0 and mx finite
-      if constexpr (SKIP) {
-        if (j > 0) {
-          const bool vote = !row_valid || !ok || (mt - m_ex < p.log2_thr);
-          if (named_bar_and(bar_id, 128, vote)) {
-            ++nskip;
-            if (r == 0) skip_flag[i] = 1;
-            tc_fence_before();
-            mbar_arrive(&bars->p_full[i]);
-            continue;
-          }
-        }
-      }
-      if (!ok) continue;
-      const float m_new = fmaxf(m_ex, mt);
-      bool need;
-      float alpha = 1.0f;
-      if constexpr (kSage) {
-        need = m_new > m_ref;
-        if (need) alpha = ex2_approx(m_ref - m_new);
-        m_ref = m_new;
-      } else {
-        need = (m_new - m_ref) > kLazyRescale;
-        if (need) {
-          alpha = ex2_approx(m_ref - m_new);
-          m_ref = m_new;
-        }
-      }
-      m_ex = m_new;
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
-#pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          float o[32];
-          tmem_ld32(t_o + 32 * cc, o);
-          tmem_ld_wait();
-          uint32_t w[32];
-#pragma unroll
-          for (int k = 0; k < 32; ++k) w[k] = __float_as_uint(o[k] * alpha);
-          tmem_st32(t_o + 32 * cc, w);
-        }
-      }
-      l *= alpha;
-      // exponentials, row sum, and P into tensor memory (over the first columns of S)
-      const float bias = kSage ? (m_ref - kLog2_448) : m_ref;
-      float lsum0 = 0.f, lsum1 = 0.f, lsum2 = 0.f, lsum3 = 0.f;
-#pragma unroll
-      for (int k = 0; k < 128; k += 4) {
-        s[k] = ex2_approx(fmaf(s[k], c, -bias));
-        s[k + 1] = ex2_approx(fmaf(s[k + 1], c, -bias));
-        s[k + 2] = ex2_approx(fmaf(s[k + 2], c, -bias));
-        s[k + 3] = ex2_approx(fmaf(s[k + 3], c, -bias));
-        if (tail) {
-          if (k >= nvalid) s[k] = 0.f;
-          if (k + 1 >= nvalid) s[k + 1] = 0.f;
-          if (k + 2 >= nvalid) s[k + 2] = 0.f;
-          if (k + 3 >= nvalid) s[k + 3] = 0.f;
-        }
-        lsum0 += s[k];
-        lsum1 += s[k + 1];
-        lsum2 += s[k + 2];
-        lsum3 += s[k + 3];
-      }
-      l += (lsum0 + lsum1) + (lsum2 + lsum3);
-      if constexpr (PVF == PV_BF16) {
-        uint32_t w[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) w[k] = pack_bf16x2(s[2 * k], s[2 * k + 1]);
-        tmem_st32(t_s, w);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) w[k] = pack_bf16x2(s[64 + 2 * k], s[64 + 2 * k + 1]);
-        tmem_st32(t_s + 32, w);
-      } else {
-        uint32_t w[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k)
-          w[k] = pack_e4m3x2(s[4 * k], s[4 * k + 1]) | (pack_e4m3x2(s[4 * k + 2], s[4 * k + 3]) << 16);
-        tmem_st32(t_s, w);
-      }
-      tmem_st_wait();
-      if constexpr (SKIP) {
-        if (r == 0) skip_flag[i] = 0;
-      }
-      tc_fence_before();
-      mbar_arrive(&bars->p_full[i]);
-    }
-
-    // ------------------------------------------------------------ epilogue: O / l -> bf16 -> TMA store
-    if (ok) {
-      ok = mbar_wait_bounded(&bars->o_full[i], 0, budget, abort_flag);
-      if constexpr (kSage) ok = ok && mbar_wait_bounded(&bars->vs_full, 0, budget, abort_flag);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok && lane == 0) record_timeout(p, bars);
-    }
-    uint8_t* stage = smem + kRingOff + i * kSlotBytes;  // the KV ring is idle once O is final
-    if (ok) {
-      tc_fence_after();
-      const float inv_l = 1.0f / l;
-#pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        float o[32];
-        tmem_ld32(t_o + 32 * cc, o);
-        tmem_ld_wait();
-        uint32_t w[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          float a0 = o[2 * k] * inv_l, a1 = o[2 * k + 1] * inv_l;
-          if constexpr (kSage) {
-            a0 *= s_vs[32 * cc + 2 * k];
-            a1 *= s_vs[32 * cc + 2 * k + 1];
-          }
-          w[k] = pack_bf16x2(a0, a1);
-        }
-        // 128-byte swizzled staging: half h holds columns 64h..64h+63; 16-byte chunk ch of row r
-        // sits at r*128 + ((ch ^ (r & 7)) * 16).
-        const int h = cc >> 1;
-        uint8_t* rowp = stage + h * 16384 + r * 128;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int ch = (cc & 1) * 4 + q;
-          *reinterpret_cast<uint4*>(rowp + ((ch ^ (r & 7)) << 4)) =
-              make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-        }
-      }
-      fence_proxy_async_smem();
-    }
-    const bool all_ok = named_bar_and(bar_id, 128, ok);
-    if (all_ok && r == 0) {
-      tma_store_4d(&tm_o, stage, 0, q0 + 128 * i, hq, b);
-      tma_store_4d(&tm_o, stage + 16384, 64, q0 + 128 * i, hq, b);
-      tma_store_commit();
-      tma_store_wait_all0();
-    }
-    if (r == 0 && p.skip_counts != nullptr) {
-      const int qt = 2 * blockIdx.x + i;
-      if (qt < p.n_q_tiles) p.skip_counts[((size_t)b * p.Hq + hq) * p.n_q_tiles + qt] = nskip;
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 2) {
-    tc_fence_after();
-    tmem_dealloc(tbase, 512);
-  }
-}
-
-template <int QKF, int PVF, bool SKIP>
-cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
-                       const FmhaParams& p, cudaStream_t stream) {
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 64 && !attr_set[dev]) {
-    // The register hand-over in the kernel (setmaxnreg) assumes exactly kLaunchRegs per thread at
-    // launch; with fewer, the softmax warpgroups' increase could never be granted.
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, fmha_fwd_kernel<QKF, PVF, SKIP>);
-    if (e != cudaSuccess) return e;
-    if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidKernelImage;
-    e = cudaFuncSetAttribute(fmha_fwd_kernel<QKF, PVF, SKIP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
-  const dim3 grid((p.Sq + 255) / 256, p.Hq, p.B);
-  fmha_fwd_kernel<QKF, PVF, SKIP><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, to, p);
-  return cudaGetLastError();
-}
-
-}  // namespace
-
-size_t fmha_smem_bytes() { return kSmemBytes; }
 
 cudaError_t launch_fmha(int qk_format, int pv_format, bool skip, const CUtensorMap& tq, const CUtensorMap& tk,
                         const CUtensorMap& tv, const CUtensorMap& to, const FmhaParams& p, cudaStream_t stream) {
-  if (qk_format == QK_BF16 && pv_format == PV_BF16)
-    return skip ? launch_one<QK_BF16, PV_BF16, true>(tq, tk, tv, to, p, stream)
-                : launch_one<QK_BF16, PV_BF16, false>(tq, tk, tv, to, p, stream);
-  if (qk_format == QK_F16 && pv_format == PV_E4M3)
-    return skip ? launch_one<QK_F16, PV_E4M3, true>(tq, tk, tv, to, p, stream)
-                : launch_one<QK_F16, PV_E4M3, false>(tq, tk, tv, to, p, stream);
-  if (qk_format == QK_E4M3 && pv_format == PV_E4M3)
-    return skip ? launch_one<QK_E4M3, PV_E4M3, true>(tq, tk, tv, to, p, stream)
-                : launch_one<QK_E4M3, PV_E4M3, false>(tq, tk, tv, to, p, stream);
+  if (qk_format == QK_BF16 && pv_format == PV_BF16) return launch_fmha_dense(skip, tq, tk, tv, to, p, stream);
+  if (qk_format == QK_F16 && pv_format == PV_E4M3) return launch_fmha_sage_i8(skip, tq, tk, tv, to, p, stream);
+  if (qk_format == QK_E4M3 && pv_format == PV_E4M3) return launch_fmha_sage_f8(skip, tq, tk, tv, to, p, stream);
   return cudaErrorInvalidValue;
 }
 
