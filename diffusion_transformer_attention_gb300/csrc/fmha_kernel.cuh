@@ -7,16 +7,22 @@
 // "SAGE + Skip-Softmax -- API Design & Test Plan", Part 1 §4: bmm1/bmm2 scales and
 // threshold = factor / seqlen). The pages give no kernel design; this one is built for GB300:
 //
-// CTA = 2 query tiles of 128 rows of one (batch, query head); 384 threads in 12 warps.
+// CTA = 2 query tiles of 128 rows of one (batch, query head); 640 threads in 20 warps.
 //   warp 0       TMA producer: Q0, Q1 once, then K_j / V_j into a ring of 4 x 32 KB slots.
 //   warp 1       MMA issuer (one thread): BMM1 S_i = Q_i K_j^T (SS), BMM2 O_i += P_i V_j (TS:
 //                P from tensor memory, V from shared memory, V is MN-major so no transpose).
 //   warp 2       tensor-memory allocator (512 columns: S0 | S1 | O0 | O1).
 //   warp 3       SAGE only: stages the per-column K scales of each KV tile and the V scales.
-//   warps 4-7    softmax for Q tile 0 (thread = row = TMEM lane);  warps 8-11: Q tile 1.
+//   warps 4-19   four softmax warpgroups: Q tile i = g / 2 and column half h = g % 2 for group g.
+//                A thread owns one row (= TMEM lane) and 64 of its 128 columns; the two halves
+//                of a row exchange partial maxima through shared memory. Halving the columns per
+//                thread halves the softmax latency, which is what bounds the pipeline: each Q
+//                tile's cycle (its MMAs, then its softmax) must fit in the time the tensor cores
+//                spend on both tiles.
 // The MMA issue order is S0(j) S1(j) | O0 += P0(j) V_j, S0(j+1) | O1 += P1(j) V_j, S1(j+1) ...
-// so while one softmax group turns S_i into P_i, the tensor cores work on the other tile.
-// P_i overwrites the first columns of S_i (bf16: 64 columns; e4m3: 32 columns).
+// so while the softmax groups of one tile turn S into P, the tensor cores work on the other.
+// Each half writes its packed P over the first columns of its own half of S (bf16: 32 columns,
+// e4m3: 16), and BMM2 reads the two P pieces at their own addresses.
 //
 // Numerics: logits are kept in log2 units (scaled by softmax_scale * log2 e). Dense mode rescales
 // O lazily (only when the running max grows by more than 8, P then stays below 2^8); SAGE rescales
@@ -25,7 +31,9 @@
 // the exact running max.
 //
 // Every wait is bounded; on expiry the kernel records a timeout in the device error word, tells
-// the other roles to stop, drains its own copies and MMAs, frees tensor memory and exits.
+// the other roles to stop, drains its own copies and MMAs, frees tensor memory and exits. Named
+// barriers are reached the same number of times on every path, so no thread waits on a peer
+// that left.
 #pragma once
 #include <cuda_runtime.h>
 
@@ -38,17 +46,19 @@
 namespace ditattn {
 namespace {
 
-constexpr int kThreads = 384;
-constexpr int kLaunchRegs = 168;          // 65536 / 384, rounded down to a multiple of 8
-constexpr int kRegsWG0 = 72, kRegsSoftmax = 216;  // 128 * 72 + 256 * 216 == 384 * 168
-static_assert(128 * kRegsWG0 + 256 * kRegsSoftmax == kThreads * kLaunchRegs, "register hand-over must balance");
+constexpr int kThreads = 640;
+constexpr int kLaunchRegs = 96;                  // 65536 / 640, rounded down to a multiple of 8
+constexpr int kRegsWG0 = 64, kRegsSoftmax = 104;  // 128 * 64 + 512 * 104 == 640 * 96
+static_assert(128 * kRegsWG0 + 512 * kRegsSoftmax <= kThreads * kLaunchRegs, "register hand-over must fit");
 constexpr int kSlots = 4;
 constexpr uint32_t kSlotBytes = 32768;
 constexpr uint32_t kQRegionBytes = 2 * 32768;
 constexpr uint32_t kRingOff = kQRegionBytes;
 constexpr uint32_t kKsOff = kRingOff + kSlots * kSlotBytes;  // 4 x 128 floats
 constexpr uint32_t kVsOff = kKsOff + kSlots * 512;           // 128 floats
-constexpr uint32_t kBarOff = kVsOff + 512;
+constexpr uint32_t kXmaxOff = kVsOff + 512;                  // [tile][half][parity][128] partial maxima
+constexpr uint32_t kXlOff = kXmaxOff + 2 * 2 * 2 * 512;      // [tile][half][128] partial row sums
+constexpr uint32_t kBarOff = kXlOff + 2 * 2 * 512;
 constexpr uint32_t kSmemBytes = kBarOff + 512 + 1024;        // + alignment slack
 constexpr float kLazyRescale = 8.0f;                         // log2 units
 constexpr float kLog2_448 = 8.807354922057604f;
@@ -82,13 +92,13 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
   return d;
 }
 
-// Max of 128 values with eight independent accumulators (short dependency chains).
-__device__ __forceinline__ float rowmax128(const float* s) {
+// Max of 64 values with eight independent accumulators.
+__device__ __forceinline__ float rowmax64(const float* s) {
   float a[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) a[j] = fmaxf(s[2 * j], s[2 * j + 1]);
 #pragma unroll
-  for (int k = 16; k < 128; k += 16)
+  for (int k = 16; k < 64; k += 16)
 #pragma unroll
     for (int j = 0; j < 8; ++j) a[j] = max3f(a[j], s[k + 2 * j], s[k + 2 * j + 1]);
   return max3f(max3f(a[0], a[1], a[2]), max3f(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
@@ -150,11 +160,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->kv_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
       mbar_init(&bars->ks_full[s], 32);
-      mbar_init(&bars->ks_empty[s], 256);
+      mbar_init(&bars->ks_empty[s], 16);  // one arrival per softmax warp
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->p_full[i], 128);
+      mbar_init(&bars->p_full[i], 8);     // one arrival per softmax warp of the tile
       mbar_init(&bars->o_full[i], 1);
     }
     mbar_init(&bars->vs_full, 32);
@@ -172,9 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = bars->tmem_base;
 
-  // Launched at 168 registers per thread (384 x 168 = 64512): warpgroup 0 (producer, MMA,
-  // allocator, scale stager) gives registers to the two softmax warpgroups, which hold a
-  // 128-float score row each: 128 x 72 + 256 x 216 = 64512.
+  // Launched at 96 registers per thread: warpgroup 0 (producer, MMA, allocator, scale stager)
+  // hands registers to the four softmax warpgroups, which hold 64 scores per thread.
   if (warp < 4) {
   regs_dec<kRegsWG0>();
   if (warp == 0) {
@@ -258,7 +267,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int kk = 0; kk < kK2Steps; ++kk) {
                 const uint32_t off = (kPVBytes == 2) ? kk * 2048 : kk * 4096;
-                mma_ts<kMma2Kind>(d, a + 8 * kk, bv + (off >> 4), kIdesc2, (j > 1 || kk > 0) ? 1u : 0u);
+                // K columns 0..63 come from the P piece in S columns 0.., 64..127 from S columns 64..
+                const uint32_t pa = a + ((kk < kK2Steps / 2) ? 8 * kk : 64 + 8 * (kk - kK2Steps / 2));
+                mma_ts<kMma2Kind>(d, pa, bv + (off >> 4), kIdesc2, (j > 1 || kk > 0) ? 1u : 0u);
               }
             }
           }
@@ -315,14 +326,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ softmax groups
     regs_inc<kRegsSoftmax>();
-    const int i = (warp - 4) >> 2;                 // Q tile within the CTA
+    const int g = (warp - 4) >> 2;                 // softmax warpgroup 0..3
+    const int i = g >> 1;                          // Q tile within the CTA
+    const int h = g & 1;                           // column half: S/O columns 64h .. 64h+63
     const int r = ((warp & 3) << 5) + lane;        // row within the tile == TMEM lane
     const uint32_t lane_base = (uint32_t)((warp & 3) << 5) << 16;
-    const uint32_t t_s = tbase + lane_base + 128 * i;
-    const uint32_t t_o = tbase + lane_base + 256 + 128 * i;
+    const uint32_t t_s = tbase + lane_base + 128 * i + 64 * h;
+    const uint32_t t_o = tbase + lane_base + 256 + 128 * i + 64 * h;
     const int qrow = q0 + 128 * i + r;
     const bool row_valid = qrow < p.Sq;
-    const int bar_id = 1 + i;
+    const uint32_t tile_bar = 1 + i;               // the 256 threads of this Q tile
+    const uint32_t group_bar = 3 + g;              // the 128 threads of this warpgroup
+    float* xmax = reinterpret_cast<float*>(smem + kXmaxOff);
+    float* xl = reinterpret_cast<float*>(smem + kXlOff);
     float c = p.c_scale;
     if constexpr (kSage) {
       const float qs = row_valid ? __ldg(p.q_scale + ((size_t)b * p.Hq + hq) * p.nqb + qrow / p.q_block) : 0.0f;
@@ -340,27 +356,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok && lane == 0) record_timeout(p, bars);
       }
       if (!ok) {
-        if (SKIP && j > 0) named_bar_and(bar_id, 128, true);  // keep the group's barrier count in step
+        // keep this tile's named barriers in step with the peer half
+        named_bar_sync(tile_bar, 256);
+        if (SKIP && j > 0) named_bar_and(tile_bar, 256, true);
         continue;
       }
       tc_fence_after();
-      float2 s2[64];
+      float2 s2[32];
       float* s = reinterpret_cast<float*>(s2);
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) tmem_ld32(t_s + 32 * cc, s + 32 * cc);
+      tmem_ld32(t_s, s);
+      tmem_ld32(t_s + 32, s + 32);
       tmem_ld_wait();
-      const int nvalid = min(128, p.Skv - 128 * j);
-      const bool tail = nvalid < 128;
+      const int nvalid = min(64, p.Skv - 128 * j - 64 * h);  // may be <= 0 for the upper half
+      const bool tail = nvalid < 64;
       if (tail) {
 #pragma unroll
-        for (int k = 0; k < 128; ++k)
+        for (int k = 0; k < 64; ++k)
           if (k >= nvalid) s[k] = -INFINITY;
       }
       // Exponent weight per column group (log2 units): the row constant c, times the K block
       // scale in SAGE. KB >= 4 folds the block scale into the weight; KB == 1 multiplies first.
-      constexpr int kGroups = (kSage && KB >= 4) ? 128 / KB : 1;
+      constexpr int kGroups = (kSage && KB >= 4) ? 64 / KB : 1;
       float wg[kGroups];
-      float mt;
+      float mh;  // this half's max of the weighted logits
       if constexpr (kSage) {
         const int e = j & 3;
         bool ks_ok = mbar_wait_bounded(&bars->ks_full[e], (j >> 2) & 1, budget, abort_flag);
@@ -369,34 +387,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) record_timeout(p, bars);
           ok = false;
         }
-        const float* ks = s_ks + e * 128;
+        const float* ks = s_ks + e * 128 + 64 * h;
         if constexpr (KB == 1) {
           const float2* ks2 = reinterpret_cast<const float2*>(ks);
 #pragma unroll
-          for (int k = 0; k < 64; ++k) s2[k] = __fmul2_rn(s2[k], ks2[k]);
+          for (int k = 0; k < 32; ++k) s2[k] = __fmul2_rn(s2[k], ks2[k]);
           wg[0] = c;
-          mt = rowmax128(s) * c;
+          mh = rowmax64(s) * c;
         } else {
-          mt = -INFINITY;
+          mh = -INFINITY;
 #pragma unroll
-          for (int g = 0; g < kGroups; ++g) {
-            wg[g] = ks[g * KB] * c;
-            mt = fmaxf(mt, groupmax<KB>(s + g * KB) * wg[g]);  // a NaN from -inf * 0 is ignored
+          for (int q = 0; q < kGroups; ++q) {
+            wg[q] = ks[q * KB] * c;
+            mh = fmaxf(mh, groupmax<KB>(s + q * KB) * wg[q]);  // a NaN from -inf * 0 is ignored
           }
         }
-        mbar_arrive(&bars->ks_empty[e]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->ks_empty[e]);
       } else {
         wg[0] = c;
-        mt = rowmax128(s) * c;  // c > 0 and at least one column is valid
+        mh = rowmax64(s) * c;  // -inf when this half has no valid column
       }
+      // full-row max from the two halves (identical on both sides: max is exact)
+      xmax[((i * 2 + h) * 2 + (j & 1)) * 128 + r] = mh;
+      named_bar_sync(tile_bar, 256);
+      const float mo = xmax[((i * 2 + (h ^ 1)) * 2 + (j & 1)) * 128 + r];
+      const float mt = fmaxf(mh, mo);
       if constexpr (SKIP) {
         if (j > 0) {
           const bool vote = !row_valid || !ok || (mt - m_ex < p.log2_thr);
-          if (named_bar_and(bar_id, 128, vote)) {
+          if (named_bar_and(tile_bar, 256, vote)) {
             ++nskip;
-            if (r == 0) skip_flag[i] = 1;
+            if (r == 0 && h == 0) skip_flag[i] = 1;
             tc_fence_before();
-            mbar_arrive(&bars->p_full[i]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->p_full[i]);
             continue;
           }
         }
@@ -417,10 +442,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       m_ex = m_new;
+      l *= alpha;
+      // exponentials (two columns per packed FMA) and this half's row sum
+      const float bias = kSage ? (m_ref - kLog2_448) : m_ref;
+      const float2 nb = make_float2(-bias, -bias);
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const float w = wg[kGroups == 1 ? 0 : (2 * k) / (kGroups == 1 ? 64 : KB)];
+        const float2 t = __ffma2_rn(s2[k], make_float2(w, w), nb);
+        s2[k].x = ex2_approx(t.x);
+        s2[k].y = ex2_approx(t.y);
+      }
+      if constexpr (kSage) {
+        // masked columns hold -inf; with a zero weight (zero scale) that gives NaN, so clear them
+        if (tail) {
+#pragma unroll
+          for (int k = 0; k < 64; ++k)
+            if (k >= nvalid) s[k] = 0.f;
+        }
+      }
+      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+      for (int k = 0; k < 32; ++k) acc[k & 3] = __fadd2_rn(acc[k & 3], s2[k]);
+      l += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
+      // P over the first columns of this half of S
+      if constexpr (PVF == PV_BF16) {
+        uint32_t w[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) w[k] = pack_bf16x2(s[2 * k], s[2 * k + 1]);
+        tmem_st32(t_s, w);
+      } else {
+        uint32_t w[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          w[k] = pack_e4m3x2(s[4 * k], s[4 * k + 1]) | (pack_e4m3x2(s[4 * k + 2], s[4 * k + 3]) << 16);
+        tmem_st16(t_s, w);
+      }
+      // O rescale for this half (after P, when the scores are no longer held in registers; still
+      // before the arrive that lets the MMA accumulate into O)
       if (j > 0 && __any_sync(0xffffffffu, need)) {
         const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < 2; ++cc) {
           float2 o[16];
           tmem_ld32(t_o + 32 * cc, reinterpret_cast<float*>(o));
           tmem_ld_wait();
@@ -429,61 +492,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(t_o + 32 * cc, reinterpret_cast<const uint32_t*>(o));
         }
       }
-      l *= alpha;
-      // exponentials (two columns per packed FMA), row sum, and P into tensor memory over the
-      // first columns of S
-      const float bias = kSage ? (m_ref - kLog2_448) : m_ref;
-      const float2 nb = make_float2(-bias, -bias);
-      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-      for (int k = 0; k < 64; ++k) {
-        const float w = wg[kGroups == 1 ? 0 : (2 * k) / (kGroups == 1 ? 128 : KB)];
-        const float2 t = __ffma2_rn(s2[k], make_float2(w, w), nb);
-        s2[k].x = ex2_approx(t.x);
-        s2[k].y = ex2_approx(t.y);
-        if (tail) {
-          if (2 * k >= nvalid) s2[k].x = 0.f;
-          if (2 * k + 1 >= nvalid) s2[k].y = 0.f;
-        }
-        acc[k & 3] = __fadd2_rn(acc[k & 3], s2[k]);
-      }
-      l += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
-      if constexpr (PVF == PV_BF16) {
-        uint32_t w[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) w[k] = pack_bf16x2(s[2 * k], s[2 * k + 1]);
-        tmem_st32(t_s, w);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) w[k] = pack_bf16x2(s[64 + 2 * k], s[64 + 2 * k + 1]);
-        tmem_st32(t_s + 32, w);
-      } else {
-        uint32_t w[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k)
-          w[k] = pack_e4m3x2(s[4 * k], s[4 * k + 1]) | (pack_e4m3x2(s[4 * k + 2], s[4 * k + 3]) << 16);
-        tmem_st32(t_s, w);
-      }
       tmem_st_wait();
       if constexpr (SKIP) {
-        if (r == 0) skip_flag[i] = 0;
+        if (r == 0 && h == 0) skip_flag[i] = 0;
       }
       tc_fence_before();
-      mbar_arrive(&bars->p_full[i]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->p_full[i]);
     }
 
     // ------------------------------------------------------------ epilogue: O / l -> bf16 -> TMA store
+    xl[(i * 2 + h) * 128 + r] = l;
+    named_bar_sync(tile_bar, 256);
+    const float l_row = xl[(i * 2 + 0) * 128 + r] + xl[(i * 2 + 1) * 128 + r];
     if (ok) {
       ok = mbar_wait_bounded(&bars->o_full[i], 0, budget, abort_flag);
       if constexpr (kSage) ok = ok && mbar_wait_bounded(&bars->vs_full, 0, budget, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok && lane == 0) record_timeout(p, bars);
     }
-    uint8_t* stage = smem + kRingOff + i * kSlotBytes;  // the KV ring is idle once O is final
+    uint8_t* stage = smem + kRingOff + i * kSlotBytes + h * 16384;  // the KV ring is idle once O is final
     if (ok) {
       tc_fence_after();
-      const float inv_l = 1.0f / l;
+      const float inv_l = 1.0f / l_row;
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
         float o[32];
         tmem_ld32(t_o + 32 * cc, o);
         tmem_ld_wait();
@@ -492,32 +525,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < 16; ++k) {
           float a0 = o[2 * k] * inv_l, a1 = o[2 * k + 1] * inv_l;
           if constexpr (kSage) {
-            a0 *= s_vs[32 * cc + 2 * k];
-            a1 *= s_vs[32 * cc + 2 * k + 1];
+            a0 *= s_vs[64 * h + 32 * cc + 2 * k];
+            a1 *= s_vs[64 * h + 32 * cc + 2 * k + 1];
           }
           w[k] = pack_bf16x2(a0, a1);
         }
-        // 128-byte swizzled staging: half h holds columns 64h..64h+63; 16-byte chunk ch of row r
+        // 128-byte swizzled staging of this half (columns 64h..64h+63): 16-byte chunk ch of row r
         // sits at r*128 + ((ch ^ (r & 7)) * 16).
-        const int h = cc >> 1;
-        uint8_t* rowp = stage + h * 16384 + r * 128;
+        uint8_t* rowp = stage + r * 128;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const int ch = (cc & 1) * 4 + q;
+          const int ch = cc * 4 + q;
           *reinterpret_cast<uint4*>(rowp + ((ch ^ (r & 7)) << 4)) =
               make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
         }
       }
       fence_proxy_async_smem();
     }
-    const bool all_ok = named_bar_and(bar_id, 128, ok);
+    const bool all_ok = named_bar_and(group_bar, 128, ok);
     if (all_ok && r == 0) {
-      tma_store_4d(&tm_o, stage, 0, q0 + 128 * i, hq, b);
-      tma_store_4d(&tm_o, stage + 16384, 64, q0 + 128 * i, hq, b);
+      tma_store_4d(&tm_o, stage, 64 * h, q0 + 128 * i, hq, b);
       tma_store_commit();
       tma_store_wait_all0();
     }
-    if (r == 0 && p.skip_counts != nullptr) {
+    if (r == 0 && h == 0 && p.skip_counts != nullptr) {
       const int qt = 2 * blockIdx.x + i;
       if (qt < p.n_q_tiles) p.skip_counts[((size_t)b * p.Hq + hq) * p.n_q_tiles + qt] = nskip;
     }
