@@ -234,70 +234,76 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      bool ok = mbar_wait_bounded(&bars->q_full, 0, budget, abort_flag);
-      if (!ok) record_timeout(p, bars);
-      tc_fence_after();
-      const uint32_t sbase = smem_u32(smem);
-      uint64_t dq[2], dk[kSlots], dv[kSlots];
-      for (int i = 0; i < 2; ++i) dq[i] = make_sdesc_sw128(sbase + i * 32768, 16, 1024);
-      for (int s = 0; s < kSlots; ++s) {
-        dk[s] = make_sdesc_sw128(sbase + kRingOff + s * kSlotBytes, 16, 1024);
-        dv[s] = make_sdesc_sw128(sbase + kRingOff + s * kSlotBytes, kPVBytes == 2 ? 16384 : 8192, 1024);
+    // The whole warp runs this loop in uniform control flow (so descriptors stay in uniform
+    // registers); one elected lane issues the tcgen05 instructions.
+    const uint32_t leader = elect_one();
+    bool ok = mbar_wait_bounded(&bars->q_full, 0, budget, abort_flag);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok && leader) record_timeout(p, bars);
+    tc_fence_after();
+    const uint32_t sbase = smem_u32(smem);
+    const uint64_t dq0 = make_sdesc_sw128(sbase, 16, 1024);
+    const uint64_t dk0 = make_sdesc_sw128(sbase + kRingOff, 16, 1024);
+    const uint64_t dv0 = make_sdesc_sw128(sbase + kRingOff, kPVBytes == 2 ? 16384 : 8192, 1024);
+    volatile int* skip_flag = bars->skip_flag;
+    for (int j = 0; j <= nt && ok; ++j) {
+      const int tk = 2 * j, tv = 2 * j - 1;
+      if (j < nt) {
+        ok = mbar_wait_bounded(&bars->kv_full[tk & 3], (tk >> 2) & 1, budget, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
       }
-      volatile int* skip_flag = bars->skip_flag;
-      for (int j = 0; j <= nt && ok; ++j) {
-        const int tk = 2 * j, tv = 2 * j - 1;
-        if (j < nt) {
-          if (!mbar_wait_bounded(&bars->kv_full[tk & 3], (tk >> 2) & 1, budget, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-        }
+      if (j >= 1) {
+        ok = mbar_wait_bounded(&bars->kv_full[tv & 3], (tv >> 2) & 1, budget, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+      }
+      // descriptor start addresses advance in 16-byte units inside the low 14 bits
+      const uint64_t bk = dk0 + (uint64_t)(((tk & 3) * kSlotBytes) >> 4);
+      const uint64_t bv = dv0 + (uint64_t)(((tv & 3) * kSlotBytes) >> 4);
+#pragma unroll 1
+      for (int i = 0; i < 2; ++i) {
         if (j >= 1) {
-          if (!mbar_wait_bounded(&bars->kv_full[tv & 3], (tv >> 2) & 1, budget, abort_flag)) { ok = false; break; }
+          ok = mbar_wait_bounded(&bars->p_full[i], (j - 1) & 1, budget, abort_flag);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
-        }
-        for (int i = 0; i < 2; ++i) {
-          if (j >= 1) {
-            if (!mbar_wait_bounded(&bars->p_full[i], (j - 1) & 1, budget, abort_flag)) { ok = false; break; }
-            tc_fence_after();
-            if (!SKIP || skip_flag[i] == 0) {
-              const uint64_t bv = dv[tv & 3];
-              const uint32_t d = tbase + 256 + 128 * i;
-              const uint32_t a = tbase + 128 * i;
+          if (!SKIP || skip_flag[i] == 0) {
+            const uint32_t d = tbase + 256 + 128 * i;
+            const uint32_t a = tbase + 128 * i;
 #pragma unroll
-              for (int kk = 0; kk < kK2Steps; ++kk) {
-                const uint32_t off = (kPVBytes == 2) ? kk * 2048 : kk * 4096;
-                // K columns 0..63 come from the P piece in S columns 0.., 64..127 from S columns 64..
-                const uint32_t pa = a + ((kk < kK2Steps / 2) ? 8 * kk : 64 + 8 * (kk - kK2Steps / 2));
-                mma_ts<kMma2Kind>(d, pa, bv + (off >> 4), kIdesc2, (j > 1 || kk > 0) ? 1u : 0u);
-              }
+            for (int kk = 0; kk < kK2Steps; ++kk) {
+              const uint32_t off = (kPVBytes == 2) ? kk * 2048 : kk * 4096;
+              // K columns 0..63 come from the P piece in S columns 0.., 64..127 from S columns 64..
+              const uint32_t pa = a + ((kk < kK2Steps / 2) ? 8 * kk : 64 + 8 * (kk - kK2Steps / 2));
+              mma_ts_if<kMma2Kind>(leader, d, pa, bv + (off >> 4), kIdesc2, (j > 1 || kk > 0) ? 1u : 0u);
             }
           }
-          if (j < nt) {
-            const uint64_t aq = dq[i], bk = dk[tk & 3];
-            const uint32_t d = tbase + 128 * i;
-#pragma unroll
-            for (int kk = 0; kk < kK1Steps; ++kk) {
-              const uint32_t off = (kQKBytes == 2) ? (kk >> 2) * 16384 + (kk & 3) * 32 : kk * 32;
-              mma_ss<kMma1Kind>(d, aq + (off >> 4), bk + (off >> 4), kIdesc1, kk > 0 ? 1u : 0u);
-            }
-            mma_commit(&bars->s_full[i]);
-          }
         }
-        if (!ok) break;
-        if (j >= 1) mma_commit(&bars->kv_empty[tv & 3]);
-        if (j < nt) mma_commit(&bars->kv_empty[tk & 3]);
+        if (j < nt) {
+          const uint64_t aq = dq0 + (uint64_t)((i * 32768) >> 4);
+          const uint32_t d = tbase + 128 * i;
+#pragma unroll
+          for (int kk = 0; kk < kK1Steps; ++kk) {
+            const uint32_t off = (kQKBytes == 2) ? (kk >> 2) * 16384 + (kk & 3) * 32 : kk * 32;
+            mma_ss_if<kMma1Kind>(leader, d, aq + (off >> 4), bk + (off >> 4), kIdesc1, kk > 0 ? 1u : 0u);
+          }
+          mma_commit_if(leader, &bars->s_full[i]);
+        }
       }
-      if (ok) {
-        mma_commit(&bars->o_full[0]);
-        mma_commit(&bars->o_full[1]);
-      } else {
-        record_timeout(p, bars);
-      }
-      // drain: no MMA may still be running when tensor memory is freed
-      mma_commit(&bars->drain);
-      mbar_wait_bounded(&bars->drain, 0, budget, nullptr);
+      if (!ok) break;
+      if (j >= 1) mma_commit_if(leader, &bars->kv_empty[tv & 3]);
+      if (j < nt) mma_commit_if(leader, &bars->kv_empty[tk & 3]);
     }
+    if (ok) {
+      mma_commit_if(leader, &bars->o_full[0]);
+      mma_commit_if(leader, &bars->o_full[1]);
+    } else if (leader) {
+      record_timeout(p, bars);
+    }
+    // drain: no MMA may still be running when tensor memory is freed
+    mma_commit_if(leader, &bars->drain);
+    mbar_wait_bounded(&bars->drain, 0, budget, nullptr);
+    __syncwarp();
   } else if (warp == 3) {
     // ------------------------------------------------------------ SAGE scale stager
     if constexpr (kSage) {
