@@ -41,7 +41,19 @@ def e4m3_encode(x) -> np.ndarray:
 
     Round to nearest, ties to even; magnitudes above 448 saturate to 448; NaN maps to the
     NaN pattern. Works on the exact value it is given, so a float32 input is rounded once.
+    Large arrays are encoded in slices (element by element, so the result is the same).
     """
+    x = np.asarray(x)
+    if x.size > (1 << 24):
+        flat = x.reshape(-1)
+        out = np.empty(flat.shape, dtype=np.uint8)
+        for s0 in range(0, flat.size, 1 << 24):
+            out[s0:s0 + (1 << 24)] = _e4m3_encode_slice(flat[s0:s0 + (1 << 24)])
+        return out.reshape(x.shape)
+    return _e4m3_encode_slice(x)
+
+
+def _e4m3_encode_slice(x) -> np.ndarray:
     x = np.asarray(x, dtype=np.float64)
     neg = np.signbit(x)
     a = np.abs(x)
