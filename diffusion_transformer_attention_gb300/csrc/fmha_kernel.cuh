@@ -9,9 +9,10 @@
 //
 // CTA = 2 query tiles of 128 rows of one (batch, query head); 640 threads in 20 warps.
 //   warp 0       TMA producer: Q0, Q1 once, then K_j / V_j into a ring of 4 x 32 KB slots.
-//   warp 1       MMA issuer (one thread): BMM1 S_i = Q_i K_j^T (SS), BMM2 O_i += P_i V_j (TS:
-//                P from tensor memory, V from shared memory, V is MN-major so no transpose).
-//   warp 2       tensor-memory allocator (512 columns: S0 | S1 | O0 | O1).
+//   warps 1, 2   MMA issuers, one per Q tile (one elected lane each): BMM1 S_i = Q_i K_j^T (SS),
+//                BMM2 O_i += P_i V_j (TS: P from tensor memory, V from shared memory, V is MN-major
+//                so no transpose). Warp 2 also allocates the 512 tensor-memory columns
+//                (S0 | S1 | O0 | O1) at the start and frees them at the end.
 //   warp 3       SAGE only: stages the per-column K scales of each KV tile and the V scales.
 //   warps 4-19   four softmax warpgroups: Q tile i = g / 2 and column half h = g % 2 for group g.
 //                A thread owns one row (= TMEM lane) and 64 of its 128 columns; the two halves
@@ -19,8 +20,8 @@
 //                thread halves the softmax latency, which is what bounds the pipeline: each Q
 //                tile's cycle (its MMAs, then its softmax) must fit in the time the tensor cores
 //                spend on both tiles.
-// The MMA issue order is S0(j) S1(j) | O0 += P0(j) V_j, S0(j+1) | O1 += P1(j) V_j, S1(j+1) ...
-// so while the softmax groups of one tile turn S into P, the tensor cores work on the other.
+// Each issuer runs O_i += P_i(j) V_j, S_i(j+1) = Q_i K_{j+1}^T as soon as P_i(j) is ready, so while
+// the softmax groups of one tile turn S into P, the tensor cores work on the other tile.
 // Each half writes its packed P over the first columns of its own half of S (bf16: 32 columns,
 // e4m3: 16), and BMM2 reads the two P pieces at their own addresses.
 //
@@ -73,7 +74,7 @@ struct Bars {
   uint64_t ks_full[kSlots];
   uint64_t ks_empty[kSlots];
   uint64_t vs_full;
-  uint64_t drain;
+  uint64_t drain[2];
   uint32_t tmem_base;
   int abort_flag;
   int skip_flag[2];
@@ -158,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->q_full, 1);
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->kv_empty[s], 2);  // one commit from each MMA issuer
       mbar_init(&bars->ks_full[s], 32);
       mbar_init(&bars->ks_empty[s], 16);  // one arrival per softmax warp
     }
@@ -168,7 +169,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->o_full[i], 1);
     }
     mbar_init(&bars->vs_full, 32);
-    mbar_init(&bars->drain, 1);
+    mbar_init(&bars->drain[0], 1);
+    mbar_init(&bars->drain[1], 1);
     bars->abort_flag = 0;
     bars->skip_flag[0] = bars->skip_flag[1] = 0;
     fence_mbar_init();
@@ -232,77 +234,69 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (issued[s] > 0) mbar_wait_bounded(&bars->kv_full[s], (issued[s] - 1) & 1, budget, nullptr);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // The whole warp runs this loop in uniform control flow (so descriptors stay in uniform
-    // registers); one elected lane issues the tcgen05 instructions.
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers, one warp per Q tile
+    // Each issuer reacts only to its own tile's barriers, so one tile's P never waits while the
+    // other tile's MMAs are being pushed into the (shallow) tensor-core queue. The whole warp runs
+    // the loop in uniform control flow; one elected lane issues the tcgen05 instructions.
+    const int i = warp - 1;
     const uint32_t leader = elect_one();
     bool ok = mbar_wait_bounded(&bars->q_full, 0, budget, abort_flag);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok && leader) record_timeout(p, bars);
     tc_fence_after();
     const uint32_t sbase = smem_u32(smem);
-    const uint64_t dq0 = make_sdesc_sw128(sbase, 16, 1024);
+    const uint64_t aq = make_sdesc_sw128(sbase + i * 32768, 16, 1024);
     const uint64_t dk0 = make_sdesc_sw128(sbase + kRingOff, 16, 1024);
     const uint64_t dv0 = make_sdesc_sw128(sbase + kRingOff, kPVBytes == 2 ? 16384 : 8192, 1024);
+    const uint32_t d_s = tbase + 128 * i;
+    const uint32_t d_o = tbase + 256 + 128 * i;
     volatile int* skip_flag = bars->skip_flag;
     for (int j = 0; j <= nt && ok; ++j) {
       const int tk = 2 * j, tv = 2 * j - 1;
       if (j < nt) {
         ok = mbar_wait_bounded(&bars->kv_full[tk & 3], (tk >> 2) & 1, budget, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        tc_fence_after();
       }
       if (j >= 1) {
         ok = mbar_wait_bounded(&bars->kv_full[tv & 3], (tv >> 2) & 1, budget, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        tc_fence_after();
+        ok = mbar_wait_bounded(&bars->p_full[i], (j - 1) & 1, budget, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       }
+      tc_fence_after();
       // descriptor start addresses advance in 16-byte units inside the low 14 bits
       const uint64_t bk = dk0 + (uint64_t)(((tk & 3) * kSlotBytes) >> 4);
       const uint64_t bv = dv0 + (uint64_t)(((tv & 3) * kSlotBytes) >> 4);
-#pragma unroll 1
-      for (int i = 0; i < 2; ++i) {
-        if (j >= 1) {
-          ok = mbar_wait_bounded(&bars->p_full[i], (j - 1) & 1, budget, abort_flag);
-          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-          tc_fence_after();
-          if (!SKIP || skip_flag[i] == 0) {
-            const uint32_t d = tbase + 256 + 128 * i;
-            const uint32_t a = tbase + 128 * i;
+      if (j >= 1 && (!SKIP || skip_flag[i] == 0)) {
 #pragma unroll
-            for (int kk = 0; kk < kK2Steps; ++kk) {
-              const uint32_t off = (kPVBytes == 2) ? kk * 2048 : kk * 4096;
-              // K columns 0..63 come from the P piece in S columns 0.., 64..127 from S columns 64..
-              const uint32_t pa = a + ((kk < kK2Steps / 2) ? 8 * kk : 64 + 8 * (kk - kK2Steps / 2));
-              mma_ts_if<kMma2Kind>(leader, d, pa, bv + (off >> 4), kIdesc2, (j > 1 || kk > 0) ? 1u : 0u);
-            }
-          }
-        }
-        if (j < nt) {
-          const uint64_t aq = dq0 + (uint64_t)((i * 32768) >> 4);
-          const uint32_t d = tbase + 128 * i;
-#pragma unroll
-          for (int kk = 0; kk < kK1Steps; ++kk) {
-            const uint32_t off = (kQKBytes == 2) ? (kk >> 2) * 16384 + (kk & 3) * 32 : kk * 32;
-            mma_ss_if<kMma1Kind>(leader, d, aq + (off >> 4), bk + (off >> 4), kIdesc1, kk > 0 ? 1u : 0u);
-          }
-          mma_commit_if(leader, &bars->s_full[i]);
+        for (int kk = 0; kk < kK2Steps; ++kk) {
+          const uint32_t off = (kPVBytes == 2) ? kk * 2048 : kk * 4096;
+          // K columns 0..63 come from the P piece in S columns 0.., 64..127 from S columns 64..
+          const uint32_t pa = d_s + ((kk < kK2Steps / 2) ? 8 * kk : 64 + 8 * (kk - kK2Steps / 2));
+          mma_ts_if<kMma2Kind>(leader, d_o, pa, bv + (off >> 4), kIdesc2, (j > 1 || kk > 0) ? 1u : 0u);
         }
       }
-      if (!ok) break;
+      if (j < nt) {
+#pragma unroll
+        for (int kk = 0; kk < kK1Steps; ++kk) {
+          const uint32_t off = (kQKBytes == 2) ? (kk >> 2) * 16384 + (kk & 3) * 32 : kk * 32;
+          mma_ss_if<kMma1Kind>(leader, d_s, aq + (off >> 4), bk + (off >> 4), kIdesc1, kk > 0 ? 1u : 0u);
+        }
+        mma_commit_if(leader, &bars->s_full[i]);
+      }
+      // a K/V slot is free once both issuers have committed their last use of it
       if (j >= 1) mma_commit_if(leader, &bars->kv_empty[tv & 3]);
       if (j < nt) mma_commit_if(leader, &bars->kv_empty[tk & 3]);
     }
     if (ok) {
-      mma_commit_if(leader, &bars->o_full[0]);
-      mma_commit_if(leader, &bars->o_full[1]);
+      mma_commit_if(leader, &bars->o_full[i]);
     } else if (leader) {
       record_timeout(p, bars);
     }
-    // drain: no MMA may still be running when tensor memory is freed
-    mma_commit_if(leader, &bars->drain);
-    mbar_wait_bounded(&bars->drain, 0, budget, nullptr);
+    // drain: no MMA of this issuer may still be running when tensor memory is freed
+    mma_commit_if(leader, &bars->drain[i]);
+    mbar_wait_bounded(&bars->drain[i], 0, budget, nullptr);
     __syncwarp();
   } else if (warp == 3) {
     // ------------------------------------------------------------ SAGE scale stager
@@ -320,10 +314,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) record_timeout(p, bars);
           break;
         }
+        // one value per K block of the tile (128 / k_block of them); 0 past the end of K
+        const int nb = 128 / p.k_block;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const int col = 128 * j + lane * 4 + q;
-          s_ks[e * 128 + lane * 4 + q] = (col < p.Skv) ? __ldg(ks + col / p.k_block) : 0.0f;
+          const int g = lane * 4 + q;
+          const int col = 128 * j + g * p.k_block;
+          if (g < nb) s_ks[e * 128 + g] = (col < p.Skv) ? __ldg(ks + col / p.k_block) : 0.0f;
         }
         mbar_arrive(&bars->ks_full[e]);
       }
@@ -362,9 +359,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok && lane == 0) record_timeout(p, bars);
       }
       if (!ok) {
-        // keep this tile's named barriers in step with the peer half
-        named_bar_sync(tile_bar, 256);
-        if (SKIP && j > 0) named_bar_and(tile_bar, 256, true);
+        // keep this tile's named barrier in step with the peer half
+        if (SKIP && j > 0) {
+          named_bar_and(tile_bar, 256, true);
+        } else {
+          named_bar_sync(tile_bar, 256);
+        }
         continue;
       }
       tc_fence_after();
@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) record_timeout(p, bars);
           ok = false;
         }
-        const float* ks = s_ks + e * 128 + 64 * h;
+        const float* ks = s_ks + e * 128 + (64 / KB) * h;  // this half's block scales
         if constexpr (KB == 1) {
           const float2* ks2 = reinterpret_cast<const float2*>(ks);
 #pragma unroll
@@ -402,11 +402,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           mh = rowmax64(s) * c;
         } else {
           mh = -INFINITY;
+          const float4* ks4 = reinterpret_cast<const float4*>(ks);
 #pragma unroll
-          for (int q = 0; q < kGroups; ++q) {
-            wg[q] = ks[q * KB] * c;
-            mh = fmaxf(mh, groupmax<KB>(s + q * KB) * wg[q]);  // a NaN from -inf * 0 is ignored
+          for (int q4 = 0; q4 < kGroups / 4; ++q4) {
+            const float4 k4 = ks4[q4];
+            wg[4 * q4 + 0] = k4.x * c;
+            wg[4 * q4 + 1] = k4.y * c;
+            wg[4 * q4 + 2] = k4.z * c;
+            wg[4 * q4 + 3] = k4.w * c;
           }
+#pragma unroll
+          for (int q = 0; q < kGroups; ++q)
+            mh = fmaxf(mh, groupmax<KB>(s + q * KB) * wg[q]);  // a NaN from -inf * 0 is ignored
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->ks_empty[e]);
@@ -414,24 +421,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         wg[0] = c;
         mh = rowmax64(s) * c;  // -inf when this half has no valid column
       }
-      // full-row max from the two halves (identical on both sides: max is exact)
+      // Publish this half's max; one barrier over both halves of the tile then orders the exchange
+      // and, with Skip-Softmax, carries the vote. A row's full max is below the threshold exactly
+      // when both halves' maxima are, so each half votes on its own max.
       xmax[((i * 2 + h) * 2 + (j & 1)) * 128 + r] = mh;
-      named_bar_sync(tile_bar, 256);
-      const float mo = xmax[((i * 2 + (h ^ 1)) * 2 + (j & 1)) * 128 + r];
-      const float mt = fmaxf(mh, mo);
-      if constexpr (SKIP) {
-        if (j > 0) {
-          const bool vote = !row_valid || !ok || (mt - m_ex < p.log2_thr);
-          if (named_bar_and(tile_bar, 256, vote)) {
-            ++nskip;
-            if (r == 0 && h == 0) skip_flag[i] = 1;
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->p_full[i]);
-            continue;
-          }
-        }
+      bool skip_tile = false;
+      if (SKIP && j > 0) {
+        const bool vote = !row_valid || !ok || (mh - m_ex < p.log2_thr);
+        skip_tile = named_bar_and(tile_bar, 256, vote);
+      } else {
+        named_bar_sync(tile_bar, 256);
       }
+      if (skip_tile) {
+        ++nskip;
+        if (r == 0 && h == 0) skip_flag[i] = 1;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->p_full[i]);
+        continue;
+      }
+      const float mo = xmax[((i * 2 + (h ^ 1)) * 2 + (j & 1)) * 128 + r];
+      const float mt = fmaxf(mh, mo);  // identical on both halves: max is exact
       if (!ok) continue;
       const float m_new = fmaxf(m_ex, mt);
       bool need;
@@ -517,7 +527,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok && lane == 0) record_timeout(p, bars);
     }
-    uint8_t* stage = smem + kRingOff + i * kSlotBytes + h * 16384;  // the KV ring is idle once O is final
+    // Stage O in this tile's own Q buffer (32 KB reserved per tile): only this tile's issuer reads
+    // it, and all of that issuer's MMAs are complete once O is final. (The K/V ring may still be
+    // read by the other tile's issuer.)
+    uint8_t* stage = smem + i * 32768 + h * 16384;
     if (ok) {
       tc_fence_after();
       const float inv_l = 1.0f / l_row;
