@@ -188,6 +188,28 @@ def oracle_sample(w: workloads.Workload, budget_s: float = 15.0, max_tiles: int 
     return flop / dt / 1e12, dt / max(tiles, 1), tiles, threads, desc
 
 
+def dense_kernel_traffic():
+    """DRAM bytes per launch of the dense attention kernel from the committed ncu summary, or None
+    when the kernel sources changed since those counters were taken."""
+    import hashlib
+    import re
+    path = os.path.join(ROOT, "profiles", "fmha_dense_bf16_dit32k_traffic.md")
+    csrc = os.path.join(ROOT, "diffusion_transformer_attention_gb300", "csrc")
+    try:
+        text = open(path).read()
+        h = hashlib.sha256()
+        for name in ("fmha_kernel.cuh", "fmha_dense.cu", "sm103_ptx.cuh"):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+    except OSError:
+        return None
+    m = re.search(r"first 16 hex\): ([0-9a-f]{16})", text)
+    t = re.search(r"traffic_bytes_per_launch: (\d+)", text)
+    if not m or not t or m.group(1) != h.hexdigest()[:16]:
+        return None
+    return int(t.group(1))
+
+
 # ------------------------------------------------------------------ timing helpers
 def time_steps(fn, steps, warmup, world, stream):
     for _ in range(warmup):
@@ -343,11 +365,7 @@ def main():
     if not args.no_cpu_baseline:
         tf, _, tiles, threads, desc = oracle_sample(w)
         cpu = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc}
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", "fmha_dense_bf16_dit32k.json")
-    if os.path.exists(prof):
-        with open(prof) as f:
-            traffic = json.load(f).get("dram_bytes_per_launch")
+    traffic = dense_kernel_traffic()
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": warmup, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
