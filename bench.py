@@ -138,12 +138,21 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The largest of the ranks' values (the slowest rank's time); x itself on one rank."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cpu" if dist.get_backend() == "gloo" else "cuda"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate_value(flop_per_step: float, steps: int, elapsed_ms: float, world: int) -> float:
+    """Whole-job TFLOP/s: every rank ran `steps` steps of the same workload (weak scaling), and the
+    job took as long as its slowest rank."""
+    tmax = max_over_ranks(elapsed_ms, world)
+    return world * flop_per_step * steps / (tmax * 1e-3) / 1e12
 
 
 # ------------------------------------------------------------------ CPU oracle sample
@@ -331,9 +340,8 @@ def main():
         elapsed = time_steps(step, args.steps, warmup, world, stream)
     clocks = clk.summary()
     dit.dit_attn_check_errors(stream)
-    tmax = max_over_ranks(elapsed, world)
-    ms = tmax / args.steps
-    value = world * flop * args.steps / (tmax * 1e-3) / 1e12
+    value = aggregate_value(flop, args.steps, elapsed, world)
+    ms = world * flop / (value * 1e12) * 1e3  # the slowest rank's time per step
     kernel_tflops = flop / (elapsed / args.steps * 1e-3) / 1e12  # this rank's launch average
 
     # end to end through the public API with pinned host buffers
