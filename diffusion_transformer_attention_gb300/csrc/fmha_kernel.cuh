@@ -8,22 +8,22 @@
 // threshold = factor / seqlen). The pages give no kernel design; this one is built for GB300:
 //
 // CTA = 2 query tiles of 128 rows of one (batch, query head); 640 threads in 20 warps.
-//   warp 0       TMA producer: Q0, Q1 once, then K_j / V_j into a ring of 4 x 32 KB slots.
+//   warp 0       TMA producer: Q0, Q1 once, then K_j / V_j into two K and two V buffers.
 //   warps 1, 2   MMA issuers, one per Q tile (one elected lane each): BMM1 S_i = Q_i K_j^T (SS),
-//                BMM2 O_i += P_i V_j (TS: P from tensor memory, V from shared memory, V is MN-major
-//                so no transpose). Warp 2 also allocates the 512 tensor-memory columns
-//                (S0 | S1 | O0 | O1) at the start and frees them at the end.
+//                BMM2 O_i += P_i V_j (V is MN-major, so no transpose). Warp 2 also allocates the 512
+//                tensor-memory columns (S0 | S1 | O0 | O1) at the start and frees them at the end.
 //   warp 3       SAGE only: stages the per-column K scales of each KV tile and the V scales.
 //   warps 4-19   four softmax warpgroups: Q tile i = g / 2 and column half h = g % 2 for group g.
 //                A thread owns one row (= TMEM lane) and 64 of its 128 columns; the two halves
 //                of a row exchange partial maxima through shared memory. Halving the columns per
-//                thread halves the softmax latency, which is what bounds the pipeline: each Q
-//                tile's cycle (its MMAs, then its softmax) must fit in the time the tensor cores
-//                spend on both tiles.
-// Each issuer runs O_i += P_i(j) V_j, S_i(j+1) = Q_i K_{j+1}^T as soon as P_i(j) is ready, so while
-// the softmax groups of one tile turn S into P, the tensor cores work on the other tile.
-// Each half writes its packed P over the first columns of its own half of S (bf16: 32 columns,
-// e4m3: 16), and BMM2 reads the two P pieces at their own addresses.
+//                thread halves the softmax latency, which is what bounds the pipeline.
+// Dense (BF16 P): each half writes its packed P over the first columns of its own half of S, and
+// BMM2 reads P from tensor memory (TS). The issuer runs O_i += P_i(j-1) V_{j-1}, S_i = Q_i K_j^T as
+// soon as P_i(j-1) is ready, so while one tile's softmax turns S into P, the tensor cores work on
+// the other tile.
+// SAGE (E4M3 P, 16 KB per tile): P goes to a shared-memory buffer and BMM2 is an SS MMA. S is free
+// as soon as the softmax has loaded it, so the issuer computes S_i(j+1) while the softmax works on
+// S_i(j); a per-tile barrier (o_done) returns P's buffer and O to the softmax after each BMM2.
 //
 // Numerics: logits are kept in log2 units (scaled by softmax_scale * log2 e). Dense mode rescales
 // O lazily (only when the running max grows by more than 8, P then stays below 2^8); SAGE rescales
@@ -52,16 +52,28 @@ constexpr int kThreads = 640;
 constexpr int kLaunchRegs = 96;                  // 65536 / 640, rounded down to a multiple of 8
 constexpr int kRegsWG0 = 64, kRegsSoftmax = 104;  // 128 * 64 + 512 * 104 == 640 * 96
 static_assert(128 * kRegsWG0 + 512 * kRegsSoftmax <= kThreads * kLaunchRegs, "register hand-over must fit");
-constexpr int kSlots = 4;
-constexpr uint32_t kSlotBytes = 32768;
-constexpr uint32_t kQRegionBytes = 2 * 32768;
-constexpr uint32_t kRingOff = kQRegionBytes;
-constexpr uint32_t kKsOff = kRingOff + kSlots * kSlotBytes;  // 4 x 128 floats
-constexpr uint32_t kVsOff = kKsOff + kSlots * 512;           // 128 floats
-constexpr uint32_t kXmaxOff = kVsOff + 512;                  // [tile][half][parity][128] partial maxima
-constexpr uint32_t kXlOff = kXmaxOff + 2 * 2 * 2 * 512;      // [tile][half][128] partial row sums
-constexpr uint32_t kBarOff = kXlOff + 2 * 2 * 512;
-constexpr uint32_t kSmemBytes = kBarOff + 512 + 1024;        // + alignment slack
+constexpr int kSlots = 4;  // ring of K/V tiles: K_j in slot 2j mod 4, V_j in slot 2j+1 mod 4
+
+// Shared-memory layout for operand formats QKF / PVF. Two Q buffers of 32 KB (also the output
+// staging), two K buffers and two V buffers sized to their tiles, and in SAGE mode two 16 KB
+// buffers for the E4M3 P of the two query tiles, which BMM2 reads from shared memory.
+template <int QKF, int PVF>
+struct SmemLayout {
+  static constexpr uint32_t kKTile = 128u * 128u * (QKF == QK_E4M3 ? 1u : 2u);
+  static constexpr uint32_t kVTile = 128u * 128u * (PVF == PV_E4M3 ? 1u : 2u);
+  static constexpr bool kPInSmem = (PVF == PV_E4M3);
+  static constexpr uint32_t kQOff = 0;
+  static constexpr uint32_t kKOff = 2 * 32768;
+  static constexpr uint32_t kVOff = kKOff + 2 * kKTile;
+  static constexpr uint32_t kPOff = kVOff + 2 * kVTile;
+  static constexpr uint32_t kKsOff = kPOff + (kPInSmem ? 2 * 16384 : 0);  // 4 x 128 floats
+  static constexpr uint32_t kVsOff = kKsOff + kSlots * 512;                // 128 floats
+  static constexpr uint32_t kXmaxOff = kVsOff + 512;        // [tile][half][parity][128] partial maxima
+  static constexpr uint32_t kXlOff = kXmaxOff + 2 * 2 * 2 * 512;  // [tile][half][128] partial row sums
+  static constexpr uint32_t kBarOff = kXlOff + 2 * 2 * 512;
+  static constexpr uint32_t kSmemBytes = kBarOff + 512 + 1024;     // + alignment slack
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
 constexpr float kLazyRescale = 8.0f;                         // log2 units
 constexpr float kLog2_448 = 8.807354922057604f;
 
@@ -76,6 +88,8 @@ struct Bars {
   uint64_t ks_empty[kSlots];
   uint64_t vs_full;
   uint64_t drain[2];
+  uint64_t s_free[2];   // SAGE: the tile's softmax has loaded S (BMM1 of the next KV tile may overwrite it)
+  uint64_t o_done[2];   // SAGE: BMM2 of the tile's latest KV tile is complete (P buffer free, O stable)
   uint32_t tmem_base;
   int abort_flag;
   int skip_flag[2];
@@ -107,11 +121,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                  : make_idesc(0, 0, 0, 0, 128, 128);
   constexpr uint32_t kIdesc2 = (PVF == PV_BF16) ? make_idesc(1, 1, 0, 1, 128, 128) : make_idesc(0, 0, 0, 1, 128, 128);
 
+  using L = SmemLayout<QKF, PVF>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Bars* bars = reinterpret_cast<Bars*>(smem + kBarOff);
-  float* s_ks = reinterpret_cast<float*>(smem + kKsOff);
-  float* s_vs = reinterpret_cast<float*>(smem + kVsOff);
+  Bars* bars = reinterpret_cast<Bars*>(smem + L::kBarOff);
+  float* s_ks = reinterpret_cast<float*>(smem + L::kKsOff);
+  float* s_vs = reinterpret_cast<float*>(smem + L::kVsOff);
   const volatile int* abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -141,6 +156,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->vs_full, 32);
     mbar_init(&bars->drain[0], 1);
     mbar_init(&bars->drain[1], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->s_free[i], 8);  // one arrival per softmax warp of the tile
+      mbar_init(&bars->o_done[i], 1);
+    }
     bars->abort_flag = 0;
     bars->skip_flag[0] = bars->skip_flag[1] = 0;
     fence_mbar_init();
@@ -167,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       mbar_arrive_expect_tx(&bars->q_full, 2 * kQTileBytes);
       for (int i = 0; i < 2; ++i) {
-        uint8_t* dst = smem + i * 32768;
+        uint8_t* dst = smem + L::kQOff + i * 32768;
         if (kQKBytes == 2) {
           tma_load_4d(dst, &tm_q, &bars->q_full, 0, q0 + 128 * i, hq, b, pol_q);
           tma_load_4d(dst + 16384, &tm_q, &bars->q_full, 64, q0 + 128 * i, hq, b, pol_q);
@@ -183,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          uint8_t* dst = smem + kRingOff + s * kSlotBytes;
+          uint8_t* dst = smem + (kv ? L::kVOff + (s >> 1) * L::kVTile : L::kKOff + (s >> 1) * L::kKTile);
           const CUtensorMap* map = kv ? &tm_v : &tm_k;
           const int bytes = kv ? kVTileBytes : kQTileBytes;
           const int eb = kv ? kPVBytes : kQKBytes;
@@ -216,48 +235,87 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok && leader) record_timeout(p, bars);
     tc_fence_after();
     const uint32_t sbase = smem_u32(smem);
-    const uint64_t aq = make_sdesc_sw128(sbase + i * 32768, 16, 1024);
-    const uint64_t dk0 = make_sdesc_sw128(sbase + kRingOff, 16, 1024);
-    const uint64_t dv0 = make_sdesc_sw128(sbase + kRingOff, kPVBytes == 2 ? 16384 : 8192, 1024);
+    const uint64_t aq = make_sdesc_sw128(sbase + L::kQOff + i * 32768, 16, 1024);
+    const uint64_t dk0 = make_sdesc_sw128(sbase + L::kKOff, 16, 1024);
+    const uint64_t dv0 = make_sdesc_sw128(sbase + L::kVOff, kPVBytes == 2 ? 16384 : 8192, 1024);
     const uint32_t d_s = tbase + 128 * i;
     const uint32_t d_o = tbase + 256 + 128 * i;
     volatile int* skip_flag = bars->skip_flag;
-    for (int j = 0; j <= nt && ok; ++j) {
-      const int tk = 2 * j, tv = 2 * j - 1;
-      if (j < nt) {
-        ok = mbar_wait_bounded(&bars->kv_full[tk & 3], (tk >> 2) & 1, budget, abort_flag);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      }
-      if (j >= 1) {
-        ok = mbar_wait_bounded(&bars->kv_full[tv & 3], (tv >> 2) & 1, budget, abort_flag);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        ok = mbar_wait_bounded(&bars->p_full[i], (j - 1) & 1, budget, abort_flag);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      }
-      tc_fence_after();
-      // descriptor start addresses advance in 16-byte units inside the low 14 bits
-      const uint64_t bk = dk0 + (uint64_t)(((tk & 3) * kSlotBytes) >> 4);
-      const uint64_t bv = dv0 + (uint64_t)(((tv & 3) * kSlotBytes) >> 4);
-      if (j >= 1 && (!SKIP || skip_flag[i] == 0)) {
+    auto wait = [&](uint64_t* bar, int parity) {
+      return __all_sync(0xffffffffu, mbar_wait_bounded(bar, (uint32_t)parity, budget, abort_flag));
+    };
+    // K_j sits in K buffer j % 2 and V_j in V buffer j % 2 (ring slots 2j and 2j + 1 mod 4); the
+    // descriptor start address advances in 16-byte units inside its low 14 bits.
+    auto bmm1 = [&](int j) {  // S_i = Q_i K_j^T, then release K_j's slot
+      const uint64_t bk = dk0 + (uint64_t)(((j & 1) * L::kKTile) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kK2Steps; ++kk) {
-          const uint32_t off = (kPVBytes == 2) ? kk * 2048 : kk * 4096;
-          // K columns 0..63 come from the P piece in S columns 0.., 64..127 from S columns 64..
-          const uint32_t pa = d_s + ((kk < kK2Steps / 2) ? 8 * kk : 64 + 8 * (kk - kK2Steps / 2));
-          mma_ts_if<kMma2Kind>(leader, d_o, pa, bv + (off >> 4), kIdesc2, (j > 1 || kk > 0) ? 1u : 0u);
-        }
+      for (int kk = 0; kk < kK1Steps; ++kk) {
+        const uint32_t off = (kQKBytes == 2) ? (kk >> 2) * 16384 + (kk & 3) * 32 : kk * 32;
+        mma_ss_if<kMma1Kind>(leader, d_s, aq + (off >> 4), bk + (off >> 4), kIdesc1, kk > 0 ? 1u : 0u);
       }
-      if (j < nt) {
+      mma_commit_if(leader, &bars->s_full[i]);
+      mma_commit_if(leader, &bars->kv_empty[(2 * j) & 3]);
+    };
+    if constexpr (L::kPInSmem) {
+      // E4M3 P in shared memory: BMM1 of the next KV tile overwrites S as soon as the softmax has
+      // loaded it, so each tile's S(j+1) is computed while its softmax turns S(j) into P(j).
+      // BMM2 is an SS MMA (P K-major, V MN-major); o_done tells the softmax when P's buffer and O
+      // are free again.
+      const uint64_t ap = make_sdesc_sw128(sbase + L::kPOff + i * 16384, 16, 1024);
+      if (ok) ok = wait(&bars->kv_full[0], 0);
+      if (ok) {
+        tc_fence_after();
+        bmm1(0);
+      }
+      for (int j = 0; j < nt && ok; ++j) {
+        if (j + 1 < nt) {
+          const int tk = 2 * (j + 1);
+          ok = wait(&bars->s_free[i], j & 1) && wait(&bars->kv_full[tk & 3], (tk >> 2) & 1);
+          if (!ok) break;
+          tc_fence_after();
+          bmm1(j + 1);
+        }
+        const int tv = 2 * j + 1;
+        ok = wait(&bars->kv_full[tv & 3], (tv >> 2) & 1) && wait(&bars->p_full[i], j & 1);
+        if (!ok) break;
+        tc_fence_after();
+        if (!SKIP || skip_flag[i] == 0) {
+          const uint64_t bv = dv0 + (uint64_t)(((j & 1) * L::kVTile) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kK1Steps; ++kk) {
-          const uint32_t off = (kQKBytes == 2) ? (kk >> 2) * 16384 + (kk & 3) * 32 : kk * 32;
-          mma_ss_if<kMma1Kind>(leader, d_s, aq + (off >> 4), bk + (off >> 4), kIdesc1, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < kK2Steps; ++kk)
+            mma_ss_if<kMma2Kind>(leader, d_o, ap + (uint64_t)((kk * 32) >> 4), bv + (uint64_t)((kk * 4096) >> 4),
+                                 kIdesc2, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit_if(leader, &bars->s_full[i]);
+        mma_commit_if(leader, &bars->o_done[i]);
+        mma_commit_if(leader, &bars->kv_empty[tv & 3]);
       }
-      // a K/V slot is free once both issuers have committed their last use of it
-      if (j >= 1) mma_commit_if(leader, &bars->kv_empty[tv & 3]);
-      if (j < nt) mma_commit_if(leader, &bars->kv_empty[tk & 3]);
+    } else {
+      // P in tensor memory over S: O_i += P_i(j-1) V_{j-1} then S_i = Q_i K_j^T, once P_i(j-1) is ready.
+      for (int j = 0; j <= nt && ok; ++j) {
+        const int tk = 2 * j, tv = 2 * j - 1;
+        if (j < nt) {
+          ok = wait(&bars->kv_full[tk & 3], (tk >> 2) & 1);
+          if (!ok) break;
+        }
+        if (j >= 1) {
+          ok = wait(&bars->kv_full[tv & 3], (tv >> 2) & 1) && wait(&bars->p_full[i], (j - 1) & 1);
+          if (!ok) break;
+        }
+        tc_fence_after();
+        if (j >= 1 && (!SKIP || skip_flag[i] == 0)) {
+          const uint64_t bv = dv0 + (uint64_t)((((j - 1) & 1) * L::kVTile) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < kK2Steps; ++kk) {
+            const uint32_t off = (kPVBytes == 2) ? kk * 2048 : kk * 4096;
+            // K columns 0..63 come from the P piece in S columns 0.., 64..127 from S columns 64..
+            const uint32_t pa = d_s + ((kk < kK2Steps / 2) ? 8 * kk : 64 + 8 * (kk - kK2Steps / 2));
+            mma_ts_if<kMma2Kind>(leader, d_o, pa, bv + (off >> 4), kIdesc2, (j > 1 || kk > 0) ? 1u : 0u);
+          }
+        }
+        // a K/V slot is free once both issuers have committed their last use of it
+        if (j >= 1) mma_commit_if(leader, &bars->kv_empty[tv & 3]);
+        if (j < nt) bmm1(j);
+      }
     }
     if (ok) {
       mma_commit_if(leader, &bars->o_full[i]);
@@ -310,8 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool row_valid = qrow < p.Sq;
     const uint32_t tile_bar = 1 + i;               // the 256 threads of this Q tile
     const uint32_t group_bar = 3 + g;              // the 128 threads of this warpgroup
-    float* xmax = reinterpret_cast<float*>(smem + kXmaxOff);
-    float* xl = reinterpret_cast<float*>(smem + kXlOff);
+    float* xmax = reinterpret_cast<float*>(smem + L::kXmaxOff);
+    float* xl = reinterpret_cast<float*>(smem + L::kXlOff);
     float c = p.c_scale;
     if constexpr (kSage) {
       const float qs = row_valid ? __ldg(p.q_scale + ((size_t)b * p.Hq + hq) * p.nqb + qrow / p.q_block) : 0.0f;
@@ -343,6 +401,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(t_s, s);
       tmem_ld32(t_s + 32, s + 32);
       tmem_ld_wait();
+      if constexpr (L::kPInSmem) {
+        // S is in registers: the issuer may compute the next tile's S into the same columns
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->s_free[i]);
+      }
       const int nvalid = min(64, p.Skv - 128 * j - 64 * h);  // may be <= 0 for the upper half
       const bool tail = nvalid < 64;
       if (tail) {
@@ -402,6 +466,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         named_bar_sync(tile_bar, 256);
       }
+      if constexpr (L::kPInSmem) {
+        // BMM2 of the previous KV tile must be complete before P's buffer, O or the skip flag
+        // (which that BMM2's issue read) change. Waiting on every tile keeps the waits in step with
+        // the barrier's phases.
+        if (j > 0 && ok) {
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->o_done[i], (j - 1) & 1, budget, abort_flag));
+          if (!ok && lane == 0) record_timeout(p, bars);
+        }
+        if (!ok) continue;
+      }
       if (skip_tile) {
         ++nskip;
         if (r == 0 && h == 0) skip_flag[i] = 1;
@@ -451,18 +525,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int k = 0; k < 32; ++k) acc[k & 3] = __fadd2_rn(acc[k & 3], s2[k]);
       l += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
-      // P over the first columns of this half of S
       if constexpr (PVF == PV_BF16) {
+        // P over the first columns of this half of S
         uint32_t w[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) w[k] = pack_bf16x2(s[2 * k], s[2 * k + 1]);
         tmem_st32(t_s, w);
       } else {
+        // E4M3 P into the tile's shared-memory buffer, laid out as a K-major operand with the
+        // 128-byte swizzle: row r's 16-byte chunk ch sits at (r/8)*1024 + (r%8)*128 + (ch ^ r%8)*16.
+        // This half holds chunks 4h .. 4h+3 (columns 64h .. 64h+63).
         uint32_t w[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k)
-          w[k] = pack_e4m3x2(s[4 * k], s[4 * k + 1]) | (pack_e4m3x2(s[4 * k + 2], s[4 * k + 3]) << 16);
-        tmem_st16(t_s, w);
+          w[k] = pack_e4m3x4(s[4 * k], s[4 * k + 1], s[4 * k + 2], s[4 * k + 3]);
+        uint8_t* prow = smem + L::kPOff + i * 16384 + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int ch = 4 * h + q;
+          *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) =
+              make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+        }
+        fence_proxy_async_smem();  // visible to the tensor cores' reads
       }
       // O rescale for this half (after P, when the scores are no longer held in registers; still
       // before the arrive that lets the MMA accumulate into O)
@@ -500,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Stage O in this tile's own Q buffer (32 KB reserved per tile): only this tile's issuer reads
     // it, and all of that issuer's MMAs are complete once O is final. (The K/V ring may still be
     // read by the other tile's issuer.)
-    uint8_t* stage = smem + i * 32768 + h * 16384;
+    uint8_t* stage = smem + L::kQOff + i * 32768 + h * 16384;
     if (ok) {
       tc_fence_after();
       const float inv_l = 1.0f / l_row;
@@ -566,12 +650,12 @@ cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
     if (e != cudaSuccess) return e;
     if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidKernelImage;
     e = cudaFuncSetAttribute(fmha_fwd_kernel<QKF, PVF, KB, SKIP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes);
+                             (int)SmemLayout<QKF, PVF>::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   const dim3 grid((p.Sq + 255) / 256, p.Hq, p.B);
-  fmha_fwd_kernel<QKF, PVF, KB, SKIP><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, to, p);
+  fmha_fwd_kernel<QKF, PVF, KB, SKIP><<<grid, kThreads, SmemLayout<QKF, PVF>::kSmemBytes, stream>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 

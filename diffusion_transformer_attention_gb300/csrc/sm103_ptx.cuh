@@ -44,18 +44,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// One try_wait that may suspend the thread (instead of spinning) for up to `hint_ns` nanoseconds
+// while the phase is incomplete; the thread resumes as soon as the phase completes.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait until the phase with the given parity has completed. Gives up after `budget_ns`
 // nanoseconds of wall time or when *abort becomes non-zero; returns false in both cases.
+// The thread sleeps inside try_wait between checks, so a waiting warp takes almost no issue
+// slots from the warps doing the work.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t budget_ns,
                                                   const volatile int* abort) {
+  constexpr uint32_t kSuspendNs = 500000;
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0u) {
-      if (abort != nullptr && *abort != 0) return false;
-      if (globaltimer_ns() - t0 > budget_ns) return false;
-    }
+  for (;;) {
+    if (mbar_try_wait_suspend(bar, parity, kSuspendNs)) return true;
+    if (abort != nullptr && *abort != 0) return false;
+    if (globaltimer_ns() - t0 > budget_ns) return false;
   }
 }
 
@@ -323,11 +336,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
-// Pack two f32 into e4m3x2 (round to nearest even, saturate to +-448); `lo` lands in bits 0..7.
-__device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return (uint32_t)r;
+// Pack four f32 into four e4m3 bytes (round to nearest even, saturate to +-448); a lands in bits
+// 0..7, b in 8..15, c in 16..23, d in 24..31.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  uint32_t r;
+  asm("{\n .reg .b16 lo, hi;\n cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n"
+      " mov.b32 %0, {lo, hi};\n}\n"
+      : "=r"(r)
+      : "f"(a), "f"(b), "f"(c), "f"(d));
+  return r;
 }
 
 }  // namespace ditattn
