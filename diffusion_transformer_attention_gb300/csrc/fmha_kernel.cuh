@@ -335,6 +335,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int e = 0; e < 4; ++e) s_vs[lane * 4 + e] = vs[lane * 4 + e];
       mbar_arrive(&bars->vs_full);
       const float* ks = p.k_scale + ((size_t)b * p.Hkv + hkv) * p.nkb;
+      // A tile's 128 / KB block scales, four slots per lane (0 for slots past them and past the
+      // end of K). The loads run kAhead tiles ahead of the ring, so their latency stays off the
+      // softmax's path even when most tiles are skipped and the ring turns over quickly.
+      auto load_tile = [&](int j, float* v) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int g = lane * 4 + q;
+          const int col = 128 * j + g * KB;
+          v[q] = (j < nt && g < 128 / KB && col < p.Skv) ? __ldg(ks + col / KB) : 0.0f;
+        }
+      };
+      constexpr int kAhead = 4;
+      float pre[kAhead][4];
+#pragma unroll
+      for (int d = 0; d < kAhead; ++d) load_tile(d, pre[d]);
       for (int j = 0; j < nt; ++j) {
         const int e = j & 3, u = j >> 2;
         ok = mbar_wait_bounded(&bars->ks_empty[e], (u & 1) ^ 1, budget, abort_flag);
@@ -342,15 +357,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) record_timeout(p, bars);
           break;
         }
-        // one value per K block of the tile (128 / k_block of them); 0 past the end of K
-        const int nb = 128 / p.k_block;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int g = lane * 4 + q;
-          const int col = 128 * j + g * p.k_block;
-          if (g < nb) s_ks[e * 128 + g] = (col < p.Skv) ? __ldg(ks + col / p.k_block) : 0.0f;
-        }
+        for (int q = 0; q < 4; ++q)
+          if (lane * 4 + q < 128 / KB) s_ks[e * 128 + lane * 4 + q] = pre[0][q];
         mbar_arrive(&bars->ks_full[e]);
+#pragma unroll
+        for (int d = 0; d + 1 < kAhead; ++d)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) pre[d][q] = pre[d + 1][q];
+        load_tile(j + kAhead, pre[kAhead - 1]);
       }
     }
   }
@@ -552,14 +567,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       // before the arrive that lets the MMA accumulate into O)
       if (j > 0 && __any_sync(0xffffffffu, need)) {
         const float2 a2 = make_float2(alpha, alpha);
-#pragma unroll 1
-        for (int cc = 0; cc < 2; ++cc) {
-          float2 o[16];
-          tmem_ld32(t_o + 32 * cc, reinterpret_cast<float*>(o));
+        if constexpr (kSage && KB >= 16) {
+          // frequent (every new running max): all 64 columns with one wait. Measured faster with
+          // K blocks of 16; with finer blocks the two-round form below is faster.
+          float2 o[32];
+          tmem_ld32(t_o, reinterpret_cast<float*>(o));
+          tmem_ld32(t_o + 32, reinterpret_cast<float*>(o + 16));
           tmem_ld_wait();
 #pragma unroll
-          for (int k = 0; k < 16; ++k) o[k] = __fmul2_rn(o[k], a2);
-          tmem_st32(t_o + 32 * cc, reinterpret_cast<const uint32_t*>(o));
+          for (int k = 0; k < 32; ++k) o[k] = __fmul2_rn(o[k], a2);
+          tmem_st32(t_o, reinterpret_cast<const uint32_t*>(o));
+          tmem_st32(t_o + 32, reinterpret_cast<const uint32_t*>(o + 16));
+        } else {
+          // two rounds of 32 columns keep register pressure low
+#pragma unroll 1
+          for (int cc = 0; cc < 2; ++cc) {
+            float2 o[16];
+            tmem_ld32(t_o + 32 * cc, reinterpret_cast<float*>(o));
+            tmem_ld_wait();
+#pragma unroll
+            for (int k = 0; k < 16; ++k) o[k] = __fmul2_rn(o[k], a2);
+            tmem_st32(t_o + 32 * cc, reinterpret_cast<const uint32_t*>(o));
+          }
         }
       }
       tmem_st_wait();
