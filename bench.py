@@ -207,7 +207,7 @@ def dense_kernel_traffic():
     try:
         text = open(path).read()
         h = hashlib.sha256()
-        for name in ("fmha_kernel.cuh", "fmha_dense.cu", "sm103_ptx.cuh"):
+        for name in ("fmha_kernel.cuh", "fmha_common.cuh", "fmha_dense.cu", "sm103_ptx.cuh"):
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(f.read())
     except OSError:
