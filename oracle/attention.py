@@ -28,6 +28,9 @@ Readings where the pages are silent:
   re-quantized for BMM2 as E4M3(p * 448) / 448 with p = exp(s - m_new), m_new the exact
   running row max (so p lies in [0, 1]); the row sum l uses the unquantized p. The
   accumulator runs on V codes and is multiplied by v_scale per channel at the end.
+* QK16PV8 ("VisualGen Quantized Attention", section "QK16PV8 Attention Kernels in the CUTEDSL
+  Backend": Q/K stay BF16, only V is FP8): the dense logits, and P and V exactly as in SAGE
+  (the pages give BMM2 the same FP8 path; P's scale and l follow the SAGE readings).
 """
 
 from __future__ import annotations
@@ -136,8 +139,9 @@ def attention_q_tile(inputs: dict, b: int, hq: int, tile: int, *, mode: str, qk_
     """Oracle output of one 128-row Q tile of one (batch, query head).
 
     inputs: dict with float32 arrays 'q' [B,Sq,Hq,128], 'k', 'v' [B,Skv,Hkv,128] holding bf16 values.
-    mode:   'dense' or 'sage'; ``factor`` switches Skip-Softmax on (threshold = factor / Skv).
-    quant:  the output of ``sage_quant.sage_quantize`` (needed for mode 'sage').
+    mode:   'dense', 'sage' or 'qk16pv8'; ``factor`` switches Skip-Softmax on (threshold = factor / Skv).
+    quant:  the output of ``sage_quant.sage_quantize`` (mode 'sage') or ``sage_quant.qk16pv8_quantize``
+            (mode 'qk16pv8').
     Returns (O [rows, 128] float64, skipped tile count, row indices).
     """
     q, k, v = inputs["q"], inputs["k"], inputs["v"]
@@ -155,6 +159,11 @@ def attention_q_tile(inputs: dict, b: int, hq: int, tile: int, *, mode: str, qk_
         qs_rows = quant["q_scale"][b, hq, rows // q_block]
         ks_cols = quant["k_scale"][b, g, np.arange(Skv) // k_block]
         s = sage_scores(quant["q_codes"][b, r0:r1, hq, :], quant["k_codes"][b, :, g, :], qs_rows, ks_cols, qk_dtype)
+        vals = formats.e4m3_decode(quant["v_codes"][b, :, g, :])
+        o, skipped = tiled_attention(s, vals, quantize_p=True, threshold=thr)
+        return o * np.asarray(quant["v_scale"][b, g, :], np.float64)[None, :], skipped, rows
+    if mode == "qk16pv8":
+        s = dense_scores(q[b, r0:r1, hq, :], k[b, :, g, :])
         vals = formats.e4m3_decode(quant["v_codes"][b, :, g, :])
         o, skipped = tiled_attention(s, vals, quantize_p=True, threshold=thr)
         return o * np.asarray(quant["v_scale"][b, g, :], np.float64)[None, :], skipped, rows

@@ -105,6 +105,33 @@ def quantize_v_per_channel(v: np.ndarray):
     return formats.e4m3_encode(quot), scales
 
 
+def quantize_v_per_tensor(v: np.ndarray):
+    """FP8 E4M3 codes of V with one tensor-wide scale = max |V| over the whole tensor / 448.
+
+    "VisualGen Quantized Attention", quant_attention_config table: v_block_size 0 means one
+    tensor-wide V scale. Reading: "tensor-wide" spans every batch, token, head and channel. The
+    division and the codes follow the per-channel rule (float32 division, E4M3 round to nearest
+    even with saturation, a zero scale gives zero codes). The scale is returned broadcast to
+    [B, H, 128], the shape of the per-channel scales.
+    """
+    v = np.asarray(v, dtype=np.float32)
+    B, _, H, D = v.shape
+    scale = np.float32(np.float32(np.abs(v).max()) / QMAX["fp8_e4m3"])
+    if scale == 0:
+        return np.zeros(v.shape, dtype=np.uint8), np.zeros((B, H, D), dtype=np.float32)
+    quot = (v / scale).astype(np.float32)
+    return formats.e4m3_encode(quot), np.full((B, H, D), scale, dtype=np.float32)
+
+
+def qk16pv8_quantize(v: np.ndarray, per_tensor: bool) -> dict:
+    """The QK16PV8 prepass ("VisualGen Quantized Attention", section "QK16PV8 Attention Kernels in
+    the CUTEDSL Backend"): Q and K stay BF16; only V is quantized to FP8 E4M3, with one
+    tensor-wide scale (v_block_size 0, the recipe table's (0, 0, 0)) or one scale per
+    (batch, head, channel) (v_block_size 1)."""
+    v_codes, v_scale = quantize_v_per_tensor(v) if per_tensor else quantize_v_per_channel(v)
+    return dict(v_codes=v_codes, v_scale=v_scale)
+
+
 def sage_quantize(q: np.ndarray, k: np.ndarray, v: np.ndarray, qk_dtype: str, q_block: int, k_block: int) -> dict:
     """The whole SAGE prepass: K mean, smoothed K, Q/K token-block codes and scales, V codes.
 

@@ -96,3 +96,31 @@ def test_skip_rule_with_wrong_sign_is_caught(monkeypatch):
 def test_wrong_p_scale_is_caught(monkeypatch):
     monkeypatch.setattr(formats, "E4M3_MAX", 256.0)
     _fails(TA.test_sage_single_tile_formula, "int8")
+
+
+# ---- QK16PV8 (V in FP8 with a tensor-wide or per-channel scale, BF16 Q/K)
+from . import test_oracle_qk16pv8 as TP  # noqa: E402
+
+
+def test_channel_max_used_as_tensor_scale_is_caught(monkeypatch):
+    monkeypatch.setattr(sage_quant, "quantize_v_per_tensor", sage_quant.quantize_v_per_channel)
+    _fails(TP.test_tensor_scale_closed_form_and_extreme_code)
+
+
+def test_unquantized_p_in_qk16pv8_is_caught(monkeypatch):
+    good = att.tiled_attention
+    monkeypatch.setattr(att, "tiled_attention",
+                        lambda s, values, quantize_p, threshold=None: good(s, values, quantize_p=False,
+                                                                            threshold=threshold))
+    _fails(TP.test_one_row_matches_scalar_definition)
+
+
+def test_dropped_v_scale_in_qk16pv8_is_caught(monkeypatch):
+    good = sage_quant.qk16pv8_quantize
+
+    def unit_scale(v, per_tensor):
+        res = good(v, per_tensor)
+        res["v_scale"] = np.ones_like(res["v_scale"])
+        return res
+    monkeypatch.setattr(sage_quant, "qk16pv8_quantize", unit_scale)
+    _fails(TP.test_large_logits_give_the_target_value_row, True)
