@@ -238,27 +238,64 @@ def time_steps(fn, steps, warmup, world, stream):
     return e0.elapsed_time(e1)  # ms on this rank
 
 
-def run_modes(dit, steps, warmup, world, stream, peak16):
-    """The other workloads, each as one call of the whole path (prepass + attention)."""
+def run_modes(dit, steps, warmup, world, stream, peak16, hbm_gbs):
+    """The other workloads. Each quantized one is timed as one call of the whole path (prepass +
+    attention), and also in its two halves through the split entry points: the prepass alone
+    (against the measured HBM bandwidth: it is memory-bound) and the attention over
+    precomputed codes (against the tensor peak of its operand types)."""
     res = {}
     peak8 = 2.0 * peak16                               # FP8 dense = 2 x BF16 (nominal ratio)
-    peak_i8 = 2.0 * peak16 * peak8 / (peak16 + peak8)  # BMM1 on fp16 codes, BMM2 on FP8
-    for name, peak, peak_desc in [("dit_sage_int8_32k", peak_i8, "BMM1 f16 + BMM2 e4m3 harmonic peak"),
-                                  ("gqa_sage_fp8_16k", peak8, "2 x measured bf16 (e4m3 nominal ratio)")]:
+    peak_mix = 2.0 * peak16 * peak8 / (peak16 + peak8)  # BMM1 on 16-bit operands, BMM2 on FP8
+    table = [("dit_sage_int8_32k", peak_mix, "BMM1 f16 + BMM2 e4m3 harmonic peak"),
+             ("gqa_sage_fp8_16k", peak8, "2 x measured bf16 (e4m3 nominal ratio)"),
+             ("dit_qk16pv8_32k", peak_mix, "BMM1 bf16 + BMM2 e4m3 harmonic peak")]
+    for name, peak, peak_desc in table:
         w = workloads.WORKLOADS[name]
         q, k, v = workloads.generate(w, seed=1, device="cuda")
-        ws = torch.empty(dit.dit_attn_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, dit.MODE_SAGE, w.qk_dtype,
+        qk16 = w.mode == "qk16pv8"
+        mode = dit.MODE_SAGE | (dit.MODE_V_PER_TENSOR if qk16 else 0)
+        ws = torch.empty(dit.dit_attn_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, mode, w.qk_dtype,
                                                       w.q_block, w.k_block), dtype=torch.uint8, device="cuda")
         out = torch.empty_like(q)
 
         def step():
-            dit.dit_attn_fwd(q, k, v, out, mode=dit.MODE_SAGE, qk_dtype=w.qk_dtype, q_block=w.q_block,
+            dit.dit_attn_fwd(q, k, v, out, mode=mode, qk_dtype=w.qk_dtype, q_block=w.q_block,
                              k_block=w.k_block, workspace=ws, stream=stream)
         ms = max_over_ranks(time_steps(step, steps, warmup, world, stream), world) / steps
         tf = w.dense_equiv_flop / (ms * 1e-3) / 1e12
-        res[name] = {"ms": round(ms, 3), "tflops": round(tf, 1), "peak_tflops": round(peak, 1),
-                     "frac": round(tf / peak, 3), "peak": peak_desc, "launches_per_step": 5}
-        del q, k, v, ws, out
+        entry = {"ms": round(ms, 3), "tflops": round(tf, 1), "peak_tflops": round(peak, 1),
+                 "frac": round(tf / peak, 3), "peak": peak_desc,
+                 "launches_per_step": 4 if qk16 else 5}
+        # the two halves, through the split entry points
+        bq, bkv = q.numel() * 2, k.numel() * 2
+        if qk16:
+            pre = lambda: dit.sage_quantize_v(v, per_tensor=True, stream=stream)  # noqa: E731
+            # V read twice (absmax, then codes), 1-byte codes written
+            pre_bytes, pre_desc = 2 * bkv + bkv // 2, "V read twice, 1-byte V codes written"
+        else:
+            pre = lambda: dit.sage_quantize_qkv(q, k, v, qk_dtype=w.qk_dtype, q_block=w.q_block,  # noqa: E731
+                                                k_block=w.k_block, stream=stream)
+            # K, V read in the stats pass and again with Q in the code pass; 1-byte codes written
+            pre_bytes = bq + 4 * bkv + (bq + 2 * bkv) // 2
+            pre_desc = "K, V read twice, Q once, 1-byte Q/K/V codes written"
+        quant = pre()
+        if qk16:
+            quant.update(q_codes=q, k_codes=k)
+        pre_ms = max_over_ranks(time_steps(pre, steps, warmup, world, stream), world) / steps
+
+        def attn():
+            dit.dit_attn_fwd_quantized(quant, out, mode=mode, qk_dtype=w.qk_dtype, q_block=w.q_block,
+                                       k_block=w.k_block, stream=stream)
+        attn_ms = max_over_ranks(time_steps(attn, steps, warmup, world, stream), world) / steps
+        atf = w.dense_equiv_flop / (attn_ms * 1e-3) / 1e12
+        entry["prepass"] = {"ms": round(pre_ms, 3), "gbs": round(pre_bytes / (pre_ms * 1e-3) / 1e9, 1),
+                            "frac_hbm": round(pre_bytes / (pre_ms * 1e-3) / 1e9 / hbm_gbs, 3),
+                            "bytes": int(pre_bytes), "bytes_desc": pre_desc}
+        entry["attention"] = {"ms": round(attn_ms, 3), "tflops": round(atf, 1), "frac": round(atf / peak, 3),
+                              "note": "INT8 codes are widened to fp16 inside this call" if w.qk_dtype == "int8"
+                              else "the attention kernel alone"}
+        res[name] = entry
+        del q, k, v, ws, out, quant
     # Skip-Softmax sweep on the video grid, against dense BF16 on the same shape
     w = workloads.WORKLOADS["video_skip_int8_75600"]
     q, k, v = workloads.generate(w, seed=1, device="cuda")
@@ -365,7 +402,7 @@ def main():
     if not args.no_modes:
         del q, k, v, out
         torch.cuda.empty_cache()
-        modes = run_modes(dit, args.steps, warmup, world, stream, peak16)
+        modes = run_modes(dit, args.steps, warmup, world, stream, peak16, hbm)
 
     if rank != 0:
         return

@@ -6,8 +6,9 @@ and raises ``DitAttnError`` for any non-OK status. There is no fallback: if the 
 library is missing, importing the binding's functions raises.
 
 Modes follow the pages ("TRTLLM Attention" user guide): dense BF16; SAGE with INT8 or FP8 E4M3
-Q/K per token block (block sizes 1, 4, 16) and per-channel FP8 V; Skip-Softmax with
-threshold = threshold_scale_factor / Skv.
+Q/K per token block (block sizes 1, 4, 16) and per-channel FP8 V; QK16PV8 (SAGE with BF16 Q/K:
+only V in FP8, per channel or with one tensor-wide scale, "VisualGen Quantized Attention");
+Skip-Softmax with threshold = threshold_scale_factor / Skv.
 """
 
 from __future__ import annotations
@@ -18,7 +19,7 @@ import os
 
 import torch
 
-MODE_DENSE, MODE_SAGE, MODE_SKIP = 0, 1, 2
+MODE_DENSE, MODE_SAGE, MODE_SKIP, MODE_V_PER_TENSOR = 0, 1, 2, 4
 QK_BF16, QK_INT8, QK_FP8_E4M3 = 0, 1, 2
 HEAD_DIM = 128
 TILE = 128
@@ -38,6 +39,8 @@ SIGNATURES = {
     "sage_quantize_workspace_bytes": (_c_size, [_c_int] * 3),
     "sage_quantize_qkv": (_c_int, [_vp, _vp, _vp] + [_c_int] * 8 + [_vp] * 8 + [_c_size, _vp]),
     "sage_quantize_qkv_noalloc": (_c_int, [_vp, _vp, _vp] + [_c_int] * 8 + [_vp] * 7 + [_vp]),
+    "sage_quantize_v_workspace_bytes": (_c_size, [_c_int] * 3),
+    "sage_quantize_v": (_c_int, [_vp] + [_c_int] * 4 + [_vp, _vp, _vp, _c_size, _vp]),
     "dit_attn_quantized_workspace_bytes": (_c_size, [_c_int] * 6),
     "dit_attn_fwd_quantized": (_c_int, [_vp] * 7 + [_c_int] * 9 + [_c_float, _vp, _vp, _c_size, _vp]),
     "dit_attn_check_errors": (_c_int, [_vp]),
@@ -164,9 +167,31 @@ def sage_quantize_qkv_noalloc(q, k, v, out: dict, *, qk_dtype="int8", q_block=1,
     return out
 
 
+def sage_quantize_v_workspace_bytes(B, Hkv, Skv) -> int:
+    return int(_lib().sage_quantize_v_workspace_bytes(B, Hkv, Skv))
+
+
+def sage_quantize_v(v, *, per_tensor=False, stream=None, workspace=None):
+    """The QK16PV8 prepass alone: E4M3 codes of V and its scales ([B, Hkv, 128]; one tensor-wide
+    value broadcast there when ``per_tensor``)."""
+    B, Skv, Hkv, _ = v.shape
+    dev = v.device
+    res = dict(v_codes=torch.empty(v.shape, dtype=torch.uint8, device=dev),
+               v_scale=torch.empty((B, Hkv, HEAD_DIM), dtype=torch.float32, device=dev))
+    need = _lib().sage_quantize_v_workspace_bytes(B, Hkv, Skv)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    st = _lib().sage_quantize_v(_ptr(v), B, Hkv, Skv, 1 if per_tensor else 0, _ptr(res["v_codes"]),
+                                _ptr(res["v_scale"]), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "sage_quantize_v")
+    return res
+
+
 def dit_attn_fwd_quantized(quant: dict, out, *, mode=MODE_SAGE, qk_dtype="int8", q_block=1, k_block=16,
                            threshold_scale_factor=0.0, stream=None, workspace=None, skip_counts=None):
-    """Attention over the codes and scales that ``sage_quantize_qkv`` returned."""
+    """Attention over the codes and scales that ``sage_quantize_qkv`` returned. For QK16PV8
+    (``qk_dtype="bf16"``, blocks 0) ``quant`` holds the BF16 Q and K as ``q_codes`` / ``k_codes``
+    and the result of ``sage_quantize_v``; it needs no Q/K scales."""
     qc, kc = quant["q_codes"], quant["k_codes"]
     B, Sq, Hq, _ = qc.shape
     _, Skv, Hkv, _ = kc.shape
@@ -175,8 +200,8 @@ def dit_attn_fwd_quantized(quant: dict, out, *, mode=MODE_SAGE, qk_dtype="int8",
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=qc.device)
     ws_bytes = 0 if workspace is None else workspace.numel()
-    st = _lib().dit_attn_fwd_quantized(_ptr(qc), _ptr(kc), _ptr(quant["v_codes"]), _ptr(quant["q_scale"]),
-                                       _ptr(quant["k_scale"]), _ptr(quant["v_scale"]), _ptr(out), B, Hq, Hkv, Sq,
+    st = _lib().dit_attn_fwd_quantized(_ptr(qc), _ptr(kc), _ptr(quant["v_codes"]), _ptr(quant.get("q_scale")),
+                                       _ptr(quant.get("k_scale")), _ptr(quant["v_scale"]), _ptr(out), B, Hq, Hkv, Sq,
                                        Skv, mode, qk, q_block, k_block, float(threshold_scale_factor),
                                        _stream(stream), _ptr(workspace), ws_bytes, _ptr(skip_counts))
     _check(st, "dit_attn_fwd_quantized")

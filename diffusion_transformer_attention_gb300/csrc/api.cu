@@ -17,7 +17,7 @@ using namespace ditattn;
 
 namespace {
 
-constexpr int kAbiVersion = 1;
+constexpr int kAbiVersion = 2;
 constexpr unsigned long long kWaitBudgetNs = 4000000000ull;  // far beyond any legitimate wait
 
 __device__ int g_device_error = 0;
@@ -39,12 +39,19 @@ bool valid_shape(int B, int Hq, int Hkv, int Sq, int Skv) {
 }
 
 bool valid_mode(int mode, int qk_dtype, int q_block, int k_block, float factor) {
-  if (mode < 0 || mode > (DIT_MODE_SAGE | DIT_MODE_SKIP)) return false;
+  if (mode < 0 || mode > (DIT_MODE_SAGE | DIT_MODE_SKIP | DIT_MODE_V_PER_TENSOR)) return false;
   if (mode & DIT_MODE_SAGE) {
-    if (qk_dtype != DIT_QK_INT8 && qk_dtype != DIT_QK_FP8_E4M3) return false;
-    if (!is_block(q_block) || !is_block(k_block)) return false;
-  } else if (qk_dtype != DIT_QK_BF16) {
-    return false;  // a quantized dtype without SAGE is a contradictory request
+    if (qk_dtype == DIT_QK_BF16) {
+      // QK16PV8: Q/K stay BF16, so there are no Q/K blocks (the pages' block sizes (0, 0, v))
+      if (q_block != 0 || k_block != 0) return false;
+    } else {
+      if (qk_dtype != DIT_QK_INT8 && qk_dtype != DIT_QK_FP8_E4M3) return false;
+      if (!is_block(q_block) || !is_block(k_block)) return false;
+      if (mode & DIT_MODE_V_PER_TENSOR) return false;  // the SAGE recipes scale V per channel
+    }
+  } else {
+    if (qk_dtype != DIT_QK_BF16) return false;       // a quantized dtype without SAGE is contradictory
+    if (mode & DIT_MODE_V_PER_TENSOR) return false;  // V is not quantized without SAGE
   }
   if (mode & DIT_MODE_SKIP) {
     if (!std::isfinite(factor) || factor < 0.0f) return false;
@@ -56,18 +63,21 @@ struct SageLayout {
   size_t q_codes, k_codes, v_codes, q_scale, k_scale, v_scale, k_mean, psum, pmax, total;
 };
 
+// Workspace of the all-in-one call. QK16PV8 (BF16 Q/K) needs only the V codes, V scales and the
+// V-absmax partials; its Q/K regions have size zero.
 SageLayout sage_layout(int B, int Hq, int Hkv, int Sq, int Skv, int qk_dtype, int q_block, int k_block) {
   SageLayout L{};
-  const size_t code_bytes = (qk_dtype == DIT_QK_INT8) ? 2 : 1;  // INT8 codes are held as exact fp16
+  const bool qk16 = (qk_dtype == DIT_QK_BF16);
+  const size_t code_bytes = qk16 ? 0 : (qk_dtype == DIT_QK_INT8) ? 2 : 1;  // INT8 codes are held as exact fp16
   size_t off = 0;
   L.q_codes = off; off = align256(off + (size_t)B * Sq * Hq * kHeadDim * code_bytes);
   L.k_codes = off; off = align256(off + (size_t)B * Skv * Hkv * kHeadDim * code_bytes);
   L.v_codes = off; off = align256(off + (size_t)B * Skv * Hkv * kHeadDim);
-  L.q_scale = off; off = align256(off + (size_t)B * Hq * ceil_div(Sq, q_block) * 4);
-  L.k_scale = off; off = align256(off + (size_t)B * Hkv * ceil_div(Skv, k_block) * 4);
+  L.q_scale = off; off = align256(off + (qk16 ? 0 : (size_t)B * Hq * ceil_div(Sq, q_block) * 4));
+  L.k_scale = off; off = align256(off + (qk16 ? 0 : (size_t)B * Hkv * ceil_div(Skv, k_block) * 4));
   L.v_scale = off; off = align256(off + (size_t)B * Hkv * kHeadDim * 4);
-  L.k_mean = off;  off = align256(off + (size_t)B * Hkv * kHeadDim * 4);
-  L.psum = off;    off = align256(off + (size_t)B * Hkv * stats_chunks(Skv) * kHeadDim * 8);
+  L.k_mean = off;  off = align256(off + (qk16 ? 0 : (size_t)B * Hkv * kHeadDim * 4));
+  L.psum = off;    off = align256(off + (qk16 ? 0 : (size_t)B * Hkv * stats_chunks(Skv) * kHeadDim * 8));
   L.pmax = off;    off = align256(off + (size_t)B * Hkv * stats_chunks(Skv) * kHeadDim * 4);
   L.total = off;
   return L;
@@ -230,6 +240,17 @@ dit_status dit_attn_fwd(const void* q, const void* k, const void* v, void* out, 
     return run_attention(q, k, v, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, QK_BF16, PV_BF16, B, Hq, Hkv, Sq, Skv,
                          mode, 1, 1, threshold_scale_factor, nullptr, nullptr, nullptr, skip_counts, err, st);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (qk_dtype == DIT_QK_BF16) {
+    // QK16PV8: V scales (per channel or one tensor-wide) and V codes; Q/K go to BMM1 as they are
+    float* v_scale = reinterpret_cast<float*>(ws + L.v_scale);
+    cudaError_t e = launch_v_stats(v, B, Hkv, Skv, reinterpret_cast<float*>(ws + L.pmax), v_scale,
+                                   (mode & DIT_MODE_V_PER_TENSOR) != 0, st);
+    if (e == cudaSuccess) e = launch_quant_v(v, B, Hkv, Skv, v_scale, ws + L.v_codes, st);
+    if (e != cudaSuccess) return from_cuda(e);
+    return run_attention(q, k, ws + L.v_codes, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, QK_BF16, PV_E4M3, B, Hq,
+                         Hkv, Sq, Skv, mode, 1, 1, threshold_scale_factor, nullptr, nullptr, v_scale, skip_counts,
+                         err, st);
+  }
   float* q_scale = reinterpret_cast<float*>(ws + L.q_scale);
   float* k_scale = reinterpret_cast<float*>(ws + L.k_scale);
   float* v_scale = reinterpret_cast<float*>(ws + L.v_scale);
@@ -283,6 +304,29 @@ dit_status sage_quantize_qkv(const void* q, const void* k, const void* v, int B,
   return from_cuda(e);
 }
 
+size_t sage_quantize_v_workspace_bytes(int B, int Hkv, int Skv) {
+  if (B < 0 || Hkv < 1 || Skv < 1) return 0;
+  return align256((size_t)B * Hkv * stats_chunks(Skv) * kHeadDim * 4);
+}
+
+dit_status sage_quantize_v(const void* v, int B, int Hkv, int Skv, int v_per_tensor, void* v_codes, float* v_scale,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  if (!valid_shape(B, Hkv, Hkv, 0, Skv) || (v_per_tensor != 0 && v_per_tensor != 1)) return DIT_E_INVALID_ARG;
+  if (B == 0) return DIT_OK;
+  if (!v || !v_codes || !v_scale || !aligned16(v) || !aligned16(v_codes) || !aligned16(v_scale))
+    return DIT_E_INVALID_ARG;
+  const size_t need = sage_quantize_v_workspace_bytes(B, Hkv, Skv);
+  if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return DIT_E_WORKSPACE;
+  int* err = nullptr;
+  const dit_status ds = prepare_device(&err);
+  if (ds != DIT_OK) return ds;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_v_stats(v, B, Hkv, Skv, static_cast<float*>(workspace), v_scale, v_per_tensor != 0, st);
+  if (e == cudaSuccess) e = launch_quant_v(v, B, Hkv, Skv, v_scale, v_codes, st);
+  return from_cuda(e);
+}
+
 size_t dit_attn_quantized_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int qk_dtype) {
   if (!valid_shape(B, Hq, Hkv, Sq, Skv)) return 0;
   if (qk_dtype == DIT_QK_FP8_E4M3) return 0;
@@ -299,9 +343,11 @@ dit_status dit_attn_fwd_quantized(const void* q_codes, const void* k_codes, cons
       !valid_mode(mode, qk_dtype, q_block, k_block, threshold_scale_factor))
     return DIT_E_INVALID_ARG;
   if (B == 0 || Sq == 0) return DIT_OK;
-  const void* ptrs[] = {q_codes, k_codes, v_codes, q_scale, k_scale, v_scale, out};
+  const bool qk16 = (qk_dtype == DIT_QK_BF16);  // QK16PV8: q_codes / k_codes are the BF16 Q / K, no Q/K scales
+  const void* ptrs[] = {q_codes, k_codes, v_codes, v_scale, out};
   for (const void* ptr : ptrs)
     if (!ptr) return DIT_E_INVALID_ARG;
+  if (!qk16 && (!q_scale || !k_scale)) return DIT_E_INVALID_ARG;
   if (!aligned16(q_codes) || !aligned16(k_codes) || !aligned16(v_codes) || !aligned16(out) ||
       !aligned16(skip_counts))
     return DIT_E_INVALID_ARG;
@@ -326,10 +372,12 @@ dit_status dit_attn_fwd_quantized(const void* q_codes, const void* k_codes, cons
     qa = q16;
     ka = k16;
   }
+  if (qk16)
+    return run_attention(qa, ka, v_codes, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, QK_BF16, PV_E4M3, B, Hq, Hkv, Sq,
+                         Skv, mode, 1, 1, threshold_scale_factor, nullptr, nullptr, v_scale, skip_counts, err, st);
   return run_attention(qa, ka, v_codes, out, i8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
                        i8 ? 2 : 1, i8 ? QK_F16 : QK_E4M3, PV_E4M3, B, Hq, Hkv, Sq, Skv, mode, q_block, k_block,
-                       threshold_scale_factor, q_scale, k_scale, v_scale, skip_counts, err,
-                       static_cast<cudaStream_t>(stream));
+                       threshold_scale_factor, q_scale, k_scale, v_scale, skip_counts, err, st);
 }
 
 dit_status dit_attn_check_errors(void* stream) {

@@ -32,7 +32,7 @@ struct FmhaParams {
   int q_block, nqb;
   const float* k_scale;  // SAGE: [B, Hkv, nkb]
   int k_block, nkb;
-  const float* v_scale;  // SAGE: [B, Hkv, 128]
+  const float* v_scale;  // E4M3 V (SAGE, QK16PV8): [B, Hkv, 128]
   int32_t* skip_counts;  // optional [B, Hq, n_q_tiles]
   int* err;              // device error word
   unsigned long long wait_budget_ns;
@@ -48,10 +48,18 @@ cudaError_t launch_fmha_sage_i8(bool skip, const CUtensorMap& tq, const CUtensor
                                 const CUtensorMap& to, const FmhaParams& p, cudaStream_t stream);
 cudaError_t launch_fmha_sage_f8(bool skip, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const CUtensorMap& to, const FmhaParams& p, cudaStream_t stream);
+cudaError_t launch_fmha_qk16pv8(bool skip, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                const CUtensorMap& to, const FmhaParams& p, cudaStream_t stream);
 
 // Quantize-prepass launchers (prepass.cu).
 cudaError_t launch_kv_stats(const void* k, const void* v, int B, int Hkv, int Skv, double* psum, float* pmax,
                             float* k_mean, float* v_scale, cudaStream_t stream);
+// V alone (QK16PV8): per-channel absmax scales, optionally reduced to one tensor-wide scale
+// broadcast over [B, Hkv, 128], then E4M3 codes of V / scale.
+cudaError_t launch_v_stats(const void* v, int B, int Hkv, int Skv, float* pmax, float* v_scale, bool per_tensor,
+                           cudaStream_t stream);
+cudaError_t launch_quant_v(const void* v, int B, int Hkv, int Skv, const float* v_scale, void* v_codes,
+                           cudaStream_t stream);
 cudaError_t launch_quant_q(const void* q, int B, int Hq, int Sq, int q_block, int code_out, void* q_codes,
                            float* q_scale, cudaStream_t stream);
 cudaError_t launch_quant_kv(const void* k, const void* v, int B, int Hkv, int Skv, int k_block, int code_out,

@@ -1,7 +1,7 @@
 // Fused attention forward kernel for sm_103a (template; instantiated by fmha_dense.cu,
-// fmha_sage_i8.cu and fmha_sage_f8.cu): TMA-staged Q/K/V tiles, tcgen05 MMAs accumulating
-// S = Q K^T and O += P V in tensor memory, online softmax with exp2, optional SAGE dequantization
-// and P re-quantization to FP8, and the Skip-Softmax tile test.
+// fmha_sage_i8.cu, fmha_sage_f8.cu and fmha_qk16pv8.cu): TMA-staged Q/K/V tiles, tcgen05 MMAs
+// accumulating S = Q K^T and O += P V in tensor memory, online softmax with exp2, optional SAGE
+// dequantization, P re-quantization to FP8 (SAGE and QK16PV8), and the Skip-Softmax tile test.
 //
 // The method is fixed by the pages ("TRTLLM Attention" user guide: dense BF16, SAGE, Skip-Softmax;
 // "SAGE + Skip-Softmax -- API Design & Test Plan", Part 1 §4: bmm1/bmm2 scales and
@@ -12,7 +12,7 @@
 //   warps 1, 2   MMA issuers, one per Q tile (one elected lane each): BMM1 S_i = Q_i K_j^T (SS),
 //                BMM2 O_i += P_i V_j (V is MN-major, so no transpose). Warp 2 also allocates the 512
 //                tensor-memory columns (S0 | S1 | O0 | O1) at the start and frees them at the end.
-//   warp 3       SAGE only: stages the per-column K scales of each KV tile and the V scales.
+//   warp 3       stages the V scales (E4M3 V) and, in SAGE, the K-block scales of each KV tile.
 //   warps 4-19   four softmax warpgroups: Q tile i = g / 2 and column half h = g % 2 for group g.
 //                A thread owns one row (= TMEM lane) and 64 of its 128 columns; the two halves
 //                of a row exchange partial maxima through shared memory. Halving the columns per
@@ -21,14 +21,14 @@
 // BMM2 reads P from tensor memory (TS). The issuer runs O_i += P_i(j-1) V_{j-1}, S_i = Q_i K_j^T as
 // soon as P_i(j-1) is ready, so while one tile's softmax turns S into P, the tensor cores work on
 // the other tile.
-// SAGE (E4M3 P, 16 KB per tile): P goes to a shared-memory buffer and BMM2 is an SS MMA. S is free
+// E4M3 P (SAGE and QK16PV8, 16 KB per tile): P goes to a shared-memory buffer and BMM2 is an SS MMA. S is free
 // as soon as the softmax has loaded it, so the issuer computes S_i(j+1) while the softmax works on
 // S_i(j); a per-tile barrier (o_done) returns P's buffer and O to the softmax after each BMM2.
 //
-// Numerics: logits are kept in log2 units (scaled by softmax_scale * log2 e). Dense mode rescales
-// O lazily (only when the running max grows by more than 8, P then stays below 2^8); SAGE rescales
-// eagerly so P = exp2(s - m_run) lies in [0, 1] and P * 448 re-quantizes on the same grid as the
-// definition. The row sum uses the unquantized P. Skip-Softmax compares the tile max against
+// Numerics: logits are kept in log2 units (scaled by softmax_scale * log2 e). With BF16 P, O is
+// rescaled lazily (only when the running max grows by more than 8, P then stays below 2^8); with
+// E4M3 P it is rescaled eagerly so P = exp2(s - m_run) lies in [0, 1] and P * 448 re-quantizes on
+// the same grid as the definition. The row sum uses the unquantized P. Skip-Softmax compares the tile max against
 // the exact running max.
 //
 // Every wait is bounded; on expiry the kernel records a timeout in the device error word, tells
@@ -107,7 +107,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     fmha_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                     const FmhaParams p) {
-  constexpr bool kSage = (QKF != QK_BF16);
+  constexpr bool kQKScaled = (QKF != QK_BF16);  // Q/K codes with token-block scales (SAGE)
+  constexpr bool kPV8 = (PVF == PV_E4M3);        // E4M3 P and V with per-channel V scales (SAGE, QK16PV8)
   constexpr int kQKBytes = (QKF == QK_E4M3) ? 1 : 2;
   constexpr int kPVBytes = (PVF == PV_E4M3) ? 1 : 2;
   constexpr uint32_t kQTileBytes = 128u * 128u * kQKBytes;
@@ -327,13 +328,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait_bounded(&bars->drain[i], 0, budget, nullptr);
     __syncwarp();
   } else if (warp == 3) {
-    // ------------------------------------------------------------ SAGE scale stager
-    if constexpr (kSage) {
-      bool ok = true;
+    // ------------------------------------------------------------ scale stager (V scales; SAGE K scales)
+    if constexpr (kPV8) {
       const float* vs = p.v_scale + ((size_t)b * p.Hkv + hkv) * kHeadDim;
 #pragma unroll
       for (int e = 0; e < 4; ++e) s_vs[lane * 4 + e] = vs[lane * 4 + e];
       mbar_arrive(&bars->vs_full);
+    }
+    if constexpr (kQKScaled) {
+      bool ok = true;
       const float* ks = p.k_scale + ((size_t)b * p.Hkv + hkv) * p.nkb;
       // A tile's 128 / KB block scales, four slots per lane (0 for slots past them and past the
       // end of K). The loads run kAhead tiles ahead of the ring, so their latency stays off the
@@ -386,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* xmax = reinterpret_cast<float*>(smem + L::kXmaxOff);
     float* xl = reinterpret_cast<float*>(smem + L::kXlOff);
     float c = p.c_scale;
-    if constexpr (kSage) {
+    if constexpr (kQKScaled) {
       const float qs = row_valid ? __ldg(p.q_scale + ((size_t)b * p.Hq + hq) * p.nqb + qrow / p.q_block) : 0.0f;
       c = qs * p.c_scale;
     }
@@ -431,10 +434,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Exponent weight per column group (log2 units): the row constant c, times the K block
       // scale in SAGE. KB >= 4 folds the block scale into the weight; KB == 1 multiplies first.
-      constexpr int kGroups = (kSage && KB >= 4) ? 64 / KB : 1;
+      constexpr int kGroups = (kQKScaled && KB >= 4) ? 64 / KB : 1;
       float wg[kGroups];
       float mh;  // this half's max of the weighted logits
-      if constexpr (kSage) {
+      if constexpr (kQKScaled) {
         const int e = j & 3;
         bool ks_ok = mbar_wait_bounded(&bars->ks_full[e], (j >> 2) & 1, budget, abort_flag);
         ks_ok = __all_sync(0xffffffffu, ks_ok);
@@ -505,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_new = fmaxf(m_ex, mt);
       bool need;
       float alpha = 1.0f;
-      if constexpr (kSage) {
+      if constexpr (kPV8) {
         need = m_new > m_ref;
         if (need) alpha = ex2_approx(m_ref - m_new);
         m_ref = m_new;
@@ -519,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       m_ex = m_new;
       l *= alpha;
       // exponentials (two columns per packed FMA) and this half's row sum
-      const float bias = kSage ? (m_ref - kLog2_448) : m_ref;
+      const float bias = kPV8 ? (m_ref - kLog2_448) : m_ref;
       const float2 nb = make_float2(-bias, -bias);
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
@@ -528,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         s2[k].x = ex2_approx(t.x);
         s2[k].y = ex2_approx(t.y);
       }
-      if constexpr (kSage) {
+      if constexpr (kQKScaled) {
         // masked columns hold -inf; with a zero weight (zero scale) that gives NaN, so clear them
         if (tail) {
 #pragma unroll
@@ -567,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // before the arrive that lets the MMA accumulate into O)
       if (j > 0 && __any_sync(0xffffffffu, need)) {
         const float2 a2 = make_float2(alpha, alpha);
-        if constexpr (kSage && KB >= 16) {
+        if constexpr (kQKScaled && KB >= 16) {
           // frequent (every new running max): all 64 columns with one wait. Measured faster with
           // K blocks of 16; with finer blocks the two-round form below is faster.
           float2 o[32];
@@ -606,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float l_row = xl[(i * 2 + 0) * 128 + r] + xl[(i * 2 + 1) * 128 + r];
     if (ok) {
       ok = mbar_wait_bounded(&bars->o_full[i], 0, budget, abort_flag);
-      if constexpr (kSage) ok = ok && mbar_wait_bounded(&bars->vs_full, 0, budget, abort_flag);
+      if constexpr (kPV8) ok = ok && mbar_wait_bounded(&bars->vs_full, 0, budget, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok && lane == 0) record_timeout(p, bars);
     }
@@ -626,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
           float a0 = o[2 * k] * inv_l, a1 = o[2 * k + 1] * inv_l;
-          if constexpr (kSage) {
+          if constexpr (kPV8) {
             a0 *= s_vs[64 * h + 32 * cc + 2 * k];
             a1 *= s_vs[64 * h + 32 * cc + 2 * k + 1];
           }

@@ -57,8 +57,10 @@ __device__ __forceinline__ int int8_code(float q) {
 
 // ------------------------------------------------------------------ K mean / V absmax
 // Pass 1: each CTA reduces kStatsChunk tokens of one (batch, kv head): float64 sums of K
-// and float32 max |V| per channel. Thread t handles channels 8*(t%16).. and tokens t/16 + 16i.
-// The 16 partial rows are then combined in a fixed order, so the result is deterministic.
+// (WITH_K) and float32 max |V| per channel. Thread t handles channels 8*(t%16).. and tokens
+// t/16 + 16i. The 16 partial rows are then combined in a fixed order, so the result is
+// deterministic.
+template <bool WITH_K>
 __global__ void __launch_bounds__(256) kv_stats_partial_kernel(const __nv_bfloat16* __restrict__ k,
                                                                const __nv_bfloat16* __restrict__ v, int Skv, int Hkv,
                                                                int nchunk, double* __restrict__ psum,
@@ -79,11 +81,11 @@ __global__ void __launch_bounds__(256) kv_stats_partial_kernel(const __nv_bfloat
   for (int j = j0 + tr; j < j1; j += 16) {
     const size_t off = (((size_t)b * Skv + j) * Hkv + h) * kHeadDim + cg * 8;
     float kf[8], vf[8];
-    bf16x8_to_f32(ld_stream_v4(k + off), kf);
+    if constexpr (WITH_K) bf16x8_to_f32(ld_stream_v4(k + off), kf);
     bf16x8_to_f32(ld_stream_v4(v + off), vf);
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      s[e] += (double)kf[e];
+      if constexpr (WITH_K) s[e] += (double)kf[e];
       m[e] = fmaxf(m[e], fabsf(vf[e]));
     }
   }
@@ -101,12 +103,13 @@ __global__ void __launch_bounds__(256) kv_stats_partial_kernel(const __nv_bfloat
       mx = fmaxf(mx, smax[r][threadIdx.x]);
     }
     const size_t o = (((size_t)b * Hkv + h) * nchunk + chunk) * kHeadDim + threadIdx.x;
-    psum[o] = a;
+    if constexpr (WITH_K) psum[o] = a;
     pmax[o] = mx;
   }
 }
 
 // Pass 2: combine the chunks of one (batch, kv head) in chunk order.
+template <bool WITH_K>
 __global__ void __launch_bounds__(128) kv_stats_final_kernel(const double* __restrict__ psum,
                                                              const float* __restrict__ pmax, int Skv, int Hkv,
                                                              int nchunk, float* __restrict__ k_mean,
@@ -116,12 +119,58 @@ __global__ void __launch_bounds__(128) kv_stats_final_kernel(const double* __res
   double a = 0.0;
   float mx = 0.0f;
   for (int i = 0; i < nchunk; ++i) {
-    a += psum[base + (size_t)i * kHeadDim];
+    if constexpr (WITH_K) a += psum[base + (size_t)i * kHeadDim];
     mx = fmaxf(mx, pmax[base + (size_t)i * kHeadDim]);
   }
   const size_t o = ((size_t)b * Hkv + h) * kHeadDim + c;
-  k_mean[o] = __double2float_rn(__ddiv_rn(a, (double)Skv));
+  if constexpr (WITH_K) k_mean[o] = __double2float_rn(__ddiv_rn(a, (double)Skv));
   v_scale[o] = __fdiv_rn(mx, 448.0f);
+}
+
+// One tensor-wide V scale (QK16PV8 with v_block_size 0): the max of the per-channel scales,
+// written back over all of them. Dividing by 448 rounds monotonically, so this equals
+// (max |V| over the whole tensor) / 448. One CTA; the array is B * Hkv * 128 floats.
+__global__ void __launch_bounds__(1024) v_scale_tensor_kernel(float* __restrict__ v_scale, long long n) {
+  __shared__ float red[32];
+  float m = 0.0f;
+  for (long long i = threadIdx.x; i < n; i += blockDim.x) m = fmaxf(m, v_scale[i]);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    m = (threadIdx.x < (blockDim.x >> 5)) ? red[threadIdx.x] : 0.0f;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (threadIdx.x == 0) red[0] = m;
+  }
+  __syncthreads();
+  m = red[0];
+  for (long long i = threadIdx.x; i < n; i += blockDim.x) v_scale[i] = m;
+}
+
+// E4M3 codes of V / v_scale[b, h, c] (V alone, for QK16PV8): the same arithmetic as the V part of
+// the token-block quantizer. Item i is 8 channels (16 bytes) of row i / 16 = (b * Skv + j) * Hkv + h.
+__global__ void __launch_bounds__(256) quant_v_kernel(const __nv_bfloat16* __restrict__ v, int Hkv, int Skv,
+                                                      size_t n8, const float* __restrict__ v_scale,
+                                                      uint8_t* __restrict__ v_codes) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+    const int cg = (int)(i & 15);
+    const size_t row = i >> 4;
+    const int h = (int)(row % (size_t)Hkv);
+    const size_t b = row / ((size_t)Hkv * Skv);
+    const float4* sp = reinterpret_cast<const float4*>(v_scale + (b * Hkv + h) * kHeadDim + cg * 8);
+    const float4 s0 = sp[0], s1 = sp[1];
+    const float vs[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+    float vf[8];
+    bf16x8_to_f32(ld_stream_v4(v + i * 8), vf);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) vf[e] = (vs[e] == 0.0f) ? 0.0f : __fdiv_rn(vf[e], vs[e]);
+    uint2 w;
+    w.x = e4m3x2(vf[0], vf[1]) | (e4m3x2(vf[2], vf[3]) << 16);
+    w.y = e4m3x2(vf[4], vf[5]) | (e4m3x2(vf[6], vf[7]) << 16);
+    *reinterpret_cast<uint2*>(v_codes + i * 8) = w;
+  }
 }
 
 // ------------------------------------------------------------------ token-block quantizer
@@ -293,12 +342,35 @@ cudaError_t launch_quant_tokens(const void* x, int B, int S, int H, int block, c
 cudaError_t launch_kv_stats(const void* k, const void* v, int B, int Hkv, int Skv, double* psum, float* pmax,
                             float* k_mean, float* v_scale, cudaStream_t stream) {
   const int nchunk = stats_chunks(Skv);
-  kv_stats_partial_kernel<<<dim3(nchunk, Hkv, B), 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(k),
-                                                                    static_cast<const __nv_bfloat16*>(v), Skv, Hkv,
-                                                                    nchunk, psum, pmax);
+  kv_stats_partial_kernel<true><<<dim3(nchunk, Hkv, B), 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(k),
+                                                                          static_cast<const __nv_bfloat16*>(v), Skv,
+                                                                          Hkv, nchunk, psum, pmax);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  kv_stats_final_kernel<<<dim3(Hkv, B), kHeadDim, 0, stream>>>(psum, pmax, Skv, Hkv, nchunk, k_mean, v_scale);
+  kv_stats_final_kernel<true><<<dim3(Hkv, B), kHeadDim, 0, stream>>>(psum, pmax, Skv, Hkv, nchunk, k_mean, v_scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_v_stats(const void* v, int B, int Hkv, int Skv, float* pmax, float* v_scale, bool per_tensor,
+                           cudaStream_t stream) {
+  const int nchunk = stats_chunks(Skv);
+  kv_stats_partial_kernel<false><<<dim3(nchunk, Hkv, B), 256, 0, stream>>>(
+      nullptr, static_cast<const __nv_bfloat16*>(v), Skv, Hkv, nchunk, nullptr, pmax);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  kv_stats_final_kernel<false><<<dim3(Hkv, B), kHeadDim, 0, stream>>>(nullptr, pmax, Skv, Hkv, nchunk, nullptr,
+                                                                       v_scale);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || !per_tensor) return e;
+  v_scale_tensor_kernel<<<1, 1024, 0, stream>>>(v_scale, (long long)B * Hkv * kHeadDim);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_v(const void* v, int B, int Hkv, int Skv, const float* v_scale, void* v_codes,
+                           cudaStream_t stream) {
+  const size_t n8 = (size_t)B * Skv * Hkv * (kHeadDim / 8);
+  quant_v_kernel<<<grid_for((long long)n8, 256), 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(v), Hkv, Skv,
+                                                                   n8, v_scale, static_cast<uint8_t*>(v_codes));
   return cudaGetLastError();
 }
 

@@ -11,6 +11,11 @@
  *          tensor cores with dequantization scales ("TRTLLM Attention" user guide, section
  *          "SAGE quantization"; "VisualGen Quantized Attention", section "SageAttention in the
  *          TRTLLM backend").
+ *          With qk_dtype DIT_QK_BF16, SAGE is the QK16PV8 recipe: Q and K stay BF16 (BMM1 at full
+ *          input precision) and only V is quantized to FP8 E4M3, with one tensor-wide scale or one
+ *          scale per channel ("VisualGen Quantized Attention", section "QK16PV8 Attention Kernels
+ *          in the CUTEDSL Backend", and the quant_attention_config table: v_block_size 0 = one
+ *          tensor-wide V scale, 1 = one scale per channel).
  *   SKIP   Skip-Softmax: a 128-column KV tile's exp and P.V work is skipped for a 128-row Q
  *          tile when every valid row has exp(m_tile - m_run) < threshold, with
  *          threshold = threshold_scale_factor / Skv ("SAGE + Skip-Softmax -- API Design & Test
@@ -51,17 +56,20 @@ typedef enum dit_status {
   DIT_E_WORKSPACE = 5    /* workspace missing or smaller than the *_workspace_bytes query */
 } dit_status;
 
-/* Mode bits (or-able): DIT_MODE_SAGE | DIT_MODE_SKIP is SAGE with Skip-Softmax. */
-enum { DIT_MODE_DENSE = 0, DIT_MODE_SAGE = 1, DIT_MODE_SKIP = 2 };
+/* Mode bits (or-able): DIT_MODE_SAGE | DIT_MODE_SKIP is SAGE with Skip-Softmax.
+ * DIT_MODE_V_PER_TENSOR is valid only with DIT_MODE_SAGE and DIT_QK_BF16 (QK16PV8): V gets one
+ * tensor-wide scale, max |V| over the whole [B, Skv, Hkv, 128] tensor / 448 (v_block_size 0);
+ * without it V is scaled per (batch, kv head, channel) (v_block_size 1). */
+enum { DIT_MODE_DENSE = 0, DIT_MODE_SAGE = 1, DIT_MODE_SKIP = 2, DIT_MODE_V_PER_TENSOR = 4 };
 
 /* Q/K element type. DENSE uses BF16; SAGE takes INT8 or FP8 E4M3 ("TRTLLM Attention" user guide,
- * SAGE table: dtype_qk in {int8, fp8_e4m3}). */
+ * SAGE table: dtype_qk in {int8, fp8_e4m3}), or BF16 for QK16PV8. */
 enum { DIT_QK_BF16 = 0, DIT_QK_INT8 = 1, DIT_QK_FP8_E4M3 = 2 };
 
 /* Rows and columns of one attention tile; skip counts are kept per 128-row Q tile. */
 enum { DIT_HEAD_DIM = 128, DIT_TILE = 128 };
 
-/* Version of this interface. */
+/* Version of this interface (2: QK16PV8, DIT_MODE_V_PER_TENSOR and sage_quantize_v). */
 int dit_abi_version(void);
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -69,7 +77,8 @@ const char* dit_status_string(dit_status status);
 
 /*
  * Bytes of device workspace dit_attn_fwd needs for these arguments: 0 for DENSE (with or without
- * SKIP), otherwise room for the quantized codes, their scales and the K-mean partial sums.
+ * SKIP), otherwise room for the quantized codes, their scales and the K-mean / V-absmax partials
+ * (QK16PV8: the V codes, V scales and V-absmax partials only).
  * Returns 0 for arguments dit_attn_fwd would reject.
  */
 size_t dit_attn_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int mode, int qk_dtype, int q_block,
@@ -82,9 +91,11 @@ size_t dit_attn_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int mod
  *   k, v       device bf16 [B, Skv, Hkv, 128]
  *   out        device bf16 [B, Sq, Hq, 128], written completely
  *   mode       DIT_MODE_* bits
- *   qk_dtype   DIT_QK_BF16 without SAGE; DIT_QK_INT8 or DIT_QK_FP8_E4M3 with SAGE
- *   q_block, k_block   SAGE tokens per Q / K scale block, each in {1, 4, 16}
- *              ("TRTLLM Attention" user guide, SAGE table); ignored without SAGE
+ *   qk_dtype   DIT_QK_BF16 without SAGE; DIT_QK_INT8, DIT_QK_FP8_E4M3 or (QK16PV8) DIT_QK_BF16
+ *              with SAGE
+ *   q_block, k_block   SAGE with INT8/FP8: tokens per Q / K scale block, each in {1, 4, 16}
+ *              ("TRTLLM Attention" user guide, SAGE table); QK16PV8: both must be 0; ignored
+ *              without SAGE
  *   threshold_scale_factor   with SKIP: finite and >= 0, threshold = factor / Skv (0 never
  *              skips and gives the same output as the mode without SKIP); ignored without SKIP
  *   workspace  device scratch of at least dit_attn_workspace_bytes(...) bytes, 256-byte
@@ -148,12 +159,32 @@ dit_status sage_quantize_qkv_noalloc(const void* q, const void* k, const void* v
                                      void* v_codes, float* q_scale, float* k_scale, float* v_scale, float* k_mean,
                                      void* stream);
 
+/* Bytes of device scratch sage_quantize_v needs (the V-absmax partials). */
+size_t sage_quantize_v_workspace_bytes(int B, int Hkv, int Skv);
+
+/*
+ * The QK16PV8 prepass alone: V's scales and E4M3 codes, Q and K untouched.
+ *
+ *   v             device bf16 [B, Skv, Hkv, 128]
+ *   v_per_tensor  1: one tensor-wide scale, max |V| over the whole tensor / 448, written to every
+ *                 entry of v_scale; 0: one scale per (batch, kv head, channel) = channel absmax / 448
+ *   v_codes       device [B, Skv, Hkv, 128], E4M3 bit patterns of V / scale (round to nearest
+ *                 even, saturating); a zero scale gives zero codes
+ *   v_scale       device float [B, Hkv, 128], 16-byte aligned
+ *   workspace     device scratch of sage_quantize_v_workspace_bytes(B, Hkv, Skv) bytes, 256-byte aligned
+ * The codes and scales are those the QK16PV8 path of dit_attn_fwd computes, bit for bit.
+ */
+dit_status sage_quantize_v(const void* v, int B, int Hkv, int Skv, int v_per_tensor, void* v_codes, float* v_scale,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
 /* Bytes of device workspace dit_attn_fwd_quantized needs (INT8 codes are widened there). */
 size_t dit_attn_quantized_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int qk_dtype);
 
 /*
  * Attention over codes and scales produced by sage_quantize_qkv (same layouts and meanings).
- * mode must include DIT_MODE_SAGE; the other arguments are as for dit_attn_fwd.
+ * mode must include DIT_MODE_SAGE; the other arguments are as for dit_attn_fwd. For QK16PV8
+ * (qk_dtype DIT_QK_BF16, q_block = k_block = 0) q_codes and k_codes are the BF16 Q and K,
+ * q_scale and k_scale are unused (may be NULL), and v_codes / v_scale come from sage_quantize_v.
  */
 dit_status dit_attn_fwd_quantized(const void* q_codes, const void* k_codes, const void* v_codes,
                                   const float* q_scale, const float* k_scale, const float* v_scale, void* out, int B,

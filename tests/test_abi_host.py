@@ -50,7 +50,7 @@ def test_status_strings(lib):
     assert dit.dit_status_string(0) == "ok"
     for s in range(6):
         assert dit.dit_status_string(s)
-    assert lib.dit_abi_version() == 1
+    assert lib.dit_abi_version() == 2
 
 
 FAKE = ctypes.c_void_p(1 << 20)           # a 16-byte aligned, never-dereferenced address
@@ -66,9 +66,12 @@ def _fwd(lib, q=FAKE, B=1, Hq=4, Hkv=2, Sq=256, Skv=256, mode=0, qk=0, qb=1, kb=
 @pytest.mark.parametrize("kw", [
     dict(Hq=5, Hkv=2),                      # Hq not a multiple of Hkv
     dict(Hkv=0), dict(Hq=0), dict(Skv=0), dict(B=-1), dict(Sq=-1),
-    dict(mode=4), dict(mode=-1),
+    dict(mode=4), dict(mode=8), dict(mode=-1),
+    dict(mode=6, qk=0, qb=0, kb=0),         # V per tensor without SAGE
+    dict(mode=5, qk=1),                     # V per tensor with INT8 SAGE (its recipes scale V per channel)
+    dict(mode=1, qk=0, qb=0, kb=16), dict(mode=5, qk=0, qb=1, kb=0),  # QK16PV8 has no Q/K blocks
     dict(mode=0, qk=1),                     # a quantized dtype without SAGE
-    dict(mode=1, qk=0),                     # SAGE without a quantized dtype
+    dict(mode=1, qk=0),                     # QK16PV8 with Q/K block sizes
     dict(mode=1, qk=3),
     dict(mode=1, qk=1, qb=2), dict(mode=1, qk=2, kb=8), dict(mode=1, qk=1, kb=0),
     dict(mode=2, factor=-1.0), dict(mode=2, factor=float("nan")), dict(mode=3, qk=1, factor=float("inf")),
@@ -111,10 +114,15 @@ def _recipes():
 @pytest.mark.parametrize("recipe", _recipes())
 def test_every_printed_recipe_is_accepted(lib, recipe):
     _, dt, qb, kb, vb = recipe
-    assert vb == 1  # V is always per channel
     qk = dit.QK_DTYPES[dt]
-    assert lib.dit_attn_workspace_bytes(2, 32, 8, 1000, 1000, 1, qk, qb, kb) > 0
-    assert lib.dit_attn_workspace_bytes(2, 32, 8, 1000, 1000, 3, qk, qb, kb) > 0
+    if dt == "bf16":  # QK16PV8: one tensor-wide V scale (v_block 0) or one per channel (1)
+        assert vb in (0, 1)
+        mode = dit.MODE_SAGE | (dit.MODE_V_PER_TENSOR if vb == 0 else 0)
+    else:
+        assert vb == 1  # the SAGE recipes scale V per channel
+        mode = dit.MODE_SAGE
+    assert lib.dit_attn_workspace_bytes(2, 32, 8, 1000, 1000, mode, qk, qb, kb) > 0
+    assert lib.dit_attn_workspace_bytes(2, 32, 8, 1000, 1000, mode | dit.MODE_SKIP, qk, qb, kb) > 0
 
 
 @pytest.mark.parametrize("bad", [0, 2, 3, 8, 32])
@@ -133,3 +141,18 @@ def test_workspace_layout_size():
     assert 3 * n <= f8 < 3 * n + 16 * 2**20
     assert dit.dit_attn_workspace_bytes(B, Hq, Hkv, S, S, 0, "bf16") == 0
     assert dit.dit_attn_workspace_bytes(B, Hq, Hkv, S, S, 2, "bf16") == 0
+    # QK16PV8 keeps Q/K as they are: only V codes (1 byte), V scales and the V-absmax partials
+    nkv = B * S * Hkv * 128
+    qk16 = dit.dit_attn_workspace_bytes(B, Hq, Hkv, S, S, 1, "bf16", 0, 0)
+    assert nkv <= qk16 < nkv + 16 * 2**20
+    assert dit.dit_attn_workspace_bytes(B, Hq, Hkv, S, S, 5, "bf16", 0, 0) == qk16
+
+
+def test_v_prepass_arguments_rejected_on_host(lib):
+    ws = lib.sage_quantize_v_workspace_bytes(1, 2, 256)
+    assert ws > 0
+    assert lib.sage_quantize_v(FAKE, 1, 2, 256, 2, FAKE, FAKE, FAKE, ws, None) == INVALID  # v_per_tensor not 0/1
+    assert lib.sage_quantize_v(MISALIGNED, 1, 2, 256, 0, FAKE, FAKE, FAKE, ws, None) == INVALID
+    assert lib.sage_quantize_v(FAKE, 1, 2, 0, 0, FAKE, FAKE, FAKE, ws, None) == INVALID
+    assert lib.sage_quantize_v(FAKE, 1, 2, 256, 0, FAKE, FAKE, None, 0, None) == WORKSPACE
+    assert lib.sage_quantize_v(FAKE, 0, 2, 256, 0, FAKE, FAKE, None, 0, None) == 0

@@ -4,6 +4,7 @@ The oracle cannot compute whole outputs at these sizes in seconds, so the checks
 * the SAGE prepass in full: every code and scale bit-exact (quantization is cheap on the CPU);
 * the attention output on sampled whole 128-row query tiles of sampled heads (first tile, last
   tile and seeded random tiles), each computed by the oracle against all Skv keys;
+* QK16PV8: the V codes and the tensor-wide scale bit-exact, and sampled tiles as above;
 * for Skip-Softmax, the skipped-tile counts of the sampled tiles, summed, within 0.5% of the
   oracle's, at every threshold_scale_factor of the sweep.
 Inputs come from the canonical CPU generator with seed 0, the same as the small tests.
@@ -138,3 +139,21 @@ def test_video_skip_sampled_tiles_and_counts(factor):
     assert abs(got_total - want_total) <= max(1, 0.005 * want_total), (got_total, want_total)
     if factor == 0.0:
         assert gc.sum() == 0
+
+
+def test_dit_qk16pv8_32k_v_prepass_bit_exact_and_sampled_tiles():
+    # QK16PV8 with one tensor-wide V scale (the recipe table's block sizes (0, 0, 0)) on the DiT inputs
+    case = _case("dit_qk16pv8_32k")
+    want = sage_quant.qk16pv8_quantize(case.inp["v"], True)
+    got = dit.sage_quantize_v(case.gpu[2], per_tensor=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(got["v_scale"].cpu().numpy().view(np.uint32), want["v_scale"].view(np.uint32))
+    bad = np.count_nonzero(got["v_codes"].cpu().numpy() != want["v_codes"])
+    assert bad == 0, f"{bad} V codes differ"
+    del got
+    out = dit.dit_attn_fwd(*case.gpu, mode=dit.MODE_SAGE | dit.MODE_V_PER_TENSOR, qk_dtype="bf16", q_block=0,
+                           k_block=0)
+    dit.dit_attn_check_errors()
+    for b, h, t in case.sample_tiles():
+        o, _, rows = oatt.attention_q_tile(case.inp, b, h, t, mode="qk16pv8", quant=want)
+        assert _rel(_np(out[b, rows, h]), o) <= SAGE_REL, (b, h, t)
