@@ -9,7 +9,8 @@ namespace ditattn {
 
 constexpr int kHeadDim = 128;
 constexpr int kTile = 128;
-constexpr int kStatsChunk = 256;  // tokens per CTA in the K-mean / V-absmax partial pass
+constexpr int kStatsChunk = 1024;  // tokens per CTA in the K-mean / V-absmax partial pass
+constexpr int kQuantRows = 256;    // tokens per CTA in the quantizers
 
 // Storage formats of the Q/K operands of BMM1 and the V operand of BMM2.
 enum QKFormat { QK_BF16 = 0, QK_F16 = 1, QK_E4M3 = 2 };  // QK_F16: INT8 codes held exactly as fp16

@@ -20,7 +20,7 @@ using namespace ditattn;
 namespace {
 
 // Largest scratch this entry point can use: the partial sums (8 bytes) and maxima (4 bytes) of
-// B * Hkv * ceil(Skv / 256) chunks of 128 channels, each part rounded up to 256 bytes.
+// B * Hkv * ceil(Skv / 1024) chunks of 128 channels, each part rounded up to 256 bytes.
 constexpr size_t kScratchBytes = size_t(32) << 20;  // 32 MiB
 
 static __device__ __align__(256) uint8_t g_prepass_scratch[kScratchBytes];

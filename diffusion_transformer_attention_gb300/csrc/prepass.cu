@@ -11,7 +11,8 @@
 //   * scale = absmax / QMAX (QMAX 127 or 448) and code = f(x / scale), both IEEE float32
 //     divisions (true division, round to nearest); INT8 rounds half to even and clamps to
 //     +-127; E4M3 rounds to nearest even and saturates; an all-zero block has scale 0 and
-//     zero codes.
+//     zero codes. The quotients x / scale are computed from the scale's correctly rounded
+//     reciprocal with one remainder correction (quant_math.cuh), which gives the same codes.
 //
 // Access pattern: a row of one head is 128 bf16 = 256 contiguous bytes; 16 lanes read it with
 // 16-byte vector loads, so a warp covers two rows per instruction. Results are written with
@@ -23,6 +24,7 @@
 #include <cstdint>
 
 #include "ditattn_internal.h"
+#include "quant_math.cuh"
 
 namespace ditattn {
 namespace {
@@ -50,16 +52,32 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   return (uint32_t)r;
 }
 
+// x / scale for a scale whose reciprocal rcp was taken when fast (see quant_math.cuh); 0 for a
+// zero scale.
+__device__ __forceinline__ float quotient(float x, float scale, bool fast, float rcp) {
+  if (fast) return div_by_scale(x, scale, rcp);
+  return (scale == 0.0f) ? 0.0f : __fdiv_rn(x, scale);
+}
+
 __device__ __forceinline__ int int8_code(float q) {
   int c = __float2int_rn(q);  // round half to even
   return max(-127, min(127, c));
 }
 
 // ------------------------------------------------------------------ K mean / V absmax
-// Pass 1: each CTA reduces kStatsChunk tokens of one (batch, kv head): float64 sums of K
-// (WITH_K) and float32 max |V| per channel. Thread t handles channels 8*(t%16).. and tokens
-// t/16 + 16i. The 16 partial rows are then combined in a fixed order, so the result is
-// deterministic.
+// Exact float32 sums of K by exponent bin. A bf16 value has 8 significant bits; 64 values whose
+// float32 exponent fields lie in one 10-wide window [lo, lo + 10) sum to a multiple of
+// 2^(lo - 134) below 2^(lo - 111), i.e. within 23 bits, so a float32 accumulator per window adds
+// them without rounding. Five windows cover |x| in [2^-32, 2^18); anything else that is not zero
+// (including subnormals) is added in float64 directly. GB300's float64 rate is low, so this
+// moves the per-element work to the float32 pipes and leaves a few float64 additions per thread.
+constexpr int kBinLo = 127 - 32, kBinWidth = 10, kBins = 5;
+
+// Pass 1: each CTA reduces kStatsChunk tokens of one (batch, kv head): sums of K (WITH_K) and
+// float32 max |V| per channel. Thread t handles channels 8*(t%16).. and tokens t/16 + 16i (64
+// tokens: the bins above are exact for 64 values). Each thread's sum is the exact sum of its 64
+// values rounded once to float64 (its bins are added smallest first); the 16 partial rows are
+// then combined in a fixed order, so the result is deterministic.
 template <bool WITH_K>
 __global__ void __launch_bounds__(256) kv_stats_partial_kernel(const __nv_bfloat16* __restrict__ k,
                                                                const __nv_bfloat16* __restrict__ v, int Skv, int Hkv,
@@ -67,17 +85,22 @@ __global__ void __launch_bounds__(256) kv_stats_partial_kernel(const __nv_bfloat
                                                                float* __restrict__ pmax) {
   __shared__ double ssum[16][kHeadDim];
   __shared__ float smax[16][kHeadDim];
+  static_assert(kStatsChunk == 1024, "64 tokens per thread: the exponent bins are exact for 64 values");
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int cg = threadIdx.x & 15, tr = threadIdx.x >> 4;
   double s[8];
   float m[8];
+  float acc[8][kBins];
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     s[e] = 0.0;
     m[e] = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kBins; ++k) acc[e][k] = 0.0f;
   }
   const int j0 = chunk * kStatsChunk;
   const int j1 = min(Skv, j0 + kStatsChunk);
+#pragma unroll 4
   for (int j = j0 + tr; j < j1; j += 16) {
     const size_t off = (((size_t)b * Skv + j) * Hkv + h) * kHeadDim + cg * 8;
     float kf[8], vf[8];
@@ -85,13 +108,28 @@ __global__ void __launch_bounds__(256) kv_stats_partial_kernel(const __nv_bfloat
     bf16x8_to_f32(ld_stream_v4(v + off), vf);
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      if constexpr (WITH_K) s[e] += (double)kf[e];
+      if constexpr (WITH_K) {
+        const float x = kf[e];
+        const unsigned d = ((__float_as_uint(x) >> 23) & 0xFFu) - (unsigned)kBinLo;  // wraps below the window
+        if (d < (unsigned)(kBins * kBinWidth)) {
+          const unsigned bin = (d * 205u) >> 11;  // d / 10 for d < 50
+#pragma unroll
+          for (int k = 0; k < kBins; ++k) acc[e][k] += (bin == (unsigned)k) ? x : 0.0f;
+        } else if (x != 0.0f) {
+          s[e] += (double)x;
+        }
+      }
       m[e] = fmaxf(m[e], fabsf(vf[e]));
     }
   }
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    ssum[tr][cg * 8 + e] = s[e];
+    if constexpr (WITH_K) {
+      double t = (double)acc[e][0];
+#pragma unroll
+      for (int k = 1; k < kBins; ++k) t += (double)acc[e][k];
+      ssum[tr][cg * 8 + e] = t + s[e];
+    }
     smax[tr][cg * 8 + e] = m[e];
   }
   __syncthreads();
@@ -150,61 +188,66 @@ __global__ void __launch_bounds__(1024) v_scale_tensor_kernel(float* __restrict_
 }
 
 // E4M3 codes of V / v_scale[b, h, c] (V alone, for QK16PV8): the same arithmetic as the V part of
-// the token-block quantizer. Item i is 8 channels (16 bytes) of row i / 16 = (b * Skv + j) * Hkv + h.
+// the token-block quantizer. A CTA covers kQuantRows tokens of one (batch, kv head); thread t
+// keeps channels 8*(t%16).. (and their scales' reciprocals) over tokens t/16 + 16i.
 __global__ void __launch_bounds__(256) quant_v_kernel(const __nv_bfloat16* __restrict__ v, int Hkv, int Skv,
-                                                      size_t n8, const float* __restrict__ v_scale,
+                                                      const float* __restrict__ v_scale,
                                                       uint8_t* __restrict__ v_codes) {
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
-    const int cg = (int)(i & 15);
-    const size_t row = i >> 4;
-    const int h = (int)(row % (size_t)Hkv);
-    const size_t b = row / ((size_t)Hkv * Skv);
-    const float4* sp = reinterpret_cast<const float4*>(v_scale + (b * Hkv + h) * kHeadDim + cg * 8);
-    const float4 s0 = sp[0], s1 = sp[1];
-    const float vs[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-    float vf[8];
-    bf16x8_to_f32(ld_stream_v4(v + i * 8), vf);
+  const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int cg = threadIdx.x & 15, tr = threadIdx.x >> 4;
+  const float4* sp = reinterpret_cast<const float4*>(v_scale + ((size_t)b * Hkv + h) * kHeadDim + cg * 8);
+  const float4 s0 = sp[0], s1 = sp[1];
+  const float vs[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+  bool fast[8];
+  float rcp[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) vf[e] = (vs[e] == 0.0f) ? 0.0f : __fdiv_rn(vf[e], vs[e]);
+  for (int e = 0; e < 8; ++e) {
+    fast[e] = scale_in_fast_range(vs[e]);
+    rcp[e] = fast[e] ? __frcp_rn(vs[e]) : 0.0f;
+  }
+  const int j0 = chunk * kQuantRows;
+  const int j1 = min(Skv, j0 + kQuantRows);
+#pragma unroll 4
+  for (int j = j0 + tr; j < j1; j += 16) {
+    const size_t off = (((size_t)b * Skv + j) * Hkv + h) * kHeadDim + cg * 8;
+    float vf[8];
+    bf16x8_to_f32(ld_stream_v4(v + off), vf);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) vf[e] = quotient(vf[e], vs[e], fast[e], rcp[e]);
     uint2 w;
     w.x = e4m3x2(vf[0], vf[1]) | (e4m3x2(vf[2], vf[3]) << 16);
     w.y = e4m3x2(vf[4], vf[5]) | (e4m3x2(vf[6], vf[7]) << 16);
-    *reinterpret_cast<uint2*>(v_codes + i * 8) = w;
+    *reinterpret_cast<uint2*>(v_codes + off) = w;
   }
 }
 
 // ------------------------------------------------------------------ token-block quantizer
-// One warp unit covers ROWS = max(QB, 2) consecutive tokens of one (batch, head): two rows per
-// iteration, 16 lanes per row. For QB == 1 each half-warp is its own block; otherwise the whole
-// unit is one block. WITH_V also quantizes V (same rows) with the per-channel v_scale.
-template <int QB, int OUT, bool SMOOTH, bool WITH_V>
-__global__ void __launch_bounds__(256) quant_tokens_kernel(const __nv_bfloat16* __restrict__ x, int B, int S, int H,
+// A CTA covers kQuantRows consecutive tokens of one (batch, head), in warp units of ROWS =
+// max(QB, 2) tokens: two rows per iteration, 16 lanes per row (16-byte loads). For QB == 1 each
+// half-warp is its own block; otherwise the whole unit is one block. SMOOTH subtracts the K mean.
+template <int QB, int OUT, bool SMOOTH>
+__global__ void __launch_bounds__(256) quant_tokens_kernel(const __nv_bfloat16* __restrict__ x, int S, int H,
                                                            const float* __restrict__ mean, void* __restrict__ codes,
-                                                           float* __restrict__ scales, int nblk,
-                                                           const __nv_bfloat16* __restrict__ v,
-                                                           const float* __restrict__ v_scale,
-                                                           uint8_t* __restrict__ v_codes) {
+                                                           float* __restrict__ scales, int nblk) {
   constexpr int ROWS = QB < 2 ? 2 : QB;
   constexpr int IT = ROWS / 2;
+  constexpr int UNITS = kQuantRows / ROWS;  // warp units per CTA
   constexpr float QMAX = (OUT == CODE_E4M3) ? 448.0f : 127.0f;
-  const int lane = threadIdx.x & 31;
+  static_assert(kQuantRows % 16 == 0, "whole blocks per CTA");
+  const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int half = lane >> 4, cg = lane & 15;
-  const int warps_per_cta = blockDim.x >> 5;
-  const long long nrb = (S + ROWS - 1) / ROWS;
-  const long long nunits = (long long)B * nrb * H;
-  for (long long unit = (long long)blockIdx.x * warps_per_cta + (threadIdx.x >> 5); unit < nunits;
-       unit += (long long)gridDim.x * warps_per_cta) {
-    const int h = (int)(unit % H);
-    const long long rest = unit / H;
-    const int rb = (int)(rest % nrb);
-    const int b = (int)(rest / nrb);
-    float mu[8];
-    if constexpr (SMOOTH) {
-      const float4* mp = reinterpret_cast<const float4*>(mean + ((size_t)b * H + h) * kHeadDim + cg * 8);
-      const float4 m0 = mp[0], m1 = mp[1];
-      mu[0] = m0.x; mu[1] = m0.y; mu[2] = m0.z; mu[3] = m0.w;
-      mu[4] = m1.x; mu[5] = m1.y; mu[6] = m1.z; mu[7] = m1.w;
-    }
+  float mu[8];
+  if constexpr (SMOOTH) {
+    const float4* mp = reinterpret_cast<const float4*>(mean + ((size_t)b * H + h) * kHeadDim + cg * 8);
+    const float4 m0 = mp[0], m1 = mp[1];
+    mu[0] = m0.x; mu[1] = m0.y; mu[2] = m0.z; mu[3] = m0.w;
+    mu[4] = m1.x; mu[5] = m1.y; mu[6] = m1.z; mu[7] = m1.w;
+  }
+#pragma unroll 2
+  for (int u = warp; u < UNITS; u += 8) {
+    const int rb = chunk * UNITS + u;  // block of rows (a whole warp unit) within this (b, h)
+    if (rb * ROWS >= S) break;
     float val[IT][8];
     float amax = 0.0f;
 #pragma unroll
@@ -228,6 +271,8 @@ __global__ void __launch_bounds__(256) quant_tokens_kernel(const __nv_bfloat16* 
     for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     if constexpr (QB > 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
     const float scale = __fdiv_rn(amax, QMAX);
+    const bool fast = scale_in_fast_range(scale);
+    const float rcp = fast ? __frcp_rn(scale) : 0.0f;
 #pragma unroll
     for (int it = 0; it < IT; ++it) {
       const int row = rb * ROWS + 2 * it + half;
@@ -235,7 +280,7 @@ __global__ void __launch_bounds__(256) quant_tokens_kernel(const __nv_bfloat16* 
       const size_t off = (((size_t)b * S + row) * H + h) * kHeadDim + cg * 8;
       float q[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) q[e] = (scale == 0.0f) ? 0.0f : __fdiv_rn(val[it][e], scale);
+      for (int e = 0; e < 8; ++e) q[e] = quotient(val[it][e], scale, fast, rcp);
       if constexpr (OUT == CODE_E4M3) {
         uint2 w;
         w.x = e4m3x2(q[0], q[1]) | (e4m3x2(q[2], q[3]) << 16);
@@ -257,19 +302,6 @@ __global__ void __launch_bounds__(256) quant_tokens_kernel(const __nv_bfloat16* 
           w[e] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
         }
         *reinterpret_cast<uint4*>(static_cast<__half*>(codes) + off) = make_uint4(w[0], w[1], w[2], w[3]);
-      }
-      if constexpr (WITH_V) {
-        const float4* sp = reinterpret_cast<const float4*>(v_scale + ((size_t)b * H + h) * kHeadDim + cg * 8);
-        const float4 s0 = sp[0], s1 = sp[1];
-        const float vs[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-        float vf[8];
-        bf16x8_to_f32(ld_stream_v4(v + off), vf);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) vf[e] = (vs[e] == 0.0f) ? 0.0f : __fdiv_rn(vf[e], vs[e]);
-        uint2 w;
-        w.x = e4m3x2(vf[0], vf[1]) | (e4m3x2(vf[2], vf[3]) << 16);
-        w.y = e4m3x2(vf[4], vf[5]) | (e4m3x2(vf[6], vf[7]) << 16);
-        *reinterpret_cast<uint2*>(v_codes + off) = w;
       }
     }
     // scales: one per block; for QB == 1 lane 0 and lane 16 each own a row (= a block)
@@ -307,29 +339,21 @@ int grid_for(long long work_items, int per_cta) {
   return (int)g;
 }
 
-template <int OUT, bool SMOOTH, bool WITH_V>
+template <int OUT, bool SMOOTH>
 cudaError_t launch_quant_tokens(const void* x, int B, int S, int H, int block, const float* mean, void* codes,
-                                float* scales, const void* v, const float* v_scale, void* v_codes,
-                                cudaStream_t stream) {
+                                float* scales, cudaStream_t stream) {
   const int nblk = (S + block - 1) / block;
-  const int rows = block < 2 ? 2 : block;
-  const long long units = (long long)B * ((S + rows - 1) / rows) * H;
-  const int grid = grid_for(units, 8);
+  const dim3 grid((S + kQuantRows - 1) / kQuantRows, H, B);
   auto xb = static_cast<const __nv_bfloat16*>(x);
-  auto vb = static_cast<const __nv_bfloat16*>(v);
-  auto vc = static_cast<uint8_t*>(v_codes);
   switch (block) {
     case 1:
-      quant_tokens_kernel<1, OUT, SMOOTH, WITH_V>
-          <<<grid, 256, 0, stream>>>(xb, B, S, H, mean, codes, scales, nblk, vb, v_scale, vc);
+      quant_tokens_kernel<1, OUT, SMOOTH><<<grid, 256, 0, stream>>>(xb, S, H, mean, codes, scales, nblk);
       break;
     case 4:
-      quant_tokens_kernel<4, OUT, SMOOTH, WITH_V>
-          <<<grid, 256, 0, stream>>>(xb, B, S, H, mean, codes, scales, nblk, vb, v_scale, vc);
+      quant_tokens_kernel<4, OUT, SMOOTH><<<grid, 256, 0, stream>>>(xb, S, H, mean, codes, scales, nblk);
       break;
     case 16:
-      quant_tokens_kernel<16, OUT, SMOOTH, WITH_V>
-          <<<grid, 256, 0, stream>>>(xb, B, S, H, mean, codes, scales, nblk, vb, v_scale, vc);
+      quant_tokens_kernel<16, OUT, SMOOTH><<<grid, 256, 0, stream>>>(xb, S, H, mean, codes, scales, nblk);
       break;
     default:
       return cudaErrorInvalidValue;
@@ -368,9 +392,8 @@ cudaError_t launch_v_stats(const void* v, int B, int Hkv, int Skv, float* pmax, 
 
 cudaError_t launch_quant_v(const void* v, int B, int Hkv, int Skv, const float* v_scale, void* v_codes,
                            cudaStream_t stream) {
-  const size_t n8 = (size_t)B * Skv * Hkv * (kHeadDim / 8);
-  quant_v_kernel<<<grid_for((long long)n8, 256), 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(v), Hkv, Skv,
-                                                                   n8, v_scale, static_cast<uint8_t*>(v_codes));
+  quant_v_kernel<<<dim3((Skv + kQuantRows - 1) / kQuantRows, Hkv, B), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(v), Hkv, Skv, v_scale, static_cast<uint8_t*>(v_codes));
   return cudaGetLastError();
 }
 
@@ -378,14 +401,11 @@ cudaError_t launch_quant_q(const void* q, int B, int Hq, int Sq, int q_block, in
                            float* q_scale, cudaStream_t stream) {
   switch (code_out) {
     case CODE_I8:
-      return launch_quant_tokens<CODE_I8, false, false>(q, B, Sq, Hq, q_block, nullptr, q_codes, q_scale, nullptr,
-                                                        nullptr, nullptr, stream);
+      return launch_quant_tokens<CODE_I8, false>(q, B, Sq, Hq, q_block, nullptr, q_codes, q_scale, stream);
     case CODE_I8_AS_F16:
-      return launch_quant_tokens<CODE_I8_AS_F16, false, false>(q, B, Sq, Hq, q_block, nullptr, q_codes, q_scale,
-                                                               nullptr, nullptr, nullptr, stream);
+      return launch_quant_tokens<CODE_I8_AS_F16, false>(q, B, Sq, Hq, q_block, nullptr, q_codes, q_scale, stream);
     case CODE_E4M3:
-      return launch_quant_tokens<CODE_E4M3, false, false>(q, B, Sq, Hq, q_block, nullptr, q_codes, q_scale, nullptr,
-                                                          nullptr, nullptr, stream);
+      return launch_quant_tokens<CODE_E4M3, false>(q, B, Sq, Hq, q_block, nullptr, q_codes, q_scale, stream);
   }
   return cudaErrorInvalidValue;
 }
@@ -393,18 +413,20 @@ cudaError_t launch_quant_q(const void* q, int B, int Hq, int Sq, int q_block, in
 cudaError_t launch_quant_kv(const void* k, const void* v, int B, int Hkv, int Skv, int k_block, int code_out,
                             const float* k_mean, const float* v_scale, void* k_codes, float* k_scale, void* v_codes,
                             cudaStream_t stream) {
+  cudaError_t e = cudaErrorInvalidValue;
   switch (code_out) {
     case CODE_I8:
-      return launch_quant_tokens<CODE_I8, true, true>(k, B, Skv, Hkv, k_block, k_mean, k_codes, k_scale, v, v_scale,
-                                                      v_codes, stream);
+      e = launch_quant_tokens<CODE_I8, true>(k, B, Skv, Hkv, k_block, k_mean, k_codes, k_scale, stream);
+      break;
     case CODE_I8_AS_F16:
-      return launch_quant_tokens<CODE_I8_AS_F16, true, true>(k, B, Skv, Hkv, k_block, k_mean, k_codes, k_scale, v,
-                                                             v_scale, v_codes, stream);
+      e = launch_quant_tokens<CODE_I8_AS_F16, true>(k, B, Skv, Hkv, k_block, k_mean, k_codes, k_scale, stream);
+      break;
     case CODE_E4M3:
-      return launch_quant_tokens<CODE_E4M3, true, true>(k, B, Skv, Hkv, k_block, k_mean, k_codes, k_scale, v,
-                                                        v_scale, v_codes, stream);
+      e = launch_quant_tokens<CODE_E4M3, true>(k, B, Skv, Hkv, k_block, k_mean, k_codes, k_scale, stream);
+      break;
   }
-  return cudaErrorInvalidValue;
+  if (e != cudaSuccess) return e;
+  return launch_quant_v(v, B, Hkv, Skv, v_scale, v_codes, stream);
 }
 
 cudaError_t launch_widen_i8(const int8_t* codes, size_t n, void* out_f16, cudaStream_t stream) {

@@ -1,0 +1,27 @@
+// Arithmetic shared by the quantize-prepass kernels.
+#pragma once
+#include <cuda_runtime.h>
+
+namespace ditattn {
+
+// Scales for which div_by_scale below gives the codes exactly: for every quotient that can change
+// a code (|x / s| >= 2^-12) the reciprocal, the product and the remainder (a multiple of about
+// 2^(e(s) + e(q) - 47), so at least 2^-147 here) are representable without underflow. Outside
+// this range the kernels divide with __fdiv_rn.
+__device__ __forceinline__ bool scale_in_fast_range(float s) { return s >= 0x1p-88f && s <= 0x1p+120f; }
+
+// x / s rounded to nearest even, given r = RN(1/s) (the correctly rounded reciprocal). Markstein's
+// division theorem (P. Markstein, IBM J. Res. Dev. 34(1), 1990; the division-with-FMA theorem in
+// Muller et al., "Handbook of Floating-Point Arithmetic"): if q is within one ulp of x / s, the
+// remainder x - s * q is exact as one FMA and RN(q + remainder * r) = RN(x / s). The first guess
+// RN(x * r) can be up to two ulps away, so one correction brings it within one ulp and a second
+// one, where the theorem applies, rounds it correctly. It holds when no value underflows. The
+// quantizers only need it for |x / s| >= 2^-12: smaller quotients encode to 0 in every code
+// (INT8 rounds below 0.5 to 0, E4M3 rounds below 2^-10 to 0).
+__device__ __forceinline__ float div_by_scale(float x, float s, float r) {
+  const float q0 = __fmul_rn(x, r);
+  const float q1 = __fmaf_rn(__fmaf_rn(-q0, s, x), r, q0);
+  return __fmaf_rn(__fmaf_rn(-q1, s, x), r, q1);
+}
+
+}  // namespace ditattn

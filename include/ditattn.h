@@ -144,9 +144,9 @@ dit_status sage_quantize_qkv(const void* q, const void* k, const void* v, int B,
  *
  * Inputs, outputs and results are exactly those of sage_quantize_qkv. The scratch for the K-mean
  * and V-absmax partial sums lives in a fixed 32 MiB device array inside the library, which every
- * GPU that loads the library reserves until the process exits. It holds B * Hkv * ceil(Skv/256)
+ * GPU that loads the library reserves until the process exits. It holds B * Hkv * ceil(Skv/1024)
  * chunks of 128 channels at 12 bytes per channel (each of its two parts rounded up to 256 bytes);
- * larger problems return DIT_E_WORKSPACE (e.g. B * Hkv = 40 allows Skv up to about 140,000).
+ * larger problems return DIT_E_WORKSPACE (e.g. B * Hkv = 40 allows Skv up to about 550,000).
  * Nothing here calls cudaMalloc, cudaFree or any allocating routine.
  *
  * The first call on each device looks up the array's device address (a one-time set-up); make

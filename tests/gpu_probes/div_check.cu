@@ -1,0 +1,58 @@
+// Test probe (built by tests/test_gpu_division.py): compares the prepass's reciprocal-based
+// division with IEEE division (__fdiv_rn) bit for bit, for every quotient the quantizers can form
+// (|x / s| <= 448) that can change a code (|x / s| >= 2^-12).
+#include <cuda_runtime.h>
+
+#include "../../diffusion_transformer_attention_gb300/csrc/quant_math.cuh"
+
+__global__ void div_check_kernel(const float* xs, long long nx, const float* ss, int ns, unsigned long long* bad,
+                                 unsigned long long* checked, float* samples) {
+  unsigned long long nb = 0, nc = 0;
+  const long long total = nx * ns;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const float x = xs[i % nx], s = ss[i / nx];
+    if (!ditattn::scale_in_fast_range(s)) continue;
+    const float ref = __fdiv_rn(x, s);
+    // quotients the quantizers form (|x| <= absmax = s * QMAX, so |x / s| <= 448) that can change a code
+    if (!(fabsf(ref) >= 0x1p-12f && fabsf(ref) <= 448.0f)) continue;
+    ++nc;
+    const float q = ditattn::div_by_scale(x, s, __frcp_rn(s));
+    if (__float_as_uint(q) != __float_as_uint(ref)) {
+      ++nb;
+      const unsigned long long slot = atomicAdd(bad + 1, 1ull);  // bad[1]: samples taken so far
+      if (slot < 8) {
+        samples[4 * slot] = x;
+        samples[4 * slot + 1] = s;
+        samples[4 * slot + 2] = q;
+        samples[4 * slot + 3] = ref;
+      }
+    }
+  }
+  atomicAdd(bad, nb);
+  atomicAdd(checked, nc);
+}
+
+// result_host[0] = mismatches, [2] = quotients checked; samples_host: up to 8 (x, s, q, ref) rows.
+extern "C" int div_check(const float* xs_host, long long nx, const float* ss_host, int ns,
+                         unsigned long long* result_host, float* samples_host) {
+  float *xs = nullptr, *ss = nullptr, *smp = nullptr;
+  unsigned long long* res = nullptr;
+  if (cudaMalloc(&xs, nx * sizeof(float)) != cudaSuccess) return 1;
+  if (cudaMalloc(&ss, ns * sizeof(float)) != cudaSuccess) return 1;
+  if (cudaMalloc(&smp, 32 * sizeof(float)) != cudaSuccess) return 1;
+  if (cudaMalloc(&res, 3 * sizeof(unsigned long long)) != cudaSuccess) return 1;
+  cudaMemcpy(xs, xs_host, nx * sizeof(float), cudaMemcpyHostToDevice);
+  cudaMemcpy(ss, ss_host, ns * sizeof(float), cudaMemcpyHostToDevice);
+  cudaMemset(res, 0, 3 * sizeof(unsigned long long));
+  cudaMemset(smp, 0, 32 * sizeof(float));
+  div_check_kernel<<<152 * 8, 256>>>(xs, nx, ss, ns, res, res + 2, smp);
+  const cudaError_t e = cudaDeviceSynchronize();
+  cudaMemcpy(result_host, res, 3 * sizeof(unsigned long long), cudaMemcpyDeviceToHost);
+  cudaMemcpy(samples_host, smp, 32 * sizeof(float), cudaMemcpyDeviceToHost);
+  cudaFree(xs);
+  cudaFree(ss);
+  cudaFree(smp);
+  cudaFree(res);
+  return e == cudaSuccess ? 0 : 2;
+}

@@ -49,7 +49,8 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     t = torch.zeros(256, dtype=torch.uint8, device="cuda")
     p = ctypes.c_void_p(t.data_ptr())
     lib = dit.library()
-    # B * Hkv * ceil(Skv / 256) chunks of 128 channels at 12 bytes each exceed 32 MiB here;
-    # the size check returns before any launch, so the small placeholder buffers are never touched.
-    st = lib.sage_quantize_qkv_noalloc(p, p, p, 1, 64, 64, 1, 200_000, 1, 1, 16, p, p, p, p, p, p, p, None)
+    # B * Hkv * ceil(Skv / 1024) chunks of 128 channels at 12 bytes each (about 77 MB here) exceed
+    # 32 MiB; the size check returns before any launch, so the small placeholder buffers are never
+    # touched.
+    st = lib.sage_quantize_qkv_noalloc(p, p, p, 1, 64, 64, 1, 800_000, 1, 1, 16, p, p, p, p, p, p, p, None)
     assert st == DIT_E_WORKSPACE
