@@ -31,6 +31,13 @@ Readings where the pages are silent:
 * QK16PV8 ("VisualGen Quantized Attention", section "QK16PV8 Attention Kernels in the CUTEDSL
   Backend": Q/K stay BF16, only V is FP8): the dense logits, and P and V exactly as in SAGE
   (the pages give BMM2 the same FP8 path; P's scale and l follow the SAGE readings).
+* LSE ("VisualGen Quantized Attention", section "Requirements and behavior": a backend that
+  produces LSE composes with Attention2D / Ring context parallelism): per query row,
+  ln sum_j exp(s_ij) over the row's logits s as the mode defines them (natural log), i.e.
+  m + ln(l) of the online loop with l summed from the unquantized p; with Skip-Softmax only
+  the kept tiles contribute, as they do to the output. For SAGE these are the logits of the
+  smoothed K, so the LSE is lower by q_i . mu / sqrt(d) than that of the raw logits; partial
+  results that share one mu still merge exactly (the shift is common to a row's shards).
 """
 
 from __future__ import annotations
@@ -75,7 +82,7 @@ def dense_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, rows=None) -> n
     return out
 
 
-def tiled_attention(s: np.ndarray, values: np.ndarray, *, quantize_p: bool, threshold=None):
+def tiled_attention(s: np.ndarray, values: np.ndarray, *, quantize_p: bool, threshold=None, with_lse=False):
     """The online-softmax loop over 128-column KV tiles for one Q tile of one head.
 
     s:      [rows, Skv] float64 scaled logits of the tile's valid rows (rows <= 128).
@@ -83,8 +90,9 @@ def tiled_attention(s: np.ndarray, values: np.ndarray, *, quantize_p: bool, thre
     quantize_p: SAGE re-quantization of P to E4M3 with the static scale 448.
     threshold: None (no skipping) or factor / Skv.
 
-    Returns (acc / l as [rows, 128] float64, number of skipped KV tiles). For SAGE the
-    caller multiplies the result by v_scale per channel.
+    Returns (acc / l as [rows, 128] float64, number of skipped KV tiles), and with ``with_lse``
+    also the rows' log-sum-exp m + ln(l) (float64). For SAGE the caller multiplies the result by
+    v_scale per channel.
     """
     rows, skv = s.shape
     m = np.full(rows, -np.inf)
@@ -107,7 +115,25 @@ def tiled_attention(s: np.ndarray, values: np.ndarray, *, quantize_p: bool, thre
             p = formats.e4m3_decode(formats.e4m3_encode(p * formats.E4M3_MAX)) / formats.E4M3_MAX
         acc = alpha[:, None] * acc + p @ values[t0:t0 + TILE]
         m = m_new
+    if with_lse:
+        return acc / l[:, None], skipped, m + np.log(l)
     return acc / l[:, None], skipped
+
+
+def dense_lse(q: np.ndarray, k: np.ndarray, rows=None) -> np.ndarray:
+    """ln sum_j exp(q_i . k_j / sqrt(d)) in float64, untiled: [B, len(rows) or Sq, Hq]."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    B, Sq, Hq, _ = q.shape
+    Hkv = k.shape[2]
+    idx = np.arange(Sq) if rows is None else np.asarray(rows)
+    out = np.empty((B, len(idx), Hq), dtype=np.float64)
+    for b in range(B):
+        for h in range(Hq):
+            s = SOFTMAX_SCALE * (q[b, idx, h, :] @ k[b, :, kv_head_of(h, Hq, Hkv), :].T)
+            mx = s.max(axis=1)
+            out[b, :, h] = mx + np.log(np.exp(s - mx[:, None]).sum(axis=1))
+    return out
 
 
 def dense_scores(q_rows: np.ndarray, k_head: np.ndarray) -> np.ndarray:
@@ -135,14 +161,15 @@ def sage_scores(qc_rows, kc_head, q_scale_rows, k_scale_cols, qk_dtype: str) -> 
 
 
 def attention_q_tile(inputs: dict, b: int, hq: int, tile: int, *, mode: str, qk_dtype: str = "bf16",
-                     q_block: int = 1, k_block: int = 16, factor=None, quant: dict | None = None):
+                     q_block: int = 1, k_block: int = 16, factor=None, quant: dict | None = None, with_lse=False):
     """Oracle output of one 128-row Q tile of one (batch, query head).
 
     inputs: dict with float32 arrays 'q' [B,Sq,Hq,128], 'k', 'v' [B,Skv,Hkv,128] holding bf16 values.
     mode:   'dense', 'sage' or 'qk16pv8'; ``factor`` switches Skip-Softmax on (threshold = factor / Skv).
     quant:  the output of ``sage_quant.sage_quantize`` (mode 'sage') or ``sage_quant.qk16pv8_quantize``
             (mode 'qk16pv8').
-    Returns (O [rows, 128] float64, skipped tile count, row indices).
+    Returns (O [rows, 128] float64, skipped tile count, row indices), plus the rows' LSE
+    (float64) last when ``with_lse``.
     """
     q, k, v = inputs["q"], inputs["k"], inputs["v"]
     Sq, Hq = q.shape[1], q.shape[2]
@@ -153,18 +180,20 @@ def attention_q_tile(inputs: dict, b: int, hq: int, tile: int, *, mode: str, qk_
     thr = None if factor is None else float(factor) / float(Skv)
     if mode == "dense":
         s = dense_scores(q[b, r0:r1, hq, :], k[b, :, g, :])
-        o, skipped = tiled_attention(s, np.asarray(v[b, :, g, :], np.float64), quantize_p=False, threshold=thr)
-        return o, skipped, rows
-    if mode == "sage":
+        vals, vscale, quantize_p = np.asarray(v[b, :, g, :], np.float64), None, False
+    elif mode == "sage":
         qs_rows = quant["q_scale"][b, hq, rows // q_block]
         ks_cols = quant["k_scale"][b, g, np.arange(Skv) // k_block]
         s = sage_scores(quant["q_codes"][b, r0:r1, hq, :], quant["k_codes"][b, :, g, :], qs_rows, ks_cols, qk_dtype)
-        vals = formats.e4m3_decode(quant["v_codes"][b, :, g, :])
-        o, skipped = tiled_attention(s, vals, quantize_p=True, threshold=thr)
-        return o * np.asarray(quant["v_scale"][b, g, :], np.float64)[None, :], skipped, rows
-    if mode == "qk16pv8":
+        vals, vscale, quantize_p = formats.e4m3_decode(quant["v_codes"][b, :, g, :]), quant["v_scale"][b, g, :], True
+    elif mode == "qk16pv8":
         s = dense_scores(q[b, r0:r1, hq, :], k[b, :, g, :])
-        vals = formats.e4m3_decode(quant["v_codes"][b, :, g, :])
-        o, skipped = tiled_attention(s, vals, quantize_p=True, threshold=thr)
-        return o * np.asarray(quant["v_scale"][b, g, :], np.float64)[None, :], skipped, rows
-    raise ValueError(f"unknown mode {mode!r}")
+        vals, vscale, quantize_p = formats.e4m3_decode(quant["v_codes"][b, :, g, :]), quant["v_scale"][b, g, :], True
+    else:
+        raise ValueError(f"unknown mode {mode!r}")
+    o, skipped, lse = tiled_attention(s, vals, quantize_p=quantize_p, threshold=thr, with_lse=True)
+    if vscale is not None:
+        o = o * np.asarray(vscale, np.float64)[None, :]
+    if with_lse:
+        return o, skipped, rows, lse
+    return o, skipped, rows

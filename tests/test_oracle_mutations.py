@@ -110,8 +110,8 @@ def test_channel_max_used_as_tensor_scale_is_caught(monkeypatch):
 def test_unquantized_p_in_qk16pv8_is_caught(monkeypatch):
     good = att.tiled_attention
     monkeypatch.setattr(att, "tiled_attention",
-                        lambda s, values, quantize_p, threshold=None: good(s, values, quantize_p=False,
-                                                                            threshold=threshold))
+                        lambda s, values, quantize_p, threshold=None, with_lse=False:
+                        good(s, values, quantize_p=False, threshold=threshold, with_lse=with_lse))
     _fails(TP.test_one_row_matches_scalar_definition)
 
 
