@@ -36,6 +36,7 @@ SIGNATURES = {
     "dit_status_string": (ctypes.c_char_p, [_c_int]),
     "dit_attn_workspace_bytes": (_c_size, [_c_int] * 9),
     "dit_attn_fwd": (_c_int, [_vp, _vp, _vp, _vp] + [_c_int] * 9 + [_c_float, _vp, _vp, _c_size, _vp]),
+    "dit_attn_fwd_lse": (_c_int, [_vp] * 5 + [_c_int] * 9 + [_c_float, _vp, _vp, _c_size, _vp]),
     "sage_quantize_workspace_bytes": (_c_size, [_c_int] * 3),
     "sage_quantize_qkv": (_c_int, [_vp, _vp, _vp] + [_c_int] * 8 + [_vp] * 8 + [_c_size, _vp]),
     "sage_quantize_qkv_noalloc": (_c_int, [_vp, _vp, _vp] + [_c_int] * 8 + [_vp] * 7 + [_vp]),
@@ -108,8 +109,9 @@ def dit_attn_workspace_bytes(B, Hq, Hkv, Sq, Skv, mode, qk_dtype, q_block=1, k_b
 
 
 def dit_attn_fwd(q, k, v, out=None, *, mode=MODE_DENSE, qk_dtype="bf16", q_block=1, k_block=16,
-                 threshold_scale_factor=0.0, stream=None, workspace=None, skip_counts=None):
-    """O = softmax(Q K^T / sqrt(128)) V on the GPU; q [B,Sq,Hq,128], k/v [B,Skv,Hkv,128] bf16."""
+                 threshold_scale_factor=0.0, stream=None, workspace=None, skip_counts=None, lse=None):
+    """O = softmax(Q K^T / sqrt(128)) V on the GPU; q [B,Sq,Hq,128], k/v [B,Skv,Hkv,128] bf16.
+    ``lse``: an optional float32 [B, Hq, Sq] tensor that receives each row's log-sum-exp."""
     B, Hq, Hkv, Sq, Skv = _shape(q, k)
     if out is None:
         out = torch.empty_like(q)
@@ -118,10 +120,16 @@ def dit_attn_fwd(q, k, v, out=None, *, mode=MODE_DENSE, qk_dtype="bf16", q_block
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = _lib().dit_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, Sq, Skv, mode, qk, q_block, k_block,
-                             float(threshold_scale_factor), _stream(stream), _ptr(workspace), ws_bytes,
-                             _ptr(skip_counts))
-    _check(st, "dit_attn_fwd")
+    if lse is None:
+        st = _lib().dit_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, Sq, Skv, mode, qk, q_block,
+                                 k_block, float(threshold_scale_factor), _stream(stream), _ptr(workspace), ws_bytes,
+                                 _ptr(skip_counts))
+        _check(st, "dit_attn_fwd")
+    else:
+        st = _lib().dit_attn_fwd_lse(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Skv, mode, qk,
+                                     q_block, k_block, float(threshold_scale_factor), _stream(stream),
+                                     _ptr(workspace), ws_bytes, _ptr(skip_counts))
+        _check(st, "dit_attn_fwd_lse")
     return out
 
 

@@ -164,8 +164,8 @@ dit_status from_cuda(cudaError_t e) {
 dit_status run_attention(const void* q, const void* k, const void* v, void* out, CUtensorMapDataType qk_dt,
                          int qk_esize, int qk_format, int pv_format, int B, int Hq, int Hkv, int Sq, int Skv,
                          int mode, int q_block, int k_block, float factor, const float* q_scale,
-                         const float* k_scale, const float* v_scale, int32_t* skip_counts, int* err,
-                         cudaStream_t stream) {
+                         const float* k_scale, const float* v_scale, int32_t* skip_counts, float* lse,
+                         int* err, cudaStream_t stream) {
   CUtensorMap tq, tk, tv, to;
   const CUtensorMapDataType pv_dt =
       (pv_format == PV_BF16) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
@@ -186,6 +186,7 @@ dit_status run_attention(const void* q, const void* k, const void* v, void* out,
   p.k_scale = k_scale; p.k_block = k_block; p.nkb = ceil_div(Skv, k_block);
   p.v_scale = v_scale;
   p.skip_counts = skip_counts;
+  p.lse = lse;
   p.err = err;
   p.wait_budget_ns = kWaitBudgetNs;
   return from_cuda(launch_fmha(qk_format, pv_format, skip, tq, tk, tv, to, p, stream));
@@ -216,14 +217,19 @@ size_t dit_attn_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int mod
   return sage_layout(B, Hq, Hkv, Sq, Skv, qk_dtype, q_block, k_block).total;
 }
 
-dit_status dit_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv, int Sq,
-                        int Skv, int mode, int qk_dtype, int q_block, int k_block, float threshold_scale_factor,
-                        void* stream, void* workspace, size_t workspace_bytes, int32_t* skip_counts) {
+}  // extern "C"
+
+namespace {
+
+// dit_attn_fwd and dit_attn_fwd_lse (lse may be NULL).
+dit_status fwd_impl(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv, int Sq, int Skv,
+                    int mode, int qk_dtype, int q_block, int k_block, float threshold_scale_factor, void* stream,
+                    void* workspace, size_t workspace_bytes, int32_t* skip_counts, float* lse) {
   if (!valid_shape(B, Hq, Hkv, Sq, Skv) || !valid_mode(mode, qk_dtype, q_block, k_block, threshold_scale_factor))
     return DIT_E_INVALID_ARG;
   if (B == 0 || Sq == 0) return DIT_OK;
   if (!q || !k || !v || !out || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
-      !aligned16(skip_counts))
+      !aligned16(skip_counts) || (reinterpret_cast<uintptr_t>(lse) & 3u))
     return DIT_E_INVALID_ARG;
   const bool sage = (mode & DIT_MODE_SAGE) != 0;
   SageLayout L{};
@@ -238,7 +244,7 @@ dit_status dit_attn_fwd(const void* q, const void* k, const void* v, void* out, 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (!sage)
     return run_attention(q, k, v, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, QK_BF16, PV_BF16, B, Hq, Hkv, Sq, Skv,
-                         mode, 1, 1, threshold_scale_factor, nullptr, nullptr, nullptr, skip_counts, err, st);
+                         mode, 1, 1, threshold_scale_factor, nullptr, nullptr, nullptr, skip_counts, lse, err, st);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   if (qk_dtype == DIT_QK_BF16) {
     // QK16PV8: V scales (per channel or one tensor-wide) and V codes; Q/K go to BMM1 as they are
@@ -249,7 +255,7 @@ dit_status dit_attn_fwd(const void* q, const void* k, const void* v, void* out, 
     if (e != cudaSuccess) return from_cuda(e);
     return run_attention(q, k, ws + L.v_codes, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, QK_BF16, PV_E4M3, B, Hq,
                          Hkv, Sq, Skv, mode, 1, 1, threshold_scale_factor, nullptr, nullptr, v_scale, skip_counts,
-                         err, st);
+                         lse, err, st);
   }
   float* q_scale = reinterpret_cast<float*>(ws + L.q_scale);
   float* k_scale = reinterpret_cast<float*>(ws + L.k_scale);
@@ -267,7 +273,27 @@ dit_status dit_attn_fwd(const void* q, const void* k, const void* v, void* out, 
   return run_attention(ws + L.q_codes, ws + L.k_codes, ws + L.v_codes, out,
                        i8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, i8 ? 2 : 1,
                        i8 ? QK_F16 : QK_E4M3, PV_E4M3, B, Hq, Hkv, Sq, Skv, mode, q_block, k_block,
-                       threshold_scale_factor, q_scale, k_scale, v_scale, skip_counts, err, st);
+                       threshold_scale_factor, q_scale, k_scale, v_scale, skip_counts, lse, err, st);
+}
+
+}  // namespace
+
+extern "C" {
+
+dit_status dit_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv, int Sq,
+                        int Skv, int mode, int qk_dtype, int q_block, int k_block, float threshold_scale_factor,
+                        void* stream, void* workspace, size_t workspace_bytes, int32_t* skip_counts) {
+  return fwd_impl(q, k, v, out, B, Hq, Hkv, Sq, Skv, mode, qk_dtype, q_block, k_block, threshold_scale_factor, stream,
+                  workspace, workspace_bytes, skip_counts, nullptr);
+}
+
+dit_status dit_attn_fwd_lse(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
+                            int Hkv, int Sq, int Skv, int mode, int qk_dtype, int q_block, int k_block,
+                            float threshold_scale_factor, void* stream, void* workspace, size_t workspace_bytes,
+                            int32_t* skip_counts) {
+  if (lse == nullptr) return DIT_E_INVALID_ARG;
+  return fwd_impl(q, k, v, out, B, Hq, Hkv, Sq, Skv, mode, qk_dtype, q_block, k_block, threshold_scale_factor, stream,
+                  workspace, workspace_bytes, skip_counts, lse);
 }
 
 size_t sage_quantize_workspace_bytes(int B, int Hkv, int Skv) {
@@ -374,10 +400,11 @@ dit_status dit_attn_fwd_quantized(const void* q_codes, const void* k_codes, cons
   }
   if (qk16)
     return run_attention(qa, ka, v_codes, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, QK_BF16, PV_E4M3, B, Hq, Hkv, Sq,
-                         Skv, mode, 1, 1, threshold_scale_factor, nullptr, nullptr, v_scale, skip_counts, err, st);
+                         Skv, mode, 1, 1, threshold_scale_factor, nullptr, nullptr, v_scale, skip_counts, nullptr, err,
+                         st);
   return run_attention(qa, ka, v_codes, out, i8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
                        i8 ? 2 : 1, i8 ? QK_F16 : QK_E4M3, PV_E4M3, B, Hq, Hkv, Sq, Skv, mode, q_block, k_block,
-                       threshold_scale_factor, q_scale, k_scale, v_scale, skip_counts, err, st);
+                       threshold_scale_factor, q_scale, k_scale, v_scale, skip_counts, nullptr, err, st);
 }
 
 dit_status dit_attn_check_errors(void* stream) {

@@ -35,6 +35,7 @@ struct FmhaParams {
   int k_block, nkb;
   const float* v_scale;  // E4M3 V (SAGE, QK16PV8): [B, Hkv, 128]
   int32_t* skip_counts;  // optional [B, Hq, n_q_tiles]
+  float* lse;            // optional [B, Hq, Sq]: ln sum_j exp(s_ij) of each query row
   int* err;              // device error word
   unsigned long long wait_budget_ns;
 };

@@ -607,6 +607,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     xl[(i * 2 + h) * 128 + r] = l;
     named_bar_sync(tile_bar, 256);
     const float l_row = xl[(i * 2 + 0) * 128 + r] + xl[(i * 2 + 1) * 128 + r];
+    if (p.lse != nullptr && h == 0 && row_valid && ok) {
+      // ln sum_j exp(s_j) = ln 2 * (m_ref + log2 l), with l relative to m_ref (and carrying P's 448
+      // with E4M3 P); only the kept KV tiles contribute under Skip-Softmax, as to the output
+      const float l_true = kPV8 ? l_row * (1.0f / 448.0f) : l_row;
+      p.lse[((size_t)b * p.Hq + hq) * p.Sq + qrow] = 0.69314718055994531f * (m_ref + log2f(l_true));
+    }
     if (ok) {
       ok = mbar_wait_bounded(&bars->o_full[i], 0, budget, abort_flag);
       if constexpr (kPV8) ok = ok && mbar_wait_bounded(&bars->vs_full, 0, budget, abort_flag);

@@ -69,7 +69,7 @@ enum { DIT_QK_BF16 = 0, DIT_QK_INT8 = 1, DIT_QK_FP8_E4M3 = 2 };
 /* Rows and columns of one attention tile; skip counts are kept per 128-row Q tile. */
 enum { DIT_HEAD_DIM = 128, DIT_TILE = 128 };
 
-/* Version of this interface (2: QK16PV8, DIT_MODE_V_PER_TENSOR and sage_quantize_v). */
+/* Version of this interface (2: QK16PV8, DIT_MODE_V_PER_TENSOR, sage_quantize_v, dit_attn_fwd_lse). */
 int dit_abi_version(void);
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -109,6 +109,22 @@ size_t dit_attn_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int mod
 dit_status dit_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv, int Sq,
                         int Skv, int mode, int qk_dtype, int q_block, int k_block, float threshold_scale_factor,
                         void* stream, void* workspace, size_t workspace_bytes, int32_t* skip_counts);
+
+/*
+ * dit_attn_fwd that also writes each query row's log-sum-exp, for combining partial results
+ * across devices ("VisualGen Quantized Attention", section "Requirements and behavior": a backend
+ * that produces LSE composes with Attention2D / Ring context parallelism).
+ *
+ *   lse   device float [B, Hq, Sq], 4-byte aligned, not NULL: ln sum_j exp(s_ij) over the row's
+ *         logits s_ij as the mode computes them (softmax scale applied; SAGE: from the codes and
+ *         scales of the K-smoothed K, so lower by q_i . mean / sqrt(128) than for the raw K; with
+ *         SKIP only the KV tiles that were not skipped contribute)
+ * All other arguments, results and errors are those of dit_attn_fwd.
+ */
+dit_status dit_attn_fwd_lse(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
+                            int Hkv, int Sq, int Skv, int mode, int qk_dtype, int q_block, int k_block,
+                            float threshold_scale_factor, void* stream, void* workspace, size_t workspace_bytes,
+                            int32_t* skip_counts);
 
 /* Bytes of device scratch sage_quantize_qkv needs (the K-mean / V-absmax partials). */
 size_t sage_quantize_workspace_bytes(int B, int Hkv, int Skv);

@@ -36,7 +36,7 @@ def _declared_functions():
 def test_header_declares_the_boundary():
     names = _declared_functions()
     for required in ["dit_attn_fwd", "sage_quantize_qkv", "dit_attn_workspace_bytes", "dit_attn_fwd_quantized",
-                     "dit_attn_check_errors", "dit_status_string"]:
+                     "dit_attn_check_errors", "dit_status_string", "dit_attn_fwd_lse", "sage_quantize_v"]:
         assert required in names
 
 
@@ -80,6 +80,14 @@ def _fwd(lib, q=FAKE, B=1, Hq=4, Hkv=2, Sq=256, Skv=256, mode=0, qk=0, qb=1, kb=
 ])
 def test_invalid_arguments_rejected_on_host(lib, kw):
     assert _fwd(lib, **kw) == INVALID
+
+
+def test_lse_entry_rejects_missing_or_misaligned_lse(lib):
+    def fwd_lse(lse):
+        return lib.dit_attn_fwd_lse(FAKE, FAKE, FAKE, FAKE, lse, 1, 4, 2, 256, 256, 0, 0, 1, 16, 0.0, None, None, 0,
+                                    None)
+    assert fwd_lse(None) == INVALID
+    assert fwd_lse(ctypes.c_void_p((1 << 20) + 2)) == INVALID
 
 
 def test_empty_problem_is_a_noop(lib):
