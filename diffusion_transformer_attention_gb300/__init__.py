@@ -44,6 +44,8 @@ SIGNATURES = {
     "sage_quantize_v": (_c_int, [_vp] + [_c_int] * 4 + [_vp, _vp, _vp, _c_size, _vp]),
     "dit_attn_quantized_workspace_bytes": (_c_size, [_c_int] * 6),
     "dit_attn_fwd_quantized": (_c_int, [_vp] * 7 + [_c_int] * 9 + [_c_float, _vp, _vp, _c_size, _vp]),
+    "dit_attn_fwd_quantized_lse": (_c_int, [_vp] * 8 + [_c_int] * 9 + [_c_float, _vp, _vp, _c_size, _vp]),
+    "sage_quantize_qkv_with_mean": (_c_int, [_vp] * 4 + [_c_int] * 8 + [_vp] * 7 + [_c_size, _vp]),
     "dit_attn_check_errors": (_c_int, [_vp]),
 }
 
@@ -137,8 +139,11 @@ def sage_quantize_workspace_bytes(B, Hkv, Skv) -> int:
     return int(_lib().sage_quantize_workspace_bytes(B, Hkv, Skv))
 
 
-def sage_quantize_qkv(q, k, v, *, qk_dtype="int8", q_block=1, k_block=16, stream=None, workspace=None):
-    """The SAGE prepass alone; returns a dict of codes (uint8 views of the 1-byte codes) and scales."""
+def sage_quantize_qkv(q, k, v, *, qk_dtype="int8", q_block=1, k_block=16, stream=None, workspace=None,
+                      k_mean=None):
+    """The SAGE prepass alone; returns a dict of codes (uint8 views of the 1-byte codes) and scales.
+    ``k_mean`` (float32 [B, Hkv, 128]) smooths K with that mean instead of its own (the global-mean
+    option for a K split across devices); it is then returned as given."""
     B, Hq, Hkv, Sq, Skv = _shape(q, k)
     dev = q.device
     code_t = torch.int8 if _qk(qk_dtype) == QK_INT8 else torch.uint8
@@ -151,6 +156,18 @@ def sage_quantize_qkv(q, k, v, *, qk_dtype="int8", q_block=1, k_block=16, stream
         v_scale=torch.empty((B, Hkv, HEAD_DIM), dtype=torch.float32, device=dev),
         k_mean=torch.empty((B, Hkv, HEAD_DIM), dtype=torch.float32, device=dev),
     )
+    if k_mean is not None:
+        res["k_mean"] = k_mean
+        need = _lib().sage_quantize_v_workspace_bytes(B, Hkv, Skv)
+        if workspace is None:
+            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+        st = _lib().sage_quantize_qkv_with_mean(_ptr(q), _ptr(k), _ptr(v), _ptr(k_mean), B, Hq, Hkv, Sq, Skv,
+                                                _qk(qk_dtype), q_block, k_block, _ptr(res["q_codes"]),
+                                                _ptr(res["k_codes"]), _ptr(res["v_codes"]), _ptr(res["q_scale"]),
+                                                _ptr(res["k_scale"]), _ptr(res["v_scale"]), _ptr(workspace),
+                                                workspace.numel(), _stream(stream))
+        _check(st, "sage_quantize_qkv_with_mean")
+        return res
     need = _lib().sage_quantize_workspace_bytes(B, Hkv, Skv)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
@@ -196,7 +213,7 @@ def sage_quantize_v(v, *, per_tensor=False, stream=None, workspace=None):
 
 
 def dit_attn_fwd_quantized(quant: dict, out, *, mode=MODE_SAGE, qk_dtype="int8", q_block=1, k_block=16,
-                           threshold_scale_factor=0.0, stream=None, workspace=None, skip_counts=None):
+                           threshold_scale_factor=0.0, stream=None, workspace=None, skip_counts=None, lse=None):
     """Attention over the codes and scales that ``sage_quantize_qkv`` returned. For QK16PV8
     (``qk_dtype="bf16"``, blocks 0) ``quant`` holds the BF16 Q and K as ``q_codes`` / ``k_codes``
     and the result of ``sage_quantize_v``; it needs no Q/K scales."""
@@ -208,11 +225,18 @@ def dit_attn_fwd_quantized(quant: dict, out, *, mode=MODE_SAGE, qk_dtype="int8",
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=qc.device)
     ws_bytes = 0 if workspace is None else workspace.numel()
-    st = _lib().dit_attn_fwd_quantized(_ptr(qc), _ptr(kc), _ptr(quant["v_codes"]), _ptr(quant.get("q_scale")),
-                                       _ptr(quant.get("k_scale")), _ptr(quant["v_scale"]), _ptr(out), B, Hq, Hkv, Sq,
-                                       Skv, mode, qk, q_block, k_block, float(threshold_scale_factor),
-                                       _stream(stream), _ptr(workspace), ws_bytes, _ptr(skip_counts))
-    _check(st, "dit_attn_fwd_quantized")
+    scales = (_ptr(quant.get("q_scale")), _ptr(quant.get("k_scale")), _ptr(quant["v_scale"]))
+    if lse is None:
+        st = _lib().dit_attn_fwd_quantized(_ptr(qc), _ptr(kc), _ptr(quant["v_codes"]), *scales, _ptr(out), B, Hq, Hkv,
+                                           Sq, Skv, mode, qk, q_block, k_block, float(threshold_scale_factor),
+                                           _stream(stream), _ptr(workspace), ws_bytes, _ptr(skip_counts))
+        _check(st, "dit_attn_fwd_quantized")
+    else:
+        st = _lib().dit_attn_fwd_quantized_lse(_ptr(qc), _ptr(kc), _ptr(quant["v_codes"]), *scales, _ptr(out),
+                                               _ptr(lse), B, Hq, Hkv, Sq, Skv, mode, qk, q_block, k_block,
+                                               float(threshold_scale_factor), _stream(stream), _ptr(workspace),
+                                               ws_bytes, _ptr(skip_counts))
+        _check(st, "dit_attn_fwd_quantized_lse")
     return out
 
 

@@ -330,6 +330,33 @@ dit_status sage_quantize_qkv(const void* q, const void* k, const void* v, int B,
   return from_cuda(e);
 }
 
+dit_status sage_quantize_qkv_with_mean(const void* q, const void* k, const void* v, const float* k_mean, int B,
+                                       int Hq, int Hkv, int Sq, int Skv, int qk_dtype, int q_block, int k_block,
+                                       void* q_codes, void* k_codes, void* v_codes, float* q_scale, float* k_scale,
+                                       float* v_scale, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!valid_shape(B, Hq, Hkv, Sq, Skv) || qk_dtype == DIT_QK_BF16 ||
+      !valid_mode(DIT_MODE_SAGE, qk_dtype, q_block, k_block, 0.0f))
+    return DIT_E_INVALID_ARG;
+  if (B == 0) return DIT_OK;
+  const void* ptrs[] = {k, v, k_mean, k_codes, v_codes, k_scale, v_scale};
+  for (const void* ptr : ptrs)
+    if (!ptr || !aligned16(ptr)) return DIT_E_INVALID_ARG;
+  if (Sq > 0 && (!q || !q_codes || !q_scale || !aligned16(q) || !aligned16(q_codes))) return DIT_E_INVALID_ARG;
+  const size_t need = align256((size_t)B * Hkv * stats_chunks(Skv) * kHeadDim * 4);
+  if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return DIT_E_WORKSPACE;
+  int* err = nullptr;
+  const dit_status ds = prepare_device(&err);
+  if (ds != DIT_OK) return ds;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int code_out = (qk_dtype == DIT_QK_INT8) ? CODE_I8 : CODE_E4M3;
+  cudaError_t e = launch_v_stats(v, B, Hkv, Skv, static_cast<float*>(workspace), v_scale, false, st);
+  if (e == cudaSuccess && Sq > 0) e = launch_quant_q(q, B, Hq, Sq, q_block, code_out, q_codes, q_scale, st);
+  if (e == cudaSuccess)
+    e = launch_quant_kv(k, v, B, Hkv, Skv, k_block, code_out, k_mean, v_scale, k_codes, k_scale, v_codes, st);
+  return from_cuda(e);
+}
+
 size_t sage_quantize_v_workspace_bytes(int B, int Hkv, int Skv) {
   if (B < 0 || Hkv < 1 || Skv < 1) return 0;
   return align256((size_t)B * Hkv * stats_chunks(Skv) * kHeadDim * 4);
@@ -360,11 +387,16 @@ size_t dit_attn_quantized_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk
   return align256((size_t)B * Sq * Hq * kHeadDim * 2) + align256((size_t)B * Skv * Hkv * kHeadDim * 2);
 }
 
-dit_status dit_attn_fwd_quantized(const void* q_codes, const void* k_codes, const void* v_codes,
-                                  const float* q_scale, const float* k_scale, const float* v_scale, void* out, int B,
-                                  int Hq, int Hkv, int Sq, int Skv, int mode, int qk_dtype, int q_block, int k_block,
-                                  float threshold_scale_factor, void* stream, void* workspace,
-                                  size_t workspace_bytes, int32_t* skip_counts) {
+}  // extern "C"
+
+namespace {
+
+// dit_attn_fwd_quantized and dit_attn_fwd_quantized_lse (lse may be NULL).
+dit_status fwd_quantized_impl(const void* q_codes, const void* k_codes, const void* v_codes, const float* q_scale,
+                              const float* k_scale, const float* v_scale, void* out, int B, int Hq, int Hkv, int Sq,
+                              int Skv, int mode, int qk_dtype, int q_block, int k_block, float threshold_scale_factor,
+                              void* stream, void* workspace, size_t workspace_bytes, int32_t* skip_counts,
+                              float* lse) {
   if (!valid_shape(B, Hq, Hkv, Sq, Skv) || !(mode & DIT_MODE_SAGE) ||
       !valid_mode(mode, qk_dtype, q_block, k_block, threshold_scale_factor))
     return DIT_E_INVALID_ARG;
@@ -375,7 +407,7 @@ dit_status dit_attn_fwd_quantized(const void* q_codes, const void* k_codes, cons
     if (!ptr) return DIT_E_INVALID_ARG;
   if (!qk16 && (!q_scale || !k_scale)) return DIT_E_INVALID_ARG;
   if (!aligned16(q_codes) || !aligned16(k_codes) || !aligned16(v_codes) || !aligned16(out) ||
-      !aligned16(skip_counts))
+      !aligned16(skip_counts) || (reinterpret_cast<uintptr_t>(lse) & 3u))
     return DIT_E_INVALID_ARG;
   const bool i8 = (qk_dtype == DIT_QK_INT8);
   const size_t need = dit_attn_quantized_workspace_bytes(B, Hq, Hkv, Sq, Skv, qk_dtype);
@@ -400,11 +432,35 @@ dit_status dit_attn_fwd_quantized(const void* q_codes, const void* k_codes, cons
   }
   if (qk16)
     return run_attention(qa, ka, v_codes, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, QK_BF16, PV_E4M3, B, Hq, Hkv, Sq,
-                         Skv, mode, 1, 1, threshold_scale_factor, nullptr, nullptr, v_scale, skip_counts, nullptr, err,
-                         st);
+                         Skv, mode, 1, 1, threshold_scale_factor, nullptr, nullptr, v_scale, skip_counts, lse, err, st);
   return run_attention(qa, ka, v_codes, out, i8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
                        i8 ? 2 : 1, i8 ? QK_F16 : QK_E4M3, PV_E4M3, B, Hq, Hkv, Sq, Skv, mode, q_block, k_block,
-                       threshold_scale_factor, q_scale, k_scale, v_scale, skip_counts, nullptr, err, st);
+                       threshold_scale_factor, q_scale, k_scale, v_scale, skip_counts, lse, err, st);
+}
+
+}  // namespace
+
+extern "C" {
+
+dit_status dit_attn_fwd_quantized(const void* q_codes, const void* k_codes, const void* v_codes,
+                                  const float* q_scale, const float* k_scale, const float* v_scale, void* out, int B,
+                                  int Hq, int Hkv, int Sq, int Skv, int mode, int qk_dtype, int q_block, int k_block,
+                                  float threshold_scale_factor, void* stream, void* workspace,
+                                  size_t workspace_bytes, int32_t* skip_counts) {
+  return fwd_quantized_impl(q_codes, k_codes, v_codes, q_scale, k_scale, v_scale, out, B, Hq, Hkv, Sq, Skv, mode,
+                            qk_dtype, q_block, k_block, threshold_scale_factor, stream, workspace, workspace_bytes,
+                            skip_counts, nullptr);
+}
+
+dit_status dit_attn_fwd_quantized_lse(const void* q_codes, const void* k_codes, const void* v_codes,
+                                      const float* q_scale, const float* k_scale, const float* v_scale, void* out,
+                                      float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int mode, int qk_dtype,
+                                      int q_block, int k_block, float threshold_scale_factor, void* stream,
+                                      void* workspace, size_t workspace_bytes, int32_t* skip_counts) {
+  if (lse == nullptr) return DIT_E_INVALID_ARG;
+  return fwd_quantized_impl(q_codes, k_codes, v_codes, q_scale, k_scale, v_scale, out, B, Hq, Hkv, Sq, Skv, mode,
+                            qk_dtype, q_block, k_block, threshold_scale_factor, stream, workspace, workspace_bytes,
+                            skip_counts, lse);
 }
 
 dit_status dit_attn_check_errors(void* stream) {

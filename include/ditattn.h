@@ -69,7 +69,8 @@ enum { DIT_QK_BF16 = 0, DIT_QK_INT8 = 1, DIT_QK_FP8_E4M3 = 2 };
 /* Rows and columns of one attention tile; skip counts are kept per 128-row Q tile. */
 enum { DIT_HEAD_DIM = 128, DIT_TILE = 128 };
 
-/* Version of this interface (2: QK16PV8, DIT_MODE_V_PER_TENSOR, sage_quantize_v, dit_attn_fwd_lse). */
+/* Version of this interface (2: QK16PV8, DIT_MODE_V_PER_TENSOR, sage_quantize_v, the LSE outputs and
+ * sage_quantize_qkv_with_mean). */
 int dit_abi_version(void);
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -153,6 +154,23 @@ dit_status sage_quantize_qkv(const void* q, const void* k, const void* v, int B,
                              size_t workspace_bytes, void* stream);
 
 /*
+ * sage_quantize_qkv with a given K mean instead of this K's own: the global-mean option for a K
+ * split across devices (context parallelism). Every shard smoothed with the mean of the whole
+ * sequence gets logits shifted by the same q_i . mean / sqrt(128), so the shards' LSEs
+ * (dit_attn_fwd_quantized_lse) share the shift and their partial outputs merge exactly as
+ * O = sum_s exp(lse_s - lse) O_s with lse = ln sum_s exp(lse_s).
+ *
+ *   k_mean     device float [B, Hkv, 128], 16-byte aligned, read only (e.g. the all-reduced
+ *              sums of K over every shard divided by the total token count)
+ *   workspace  device scratch of sage_quantize_v_workspace_bytes(B, Hkv, Skv) bytes
+ * Everything else is as for sage_quantize_qkv (INT8 or FP8 E4M3 only), minus the k_mean output.
+ */
+dit_status sage_quantize_qkv_with_mean(const void* q, const void* k, const void* v, const float* k_mean, int B,
+                                       int Hq, int Hkv, int Sq, int Skv, int qk_dtype, int q_block, int k_block,
+                                       void* q_codes, void* k_codes, void* v_codes, float* q_scale, float* k_scale,
+                                       float* v_scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * sage_quantize_qkv without a workspace argument, for callers that cannot allocate device memory
  * when they call: for example a plugin whose host framework owns the whole device memory pool and
  * gives it no allocator, or a latency-critical loop where cudaMalloc (which may synchronize the
@@ -207,6 +225,13 @@ dit_status dit_attn_fwd_quantized(const void* q_codes, const void* k_codes, cons
                                   int Hq, int Hkv, int Sq, int Skv, int mode, int qk_dtype, int q_block, int k_block,
                                   float threshold_scale_factor, void* stream, void* workspace,
                                   size_t workspace_bytes, int32_t* skip_counts);
+
+/* dit_attn_fwd_quantized that also writes each query row's LSE, as dit_attn_fwd_lse does. */
+dit_status dit_attn_fwd_quantized_lse(const void* q_codes, const void* k_codes, const void* v_codes,
+                                      const float* q_scale, const float* k_scale, const float* v_scale, void* out,
+                                      float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int mode, int qk_dtype,
+                                      int q_block, int k_block, float threshold_scale_factor, void* stream,
+                                      void* workspace, size_t workspace_bytes, int32_t* skip_counts);
 
 /*
  * Synchronizes `stream`, then reports and clears the device error word: DIT_OK, or

@@ -132,12 +132,17 @@ def qk16pv8_quantize(v: np.ndarray, per_tensor: bool) -> dict:
     return dict(v_codes=v_codes, v_scale=v_scale)
 
 
-def sage_quantize(q: np.ndarray, k: np.ndarray, v: np.ndarray, qk_dtype: str, q_block: int, k_block: int) -> dict:
+def sage_quantize(q: np.ndarray, k: np.ndarray, v: np.ndarray, qk_dtype: str, q_block: int, k_block: int,
+                  k_mean: np.ndarray | None = None) -> dict:
     """The whole SAGE prepass: K mean, smoothed K, Q/K token-block codes and scales, V codes.
 
-    Inputs are bf16 values held in float32 arrays of shape [B, S, H, 128].
+    Inputs are bf16 values held in float32 arrays of shape [B, S, H, 128]. ``k_mean`` (float32
+    [B, H, 128]) replaces the mean of this K: the global-mean option for a K split across
+    devices, where every shard is smoothed with the mean of the whole sequence so that the shards'
+    LSEs share one shift and their partial results merge ("VisualGen Quantized Attention", section
+    "Requirements and behavior": Attention2D / Ring context parallelism needs LSE).
     """
-    k_mean = k_channel_mean(k)
+    k_mean = k_channel_mean(k) if k_mean is None else np.asarray(k_mean, dtype=np.float32)
     ks = smooth_k(k, k_mean)
     q_codes, q_scale = quantize_token_blocks(q, q_block, qk_dtype)
     k_codes, k_scale = quantize_token_blocks(ks, k_block, qk_dtype)

@@ -164,3 +164,12 @@ def test_v_prepass_arguments_rejected_on_host(lib):
     assert lib.sage_quantize_v(FAKE, 1, 2, 0, 0, FAKE, FAKE, FAKE, ws, None) == INVALID
     assert lib.sage_quantize_v(FAKE, 1, 2, 256, 0, FAKE, FAKE, None, 0, None) == WORKSPACE
     assert lib.sage_quantize_v(FAKE, 0, 2, 256, 0, FAKE, FAKE, None, 0, None) == 0
+
+
+def test_with_mean_prepass_rejects_bf16_and_missing_mean(lib):
+    ws = lib.sage_quantize_v_workspace_bytes(1, 2, 256)
+    args = lambda mean, qk: (FAKE, FAKE, FAKE, mean, 1, 4, 2, 256, 256, qk, 1, 16, FAKE, FAKE, FAKE, FAKE, FAKE,  # noqa
+                             FAKE, FAKE, ws, None)
+    assert lib.sage_quantize_qkv_with_mean(*args(None, 1)) == INVALID
+    assert lib.sage_quantize_qkv_with_mean(*args(FAKE, 0)) == INVALID   # BF16 Q/K has no K mean to smooth with
+    assert lib.sage_quantize_qkv_with_mean(*args(MISALIGNED, 2)) == INVALID
