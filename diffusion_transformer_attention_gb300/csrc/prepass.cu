@@ -37,6 +37,15 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   return r;
 }
 
+// Cached in L2 but not L1: for rows read twice in a row (the second read hits L2).
+__device__ __forceinline__ uint4 ld_l2_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -225,6 +234,8 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const __nv_bfloat16* __res
 // A CTA covers kQuantRows consecutive tokens of one (batch, head), in warp units of ROWS =
 // max(QB, 2) tokens: two rows per iteration, 16 lanes per row (16-byte loads). For QB == 1 each
 // half-warp is its own block; otherwise the whole unit is one block. SMOOTH subtracts the K mean.
+// Blocks of 8 or more rows take two passes over their rows (the block max, then the codes, the
+// second reading from L2) instead of holding every row in registers, which keeps occupancy up.
 template <int QB, int OUT, bool SMOOTH>
 __global__ void __launch_bounds__(256) quant_tokens_kernel(const __nv_bfloat16* __restrict__ x, int S, int H,
                                                            const float* __restrict__ mean, void* __restrict__ codes,
@@ -248,23 +259,29 @@ __global__ void __launch_bounds__(256) quant_tokens_kernel(const __nv_bfloat16* 
   for (int u = warp; u < UNITS; u += 8) {
     const int rb = chunk * UNITS + u;  // block of rows (a whole warp unit) within this (b, h)
     if (rb * ROWS >= S) break;
-    float val[IT][8];
+    constexpr bool kTwoPass = IT >= 4;
+    constexpr int KEEP = kTwoPass ? 1 : IT;  // rows held in registers between the passes
+    float val[KEEP][8];
     float amax = 0.0f;
-#pragma unroll
-    for (int it = 0; it < IT; ++it) {
+    auto load_row = [&](int it, float* out) {  // smoothed values of this lane's 8 channels of a row
       const int row = rb * ROWS + 2 * it + half;
       if (row < S) {
         const size_t off = (((size_t)b * S + row) * H + h) * kHeadDim + cg * 8;
-        bf16x8_to_f32(ld_stream_v4(x + off), val[it]);
+        bf16x8_to_f32(kTwoPass ? ld_l2_v4(x + off) : ld_stream_v4(x + off), out);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          if constexpr (SMOOTH) val[it][e] = __fsub_rn(val[it][e], mu[e]);
-          amax = fmaxf(amax, fabsf(val[it][e]));
-        }
+        for (int e = 0; e < 8; ++e)
+          if constexpr (SMOOTH) out[e] = __fsub_rn(out[e], mu[e]);
       } else {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) val[it][e] = 0.0f;
+        for (int e = 0; e < 8; ++e) out[e] = 0.0f;
       }
+    };
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+      float* vrow = val[kTwoPass ? 0 : it];
+      load_row(it, vrow);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(vrow[e]));
     }
     // block absmax: over 16 lanes (QB == 1, one row per half-warp) or the whole warp
 #pragma unroll
@@ -278,9 +295,11 @@ __global__ void __launch_bounds__(256) quant_tokens_kernel(const __nv_bfloat16* 
       const int row = rb * ROWS + 2 * it + half;
       if (row >= S) continue;
       const size_t off = (((size_t)b * S + row) * H + h) * kHeadDim + cg * 8;
+      float* vrow = val[kTwoPass ? 0 : it];
+      if constexpr (kTwoPass) load_row(it, vrow);  // the second pass reads the rows again (from L2)
       float q[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) q[e] = quotient(val[it][e], scale, fast, rcp);
+      for (int e = 0; e < 8; ++e) q[e] = quotient(vrow[e], scale, fast, rcp);
       if constexpr (OUT == CODE_E4M3) {
         uint2 w;
         w.x = e4m3x2(q[0], q[1]) | (e4m3x2(q[2], q[3]) << 16);

@@ -28,6 +28,7 @@ MODES = {
     "sage_fp8": (dit.MODE_SAGE, "fp8_e4m3"),
     "skip_dense": (dit.MODE_SKIP, "bf16"),
     "skip_sage_int8": (dit.MODE_SAGE | dit.MODE_SKIP, "int8"),
+    "qk16pv8": (dit.MODE_SAGE | dit.MODE_V_PER_TENSOR, "bf16"),
 }
 
 
@@ -45,12 +46,25 @@ def main():
     ap.add_argument("--factor", type=float, default=0.0)
     ap.add_argument("--warmup", type=int, default=1)
     ap.add_argument("--launches", type=int, default=2)
+    ap.add_argument("--prepass", action="store_true",
+                    help="run only the SAGE quantize prepass (sage_quantize_qkv) for a quantized --mode")
     args = ap.parse_args()
     mode, dt = MODES[args.mode]
+    if dt == "bf16" and mode & dit.MODE_SAGE:  # QK16PV8 has no Q/K blocks
+        args.q_block = args.k_block = 0
     grid = tuple(int(x) for x in args.grid.split(",")) if args.grid else ()
     S = args.S if not grid else grid[0] * grid[1] * grid[2]
     w = workloads.Workload("profile", args.B, args.H, args.Hkv or args.H, S, S, kind=args.kind, grid=grid)
     q, k, v = workloads.generate(w, seed=0, device="cuda")
+    if args.prepass:
+        if dt == "bf16":
+            raise SystemExit("--prepass needs a SAGE --mode with int8 or fp8 Q/K")
+        for _ in range(args.warmup + args.launches):
+            dit.sage_quantize_qkv(q, k, v, qk_dtype=dt, q_block=args.q_block, k_block=args.k_block)
+        dit.dit_attn_check_errors()
+        torch.cuda.synchronize()
+        print(f"ok: prepass {args.mode} B={w.B} H={w.Hq}/{w.Hkv} S={S} calls={args.warmup + args.launches}")
+        return
     out = torch.empty_like(q)
     ws_bytes = dit.dit_attn_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, mode, dt, args.q_block, args.k_block)
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
