@@ -37,6 +37,7 @@ SIGNATURES = {
     "dit_attn_workspace_bytes": (_c_size, [_c_int] * 9),
     "dit_attn_fwd": (_c_int, [_vp, _vp, _vp, _vp] + [_c_int] * 9 + [_c_float, _vp, _vp, _c_size, _vp]),
     "dit_attn_fwd_lse": (_c_int, [_vp] * 5 + [_c_int] * 9 + [_c_float, _vp, _vp, _c_size, _vp]),
+    "dit_attn_fwd_host": (_c_int, [_vp] * 8 + [_c_int] * 6 + [_c_float, _c_int, _vp, _vp, _vp]),
     "sage_quantize_workspace_bytes": (_c_size, [_c_int] * 3),
     "sage_quantize_qkv": (_c_int, [_vp, _vp, _vp] + [_c_int] * 8 + [_vp] * 8 + [_c_size, _vp]),
     "sage_quantize_qkv_noalloc": (_c_int, [_vp, _vp, _vp] + [_c_int] * 8 + [_vp] * 7 + [_vp]),
@@ -133,6 +134,29 @@ def dit_attn_fwd(q, k, v, out=None, *, mode=MODE_DENSE, qk_dtype="bf16", q_block
                                      _ptr(workspace), ws_bytes, _ptr(skip_counts))
         _check(st, "dit_attn_fwd_lse")
     return out
+
+
+_COPY_STREAMS = {}
+
+
+def dit_attn_fwd_host(q_host, k_host, v_host, out_host, q, k, v, out, *, mode=MODE_DENSE, threshold_scale_factor=0.0,
+                      chunks=8, stream=None, h2d_stream=None, d2h_stream=None):
+    """Dense attention from pinned host tensors into ``out_host``, with the copies overlapped with the
+    kernels over ``chunks`` groups of kv heads; q/k/v/out are device staging tensors of the same shapes.
+    Completion is signalled on ``stream`` (default: the current stream). The two copy streams default
+    to streams this module keeps per device."""
+    B, Hq, Hkv, Sq, Skv = _shape(q, k)
+    dev = q.device.index if q.device.index is not None else torch.cuda.current_device()
+    if h2d_stream is None or d2h_stream is None:
+        if dev not in _COPY_STREAMS:
+            _COPY_STREAMS[dev] = (torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev))
+        h2d_stream = h2d_stream or _COPY_STREAMS[dev][0]
+        d2h_stream = d2h_stream or _COPY_STREAMS[dev][1]
+    st = _lib().dit_attn_fwd_host(_ptr(q_host), _ptr(k_host), _ptr(v_host), _ptr(out_host), _ptr(q), _ptr(k), _ptr(v),
+                                  _ptr(out), B, Hq, Hkv, Sq, Skv, mode, float(threshold_scale_factor), int(chunks),
+                                  _stream(stream), _stream(h2d_stream), _stream(d2h_stream))
+    _check(st, "dit_attn_fwd_host")
+    return out_host
 
 
 def sage_quantize_workspace_bytes(B, Hkv, Skv) -> int:

@@ -141,17 +141,56 @@ dit_status prepare_device(int** err_out) {
 }
 
 // [B, S, H, 128] tensor as a 4-D map {128, S, H, B} with boxes of {box_inner, 128, 1, 1}
-// (box_inner * element size = 128 bytes) and 128-byte swizzling.
-bool encode_map(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int esize, int B, int S, int H) {
+// (box_inner * element size = 128 bytes) and 128-byte swizzling. Hstride >= H is the head count of
+// the tensor's rows: H heads starting at ptr form a slice of a [B, S, Hstride, 128] tensor.
+bool encode_map(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int esize, int B, int S, int H,
+                int Hstride) {
   const cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)S, (cuuint64_t)H, (cuuint64_t)B};
   const cuuint64_t row = (cuuint64_t)kHeadDim * esize;
-  const cuuint64_t strides[3] = {row * (cuuint64_t)H, row, row * (cuuint64_t)H * (cuuint64_t)S};
+  const cuuint64_t strides[3] = {row * (cuuint64_t)Hstride, row, row * (cuuint64_t)Hstride * (cuuint64_t)S};
   const cuuint32_t box[4] = {(cuuint32_t)(128 / esize), 128, 1, 1};
   const cuuint32_t es[4] = {1, 1, 1, 1};
   const CUresult r = g_encode(m, dt, 4, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// Events and a second compute stream for dit_attn_fwd_host, created once per device on first use
+// (the calls themselves create nothing): one event per chunk for "inputs copied" and "attention
+// done", plus start and finish. Consecutive chunks' kernels alternate between the caller's compute
+// stream and `aux`, so each kernel's last partial wave of CTAs overlaps the next one's first.
+constexpr int kMaxHostChunks = 64;
+struct HostEvents {
+  bool ready = false;
+  bool ok = false;
+  cudaStream_t aux;
+  cudaEvent_t start, done, aux_done, in[kMaxHostChunks], comp[kMaxHostChunks];
+};
+HostEvents g_host_events[64];
+std::mutex g_host_mu;
+
+HostEvents* host_events() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_host_mu);
+  HostEvents& h = g_host_events[dev];
+  if (!h.ready) {
+    h.ready = true;
+    bool ok = cudaStreamCreateWithFlags(&h.aux, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&h.start, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&h.done, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&h.aux_done, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; ok && i < kMaxHostChunks; ++i)
+      ok = cudaEventCreateWithFlags(&h.in[i], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&h.comp[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) cudaGetLastError();
+    h.ok = ok;
+  }
+  return h.ok ? &h : nullptr;
 }
 
 dit_status from_cuda(cudaError_t e) {
@@ -165,14 +204,18 @@ dit_status run_attention(const void* q, const void* k, const void* v, void* out,
                          int qk_esize, int qk_format, int pv_format, int B, int Hq, int Hkv, int Sq, int Skv,
                          int mode, int q_block, int k_block, float factor, const float* q_scale,
                          const float* k_scale, const float* v_scale, int32_t* skip_counts, float* lse,
-                         int* err, cudaStream_t stream) {
+                         int* err, cudaStream_t stream, int q_hstride = 0, int kv_hstride = 0) {
+  // q_hstride / kv_hstride: head counts of the full tensors' rows when q, k, v, out are head slices
+  if (q_hstride == 0) q_hstride = Hq;
+  if (kv_hstride == 0) kv_hstride = Hkv;
   CUtensorMap tq, tk, tv, to;
   const CUtensorMapDataType pv_dt =
       (pv_format == PV_BF16) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const int pv_esize = (pv_format == PV_BF16) ? 2 : 1;
-  if (!encode_map(&tq, q, qk_dt, qk_esize, B, Sq, Hq) || !encode_map(&tk, k, qk_dt, qk_esize, B, Skv, Hkv) ||
-      !encode_map(&tv, v, pv_dt, pv_esize, B, Skv, Hkv) ||
-      !encode_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, Sq, Hq))
+  if (!encode_map(&tq, q, qk_dt, qk_esize, B, Sq, Hq, q_hstride) ||
+      !encode_map(&tk, k, qk_dt, qk_esize, B, Skv, Hkv, kv_hstride) ||
+      !encode_map(&tv, v, pv_dt, pv_esize, B, Skv, Hkv, kv_hstride) ||
+      !encode_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, Sq, Hq, q_hstride))
     return DIT_E_CUDA;
   FmhaParams p{};
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Sq = Sq; p.Skv = Skv;
@@ -461,6 +504,77 @@ dit_status dit_attn_fwd_quantized_lse(const void* q_codes, const void* k_codes, 
   return fwd_quantized_impl(q_codes, k_codes, v_codes, q_scale, k_scale, v_scale, out, B, Hq, Hkv, Sq, Skv, mode,
                             qk_dtype, q_block, k_block, threshold_scale_factor, stream, workspace, workspace_bytes,
                             skip_counts, lse);
+}
+
+dit_status dit_attn_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* out_host, void* q,
+                             void* k, void* v, void* out, int B, int Hq, int Hkv, int Sq, int Skv, int mode,
+                             float threshold_scale_factor, int chunks, void* compute_stream, void* h2d_stream,
+                             void* d2h_stream) {
+  if (!valid_shape(B, Hq, Hkv, Sq, Skv) || (mode & ~DIT_MODE_SKIP) != 0 ||
+      !valid_mode(mode, DIT_QK_BF16, 1, 1, threshold_scale_factor) || chunks < 1 || chunks > Hkv ||
+      chunks > kMaxHostChunks)
+    return DIT_E_INVALID_ARG;
+  if (B == 0 || Sq == 0) return DIT_OK;
+  if (!q_host || !k_host || !v_host || !out_host || !q || !k || !v || !out || !aligned16(q) || !aligned16(k) ||
+      !aligned16(v) || !aligned16(out))
+    return DIT_E_INVALID_ARG;
+  int* err = nullptr;
+  const dit_status ds = prepare_device(&err);
+  if (ds != DIT_OK) return ds;
+  HostEvents* ev = host_events();
+  if (ev == nullptr) return DIT_E_CUDA;
+  cudaStream_t cs = static_cast<cudaStream_t>(compute_stream);
+  cudaStream_t hs = static_cast<cudaStream_t>(h2d_stream);
+  cudaStream_t ds2 = static_cast<cudaStream_t>(d2h_stream);
+  const int group = Hq / Hkv;
+  const size_t row = (size_t)kHeadDim * 2;  // bytes of one head of one token
+  // the copies may not overwrite the device buffers before earlier work on the compute stream is done
+  cudaError_t e = cudaEventRecord(ev->start, cs);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(hs, ev->start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ds2, ev->start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ev->aux, ev->start, 0);
+  // chunk c covers kv heads [Hkv*c/chunks, Hkv*(c+1)/chunks) and their query heads
+  auto kv0 = [&](int c) { return (int)((long long)Hkv * c / chunks); };
+  for (int c = 0; c < chunks && e == cudaSuccess; ++c) {
+    const int hk0 = kv0(c), hkc = kv0(c + 1) - hk0, hq0 = hk0 * group, hqc = hkc * group;
+    const size_t qo = hq0 * row, ko = hk0 * row;
+    e = cudaMemcpy2DAsync(static_cast<uint8_t*>(q) + qo, Hq * row, static_cast<const uint8_t*>(q_host) + qo, Hq * row,
+                          hqc * row, (size_t)B * Sq, cudaMemcpyHostToDevice, hs);
+    if (e == cudaSuccess)
+      e = cudaMemcpy2DAsync(static_cast<uint8_t*>(k) + ko, Hkv * row, static_cast<const uint8_t*>(k_host) + ko,
+                            Hkv * row, hkc * row, (size_t)B * Skv, cudaMemcpyHostToDevice, hs);
+    if (e == cudaSuccess)
+      e = cudaMemcpy2DAsync(static_cast<uint8_t*>(v) + ko, Hkv * row, static_cast<const uint8_t*>(v_host) + ko,
+                            Hkv * row, hkc * row, (size_t)B * Skv, cudaMemcpyHostToDevice, hs);
+    if (e == cudaSuccess) e = cudaEventRecord(ev->in[c], hs);
+  }
+  for (int c = 0; c < chunks && e == cudaSuccess; ++c) {
+    const int hk0 = kv0(c), hkc = kv0(c + 1) - hk0, hq0 = hk0 * group, hqc = hkc * group;
+    cudaStream_t ks = (c & 1) ? ev->aux : cs;
+    e = cudaStreamWaitEvent(ks, ev->in[c], 0);
+    if (e != cudaSuccess) break;
+    const dit_status st = run_attention(
+        static_cast<uint8_t*>(q) + hq0 * row, static_cast<uint8_t*>(k) + hk0 * row,
+        static_cast<uint8_t*>(v) + hk0 * row, static_cast<uint8_t*>(out) + hq0 * row, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+        2, QK_BF16, PV_BF16, B, hqc, hkc, Sq, Skv, mode, 1, 1, threshold_scale_factor, nullptr, nullptr, nullptr,
+        nullptr, nullptr, err, ks, Hq, Hkv);
+    if (st != DIT_OK) return st;
+    e = cudaEventRecord(ev->comp[c], ks);
+  }
+  for (int c = 0; c < chunks && e == cudaSuccess; ++c) {
+    const int hk0 = kv0(c), hkc = kv0(c + 1) - hk0, hq0 = hk0 * group, hqc = hkc * group;
+    const size_t qo = hq0 * row;
+    e = cudaStreamWaitEvent(ds2, ev->comp[c], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpy2DAsync(static_cast<uint8_t*>(out_host) + qo, Hq * row, static_cast<const uint8_t*>(out) + qo,
+                            Hq * row, hqc * row, (size_t)B * Sq, cudaMemcpyDeviceToHost, ds2);
+  }
+  // completion (the last output byte on the host, and all kernels) is signalled on the compute stream
+  if (e == cudaSuccess) e = cudaEventRecord(ev->done, ds2);
+  if (e == cudaSuccess) e = cudaEventRecord(ev->aux_done, ev->aux);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev->done, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev->aux_done, 0);
+  return from_cuda(e);
 }
 
 dit_status dit_attn_check_errors(void* stream) {

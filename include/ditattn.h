@@ -69,8 +69,8 @@ enum { DIT_QK_BF16 = 0, DIT_QK_INT8 = 1, DIT_QK_FP8_E4M3 = 2 };
 /* Rows and columns of one attention tile; skip counts are kept per 128-row Q tile. */
 enum { DIT_HEAD_DIM = 128, DIT_TILE = 128 };
 
-/* Version of this interface (2: QK16PV8, DIT_MODE_V_PER_TENSOR, sage_quantize_v, the LSE outputs and
- * sage_quantize_qkv_with_mean). */
+/* Version of this interface (2: QK16PV8, DIT_MODE_V_PER_TENSOR, sage_quantize_v, the LSE outputs,
+ * sage_quantize_qkv_with_mean and dit_attn_fwd_host). */
 int dit_abi_version(void);
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -126,6 +126,35 @@ dit_status dit_attn_fwd_lse(const void* q, const void* k, const void* v, void* o
                             int Hkv, int Sq, int Skv, int mode, int qk_dtype, int q_block, int k_block,
                             float threshold_scale_factor, void* stream, void* workspace, size_t workspace_bytes,
                             int32_t* skip_counts);
+
+/*
+ * Dense BF16 attention (with or without SKIP) from and to host memory, with the transfers overlapped
+ * with the attention. The pages have no counterpart; this serves callers whose Q, K, V live on the
+ * host (for example a step that offloads activations), so that the copies hide behind the kernels.
+ *
+ * The kv heads are split into `chunks` groups of (nearly) equal size, each with its query heads. Every
+ * group's Q, K and V head slices are copied in on h2d_stream, its attention runs on compute_stream once
+ * they have arrived, and its output slice is copied back on d2h_stream once it is done: group g+1's
+ * inputs and group g-1's output move while group g computes. The result equals dit_attn_fwd's bit for bit.
+ *
+ *   q_host, k_host, v_host, out_host   host buffers with the layouts of dit_attn_fwd (pinned memory
+ *              for the copies to be asynchronous); out_host is written completely
+ *   q, k, v, out   device buffers for the full tensors (16-byte aligned), used as staging
+ *   mode       DIT_MODE_DENSE or DIT_MODE_SKIP; threshold_scale_factor as for dit_attn_fwd
+ *   chunks     1 .. min(Hkv, 64)
+ *   compute_stream, h2d_stream, d2h_stream   cudaStream_t as void*; they may be the same stream (then
+ *              nothing overlaps). Work already queued on compute_stream is finished before the copies
+ *              overwrite the device buffers, and the call's completion (out_host written) is signalled
+ *              on compute_stream.
+ * Consecutive groups' kernels alternate between compute_stream and a stream of the library's, so one
+ * kernel's last partial wave overlaps the next one's first. The first call on a device creates that
+ * stream and the library's events for this entry point (a one-time set-up; make it before any stream
+ * capture). Calls must not be issued from several host threads at once.
+ */
+dit_status dit_attn_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* out_host, void* q,
+                             void* k, void* v, void* out, int B, int Hq, int Hkv, int Sq, int Skv, int mode,
+                             float threshold_scale_factor, int chunks, void* compute_stream, void* h2d_stream,
+                             void* d2h_stream);
 
 /* Bytes of device scratch sage_quantize_qkv needs (the K-mean / V-absmax partials). */
 size_t sage_quantize_workspace_bytes(int B, int Hkv, int Skv);

@@ -173,3 +173,15 @@ def test_with_mean_prepass_rejects_bf16_and_missing_mean(lib):
     assert lib.sage_quantize_qkv_with_mean(*args(None, 1)) == INVALID
     assert lib.sage_quantize_qkv_with_mean(*args(FAKE, 0)) == INVALID   # BF16 Q/K has no K mean to smooth with
     assert lib.sage_quantize_qkv_with_mean(*args(MISALIGNED, 2)) == INVALID
+
+
+def test_host_pipeline_rejects_bad_arguments(lib):
+    def call(mode=0, chunks=2, qh=FAKE, qd=FAKE, Hkv=2):
+        return lib.dit_attn_fwd_host(qh, FAKE, FAKE, FAKE, qd, FAKE, FAKE, FAKE, 1, 4, Hkv, 256, 256, mode, 0.0,
+                                     chunks, None, None, None)
+    assert call(mode=1) == INVALID          # dense (with or without skip) only
+    assert call(mode=3) == INVALID
+    assert call(chunks=0) == INVALID
+    assert call(chunks=3) == INVALID        # more groups than kv heads
+    assert call(qh=None) == INVALID
+    assert call(qd=MISALIGNED) == INVALID
