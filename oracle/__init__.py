@@ -16,6 +16,9 @@ What the oracle computes, and where each step comes from:
   tokens), one scale per token block per head for Q and K, one scale per head per
   channel for V ("TRTLLM Attention" user guide, section "SAGE quantization";
   "VisualGen Quantized Attention", section "SageAttention in the TRTLLM backend").
+* ``mx_quant``     -- MXFP8 Q/K: E4M3 elements with one E8M0 scale per 32 channels of a token
+  (OCP MX rule), no smoothing ("VisualGen Quantized Attention", section "MXFP8 and NVFP4 in the
+  CUTEDSL and FlashInfer backends"); V as in QK16PV8.
 * ``attention``    -- dense attention written out untiled, and the tiled online-softmax
   loop (128x128 tiles, KV tiles in ascending order) used for SAGE and Skip-Softmax
   ("SAGE + Skip-Softmax -- API Design & Test Plan", Part 1 §4 mapping table:

@@ -31,6 +31,9 @@ Readings where the pages are silent:
 * QK16PV8 ("VisualGen Quantized Attention", section "QK16PV8 Attention Kernels in the CUTEDSL
   Backend": Q/K stay BF16, only V is FP8): the dense logits, and P and V exactly as in SAGE
   (the pages give BMM2 the same FP8 path; P's scale and l follow the SAGE readings).
+* MXFP8 Q/K + FP8 V ("VisualGen Quantized Attention", section "MXFP8 and NVFP4 in the CUTEDSL and
+  FlashInfer backends"): the logits of the block-scaled codes (``mx_quant.mx_scores`` times the
+  softmax scale), and P and V exactly as in QK16PV8.
 * LSE ("VisualGen Quantized Attention", section "Requirements and behavior": a backend that
   produces LSE composes with Attention2D / Ring context parallelism): per query row,
   ln sum_j exp(s_ij) over the row's logits s as the mode defines them (natural log), i.e.
@@ -47,6 +50,7 @@ import math
 import numpy as np
 
 from . import formats
+from . import mx_quant
 
 HEAD_DIM = 128
 SOFTMAX_SCALE = 1.0 / math.sqrt(HEAD_DIM)
@@ -165,9 +169,10 @@ def attention_q_tile(inputs: dict, b: int, hq: int, tile: int, *, mode: str, qk_
     """Oracle output of one 128-row Q tile of one (batch, query head).
 
     inputs: dict with float32 arrays 'q' [B,Sq,Hq,128], 'k', 'v' [B,Skv,Hkv,128] holding bf16 values.
-    mode:   'dense', 'sage' or 'qk16pv8'; ``factor`` switches Skip-Softmax on (threshold = factor / Skv).
-    quant:  the output of ``sage_quant.sage_quantize`` (mode 'sage') or ``sage_quant.qk16pv8_quantize``
-            (mode 'qk16pv8').
+    mode:   'dense', 'sage', 'qk16pv8' or 'mxfp8'; ``factor`` switches Skip-Softmax on (threshold =
+            factor / Skv).
+    quant:  the output of ``sage_quant.sage_quantize`` (mode 'sage'), ``sage_quant.qk16pv8_quantize``
+            (mode 'qk16pv8') or ``mx_quant.mxfp8_quantize`` (mode 'mxfp8').
     Returns (O [rows, 128] float64, skipped tile count, row indices), plus the rows' LSE
     (float64) last when ``with_lse``.
     """
@@ -188,6 +193,10 @@ def attention_q_tile(inputs: dict, b: int, hq: int, tile: int, *, mode: str, qk_
         vals, vscale, quantize_p = formats.e4m3_decode(quant["v_codes"][b, :, g, :]), quant["v_scale"][b, g, :], True
     elif mode == "qk16pv8":
         s = dense_scores(q[b, r0:r1, hq, :], k[b, :, g, :])
+        vals, vscale, quantize_p = formats.e4m3_decode(quant["v_codes"][b, :, g, :]), quant["v_scale"][b, g, :], True
+    elif mode == "mxfp8":
+        s = SOFTMAX_SCALE * mx_quant.mx_scores(quant["q_codes"][b, r0:r1, hq, :], quant["q_sf"][b, hq, r0:r1, :],
+                                               quant["k_codes"][b, :, g, :], quant["k_sf"][b, g, :, :])
         vals, vscale, quantize_p = formats.e4m3_decode(quant["v_codes"][b, :, g, :]), quant["v_scale"][b, g, :], True
     else:
         raise ValueError(f"unknown mode {mode!r}")

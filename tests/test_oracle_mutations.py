@@ -124,3 +124,57 @@ def test_dropped_v_scale_in_qk16pv8_is_caught(monkeypatch):
         return res
     monkeypatch.setattr(sage_quant, "qk16pv8_quantize", unit_scale)
     _fails(TP.test_large_logits_give_the_target_value_row, True)
+
+
+# ---- MXFP8 Q/K (block-32 E4M3 elements with E8M0 scales)
+from oracle import mx_quant  # noqa: E402
+
+from . import test_oracle_mx as TM  # noqa: E402
+
+
+def test_scale_rounded_up_instead_of_floor_rule_is_caught(monkeypatch):
+    # the no-saturation variant: 2^ceil(log2(amax / 448)) instead of 2^(floor(log2 amax) - 8)
+    def ceil_rule(amax):
+        a = np.asarray(amax, np.float64)
+        with np.errstate(divide="ignore"):
+            e = np.ceil(np.log2(a / 448.0))
+        return np.clip(np.where(a == 0, -127, e), -127, 127).astype(np.int64)
+    monkeypatch.setattr(mx_quant, "shared_exponent", ceil_rule)
+    _fails(TM.test_hand_derived_blocks, [1.9375, 1.0], 119, [0x7E, 0x78])
+
+
+def test_off_by_one_element_emax_is_caught(monkeypatch):
+    monkeypatch.setattr(mx_quant, "E4M3_EMAX", 7)
+    _fails(TM.test_hand_derived_blocks, [3.0, -3.0, 0.0], 120, [0x7C, 0xFC, 0x00])
+
+
+def test_token_major_scale_layout_is_caught(monkeypatch):
+    good = mx_quant.mx_quantize
+
+    def token_major(x):
+        codes, sf = good(x)
+        return codes, np.ascontiguousarray(sf.transpose(0, 2, 1, 3))
+    monkeypatch.setattr(mx_quant, "mx_quantize", token_major)
+    _fails(TM.test_every_block_has_its_own_scale_in_head_major_layout)
+
+
+def test_one_block_scale_for_all_blocks_is_caught(monkeypatch):
+    def first_block_scale(qc, qs, kc, ks):
+        qs = np.repeat(np.asarray(qs)[:, :1], 4, axis=1)
+        ks = np.repeat(np.asarray(ks)[:, :1], 4, axis=1)
+        a, b = formats.e4m3_decode(qc), formats.e4m3_decode(kc)
+        return (a @ b.T) * np.ldexp(1.0, qs[:, 0].astype(np.int64) - 127)[:, None] \
+            * np.ldexp(1.0, ks[:, 0].astype(np.int64) - 127)[None, :]
+    monkeypatch.setattr(mx_quant, "mx_scores", first_block_scale)
+    _fails(TM.test_mx_scores_equal_the_product_of_dequantized_operands)
+
+
+def test_unquantized_q_k_in_mxfp8_attention_is_caught(monkeypatch):
+    good = att.attention_q_tile
+
+    def dense_logits(inputs, b, hq, tile, **kw):
+        if kw.get("mode") == "mxfp8":
+            kw = dict(kw, mode="qk16pv8")
+        return good(inputs, b, hq, tile, **kw)
+    monkeypatch.setattr(att, "attention_q_tile", dense_logits)
+    _fails(TM.test_mxfp8_attention_is_qk16pv8_attention_of_the_dequantized_q_and_k)
