@@ -251,11 +251,12 @@ def run_modes(dit, steps, warmup, world, stream, peak16, hbm_gbs):
     peak_mix = 2.0 * peak16 * peak8 / (peak16 + peak8)  # BMM1 on 16-bit operands, BMM2 on FP8
     table = [("dit_sage_int8_32k", peak_mix, "BMM1 f16 + BMM2 e4m3 harmonic peak"),
              ("gqa_sage_fp8_16k", peak8, "2 x measured bf16 (e4m3 nominal ratio)"),
-             ("dit_qk16pv8_32k", peak_mix, "BMM1 bf16 + BMM2 e4m3 harmonic peak")]
+             ("dit_qk16pv8_32k", peak_mix, "BMM1 bf16 + BMM2 e4m3 harmonic peak"),
+             ("dit_mxfp8_32k", peak8, "2 x measured bf16 (e4m3 nominal ratio; BMM1 block-scaled)")]
     for name, peak, peak_desc in table:
         w = workloads.WORKLOADS[name]
         q, k, v = workloads.generate(w, seed=1, device="cuda")
-        qk16 = w.mode == "qk16pv8"
+        qk16, mx = w.mode == "qk16pv8", w.mode == "mxfp8"
         mode = dit.MODE_SAGE | (dit.MODE_V_PER_TENSOR if qk16 else 0)
         ws = torch.empty(dit.dit_attn_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, mode, w.qk_dtype,
                                                       w.q_block, w.k_block), dtype=torch.uint8, device="cuda")
@@ -268,13 +269,21 @@ def run_modes(dit, steps, warmup, world, stream, peak16, hbm_gbs):
         tf = w.dense_equiv_flop / (ms * 1e-3) / 1e12
         entry = {"ms": round(ms, 3), "tflops": round(tf, 1), "peak_tflops": round(peak, 1),
                  "frac": round(tf / peak, 3), "peak": peak_desc,
-                 "launches_per_step": 4 if qk16 else 5}
+                 "launches_per_step": 4 if qk16 else 6 if mx else 5}
         # the two halves, through the split entry points
         bq, bkv = q.numel() * 2, k.numel() * 2
         if qk16:
             pre = lambda: dit.sage_quantize_v(v, per_tensor=True, stream=stream)  # noqa: E731
             # V read twice (absmax, then codes), 1-byte codes written
             pre_bytes, pre_desc = 2 * bkv + bkv // 2, "V read twice, 1-byte V codes written"
+        elif mx:
+            def pre():
+                res = dit.mx_quantize_qk(q, k, stream=stream)
+                res.update(dit.sage_quantize_v(v, per_tensor=False, stream=stream))
+                return res
+            # Q, K read once and V twice; 1-byte Q/K/V codes and 4 scale bytes per 128 Q/K elements written
+            pre_bytes = bq + 3 * bkv + (bq + 2 * bkv) // 2 + (bq + bkv) // 64
+            pre_desc = "Q, K read once, V twice, 1-byte Q/K/V codes and E8M0 bytes written"
         else:
             pre = lambda: dit.sage_quantize_qkv(q, k, v, qk_dtype=w.qk_dtype, q_block=w.q_block,  # noqa: E731
                                                 k_block=w.k_block, stream=stream)
@@ -287,8 +296,11 @@ def run_modes(dit, steps, warmup, world, stream, peak16, hbm_gbs):
         pre_ms = max_over_ranks(time_steps(pre, steps, warmup, world, stream), world) / steps
 
         def attn():
-            dit.dit_attn_fwd_quantized(quant, out, mode=mode, qk_dtype=w.qk_dtype, q_block=w.q_block,
-                                       k_block=w.k_block, stream=stream)
+            if mx:
+                dit.dit_attn_fwd_mxfp8(quant, out, mode=mode, stream=stream)
+            else:
+                dit.dit_attn_fwd_quantized(quant, out, mode=mode, qk_dtype=w.qk_dtype, q_block=w.q_block,
+                                           k_block=w.k_block, stream=stream)
         attn_ms = max_over_ranks(time_steps(attn, steps, warmup, world, stream), world) / steps
         atf = w.dense_equiv_flop / (attn_ms * 1e-3) / 1e12
         entry["prepass"] = {"ms": round(pre_ms, 3), "gbs": round(pre_bytes / (pre_ms * 1e-3) / 1e9, 1),

@@ -8,7 +8,8 @@ library is missing, importing the binding's functions raises.
 Modes follow the pages ("TRTLLM Attention" user guide): dense BF16; SAGE with INT8 or FP8 E4M3
 Q/K per token block (block sizes 1, 4, 16) and per-channel FP8 V; QK16PV8 (SAGE with BF16 Q/K:
 only V in FP8, per channel or with one tensor-wide scale, "VisualGen Quantized Attention");
-Skip-Softmax with threshold = threshold_scale_factor / Skv.
+MXFP8 Q/K + FP8 V (SAGE with qk_dtype "mxfp8": E4M3 Q/K with one E8M0 scale per 32 channels of
+a token, applied inside BMM1, same page); Skip-Softmax with threshold = threshold_scale_factor / Skv.
 """
 
 from __future__ import annotations
@@ -20,12 +21,12 @@ import os
 import torch
 
 MODE_DENSE, MODE_SAGE, MODE_SKIP, MODE_V_PER_TENSOR = 0, 1, 2, 4
-QK_BF16, QK_INT8, QK_FP8_E4M3 = 0, 1, 2
+QK_BF16, QK_INT8, QK_FP8_E4M3, QK_MXFP8 = 0, 1, 2, 3
 HEAD_DIM = 128
 TILE = 128
 STATUS_NAMES = {0: "DIT_OK", 1: "DIT_E_INVALID_ARG", 2: "DIT_E_UNSUPPORTED", 3: "DIT_E_CUDA", 4: "DIT_E_TIMEOUT",
                 5: "DIT_E_WORKSPACE"}
-QK_DTYPES = {"bf16": QK_BF16, "int8": QK_INT8, "fp8_e4m3": QK_FP8_E4M3}
+QK_DTYPES = {"bf16": QK_BF16, "int8": QK_INT8, "fp8_e4m3": QK_FP8_E4M3, "mxfp8": QK_MXFP8}
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libditattn.so")
 
@@ -47,6 +48,8 @@ SIGNATURES = {
     "dit_attn_fwd_quantized": (_c_int, [_vp] * 7 + [_c_int] * 9 + [_c_float, _vp, _vp, _c_size, _vp]),
     "dit_attn_fwd_quantized_lse": (_c_int, [_vp] * 8 + [_c_int] * 9 + [_c_float, _vp, _vp, _c_size, _vp]),
     "sage_quantize_qkv_with_mean": (_c_int, [_vp] * 4 + [_c_int] * 8 + [_vp] * 7 + [_c_size, _vp]),
+    "mx_quantize_qk": (_c_int, [_vp, _vp] + [_c_int] * 5 + [_vp] * 5),
+    "dit_attn_fwd_mxfp8": (_c_int, [_vp] * 8 + [_c_int] * 6 + [_c_float, _vp, _vp]),
     "dit_attn_check_errors": (_c_int, [_vp]),
 }
 
@@ -261,6 +264,35 @@ def dit_attn_fwd_quantized(quant: dict, out, *, mode=MODE_SAGE, qk_dtype="int8",
                                                float(threshold_scale_factor), _stream(stream), _ptr(workspace),
                                                ws_bytes, _ptr(skip_counts))
         _check(st, "dit_attn_fwd_quantized_lse")
+    return out
+
+
+def mx_quantize_qk(q, k, *, stream=None):
+    """The MXFP8 Q/K prepass alone: E4M3 codes (uint8 bit patterns, the shapes of q and k) and E8M0
+    scale bytes ``q_sf`` [B, Hq, Sq, 4], ``k_sf`` [B, Hkv, Skv, 4] (byte c for channels 32c..32c+31)."""
+    B, Hq, Hkv, Sq, Skv = _shape(q, k)
+    dev = q.device
+    res = dict(q_codes=torch.empty(q.shape, dtype=torch.uint8, device=dev),
+               k_codes=torch.empty(k.shape, dtype=torch.uint8, device=dev),
+               q_sf=torch.empty((B, Hq, Sq, 4), dtype=torch.uint8, device=dev),
+               k_sf=torch.empty((B, Hkv, Skv, 4), dtype=torch.uint8, device=dev))
+    st = _lib().mx_quantize_qk(_ptr(q), _ptr(k), B, Hq, Hkv, Sq, Skv, _ptr(res["q_codes"]), _ptr(res["k_codes"]),
+                               _ptr(res["q_sf"]), _ptr(res["k_sf"]), _stream(stream))
+    _check(st, "mx_quantize_qk")
+    return res
+
+
+def dit_attn_fwd_mxfp8(quant: dict, out, *, mode=MODE_SAGE, threshold_scale_factor=0.0, stream=None,
+                       skip_counts=None, lse=None):
+    """Attention over MXFP8 Q/K (``mx_quantize_qk``) and FP8 V (``sage_quantize_v``), both results
+    merged in ``quant``."""
+    qc, kc = quant["q_codes"], quant["k_codes"]
+    B, Sq, Hq, _ = qc.shape
+    _, Skv, Hkv, _ = kc.shape
+    st = _lib().dit_attn_fwd_mxfp8(_ptr(qc), _ptr(kc), _ptr(quant["v_codes"]), _ptr(quant["q_sf"]),
+                                   _ptr(quant["k_sf"]), _ptr(quant["v_scale"]), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq,
+                                   Skv, mode, float(threshold_scale_factor), _stream(stream), _ptr(skip_counts))
+    _check(st, "dit_attn_fwd_mxfp8")
     return out
 
 

@@ -17,7 +17,7 @@ using namespace ditattn;
 
 namespace {
 
-constexpr int kAbiVersion = 2;
+constexpr int kAbiVersion = 3;
 constexpr unsigned long long kWaitBudgetNs = 4000000000ull;  // far beyond any legitimate wait
 
 __device__ int g_device_error = 0;
@@ -41,8 +41,9 @@ bool valid_shape(int B, int Hq, int Hkv, int Sq, int Skv) {
 bool valid_mode(int mode, int qk_dtype, int q_block, int k_block, float factor) {
   if (mode < 0 || mode > (DIT_MODE_SAGE | DIT_MODE_SKIP | DIT_MODE_V_PER_TENSOR)) return false;
   if (mode & DIT_MODE_SAGE) {
-    if (qk_dtype == DIT_QK_BF16) {
-      // QK16PV8: Q/K stay BF16, so there are no Q/K blocks (the pages' block sizes (0, 0, v))
+    if (qk_dtype == DIT_QK_BF16 || qk_dtype == DIT_QK_MXFP8) {
+      // QK16PV8: Q/K stay BF16; MXFP8: Q/K carry their own blocks of 32 channels. Either way the
+      // token-block sizes are 0 (the pages' block sizes (0, 0, v)); V per channel or per tensor.
       if (q_block != 0 || k_block != 0) return false;
     } else {
       if (qk_dtype != DIT_QK_INT8 && qk_dtype != DIT_QK_FP8_E4M3) return false;
@@ -64,20 +65,26 @@ struct SageLayout {
 };
 
 // Workspace of the all-in-one call. QK16PV8 (BF16 Q/K) needs only the V codes, V scales and the
-// V-absmax partials; its Q/K regions have size zero.
+// V-absmax partials; its Q/K regions have size zero. MXFP8 holds 1-byte Q/K codes and, in the
+// scale regions, 4 E8M0 bytes per token and head; it has no K mean.
 SageLayout sage_layout(int B, int Hq, int Hkv, int Sq, int Skv, int qk_dtype, int q_block, int k_block) {
   SageLayout L{};
   const bool qk16 = (qk_dtype == DIT_QK_BF16);
+  const bool mx = (qk_dtype == DIT_QK_MXFP8);
   const size_t code_bytes = qk16 ? 0 : (qk_dtype == DIT_QK_INT8) ? 2 : 1;  // INT8 codes are held as exact fp16
+  const size_t q_scale_bytes = qk16 ? 0 : mx ? (size_t)B * Hq * Sq * 4 : (size_t)B * Hq * ceil_div(Sq, q_block) * 4;
+  const size_t k_scale_bytes =
+      qk16 ? 0 : mx ? (size_t)B * Hkv * Skv * 4 : (size_t)B * Hkv * ceil_div(Skv, k_block) * 4;
+  const bool smooth = !qk16 && !mx;
   size_t off = 0;
   L.q_codes = off; off = align256(off + (size_t)B * Sq * Hq * kHeadDim * code_bytes);
   L.k_codes = off; off = align256(off + (size_t)B * Skv * Hkv * kHeadDim * code_bytes);
   L.v_codes = off; off = align256(off + (size_t)B * Skv * Hkv * kHeadDim);
-  L.q_scale = off; off = align256(off + (qk16 ? 0 : (size_t)B * Hq * ceil_div(Sq, q_block) * 4));
-  L.k_scale = off; off = align256(off + (qk16 ? 0 : (size_t)B * Hkv * ceil_div(Skv, k_block) * 4));
+  L.q_scale = off; off = align256(off + q_scale_bytes);
+  L.k_scale = off; off = align256(off + k_scale_bytes);
   L.v_scale = off; off = align256(off + (size_t)B * Hkv * kHeadDim * 4);
-  L.k_mean = off;  off = align256(off + (qk16 ? 0 : (size_t)B * Hkv * kHeadDim * 4));
-  L.psum = off;    off = align256(off + (qk16 ? 0 : (size_t)B * Hkv * stats_chunks(Skv) * kHeadDim * 8));
+  L.k_mean = off;  off = align256(off + (smooth ? (size_t)B * Hkv * kHeadDim * 4 : 0));
+  L.psum = off;    off = align256(off + (smooth ? (size_t)B * Hkv * stats_chunks(Skv) * kHeadDim * 8 : 0));
   L.pmax = off;    off = align256(off + (size_t)B * Hkv * stats_chunks(Skv) * kHeadDim * 4);
   L.total = off;
   return L;
@@ -204,7 +211,8 @@ dit_status run_attention(const void* q, const void* k, const void* v, void* out,
                          int qk_esize, int qk_format, int pv_format, int B, int Hq, int Hkv, int Sq, int Skv,
                          int mode, int q_block, int k_block, float factor, const float* q_scale,
                          const float* k_scale, const float* v_scale, int32_t* skip_counts, float* lse,
-                         int* err, cudaStream_t stream, int q_hstride = 0, int kv_hstride = 0) {
+                         int* err, cudaStream_t stream, int q_hstride = 0, int kv_hstride = 0,
+                         const uint8_t* q_sf = nullptr, const uint8_t* k_sf = nullptr) {
   // q_hstride / kv_hstride: head counts of the full tensors' rows when q, k, v, out are head slices
   if (q_hstride == 0) q_hstride = Hq;
   if (kv_hstride == 0) kv_hstride = Hkv;
@@ -228,6 +236,8 @@ dit_status run_attention(const void* q, const void* k, const void* v, void* out,
   p.q_scale = q_scale; p.q_block = q_block; p.nqb = ceil_div(Sq, q_block);
   p.k_scale = k_scale; p.k_block = k_block; p.nkb = ceil_div(Skv, k_block);
   p.v_scale = v_scale;
+  p.q_sf = q_sf;
+  p.k_sf = k_sf;
   p.skip_counts = skip_counts;
   p.lse = lse;
   p.err = err;
@@ -289,6 +299,21 @@ dit_status fwd_impl(const void* q, const void* k, const void* v, void* out, int 
     return run_attention(q, k, v, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, QK_BF16, PV_BF16, B, Hq, Hkv, Sq, Skv,
                          mode, 1, 1, threshold_scale_factor, nullptr, nullptr, nullptr, skip_counts, lse, err, st);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (qk_dtype == DIT_QK_MXFP8) {
+    // MXFP8 Q/K + FP8 V: V scales and codes as in QK16PV8, Q/K codes with their E8M0 block scales
+    float* v_scale = reinterpret_cast<float*>(ws + L.v_scale);
+    uint8_t* q_sf = ws + L.q_scale;
+    uint8_t* k_sf = ws + L.k_scale;
+    cudaError_t e = launch_v_stats(v, B, Hkv, Skv, reinterpret_cast<float*>(ws + L.pmax), v_scale,
+                                   (mode & DIT_MODE_V_PER_TENSOR) != 0, st);
+    if (e == cudaSuccess) e = launch_quant_v(v, B, Hkv, Skv, v_scale, ws + L.v_codes, st);
+    if (e == cudaSuccess) e = launch_mx_quant(q, B, Sq, Hq, ws + L.q_codes, q_sf, st);
+    if (e == cudaSuccess) e = launch_mx_quant(k, B, Skv, Hkv, ws + L.k_codes, k_sf, st);
+    if (e != cudaSuccess) return from_cuda(e);
+    return run_attention(ws + L.q_codes, ws + L.k_codes, ws + L.v_codes, out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
+                         QK_MXF8, PV_E4M3, B, Hq, Hkv, Sq, Skv, mode, 1, 1, threshold_scale_factor, nullptr, nullptr,
+                         v_scale, skip_counts, lse, err, st, 0, 0, q_sf, k_sf);
+  }
   if (qk_dtype == DIT_QK_BF16) {
     // QK16PV8: V scales (per channel or one tensor-wide) and V codes; Q/K go to BMM1 as they are
     float* v_scale = reinterpret_cast<float*>(ws + L.v_scale);
@@ -348,7 +373,8 @@ dit_status sage_quantize_qkv(const void* q, const void* k, const void* v, int B,
                              int qk_dtype, int q_block, int k_block, void* q_codes, void* k_codes, void* v_codes,
                              float* q_scale, float* k_scale, float* v_scale, float* k_mean, void* workspace,
                              size_t workspace_bytes, void* stream) {
-  if (!valid_shape(B, Hq, Hkv, Sq, Skv) || !valid_mode(DIT_MODE_SAGE, qk_dtype, q_block, k_block, 0.0f))
+  if (!valid_shape(B, Hq, Hkv, Sq, Skv) || (qk_dtype != DIT_QK_INT8 && qk_dtype != DIT_QK_FP8_E4M3) ||
+      !valid_mode(DIT_MODE_SAGE, qk_dtype, q_block, k_block, 0.0f))
     return DIT_E_INVALID_ARG;
   if (B == 0) return DIT_OK;
   const void* ptrs[] = {k, v, k_codes, v_codes, k_scale, v_scale, k_mean};
@@ -377,7 +403,7 @@ dit_status sage_quantize_qkv_with_mean(const void* q, const void* k, const void*
                                        int Hq, int Hkv, int Sq, int Skv, int qk_dtype, int q_block, int k_block,
                                        void* q_codes, void* k_codes, void* v_codes, float* q_scale, float* k_scale,
                                        float* v_scale, void* workspace, size_t workspace_bytes, void* stream) {
-  if (!valid_shape(B, Hq, Hkv, Sq, Skv) || qk_dtype == DIT_QK_BF16 ||
+  if (!valid_shape(B, Hq, Hkv, Sq, Skv) || (qk_dtype != DIT_QK_INT8 && qk_dtype != DIT_QK_FP8_E4M3) ||
       !valid_mode(DIT_MODE_SAGE, qk_dtype, q_block, k_block, 0.0f))
     return DIT_E_INVALID_ARG;
   if (B == 0) return DIT_OK;
@@ -440,9 +466,9 @@ dit_status fwd_quantized_impl(const void* q_codes, const void* k_codes, const vo
                               int Skv, int mode, int qk_dtype, int q_block, int k_block, float threshold_scale_factor,
                               void* stream, void* workspace, size_t workspace_bytes, int32_t* skip_counts,
                               float* lse) {
-  if (!valid_shape(B, Hq, Hkv, Sq, Skv) || !(mode & DIT_MODE_SAGE) ||
+  if (!valid_shape(B, Hq, Hkv, Sq, Skv) || !(mode & DIT_MODE_SAGE) || qk_dtype == DIT_QK_MXFP8 ||
       !valid_mode(mode, qk_dtype, q_block, k_block, threshold_scale_factor))
-    return DIT_E_INVALID_ARG;
+    return DIT_E_INVALID_ARG;  // MXFP8 operands go through dit_attn_fwd_mxfp8
   if (B == 0 || Sq == 0) return DIT_OK;
   const bool qk16 = (qk_dtype == DIT_QK_BF16);  // QK16PV8: q_codes / k_codes are the BF16 Q / K, no Q/K scales
   const void* ptrs[] = {q_codes, k_codes, v_codes, v_scale, out};
@@ -504,6 +530,48 @@ dit_status dit_attn_fwd_quantized_lse(const void* q_codes, const void* k_codes, 
   return fwd_quantized_impl(q_codes, k_codes, v_codes, q_scale, k_scale, v_scale, out, B, Hq, Hkv, Sq, Skv, mode,
                             qk_dtype, q_block, k_block, threshold_scale_factor, stream, workspace, workspace_bytes,
                             skip_counts, lse);
+}
+
+dit_status mx_quantize_qk(const void* q, const void* k, int B, int Hq, int Hkv, int Sq, int Skv, void* q_codes,
+                          void* k_codes, uint8_t* q_sf, uint8_t* k_sf, void* stream) {
+  if (!valid_shape(B, Hq, Hkv, Sq, Skv)) return DIT_E_INVALID_ARG;
+  if (B == 0) return DIT_OK;
+  if (!k || !k_codes || !k_sf || !aligned16(k) || !aligned16(k_codes) || (reinterpret_cast<uintptr_t>(k_sf) & 3u))
+    return DIT_E_INVALID_ARG;
+  if (Sq > 0 && (!q || !q_codes || !q_sf || !aligned16(q) || !aligned16(q_codes) ||
+                 (reinterpret_cast<uintptr_t>(q_sf) & 3u)))
+    return DIT_E_INVALID_ARG;
+  int* err = nullptr;
+  const dit_status ds = prepare_device(&err);
+  if (ds != DIT_OK) return ds;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (Sq > 0) e = launch_mx_quant(q, B, Sq, Hq, q_codes, q_sf, st);
+  if (e == cudaSuccess) e = launch_mx_quant(k, B, Skv, Hkv, k_codes, k_sf, st);
+  return from_cuda(e);
+}
+
+dit_status dit_attn_fwd_mxfp8(const void* q_codes, const void* k_codes, const void* v_codes, const uint8_t* q_sf,
+                              const uint8_t* k_sf, const float* v_scale, void* out, float* lse, int B, int Hq,
+                              int Hkv, int Sq, int Skv, int mode, float threshold_scale_factor, void* stream,
+                              int32_t* skip_counts) {
+  if (!valid_shape(B, Hq, Hkv, Sq, Skv) || !(mode & DIT_MODE_SAGE) ||
+      !valid_mode(mode, DIT_QK_MXFP8, 0, 0, threshold_scale_factor))
+    return DIT_E_INVALID_ARG;
+  if (B == 0 || Sq == 0) return DIT_OK;
+  const void* ptrs[] = {q_codes, k_codes, v_codes, q_sf, k_sf, v_scale, out};
+  for (const void* ptr : ptrs)
+    if (!ptr) return DIT_E_INVALID_ARG;
+  if (!aligned16(q_codes) || !aligned16(k_codes) || !aligned16(v_codes) || !aligned16(out) ||
+      !aligned16(skip_counts) || (reinterpret_cast<uintptr_t>(q_sf) & 3u) ||
+      (reinterpret_cast<uintptr_t>(k_sf) & 3u) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return DIT_E_INVALID_ARG;
+  int* err = nullptr;
+  const dit_status ds = prepare_device(&err);
+  if (ds != DIT_OK) return ds;
+  return run_attention(q_codes, k_codes, v_codes, out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, QK_MXF8, PV_E4M3, B, Hq,
+                       Hkv, Sq, Skv, mode, 1, 1, threshold_scale_factor, nullptr, nullptr, v_scale, skip_counts, lse,
+                       err, static_cast<cudaStream_t>(stream), 0, 0, q_sf, k_sf);
 }
 
 dit_status dit_attn_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* out_host, void* q,

@@ -13,7 +13,8 @@ constexpr int kStatsChunk = 1024;  // tokens per CTA in the K-mean / V-absmax pa
 constexpr int kQuantRows = 256;    // tokens per CTA in the quantizers
 
 // Storage formats of the Q/K operands of BMM1 and the V operand of BMM2.
-enum QKFormat { QK_BF16 = 0, QK_F16 = 1, QK_E4M3 = 2 };  // QK_F16: INT8 codes held exactly as fp16
+// QK_F16: INT8 codes held exactly as fp16. QK_MXF8: E4M3 codes with E8M0 scales per 32 channels.
+enum QKFormat { QK_BF16 = 0, QK_F16 = 1, QK_E4M3 = 2, QK_MXF8 = 3 };
 enum PVFormat { PV_BF16 = 0, PV_E4M3 = 1 };
 
 // Output formats of the Q/K quantizer.
@@ -33,7 +34,9 @@ struct FmhaParams {
   int q_block, nqb;
   const float* k_scale;  // SAGE: [B, Hkv, nkb]
   int k_block, nkb;
-  const float* v_scale;  // E4M3 V (SAGE, QK16PV8): [B, Hkv, 128]
+  const float* v_scale;  // E4M3 V (SAGE, QK16PV8, MXFP8): [B, Hkv, 128]
+  const uint8_t* q_sf;   // MXFP8: E8M0 bytes [B, Hq, Sq, 4] (byte c scales channels 32c .. 32c+31)
+  const uint8_t* k_sf;   // MXFP8: E8M0 bytes [B, Hkv, Skv, 4]
   int32_t* skip_counts;  // optional [B, Hq, n_q_tiles]
   float* lse;            // optional [B, Hq, Sq]: ln sum_j exp(s_ij) of each query row
   int* err;              // device error word
@@ -52,6 +55,8 @@ cudaError_t launch_fmha_sage_f8(bool skip, const CUtensorMap& tq, const CUtensor
                                 const CUtensorMap& to, const FmhaParams& p, cudaStream_t stream);
 cudaError_t launch_fmha_qk16pv8(bool skip, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const CUtensorMap& to, const FmhaParams& p, cudaStream_t stream);
+cudaError_t launch_fmha_mxfp8(bool skip, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const CUtensorMap& to, const FmhaParams& p, cudaStream_t stream);
 
 // Quantize-prepass launchers (prepass.cu).
 cudaError_t launch_kv_stats(const void* k, const void* v, int B, int Hkv, int Skv, double* psum, float* pmax,
@@ -67,6 +72,8 @@ cudaError_t launch_quant_q(const void* q, int B, int Hq, int Sq, int q_block, in
 cudaError_t launch_quant_kv(const void* k, const void* v, int B, int Hkv, int Skv, int k_block, int code_out,
                             const float* k_mean, const float* v_scale, void* k_codes, float* k_scale, void* v_codes,
                             cudaStream_t stream);
+// MXFP8 codes of a [B, S, H, 128] BF16 tensor and its E8M0 scale bytes [B, H, S, 4].
+cudaError_t launch_mx_quant(const void* x, int B, int S, int H, void* codes, uint8_t* sf, cudaStream_t stream);
 cudaError_t launch_widen_i8(const int8_t* codes, size_t n, void* out_f16, cudaStream_t stream);
 cudaError_t launch_zero_i32(int32_t* p, size_t n, cudaStream_t stream);
 

@@ -1,5 +1,5 @@
 // Fused attention forward kernel for sm_103a (template; instantiated by fmha_dense.cu,
-// fmha_sage_i8.cu, fmha_sage_f8.cu and fmha_qk16pv8.cu): TMA-staged Q/K/V tiles, tcgen05 MMAs
+// fmha_sage_i8.cu, fmha_sage_f8.cu, fmha_qk16pv8.cu and fmha_mxfp8.cu): TMA-staged Q/K/V tiles, tcgen05 MMAs
 // accumulating S = Q K^T and O += P V in tensor memory, online softmax with exp2, optional SAGE
 // dequantization, P re-quantization to FP8 (SAGE and QK16PV8), and the Skip-Softmax tile test.
 //
@@ -12,7 +12,9 @@
 //   warps 1, 2   MMA issuers, one per Q tile (one elected lane each): BMM1 S_i = Q_i K_j^T (SS),
 //                BMM2 O_i += P_i V_j (V is MN-major, so no transpose). Warp 2 also allocates the 512
 //                tensor-memory columns (S0 | S1 | O0 | O1) at the start and frees them at the end.
-//   warp 3       stages the V scales (E4M3 V) and, in SAGE, the K-block scales of each KV tile.
+//   warp 3       stages the V scales (E4M3 V) and, in SAGE, the K-block scales of each KV tile; in
+//                MXFP8 the E8M0 block scales of Q and of each K tile, which the issuers copy into
+//                tensor memory for the block-scaled BMM1.
 //   warps 4-19   four softmax warpgroups: Q tile i = g / 2 and column half h = g % 2 for group g.
 //                A thread owns one row (= TMEM lane) and 64 of its 128 columns; the two halves
 //                of a row exchange partial maxima through shared memory. Halving the columns per
@@ -24,6 +26,10 @@
 // E4M3 P (SAGE and QK16PV8, 16 KB per tile): P goes to a shared-memory buffer and BMM2 is an SS MMA. S is free
 // as soon as the softmax has loaded it, so the issuer computes S_i(j+1) while the softmax works on
 // S_i(j); a per-tile barrier (o_done) returns P's buffer and O to the softmax after each BMM2.
+// MXFP8: the block-scaled MMA reads its scale factors from tensor memory, and S0 | S1 | O0 | O1 leave
+// no room, so the two tiles share one S buffer (S | O0 | O1 | scale factors): BMM1s alternate
+// between the tiles, each issued once the other tile's softmax has loaded the previous S. The
+// softmax groups then run about one BMM1 apart, and each S still lands before its softmax needs it.
 //
 // Numerics: logits are kept in log2 units (scaled by softmax_scale * log2 e). With BF16 P, O is
 // rescaled lazily (only when the running max grows by more than 8, P then stays below 2^8); with
@@ -59,18 +65,20 @@ constexpr int kSlots = 4;  // ring of K/V tiles: K_j in slot 2j mod 4, V_j in sl
 // buffers for the E4M3 P of the two query tiles, which BMM2 reads from shared memory.
 template <int QKF, int PVF>
 struct SmemLayout {
-  static constexpr uint32_t kKTile = 128u * 128u * (QKF == QK_E4M3 ? 1u : 2u);
+  static constexpr uint32_t kKTile = 128u * 128u * ((QKF == QK_E4M3 || QKF == QK_MXF8) ? 1u : 2u);
   static constexpr uint32_t kVTile = 128u * 128u * (PVF == PV_E4M3 ? 1u : 2u);
   static constexpr bool kPInSmem = (PVF == PV_E4M3);
   static constexpr uint32_t kQOff = 0;
   static constexpr uint32_t kKOff = 2 * 32768;
   static constexpr uint32_t kVOff = kKOff + 2 * kKTile;
   static constexpr uint32_t kPOff = kVOff + 2 * kVTile;
-  static constexpr uint32_t kKsOff = kPOff + (kPInSmem ? 2 * 16384 : 0);  // 4 x 128 floats
+  // 4 x 128 floats (SAGE K-block scales), or 4 x 512 bytes of K tiles' E8M0 scales (MXFP8)
+  static constexpr uint32_t kKsOff = kPOff + (kPInSmem ? 2 * 16384 : 0);
   static constexpr uint32_t kVsOff = kKsOff + kSlots * 512;                // 128 floats
   static constexpr uint32_t kXmaxOff = kVsOff + 512;        // [tile][half][parity][128] partial maxima
   static constexpr uint32_t kXlOff = kXmaxOff + 2 * 2 * 2 * 512;  // [tile][half][128] partial row sums
-  static constexpr uint32_t kBarOff = kXlOff + 2 * 2 * 512;
+  static constexpr uint32_t kSfaOff = kXlOff + 2 * 2 * 512;  // MXFP8: the Q tiles' E8M0 scales, 2 x 512 bytes
+  static constexpr uint32_t kBarOff = kSfaOff + (QKF == QK_MXF8 ? 2 * 512 : 0);
   static constexpr uint32_t kSmemBytes = kBarOff + 512 + 1024;     // + alignment slack
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
@@ -90,6 +98,7 @@ struct Bars {
   uint64_t drain[2];
   uint64_t s_free[2];   // SAGE: the tile's softmax has loaded S (BMM1 of the next KV tile may overwrite it)
   uint64_t o_done[2];   // SAGE: BMM2 of the tile's latest KV tile is complete (P buffer free, O stable)
+  uint64_t sfa_full;    // MXFP8: the Q tiles' scale factors are in shared memory
   uint32_t tmem_base;
   int abort_flag;
   int skip_flag[2];
@@ -107,15 +116,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     fmha_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                     const FmhaParams p) {
-  constexpr bool kQKScaled = (QKF != QK_BF16);  // Q/K codes with token-block scales (SAGE)
-  constexpr bool kPV8 = (PVF == PV_E4M3);        // E4M3 P and V with per-channel V scales (SAGE, QK16PV8)
-  constexpr int kQKBytes = (QKF == QK_E4M3) ? 1 : 2;
+  constexpr bool kQKScaled = (QKF == QK_F16 || QKF == QK_E4M3);  // Q/K codes with token-block scales (SAGE)
+  constexpr bool kMX = (QKF == QK_MXF8);         // block-scaled MXFP8 Q/K (scales applied inside BMM1)
+  constexpr bool kPV8 = (PVF == PV_E4M3);        // E4M3 P and V with per-channel V scales (SAGE, QK16PV8, MXFP8)
+  constexpr int kQKBytes = (QKF == QK_E4M3 || kMX) ? 1 : 2;
   constexpr int kPVBytes = (PVF == PV_E4M3) ? 1 : 2;
   constexpr uint32_t kQTileBytes = 128u * 128u * kQKBytes;
   constexpr uint32_t kVTileBytes = 128u * 128u * kPVBytes;
   constexpr int kMma1Kind = (QKF == QK_E4M3) ? KIND_F8F6F4 : KIND_F16;
   constexpr int kMma2Kind = (PVF == PV_E4M3) ? KIND_F8F6F4 : KIND_F16;
-  constexpr int kK1Steps = (QKF == QK_E4M3) ? 4 : 8;  // K = 128 in steps of 32 (8-bit) or 16
+  constexpr int kK1Steps = (kQKBytes == 1) ? 4 : 8;  // K = 128 in steps of 32 (8-bit) or 16
+  // tensor-memory columns: S and O of tile i; MXFP8 adds 4 columns of Q scales and 4 of K scales per tile
+  constexpr uint32_t kColS1 = kMX ? 0 : 128, kColO0 = kMX ? 128 : 256, kColSfa = 384, kColSfb = 392;
   constexpr int kK2Steps = (PVF == PV_E4M3) ? 4 : 8;
   constexpr uint32_t kIdesc1 = (QKF == QK_BF16)  ? make_idesc(1, 1, 0, 0, 128, 128)
                                : (QKF == QK_F16) ? make_idesc(0, 0, 0, 0, 128, 128)
@@ -147,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->kv_full[s], 1);
       mbar_init(&bars->kv_empty[s], 2);  // one commit from each MMA issuer
       mbar_init(&bars->ks_full[s], 32);
-      mbar_init(&bars->ks_empty[s], 16);  // one arrival per softmax warp
+      mbar_init(&bars->ks_empty[s], kMX ? 2 : 16);  // SAGE: one arrival per softmax warp; MXFP8: per issuer
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
@@ -155,6 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->o_full[i], 1);
     }
     mbar_init(&bars->vs_full, 32);
+    mbar_init(&bars->sfa_full, 32);
     mbar_init(&bars->drain[0], 1);
     mbar_init(&bars->drain[1], 1);
     for (int i = 0; i < 2; ++i) {
@@ -239,8 +252,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t aq = make_sdesc_sw128(sbase + L::kQOff + i * 32768, 16, 1024);
     const uint64_t dk0 = make_sdesc_sw128(sbase + L::kKOff, 16, 1024);
     const uint64_t dv0 = make_sdesc_sw128(sbase + L::kVOff, kPVBytes == 2 ? 16384 : 8192, 1024);
-    const uint32_t d_s = tbase + 128 * i;
-    const uint32_t d_o = tbase + 256 + 128 * i;
+    const uint32_t d_s = tbase + kColS1 * i;
+    const uint32_t d_o = tbase + kColO0 + 128 * i;
+    const uint32_t t_sfa = tbase + kColSfa + 4 * i, t_sfb = tbase + kColSfb + 4 * i;  // MXFP8 scale factors
     volatile int* skip_flag = bars->skip_flag;
     auto wait = [&](uint64_t* bar, int parity) {
       return __all_sync(0xffffffffu, mbar_wait_bounded(bar, (uint32_t)parity, budget, abort_flag));
@@ -249,13 +263,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     // descriptor start address advances in 16-byte units inside its low 14 bits.
     auto bmm1 = [&](int j) {  // S_i = Q_i K_j^T, then release K_j's slot
       const uint64_t bk = dk0 + (uint64_t)(((j & 1) * L::kKTile) >> 4);
+      if constexpr (kMX) {
+        // K_j's scale words into tensor memory (ordered before the MMAs below), then the four
+        // 32-wide K slices, each using its byte of every Q and K scale word
+        tmem_cp_32x128b_x4_if(leader, t_sfb, make_sdesc_rows16(sbase + L::kKsOff + (j & 3) * 512));
 #pragma unroll
-      for (int kk = 0; kk < kK1Steps; ++kk) {
-        const uint32_t off = (kQKBytes == 2) ? (kk >> 2) * 16384 + (kk & 3) * 32 : kk * 32;
-        mma_ss_if<kMma1Kind>(leader, d_s, aq + (off >> 4), bk + (off >> 4), kIdesc1, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < 4; ++kk)
+          mma_mxf8_if(leader, d_s, aq + (uint64_t)((kk * 32) >> 4), bk + (uint64_t)((kk * 32) >> 4),
+                      make_idesc_mxf8(128, 128, kk), t_sfa, t_sfb, kk > 0 ? 1u : 0u);
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < kK1Steps; ++kk) {
+          const uint32_t off = (kQKBytes == 2) ? (kk >> 2) * 16384 + (kk & 3) * 32 : kk * 32;
+          mma_ss_if<kMma1Kind>(leader, d_s, aq + (off >> 4), bk + (off >> 4), kIdesc1, kk > 0 ? 1u : 0u);
+        }
       }
       mma_commit_if(leader, &bars->s_full[i]);
       mma_commit_if(leader, &bars->kv_empty[(2 * j) & 3]);
+      if constexpr (kMX) mma_commit_if(leader, &bars->ks_empty[j & 3]);  // the scales' slot
+    };
+    // May S_i(j) be written? With a buffer per tile: once this tile's softmax has loaded S_i(j-1).
+    // MXFP8 (one S for both tiles, BMM1s in the order Q0 Q1 Q0 Q1 ...): once the other tile's
+    // softmax has loaded the S computed just before, which also orders every earlier BMM1 of this
+    // issuer (and its reads of the scale columns) before the new one.
+    auto s_writable = [&](int j) -> bool {
+      if constexpr (kMX) {
+        return (i == 0) ? (j == 0 || wait(&bars->s_free[1], (j - 1) & 1)) : wait(&bars->s_free[0], j & 1);
+      } else {
+        return j == 0 || wait(&bars->s_free[i], (j - 1) & 1);
+      }
+    };
+    auto k_ready = [&](int j) -> bool {  // K_j staged (and, in MXFP8, its scales)
+      const int tk = 2 * j;
+      bool r = wait(&bars->kv_full[tk & 3], (tk >> 2) & 1);
+      if constexpr (kMX) r = r && wait(&bars->ks_full[j & 3], (j >> 2) & 1);
+      return r;
     };
     if constexpr (L::kPInSmem) {
       // E4M3 P in shared memory: BMM1 of the next KV tile overwrites S as soon as the softmax has
@@ -263,15 +305,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       // BMM2 is an SS MMA (P K-major, V MN-major); o_done tells the softmax when P's buffer and O
       // are free again.
       const uint64_t ap = make_sdesc_sw128(sbase + L::kPOff + i * 16384, 16, 1024);
-      if (ok) ok = wait(&bars->kv_full[0], 0);
+      if constexpr (kMX) {
+        // this Q tile's scale words, once, ahead of every MMA that reads them
+        if (ok) ok = wait(&bars->sfa_full, 0);
+        if (ok) {
+          tc_fence_after();
+          tmem_cp_32x128b_x4_if(leader, t_sfa, make_sdesc_rows16(sbase + L::kSfaOff + i * 512));
+        }
+      }
+      if (ok) ok = s_writable(0) && k_ready(0);
       if (ok) {
         tc_fence_after();
         bmm1(0);
       }
       for (int j = 0; j < nt && ok; ++j) {
         if (j + 1 < nt) {
-          const int tk = 2 * (j + 1);
-          ok = wait(&bars->s_free[i], j & 1) && wait(&bars->kv_full[tk & 3], (tk >> 2) & 1);
+          ok = s_writable(j + 1) && k_ready(j + 1);
           if (!ok) break;
           tc_fence_after();
           bmm1(j + 1);
@@ -335,6 +384,55 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int e = 0; e < 4; ++e) s_vs[lane * 4 + e] = vs[lane * 4 + e];
       mbar_arrive(&bars->vs_full);
     }
+    if constexpr (kMX) {
+      // E8M0 scale words (4 bytes per row: channels 32c .. 32c+31 in byte c) of the two Q tiles once,
+      // then of every K tile through the ring. A 128-row tile's words go to a 32 x 16-byte matrix
+      // whose row l holds the words of rows l, l+32, l+64, l+96: the tensor-memory copy puts them in
+      // columns 0-3 of lane l of each lane quarter, where the MMA reads row 32c + l from column c.
+      // Rows past the end get 0 (their codes are zero, as TMA fills them).
+      const uint32_t* qsf = reinterpret_cast<const uint32_t*>(p.q_sf) + ((size_t)b * p.Hq + hq) * p.Sq;
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        uint32_t w[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int row = q0 + 128 * t + 32 * c + lane;
+          w[c] = row < p.Sq ? __ldg(qsf + row) : 0u;
+        }
+        *reinterpret_cast<uint4*>(smem + L::kSfaOff + t * 512 + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bars->sfa_full);
+      const uint32_t* ksf = reinterpret_cast<const uint32_t*>(p.k_sf) + ((size_t)b * p.Hkv + hkv) * p.Skv;
+      auto load_tile = [&](int j, uint32_t* w) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int key = 128 * j + 32 * c + lane;
+          w[c] = (j < nt && key < p.Skv) ? __ldg(ksf + key) : 0u;
+        }
+      };
+      constexpr int kAhead = 4;
+      uint32_t pre[kAhead][4];
+#pragma unroll
+      for (int d = 0; d < kAhead; ++d) load_tile(d, pre[d]);
+      for (int j = 0; j < nt; ++j) {
+        const int e = j & 3, u = j >> 2;
+        const bool ok = mbar_wait_bounded(&bars->ks_empty[e], (u & 1) ^ 1, budget, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
+          if (lane == 0) record_timeout(p, bars);
+          break;
+        }
+        *reinterpret_cast<uint4*>(smem + L::kKsOff + e * 512 + lane * 16) =
+            make_uint4(pre[0][0], pre[0][1], pre[0][2], pre[0][3]);
+        fence_proxy_async_smem();
+        mbar_arrive(&bars->ks_full[e]);
+#pragma unroll
+        for (int d = 0; d + 1 < kAhead; ++d)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) pre[d][c] = pre[d + 1][c];
+        load_tile(j + kAhead, pre[kAhead - 1]);
+      }
+    }
     if constexpr (kQKScaled) {
       bool ok = true;
       const float* ks = p.k_scale + ((size_t)b * p.Hkv + hkv) * p.nkb;
@@ -380,8 +478,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = g & 1;                           // column half: S/O columns 64h .. 64h+63
     const int r = ((warp & 3) << 5) + lane;        // row within the tile == TMEM lane
     const uint32_t lane_base = (uint32_t)((warp & 3) << 5) << 16;
-    const uint32_t t_s = tbase + lane_base + 128 * i + 64 * h;
-    const uint32_t t_o = tbase + lane_base + 256 + 128 * i + 64 * h;
+    const uint32_t t_s = tbase + lane_base + kColS1 * i + 64 * h;
+    const uint32_t t_o = tbase + lane_base + kColO0 + 128 * i + 64 * h;
     const int qrow = q0 + 128 * i + r;
     const bool row_valid = qrow < p.Sq;
     const uint32_t tile_bar = 1 + i;               // the 256 threads of this Q tile

@@ -333,6 +333,48 @@ __global__ void __launch_bounds__(256) quant_tokens_kernel(const __nv_bfloat16* 
   }
 }
 
+// ------------------------------------------------------------------ MXFP8 quantizer
+// MXFP8 codes of a [B, S, H, 128] BF16 tensor, one E8M0 scale per 32 channels of a token (OCP MX
+// v1.0 conversion, as "VisualGen Quantized Attention" names MXFP8 Q/K with blocks of 32 along the
+// head dimension): shared exponent e = floor(log2 amax) - 8 clamped to [-127, 127], elements
+// E4M3(x / 2^e) rounded to nearest even with saturation. With E the biased float32 exponent of
+// amax (0 for zero and subnormals), the stored byte e + 127 is max(E - 8, 0), and x / 2^e is the
+// exact product x * 2^(127 - byte) (IEEE multiply, subnormal results kept).
+// Four consecutive lanes hold one block (8 channels each, one 16-byte load) and exchange the block
+// max with two shuffles; the loop runs per warp, so every shuffle has all 32 lanes.
+__global__ void __launch_bounds__(256) mx_quant_kernel(const uint4* __restrict__ x, int S, int H, long long nvec,
+                                                       uint2* __restrict__ codes, uint8_t* __restrict__ sf) {
+  const int lane = threadIdx.x & 31;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long wb = (long long)blockIdx.x * blockDim.x + (threadIdx.x & ~31); wb < nvec; wb += stride) {
+    const long long i = wb + lane;  // 16-byte vector: row i / 16 = (b * S + s) * H + h, block (i / 4) % 4
+    const bool valid = i < nvec;
+    uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+    if (valid) raw = ld_stream_v4(x + i);
+    float f[8];
+    bf16x8_to_f32(raw, f);
+    float a = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) a = fmaxf(a, fabsf(f[e]));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+    const int byte = max((int)(__float_as_uint(a) >> 23) - 8, 0);
+    const float mult = __uint_as_float((uint32_t)(254 - byte) << 23);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] = __fmul_rn(f[e], mult);
+    uint2 w;
+    w.x = e4m3x2(f[0], f[1]) | (e4m3x2(f[2], f[3]) << 16);
+    w.y = e4m3x2(f[4], f[5]) | (e4m3x2(f[6], f[7]) << 16);
+    if (valid) {
+      codes[i] = w;
+      if ((lane & 3) == 0) {
+        const long long row = i >> 4, t = row / H, s = t % S, b = t / S, h = row % H;
+        sf[((b * H + h) * S + s) * 4 + ((i >> 2) & 3)] = (uint8_t)byte;
+      }
+    }
+  }
+}
+
 __global__ void widen_i8_kernel(const int8_t* __restrict__ in, size_t n8, __half* __restrict__ out) {
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
     const uint2 w = *reinterpret_cast<const uint2*>(in + i * 8);
@@ -446,6 +488,14 @@ cudaError_t launch_quant_kv(const void* k, const void* v, int B, int Hkv, int Sk
   }
   if (e != cudaSuccess) return e;
   return launch_quant_v(v, B, Hkv, Skv, v_scale, v_codes, stream);
+}
+
+cudaError_t launch_mx_quant(const void* x, int B, int S, int H, void* codes, uint8_t* sf, cudaStream_t stream) {
+  const long long nvec = (long long)B * S * H * (kHeadDim / 8);
+  if (nvec == 0) return cudaSuccess;
+  mx_quant_kernel<<<grid_for(nvec, 256), 256, 0, stream>>>(static_cast<const uint4*>(x), S, H, nvec,
+                                                            static_cast<uint2*>(codes), sf);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_widen_i8(const int8_t* codes, size_t n, void* out_f16, cudaStream_t stream) {

@@ -277,10 +277,46 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t fmt_a, uint32_t fmt_b
          ((M >> 4) << 24);
 }
 
+// Instruction descriptor of the block-scaled kind::mxf8f6f4 MMA with E4M3 A and B (K-major), f32 D
+// and E8M0 scale factors (bit 23). sf_id (bits 29-30 for A, 4-5 for B) picks the byte of each
+// scale-factor word that this MMA's 32-wide K slice uses.
+__host__ __device__ constexpr uint32_t make_idesc_mxf8(uint32_t M, uint32_t N, uint32_t sf_id) {
+  return (sf_id << 4) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) | (sf_id << 29);
+}
+
 // Shared-memory matrix descriptor with 128-byte swizzling. `lbo`/`sbo` in bytes.
 __device__ __forceinline__ uint64_t make_sdesc_sw128(uint32_t smem_addr, uint32_t lbo, uint32_t sbo) {
   return (uint64_t)((smem_addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Shared-memory matrix descriptor without swizzling for rows of 16 bytes stored one after another
+// (8-row core matrices of 128 bytes, consecutive): both byte offsets are 128.
+__device__ __forceinline__ uint64_t make_sdesc_rows16(uint32_t smem_addr) {
+  return (uint64_t)((smem_addr & 0x3FFFFu) >> 4) | ((uint64_t)(128 >> 4) << 16) | ((uint64_t)(128 >> 4) << 32) |
+         (1ull << 46);
+}
+
+// Copy a 32-row x 16-byte shared-memory matrix into four tensor-memory columns of lanes 0-31,
+// repeated in each lane quarter (32-127): lane 32q + l, column c receives bytes 4c..4c+3 of row l.
+// Issued by one thread; ordered before the MMAs that thread issues after it.
+__device__ __forceinline__ void tmem_cp_32x128b_x4_if(uint32_t pred, uint32_t taddr, uint64_t sdesc) {
+  asm volatile(
+      "{\n .reg .pred q;\n setp.ne.b32 q, %2, 0;\n"
+      " @q tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n}\n" ::"r"(taddr),
+      "l"(sdesc), "r"(pred)
+      : "memory");
+}
+
+// D[tmem] (+)= (A * 2^sfA) (B * 2^sfB)^T with E4M3 A/B in shared memory and their E8M0 block
+// scales in tensor memory (one per row per 32-wide K slice).
+__device__ __forceinline__ void mma_mxf8_if(uint32_t pred, uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                            uint32_t sfa, uint32_t sfb, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.b32 p, %6, 0;\n setp.ne.b32 q, %7, 0;\n"
+      " @q tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc), "r"(pred)
+      : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05: TMEM <-> registers

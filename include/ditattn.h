@@ -16,6 +16,13 @@
  *          scale per channel ("VisualGen Quantized Attention", section "QK16PV8 Attention Kernels
  *          in the CUTEDSL Backend", and the quant_attention_config table: v_block_size 0 = one
  *          tensor-wide V scale, 1 = one scale per channel).
+ *          With qk_dtype DIT_QK_MXFP8, SAGE is the MXFP8 Q/K + FP8 V recipe: Q and K become E4M3
+ *          codes with one E8M0 (power-of-two) scale per 32 channels of each token, applied inside
+ *          BMM1 by the block-scaled tensor-core MMA, and V is FP8 as in QK16PV8 ("VisualGen
+ *          Quantized Attention", section "MXFP8 and NVFP4 in the CUTEDSL and FlashInfer backends":
+ *          fixed blocks of 32 elements, q/k block sizes 0, v_block_size 0 or 1). The scale rule is
+ *          the OCP Microscaling v1.0 conversion: exponent floor(log2 amax) - 8, clamped to
+ *          [-127, 127]; elements round to nearest even and saturate at 448. K is not smoothed.
  *   SKIP   Skip-Softmax: a 128-column KV tile's exp and P.V work is skipped for a 128-row Q
  *          tile when every valid row has exp(m_tile - m_run) < threshold, with
  *          threshold = threshold_scale_factor / Skv ("SAGE + Skip-Softmax -- API Design & Test
@@ -57,20 +64,22 @@ typedef enum dit_status {
 } dit_status;
 
 /* Mode bits (or-able): DIT_MODE_SAGE | DIT_MODE_SKIP is SAGE with Skip-Softmax.
- * DIT_MODE_V_PER_TENSOR is valid only with DIT_MODE_SAGE and DIT_QK_BF16 (QK16PV8): V gets one
+ * DIT_MODE_V_PER_TENSOR is valid only with DIT_MODE_SAGE and DIT_QK_BF16 (QK16PV8) or DIT_QK_MXFP8: V gets one
  * tensor-wide scale, max |V| over the whole [B, Skv, Hkv, 128] tensor / 448 (v_block_size 0);
  * without it V is scaled per (batch, kv head, channel) (v_block_size 1). */
 enum { DIT_MODE_DENSE = 0, DIT_MODE_SAGE = 1, DIT_MODE_SKIP = 2, DIT_MODE_V_PER_TENSOR = 4 };
 
 /* Q/K element type. DENSE uses BF16; SAGE takes INT8 or FP8 E4M3 ("TRTLLM Attention" user guide,
- * SAGE table: dtype_qk in {int8, fp8_e4m3}), or BF16 for QK16PV8. */
-enum { DIT_QK_BF16 = 0, DIT_QK_INT8 = 1, DIT_QK_FP8_E4M3 = 2 };
+ * SAGE table: dtype_qk in {int8, fp8_e4m3}), BF16 for QK16PV8, or MXFP8 ("VisualGen Quantized
+ * Attention", quant_attention_config table: qk_dtype "mxfp8"). */
+enum { DIT_QK_BF16 = 0, DIT_QK_INT8 = 1, DIT_QK_FP8_E4M3 = 2, DIT_QK_MXFP8 = 3 };
 
 /* Rows and columns of one attention tile; skip counts are kept per 128-row Q tile. */
 enum { DIT_HEAD_DIM = 128, DIT_TILE = 128 };
 
 /* Version of this interface (2: QK16PV8, DIT_MODE_V_PER_TENSOR, sage_quantize_v, the LSE outputs,
- * sage_quantize_qkv_with_mean and dit_attn_fwd_host). */
+ * sage_quantize_qkv_with_mean and dit_attn_fwd_host; 3: DIT_QK_MXFP8, mx_quantize_qk and
+ * dit_attn_fwd_mxfp8). */
 int dit_abi_version(void);
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -79,7 +88,8 @@ const char* dit_status_string(dit_status status);
 /*
  * Bytes of device workspace dit_attn_fwd needs for these arguments: 0 for DENSE (with or without
  * SKIP), otherwise room for the quantized codes, their scales and the K-mean / V-absmax partials
- * (QK16PV8: the V codes, V scales and V-absmax partials only).
+ * (QK16PV8: the V codes, V scales and V-absmax partials only; MXFP8: Q/K codes and scale bytes,
+ * V codes, V scales and V-absmax partials).
  * Returns 0 for arguments dit_attn_fwd would reject.
  */
 size_t dit_attn_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int mode, int qk_dtype, int q_block,
@@ -92,11 +102,11 @@ size_t dit_attn_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int mod
  *   k, v       device bf16 [B, Skv, Hkv, 128]
  *   out        device bf16 [B, Sq, Hq, 128], written completely
  *   mode       DIT_MODE_* bits
- *   qk_dtype   DIT_QK_BF16 without SAGE; DIT_QK_INT8, DIT_QK_FP8_E4M3 or (QK16PV8) DIT_QK_BF16
- *              with SAGE
+ *   qk_dtype   DIT_QK_BF16 without SAGE; DIT_QK_INT8, DIT_QK_FP8_E4M3, (QK16PV8) DIT_QK_BF16 or
+ *              DIT_QK_MXFP8 with SAGE
  *   q_block, k_block   SAGE with INT8/FP8: tokens per Q / K scale block, each in {1, 4, 16}
- *              ("TRTLLM Attention" user guide, SAGE table); QK16PV8: both must be 0; ignored
- *              without SAGE
+ *              ("TRTLLM Attention" user guide, SAGE table); QK16PV8 and MXFP8: both must be 0;
+ *              ignored without SAGE
  *   threshold_scale_factor   with SKIP: finite and >= 0, threshold = factor / Skv (0 never
  *              skips and gives the same output as the mode without SKIP); ignored without SKIP
  *   workspace  device scratch of at least dit_attn_workspace_bytes(...) bytes, 256-byte
@@ -118,8 +128,9 @@ dit_status dit_attn_fwd(const void* q, const void* k, const void* v, void* out, 
  *
  *   lse   device float [B, Hq, Sq], 4-byte aligned, not NULL: ln sum_j exp(s_ij) over the row's
  *         logits s_ij as the mode computes them (softmax scale applied; SAGE: from the codes and
- *         scales of the K-smoothed K, so lower by q_i . mean / sqrt(128) than for the raw K; with
- *         SKIP only the KV tiles that were not skipped contribute)
+ *         scales of the K-smoothed K, so lower by q_i . mean / sqrt(128) than for the raw K;
+ *         MXFP8: from the dequantized Q and K, no smoothing; with SKIP only the KV tiles that were
+ *         not skipped contribute)
  * All other arguments, results and errors are those of dit_attn_fwd.
  */
 dit_status dit_attn_fwd_lse(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
@@ -248,6 +259,7 @@ size_t dit_attn_quantized_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk
  * mode must include DIT_MODE_SAGE; the other arguments are as for dit_attn_fwd. For QK16PV8
  * (qk_dtype DIT_QK_BF16, q_block = k_block = 0) q_codes and k_codes are the BF16 Q and K,
  * q_scale and k_scale are unused (may be NULL), and v_codes / v_scale come from sage_quantize_v.
+ * MXFP8 operands go through dit_attn_fwd_mxfp8 (qk_dtype DIT_QK_MXFP8 is rejected here).
  */
 dit_status dit_attn_fwd_quantized(const void* q_codes, const void* k_codes, const void* v_codes,
                                   const float* q_scale, const float* k_scale, const float* v_scale, void* out, int B,
@@ -261,6 +273,45 @@ dit_status dit_attn_fwd_quantized_lse(const void* q_codes, const void* k_codes, 
                                       float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int mode, int qk_dtype,
                                       int q_block, int k_block, float threshold_scale_factor, void* stream,
                                       void* workspace, size_t workspace_bytes, int32_t* skip_counts);
+
+/*
+ * The MXFP8 Q/K prepass alone ("VisualGen Quantized Attention", section "MXFP8 and NVFP4 in the
+ * CUTEDSL and FlashInfer backends": Q/K in fixed blocks of 32 elements along the head dimension);
+ * V goes through sage_quantize_v. For every token and head, each block of 32 channels
+ * 32c .. 32c+31 gets the exponent e = floor(log2 amax) - 8 of the OCP Microscaling v1.0
+ * conversion (amax = the block's max |x|; e clamped to [-127, 127]; a zero block gets -127) and
+ * its elements become E4M3(x / 2^e), round to nearest even, saturating at +-448.
+ *
+ *   q, k       device bf16 [B, Sq, Hq, 128] / [B, Skv, Hkv, 128]; q may be NULL when Sq == 0
+ *   q_codes    device [B, Sq, Hq, 128] E4M3 bit patterns (16-byte aligned)
+ *   k_codes    device [B, Skv, Hkv, 128] E4M3 bit patterns (16-byte aligned)
+ *   q_sf       device uint8 [B, Hq, Sq, 4]: the E8M0 byte e + 127 of each block (4-byte aligned)
+ *   k_sf       device uint8 [B, Hkv, Skv, 4]
+ * The codes and scale bytes are those the MXFP8 path of dit_attn_fwd computes, bit for bit.
+ */
+dit_status mx_quantize_qk(const void* q, const void* k, int B, int Hq, int Hkv, int Sq, int Skv, void* q_codes,
+                          void* k_codes, uint8_t* q_sf, uint8_t* k_sf, void* stream);
+
+/*
+ * Attention over MXFP8 Q/K (from mx_quantize_qk) and FP8 V (from sage_quantize_v, per channel or
+ * tensor-wide): BMM1 applies the E8M0 block scales inside the block-scaled MMA, the rest is the
+ * QK16PV8 path.
+ *
+ *   q_codes, k_codes, q_sf, k_sf   as mx_quantize_qk writes them
+ *   v_codes, v_scale               as sage_quantize_v writes them
+ *   out        device bf16 [B, Sq, Hq, 128]
+ *   lse        NULL, or device float [B, Hq, Sq] (4-byte aligned) for each row's log-sum-exp, as
+ *              dit_attn_fwd_lse describes
+ *   mode       must include DIT_MODE_SAGE; DIT_MODE_SKIP and threshold_scale_factor as for
+ *              dit_attn_fwd; DIT_MODE_V_PER_TENSOR is accepted and changes nothing here (the V
+ *              scales are given)
+ *   skip_counts   as for dit_attn_fwd
+ * Needs no workspace. Sq == 0 or B == 0 is a no-op.
+ */
+dit_status dit_attn_fwd_mxfp8(const void* q_codes, const void* k_codes, const void* v_codes, const uint8_t* q_sf,
+                              const uint8_t* k_sf, const float* v_scale, void* out, float* lse, int B, int Hq,
+                              int Hkv, int Sq, int Skv, int mode, float threshold_scale_factor, void* stream,
+                              int32_t* skip_counts);
 
 /*
  * Synchronizes `stream`, then reports and clears the device error word: DIT_OK, or

@@ -157,3 +157,21 @@ def test_dit_qk16pv8_32k_v_prepass_bit_exact_and_sampled_tiles():
     for b, h, t in case.sample_tiles():
         o, _, rows = oatt.attention_q_tile(case.inp, b, h, t, mode="qk16pv8", quant=want)
         assert _rel(_np(out[b, rows, h]), o) <= SAGE_REL, (b, h, t)
+
+
+def test_dit_mxfp8_32k_prepass_bit_exact_and_sampled_tiles():
+    # MXFP8 Q/K + per-channel FP8 V (the CUTEDSL recipe's block sizes (0, 0, 1)) on the DiT inputs
+    from oracle import mx_quant
+    case = _case("dit_mxfp8_32k")
+    want = mx_quant.mxfp8_quantize(case.inp["q"], case.inp["k"], case.inp["v"], per_tensor=False)
+    got = dit.mx_quantize_qk(case.gpu[0], case.gpu[1])
+    torch.cuda.synchronize()
+    for name in ["q_sf", "k_sf", "q_codes", "k_codes"]:
+        bad = np.count_nonzero(got[name].cpu().numpy() != want[name])
+        assert bad == 0, f"{name}: {bad} differ"
+    del got
+    out = dit.dit_attn_fwd(*case.gpu, mode=dit.MODE_SAGE, qk_dtype="mxfp8", q_block=0, k_block=0)
+    dit.dit_attn_check_errors()
+    for b, h, t in case.sample_tiles():
+        o, _, rows = oatt.attention_q_tile(case.inp, b, h, t, mode="mxfp8", quant=want)
+        assert _rel(_np(out[b, rows, h]), o) <= SAGE_REL, (b, h, t)
