@@ -16,8 +16,9 @@ Readings where the pages are silent (each is pinned in tests/test_oracle_mx.py):
    with amax = max |x| over the block and 8 the exponent of E4M3's largest power of two (256).
    e is clamped to the E8M0 range [-127, 127]. A zero block (amax = 0) takes e = -127.
 3. Elements are E4M3(x / X), round to nearest even with saturation to +-448 (the same
-   encoder as SAGE's, ``formats.e4m3_encode``). x / X is exact in float32 (X is a power of two
-   and the quotient stays within float32's normal range for bfloat16 inputs). Because
+   encoder as SAGE's, ``formats.e4m3_encode``). x / X is computed as the float32 product
+   x * 2^-e: exact unless it falls below float32's normal range (a block spanning more than
+   2^126), where it is far below E4M3's smallest step and its code is zero either way. Because
    amax / X lies in [256, 512), a block's largest elements can saturate at 448: that is the
    specification's rule, kept as is.
 4. There is no K-smoothing: the pages attach smoothing to SageAttention only.
