@@ -19,6 +19,8 @@ What the oracle computes, and where each step comes from:
 * ``mx_quant``     -- MXFP8 Q/K: E4M3 elements with one E8M0 scale per 32 channels of a token
   (OCP MX rule), no smoothing ("VisualGen Quantized Attention", section "MXFP8 and NVFP4 in the
   CUTEDSL and FlashInfer backends"); V as in QK16PV8.
+* ``nvfp4_quant``  -- NVFP4 Q/K: FP4 E2M1 elements, one E4M3 scale per 16 channels of a token and
+  one float32 scale per tensor (same section); V as in QK16PV8.
 * ``attention``    -- dense attention written out untiled, and the tiled online-softmax
   loop (128x128 tiles, KV tiles in ascending order) used for SAGE and Skip-Softmax
   ("SAGE + Skip-Softmax -- API Design & Test Plan", Part 1 §4 mapping table:

@@ -34,6 +34,8 @@ Readings where the pages are silent:
 * MXFP8 Q/K + FP8 V ("VisualGen Quantized Attention", section "MXFP8 and NVFP4 in the CUTEDSL and
   FlashInfer backends"): the logits of the block-scaled codes (``mx_quant.mx_scores`` times the
   softmax scale), and P and V exactly as in QK16PV8.
+* NVFP4 Q/K + FP8 V (same section): the logits of the two-level-scaled FP4 codes
+  (``nvfp4_quant.nvfp4_scores`` times the softmax scale), and P and V exactly as in QK16PV8.
 * LSE ("VisualGen Quantized Attention", section "Requirements and behavior": a backend that
   produces LSE composes with Attention2D / Ring context parallelism): per query row,
   ln sum_j exp(s_ij) over the row's logits s as the mode defines them (natural log), i.e.
@@ -51,6 +53,7 @@ import numpy as np
 
 from . import formats
 from . import mx_quant
+from . import nvfp4_quant
 
 HEAD_DIM = 128
 SOFTMAX_SCALE = 1.0 / math.sqrt(HEAD_DIM)
@@ -169,10 +172,11 @@ def attention_q_tile(inputs: dict, b: int, hq: int, tile: int, *, mode: str, qk_
     """Oracle output of one 128-row Q tile of one (batch, query head).
 
     inputs: dict with float32 arrays 'q' [B,Sq,Hq,128], 'k', 'v' [B,Skv,Hkv,128] holding bf16 values.
-    mode:   'dense', 'sage', 'qk16pv8' or 'mxfp8'; ``factor`` switches Skip-Softmax on (threshold =
-            factor / Skv).
+    mode:   'dense', 'sage', 'qk16pv8', 'mxfp8' or 'nvfp4'; ``factor`` switches Skip-Softmax on
+            (threshold = factor / Skv).
     quant:  the output of ``sage_quant.sage_quantize`` (mode 'sage'), ``sage_quant.qk16pv8_quantize``
-            (mode 'qk16pv8') or ``mx_quant.mxfp8_quantize`` (mode 'mxfp8').
+            (mode 'qk16pv8'), ``mx_quant.mxfp8_quantize`` (mode 'mxfp8') or
+            ``nvfp4_quant.nvfp4_qk_quantize`` (mode 'nvfp4').
     Returns (O [rows, 128] float64, skipped tile count, row indices), plus the rows' LSE
     (float64) last when ``with_lse``.
     """
@@ -197,6 +201,11 @@ def attention_q_tile(inputs: dict, b: int, hq: int, tile: int, *, mode: str, qk_
     elif mode == "mxfp8":
         s = SOFTMAX_SCALE * mx_quant.mx_scores(quant["q_codes"][b, r0:r1, hq, :], quant["q_sf"][b, hq, r0:r1, :],
                                                quant["k_codes"][b, :, g, :], quant["k_sf"][b, g, :, :])
+        vals, vscale, quantize_p = formats.e4m3_decode(quant["v_codes"][b, :, g, :]), quant["v_scale"][b, g, :], True
+    elif mode == "nvfp4":
+        s = SOFTMAX_SCALE * nvfp4_quant.nvfp4_scores(quant["q_codes"][b, r0:r1, hq, :], quant["q_sf"][b, hq, r0:r1, :],
+                                                     quant["q_gs"], quant["k_codes"][b, :, g, :],
+                                                     quant["k_sf"][b, g, :, :], quant["k_gs"])
         vals, vscale, quantize_p = formats.e4m3_decode(quant["v_codes"][b, :, g, :]), quant["v_scale"][b, g, :], True
     else:
         raise ValueError(f"unknown mode {mode!r}")

@@ -3,7 +3,8 @@
 FP8 E4M3 is the format the pages name for SAGE Q/K ("fp8_e4m3") and for V, which "is
 always quantized per channel to FP8 E4M3" ("TRTLLM Attention" user guide, section "SAGE
 quantization"). INT8 is the other Q/K option there. The pages give neither bit layout
-nor rounding rule, so these readings apply (each is pinned in tests/test_oracle_formats.py):
+nor rounding rule, so these readings apply (each is pinned in tests/test_oracle_formats.py; the
+FP4 E2M1 element type of NVFP4 is defined with its encoder below):
 
 * E4M3 is the "fn" variant: 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits,
   no infinities, a single NaN mantissa pattern (S.1111.111), largest finite 448,
@@ -79,6 +80,51 @@ def _e4m3_encode_slice(x) -> np.ndarray:
     code = np.where(nan, 0x7F, code)
     code = np.where(neg, code | 0x80, code)
     return code.astype(np.uint8)
+
+
+# FP4 E2M1 (the NVFP4 element type): 1 sign bit, 2 exponent bits with bias 1, 1 mantissa bit; the
+# eight magnitudes of codes 0..7, no infinities or NaN. Largest finite 6, subnormal 0.5.
+E2M1_VALUES = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+E2M1_MAX = 6.0
+
+
+def e2m1_encode(x) -> np.ndarray:
+    """Round real values to E2M1 codes (uint8 in 0..15, sign in bit 3).
+
+    Round to nearest, ties to the even code (even mantissa bit); magnitudes above 6 saturate to
+    6; the sign of a value that rounds to zero is kept (code 8 for negative zero).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    neg = np.signbit(x)
+    a = np.minimum(np.abs(x), E2M1_MAX)
+    d = np.abs(a[..., None] - E2M1_VALUES)                 # exact for float32 / float64 inputs
+    best = d.min(axis=-1, keepdims=True)
+    cand = d == best                                        # one code, or two adjacent ones on a tie
+    even = cand & (np.arange(8) % 2 == 0)
+    code = np.where(even.any(axis=-1), np.argmax(even, axis=-1), np.argmax(cand, axis=-1))
+    return np.where(neg, code | 8, code).astype(np.uint8)
+
+
+def e2m1_decode(codes) -> np.ndarray:
+    """Value of each E2M1 code (0..15) as float64."""
+    c = np.asarray(codes).astype(np.int64)
+    val = E2M1_VALUES[c & 7]
+    return np.where(c & 8, -val, val)
+
+
+def pack_nibbles(codes) -> np.ndarray:
+    """Pack 4-bit codes along the last axis two per byte: element 2i in bits 0-3, 2i+1 in bits 4-7."""
+    c = np.asarray(codes).astype(np.uint8)
+    return (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
+
+
+def unpack_nibbles(packed) -> np.ndarray:
+    """Inverse of ``pack_nibbles``."""
+    p = np.asarray(packed).astype(np.uint8)
+    out = np.empty(p.shape[:-1] + (2 * p.shape[-1],), np.uint8)
+    out[..., 0::2] = p & 0xF
+    out[..., 1::2] = p >> 4
+    return out
 
 
 def int8_code(x) -> np.ndarray:

@@ -64,7 +64,7 @@ def mx_quantize(x: np.ndarray):
     amax = np.abs(blocks).max(axis=4)                          # [B, S, H, 4]
     e = shared_exponent(amax)                                  # [B, S, H, 4]
     inv = np.ldexp(np.float32(1.0), (-e).astype(np.int32)).astype(np.float32)
-    quot = (blocks * inv[..., None]).astype(np.float32)        # x / 2^e, exact
+    quot = (blocks * inv[..., None]).astype(np.float32)        # x / 2^e (reading 3)
     codes = formats.e4m3_encode(quot).reshape(B, S, H, D)
     sf = (e + E8M0_BIAS).astype(np.uint8)
     return codes, np.ascontiguousarray(sf.transpose(0, 2, 1, 3))

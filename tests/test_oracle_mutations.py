@@ -178,3 +178,38 @@ def test_unquantized_q_k_in_mxfp8_attention_is_caught(monkeypatch):
         return good(inputs, b, hq, tile, **kw)
     monkeypatch.setattr(att, "attention_q_tile", dense_logits)
     _fails(TM.test_mxfp8_attention_is_qk16pv8_attention_of_the_dequantized_q_and_k)
+
+
+# ---- NVFP4 Q/K (E2M1 elements, E4M3 block scales per 16 channels, float32 tensor scale)
+from oracle import nvfp4_quant  # noqa: E402
+
+from . import test_oracle_nvfp4 as TN  # noqa: E402
+
+
+def test_swapped_nibble_order_is_caught(monkeypatch):
+    monkeypatch.setattr(formats, "pack_nibbles",
+                        lambda c: (np.asarray(c, np.uint8)[..., 1::2] | (np.asarray(c, np.uint8)[..., 0::2] << 4)))
+    _fails(TN.test_nibble_packing_order)
+
+
+def test_e2m1_ties_away_from_zero_is_caught(monkeypatch):
+    good = formats.e2m1_encode
+    monkeypatch.setattr(formats, "e2m1_encode", lambda x: good(np.asarray(x, np.float64) * (1 + 2.0 ** -30)))
+    _fails(TN.test_e2m1_rounding_table, 2.5, 4)
+
+
+def test_per_head_tensor_scale_is_caught(monkeypatch):
+    good = nvfp4_quant.nvfp4_quantize
+
+    def per_head(x, scale=None):
+        outs = [good(x[:, :, h:h + 1]) for h in range(x.shape[2])]
+        packed = np.concatenate([o[0] for o in outs], axis=2)
+        sf = np.concatenate([o[1] for o in outs], axis=1)
+        return packed, sf, outs[0][2]
+    monkeypatch.setattr(nvfp4_quant, "nvfp4_quantize", per_head)
+    _fails(TN.test_block_bytes_follow_the_block_max_in_head_major_layout)
+
+
+def test_missing_tensor_scale_is_caught(monkeypatch):
+    monkeypatch.setattr(nvfp4_quant, "tensor_scale", lambda x: np.float32(1.0))
+    _fails(TN.test_hand_derived_blocks)

@@ -40,8 +40,8 @@ class Workload:
     Sq: int
     Skv: int
     kind: str = "iid"            # iid | koffset | outlier | video
-    mode: str = "dense"          # dense | sage | qk16pv8 (V per tensor) | mxfp8 (V per channel)
-    qk_dtype: str = "bf16"       # bf16 | int8 | fp8_e4m3 | mxfp8
+    mode: str = "dense"          # dense | sage | qk16pv8 (V per tensor) | mxfp8, nvfp4 (V per channel)
+    qk_dtype: str = "bf16"       # bf16 | int8 | fp8_e4m3 | mxfp8 | nvfp4
     q_block: int = 1
     k_block: int = 16
     factors: tuple = ()          # Skip-Softmax threshold_scale_factor values (empty: no skip)
@@ -59,7 +59,7 @@ class Workload:
 VIDEO_GRID = (21, 45, 80)
 
 # The five workloads the measurements are quoted on, plus the QK16PV8 recipe (BF16 Q/K, FP8 V
-# with one tensor-wide scale) and the MXFP8 Q/K + FP8 V recipe (per-channel V) on the DiT inputs.
+# with one tensor-wide scale) and the MXFP8 and NVFP4 Q/K + FP8 V recipes (per-channel V) on the DiT inputs.
 WORKLOADS = {
     "tiny_dense_256": Workload("tiny_dense_256", 1, 2, 2, 256, 256),
     "dit_dense_32k": Workload("dit_dense_32k", 1, 40, 40, 32768, 32768, kind="koffset"),
@@ -71,6 +71,8 @@ WORKLOADS = {
                                 qk_dtype="bf16", q_block=0, k_block=0),
     "dit_mxfp8_32k": Workload("dit_mxfp8_32k", 1, 40, 40, 32768, 32768, kind="koffset", mode="mxfp8",
                               qk_dtype="mxfp8", q_block=0, k_block=0),
+    "dit_nvfp4_32k": Workload("dit_nvfp4_32k", 1, 40, 40, 32768, 32768, kind="koffset", mode="nvfp4",
+                              qk_dtype="nvfp4", q_block=0, k_block=0),
     "video_skip_int8_75600": Workload("video_skip_int8_75600", 1, 40, 40, 75600, 75600, kind="video", mode="sage",
                                       qk_dtype="int8", q_block=1, k_block=16, factors=(0.0, 50.0, 200.0, 800.0, 3200.0),
                                       grid=VIDEO_GRID),
