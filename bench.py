@@ -249,14 +249,17 @@ def run_modes(dit, steps, warmup, world, stream, peak16, hbm_gbs):
     res = {}
     peak8 = 2.0 * peak16                               # FP8 dense = 2 x BF16 (nominal ratio)
     peak_mix = 2.0 * peak16 * peak8 / (peak16 + peak8)  # BMM1 on 16-bit operands, BMM2 on FP8
+    peak4 = 4.0 * peak16                               # FP4 dense = 4 x BF16 (nominal ratio)
+    peak_nv = 2.0 * peak4 * peak8 / (peak4 + peak8)     # BMM1 on FP4, BMM2 on FP8
     table = [("dit_sage_int8_32k", peak_mix, "BMM1 f16 + BMM2 e4m3 harmonic peak"),
              ("gqa_sage_fp8_16k", peak8, "2 x measured bf16 (e4m3 nominal ratio)"),
              ("dit_qk16pv8_32k", peak_mix, "BMM1 bf16 + BMM2 e4m3 harmonic peak"),
-             ("dit_mxfp8_32k", peak8, "2 x measured bf16 (e4m3 nominal ratio; BMM1 block-scaled)")]
+             ("dit_mxfp8_32k", peak8, "2 x measured bf16 (e4m3 nominal ratio; BMM1 block-scaled)"),
+             ("dit_nvfp4_32k", peak_nv, "BMM1 fp4 (4 x bf16) + BMM2 e4m3 (2 x bf16) harmonic peak")]
     for name, peak, peak_desc in table:
         w = workloads.WORKLOADS[name]
         q, k, v = workloads.generate(w, seed=1, device="cuda")
-        qk16, mx = w.mode == "qk16pv8", w.mode == "mxfp8"
+        qk16, mx, nv = w.mode == "qk16pv8", w.mode == "mxfp8", w.mode == "nvfp4"
         mode = dit.MODE_SAGE | (dit.MODE_V_PER_TENSOR if qk16 else 0)
         ws = torch.empty(dit.dit_attn_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, mode, w.qk_dtype,
                                                       w.q_block, w.k_block), dtype=torch.uint8, device="cuda")
@@ -269,13 +272,22 @@ def run_modes(dit, steps, warmup, world, stream, peak16, hbm_gbs):
         tf = w.dense_equiv_flop / (ms * 1e-3) / 1e12
         entry = {"ms": round(ms, 3), "tflops": round(tf, 1), "peak_tflops": round(peak, 1),
                  "frac": round(tf / peak, 3), "peak": peak_desc,
-                 "launches_per_step": 4 if qk16 else 6 if mx else 5}
+                 "launches_per_step": 4 if qk16 else 6 if mx else 9 if nv else 5}
         # the two halves, through the split entry points
         bq, bkv = q.numel() * 2, k.numel() * 2
         if qk16:
             pre = lambda: dit.sage_quantize_v(v, per_tensor=True, stream=stream)  # noqa: E731
             # V read twice (absmax, then codes), 1-byte codes written
             pre_bytes, pre_desc = 2 * bkv + bkv // 2, "V read twice, 1-byte V codes written"
+        elif nv:
+            def pre():
+                res = dit.nvfp4_quantize_qk(q, k, stream=stream)
+                res.update(dit.sage_quantize_v(v, per_tensor=False, stream=stream))
+                return res
+            # Q, K read twice (tensor max, then codes), V twice; half-byte Q/K codes, 1-byte V codes and
+            # 8 scale bytes per 128 Q/K elements written
+            pre_bytes = 2 * bq + 4 * bkv + (bq + bkv) // 4 + bkv // 2 + (bq + bkv) // 32
+            pre_desc = "Q, K, V read twice, half-byte Q/K codes, 1-byte V codes and E4M3 block scales written"
         elif mx:
             def pre():
                 res = dit.mx_quantize_qk(q, k, stream=stream)
@@ -298,6 +310,8 @@ def run_modes(dit, steps, warmup, world, stream, peak16, hbm_gbs):
         def attn():
             if mx:
                 dit.dit_attn_fwd_mxfp8(quant, out, mode=mode, stream=stream)
+            elif nv:
+                dit.dit_attn_fwd_nvfp4(quant, out, mode=mode, stream=stream)
             else:
                 dit.dit_attn_fwd_quantized(quant, out, mode=mode, qk_dtype=w.qk_dtype, q_block=w.q_block,
                                            k_block=w.k_block, stream=stream)

@@ -9,7 +9,8 @@ Modes follow the pages ("TRTLLM Attention" user guide): dense BF16; SAGE with IN
 Q/K per token block (block sizes 1, 4, 16) and per-channel FP8 V; QK16PV8 (SAGE with BF16 Q/K:
 only V in FP8, per channel or with one tensor-wide scale, "VisualGen Quantized Attention");
 MXFP8 Q/K + FP8 V (SAGE with qk_dtype "mxfp8": E4M3 Q/K with one E8M0 scale per 32 channels of
-a token, applied inside BMM1, same page); Skip-Softmax with threshold = threshold_scale_factor / Skv.
+a token, applied inside BMM1, same page); NVFP4 Q/K + FP8 V (qk_dtype "nvfp4": E2M1 Q/K with one
+E4M3 scale per 16 channels and one float32 scale per tensor); Skip-Softmax with threshold = threshold_scale_factor / Skv.
 """
 
 from __future__ import annotations
@@ -21,12 +22,12 @@ import os
 import torch
 
 MODE_DENSE, MODE_SAGE, MODE_SKIP, MODE_V_PER_TENSOR = 0, 1, 2, 4
-QK_BF16, QK_INT8, QK_FP8_E4M3, QK_MXFP8 = 0, 1, 2, 3
+QK_BF16, QK_INT8, QK_FP8_E4M3, QK_MXFP8, QK_NVFP4 = 0, 1, 2, 3, 4
 HEAD_DIM = 128
 TILE = 128
 STATUS_NAMES = {0: "DIT_OK", 1: "DIT_E_INVALID_ARG", 2: "DIT_E_UNSUPPORTED", 3: "DIT_E_CUDA", 4: "DIT_E_TIMEOUT",
                 5: "DIT_E_WORKSPACE"}
-QK_DTYPES = {"bf16": QK_BF16, "int8": QK_INT8, "fp8_e4m3": QK_FP8_E4M3, "mxfp8": QK_MXFP8}
+QK_DTYPES = {"bf16": QK_BF16, "int8": QK_INT8, "fp8_e4m3": QK_FP8_E4M3, "mxfp8": QK_MXFP8, "nvfp4": QK_NVFP4}
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libditattn.so")
 
@@ -50,6 +51,8 @@ SIGNATURES = {
     "sage_quantize_qkv_with_mean": (_c_int, [_vp] * 4 + [_c_int] * 8 + [_vp] * 7 + [_c_size, _vp]),
     "mx_quantize_qk": (_c_int, [_vp, _vp] + [_c_int] * 5 + [_vp] * 5),
     "dit_attn_fwd_mxfp8": (_c_int, [_vp] * 8 + [_c_int] * 6 + [_c_float, _vp, _vp]),
+    "nvfp4_quantize_qk": (_c_int, [_vp, _vp] + [_c_int] * 5 + [_vp] * 7),
+    "dit_attn_fwd_nvfp4": (_c_int, [_vp] * 10 + [_c_int] * 6 + [_c_float, _vp, _vp]),
     "dit_attn_check_errors": (_c_int, [_vp]),
 }
 
@@ -293,6 +296,40 @@ def dit_attn_fwd_mxfp8(quant: dict, out, *, mode=MODE_SAGE, threshold_scale_fact
                                    _ptr(quant["k_sf"]), _ptr(quant["v_scale"]), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq,
                                    Skv, mode, float(threshold_scale_factor), _stream(stream), _ptr(skip_counts))
     _check(st, "dit_attn_fwd_mxfp8")
+    return out
+
+
+def nvfp4_quantize_qk(q, k, *, stream=None):
+    """The NVFP4 Q/K prepass alone: packed E2M1 codes ``q_codes`` [B, Sq, Hq, 64], ``k_codes``
+    [B, Skv, Hkv, 64] (channel 2i in the low nibble), E4M3 block-scale bytes ``q_sf`` [B, Hq, Sq, 8],
+    ``k_sf`` [B, Hkv, Skv, 8], and the float32 tensor scales ``q_gs``, ``k_gs`` (one element each)."""
+    B, Hq, Hkv, Sq, Skv = _shape(q, k)
+    dev = q.device
+    gs = torch.empty(2, dtype=torch.float32, device=dev)
+    res = dict(q_codes=torch.empty((B, Sq, Hq, HEAD_DIM // 2), dtype=torch.uint8, device=dev),
+               k_codes=torch.empty((B, Skv, Hkv, HEAD_DIM // 2), dtype=torch.uint8, device=dev),
+               q_sf=torch.empty((B, Hq, Sq, 8), dtype=torch.uint8, device=dev),
+               k_sf=torch.empty((B, Hkv, Skv, 8), dtype=torch.uint8, device=dev),
+               q_gs=gs[0:1], k_gs=gs[1:2])
+    st = _lib().nvfp4_quantize_qk(_ptr(q), _ptr(k), B, Hq, Hkv, Sq, Skv, _ptr(res["q_codes"]), _ptr(res["k_codes"]),
+                                  _ptr(res["q_sf"]), _ptr(res["k_sf"]), _ptr(res["q_gs"]), _ptr(res["k_gs"]),
+                                  _stream(stream))
+    _check(st, "nvfp4_quantize_qk")
+    return res
+
+
+def dit_attn_fwd_nvfp4(quant: dict, out, *, mode=MODE_SAGE, threshold_scale_factor=0.0, stream=None,
+                       skip_counts=None, lse=None):
+    """Attention over NVFP4 Q/K (``nvfp4_quantize_qk``) and FP8 V (``sage_quantize_v``), both results
+    merged in ``quant``."""
+    qc, kc = quant["q_codes"], quant["k_codes"]
+    B, Sq, Hq, _ = qc.shape
+    _, Skv, Hkv, _ = kc.shape
+    st = _lib().dit_attn_fwd_nvfp4(_ptr(qc), _ptr(kc), _ptr(quant["v_codes"]), _ptr(quant["q_sf"]),
+                                   _ptr(quant["k_sf"]), _ptr(quant["q_gs"]), _ptr(quant["k_gs"]),
+                                   _ptr(quant["v_scale"]), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Skv, mode,
+                                   float(threshold_scale_factor), _stream(stream), _ptr(skip_counts))
+    _check(st, "dit_attn_fwd_nvfp4")
     return out
 
 

@@ -17,7 +17,7 @@ using namespace ditattn;
 
 namespace {
 
-constexpr int kAbiVersion = 3;
+constexpr int kAbiVersion = 4;
 constexpr unsigned long long kWaitBudgetNs = 4000000000ull;  // far beyond any legitimate wait
 
 __device__ int g_device_error = 0;
@@ -41,9 +41,9 @@ bool valid_shape(int B, int Hq, int Hkv, int Sq, int Skv) {
 bool valid_mode(int mode, int qk_dtype, int q_block, int k_block, float factor) {
   if (mode < 0 || mode > (DIT_MODE_SAGE | DIT_MODE_SKIP | DIT_MODE_V_PER_TENSOR)) return false;
   if (mode & DIT_MODE_SAGE) {
-    if (qk_dtype == DIT_QK_BF16 || qk_dtype == DIT_QK_MXFP8) {
-      // QK16PV8: Q/K stay BF16; MXFP8: Q/K carry their own blocks of 32 channels. Either way the
-      // token-block sizes are 0 (the pages' block sizes (0, 0, v)); V per channel or per tensor.
+    if (qk_dtype == DIT_QK_BF16 || qk_dtype == DIT_QK_MXFP8 || qk_dtype == DIT_QK_NVFP4) {
+      // QK16PV8: Q/K stay BF16; MXFP8 / NVFP4: Q/K carry their own blocks of 32 / 16 channels. Either way
+      // the token-block sizes are 0 (the pages' block sizes (0, 0, v)); V per channel or per tensor.
       if (q_block != 0 || k_block != 0) return false;
     } else {
       if (qk_dtype != DIT_QK_INT8 && qk_dtype != DIT_QK_FP8_E4M3) return false;
@@ -61,24 +61,29 @@ bool valid_mode(int mode, int qk_dtype, int q_block, int k_block, float factor) 
 }
 
 struct SageLayout {
-  size_t q_codes, k_codes, v_codes, q_scale, k_scale, v_scale, k_mean, psum, pmax, total;
+  size_t q_codes, k_codes, v_codes, q_scale, k_scale, v_scale, k_mean, psum, pmax, gs, total;
 };
 
 // Workspace of the all-in-one call. QK16PV8 (BF16 Q/K) needs only the V codes, V scales and the
 // V-absmax partials; its Q/K regions have size zero. MXFP8 holds 1-byte Q/K codes and, in the
-// scale regions, 4 E8M0 bytes per token and head; it has no K mean.
+// scale regions, 4 E8M0 bytes per token and head; NVFP4 holds half-byte codes, 8 E4M3 bytes per
+// token and head and the two tensor scales. Neither has a K mean.
 SageLayout sage_layout(int B, int Hq, int Hkv, int Sq, int Skv, int qk_dtype, int q_block, int k_block) {
   SageLayout L{};
   const bool qk16 = (qk_dtype == DIT_QK_BF16);
   const bool mx = (qk_dtype == DIT_QK_MXFP8);
-  const size_t code_bytes = qk16 ? 0 : (qk_dtype == DIT_QK_INT8) ? 2 : 1;  // INT8 codes are held as exact fp16
-  const size_t q_scale_bytes = qk16 ? 0 : mx ? (size_t)B * Hq * Sq * 4 : (size_t)B * Hq * ceil_div(Sq, q_block) * 4;
+  const bool nv = (qk_dtype == DIT_QK_NVFP4);
+  // bytes per 128-channel row of codes: INT8 codes are held as exact fp16, NVFP4 packs two per byte
+  const size_t row_bytes = qk16 ? 0 : (qk_dtype == DIT_QK_INT8) ? 256 : nv ? 64 : 128;
+  const size_t sf_row = mx ? 4 : 8;  // block-scale bytes per token and head
+  const size_t q_scale_bytes =
+      qk16 ? 0 : (mx || nv) ? (size_t)B * Hq * Sq * sf_row : (size_t)B * Hq * ceil_div(Sq, q_block) * 4;
   const size_t k_scale_bytes =
-      qk16 ? 0 : mx ? (size_t)B * Hkv * Skv * 4 : (size_t)B * Hkv * ceil_div(Skv, k_block) * 4;
-  const bool smooth = !qk16 && !mx;
+      qk16 ? 0 : (mx || nv) ? (size_t)B * Hkv * Skv * sf_row : (size_t)B * Hkv * ceil_div(Skv, k_block) * 4;
+  const bool smooth = !qk16 && !mx && !nv;
   size_t off = 0;
-  L.q_codes = off; off = align256(off + (size_t)B * Sq * Hq * kHeadDim * code_bytes);
-  L.k_codes = off; off = align256(off + (size_t)B * Skv * Hkv * kHeadDim * code_bytes);
+  L.q_codes = off; off = align256(off + (size_t)B * Sq * Hq * row_bytes);
+  L.k_codes = off; off = align256(off + (size_t)B * Skv * Hkv * row_bytes);
   L.v_codes = off; off = align256(off + (size_t)B * Skv * Hkv * kHeadDim);
   L.q_scale = off; off = align256(off + q_scale_bytes);
   L.k_scale = off; off = align256(off + k_scale_bytes);
@@ -86,6 +91,7 @@ SageLayout sage_layout(int B, int Hq, int Hkv, int Sq, int Skv, int qk_dtype, in
   L.k_mean = off;  off = align256(off + (smooth ? (size_t)B * Hkv * kHeadDim * 4 : 0));
   L.psum = off;    off = align256(off + (smooth ? (size_t)B * Hkv * stats_chunks(Skv) * kHeadDim * 8 : 0));
   L.pmax = off;    off = align256(off + (size_t)B * Hkv * stats_chunks(Skv) * kHeadDim * 4);
+  L.gs = off;      off = align256(off + (nv ? 2 * sizeof(float) : 0));
   L.total = off;
   return L;
 }
@@ -150,16 +156,19 @@ dit_status prepare_device(int** err_out) {
 // [B, S, H, 128] tensor as a 4-D map {128, S, H, B} with boxes of {box_inner, 128, 1, 1}
 // (box_inner * element size = 128 bytes) and 128-byte swizzling. Hstride >= H is the head count of
 // the tensor's rows: H heads starting at ptr form a slice of a [B, S, Hstride, 128] tensor.
+// packed4: NVFP4 codes, two per byte: 64-byte rows as a {64, S, H, B} byte tensor, boxes of
+// {64, 128, 1, 1} with 64-byte swizzling.
 bool encode_map(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int esize, int B, int S, int H,
-                int Hstride) {
-  const cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)S, (cuuint64_t)H, (cuuint64_t)B};
-  const cuuint64_t row = (cuuint64_t)kHeadDim * esize;
+                int Hstride, bool packed4 = false) {
+  const cuuint64_t inner = packed4 ? kHeadDim / 2 : kHeadDim;
+  const cuuint64_t dims[4] = {inner, (cuuint64_t)S, (cuuint64_t)H, (cuuint64_t)B};
+  const cuuint64_t row = inner * esize;
   const cuuint64_t strides[3] = {row * (cuuint64_t)Hstride, row, row * (cuuint64_t)Hstride * (cuuint64_t)S};
-  const cuuint32_t box[4] = {(cuuint32_t)(128 / esize), 128, 1, 1};
+  const cuuint32_t box[4] = {(cuuint32_t)(packed4 ? 64 : 128 / esize), 128, 1, 1};
   const cuuint32_t es[4] = {1, 1, 1, 1};
   const CUresult r = g_encode(m, dt, 4, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                              packed4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -212,7 +221,8 @@ dit_status run_attention(const void* q, const void* k, const void* v, void* out,
                          int mode, int q_block, int k_block, float factor, const float* q_scale,
                          const float* k_scale, const float* v_scale, int32_t* skip_counts, float* lse,
                          int* err, cudaStream_t stream, int q_hstride = 0, int kv_hstride = 0,
-                         const uint8_t* q_sf = nullptr, const uint8_t* k_sf = nullptr) {
+                         const uint8_t* q_sf = nullptr, const uint8_t* k_sf = nullptr,
+                         const float* q_gs = nullptr, const float* k_gs = nullptr) {
   // q_hstride / kv_hstride: head counts of the full tensors' rows when q, k, v, out are head slices
   if (q_hstride == 0) q_hstride = Hq;
   if (kv_hstride == 0) kv_hstride = Hkv;
@@ -220,8 +230,9 @@ dit_status run_attention(const void* q, const void* k, const void* v, void* out,
   const CUtensorMapDataType pv_dt =
       (pv_format == PV_BF16) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const int pv_esize = (pv_format == PV_BF16) ? 2 : 1;
-  if (!encode_map(&tq, q, qk_dt, qk_esize, B, Sq, Hq, q_hstride) ||
-      !encode_map(&tk, k, qk_dt, qk_esize, B, Skv, Hkv, kv_hstride) ||
+  const bool packed4 = (qk_format == QK_NVF4);
+  if (!encode_map(&tq, q, qk_dt, qk_esize, B, Sq, Hq, q_hstride, packed4) ||
+      !encode_map(&tk, k, qk_dt, qk_esize, B, Skv, Hkv, kv_hstride, packed4) ||
       !encode_map(&tv, v, pv_dt, pv_esize, B, Skv, Hkv, kv_hstride) ||
       !encode_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, Sq, Hq, q_hstride))
     return DIT_E_CUDA;
@@ -238,6 +249,8 @@ dit_status run_attention(const void* q, const void* k, const void* v, void* out,
   p.v_scale = v_scale;
   p.q_sf = q_sf;
   p.k_sf = k_sf;
+  p.q_gs = q_gs;
+  p.k_gs = k_gs;
   p.skip_counts = skip_counts;
   p.lse = lse;
   p.err = err;
@@ -299,6 +312,21 @@ dit_status fwd_impl(const void* q, const void* k, const void* v, void* out, int 
     return run_attention(q, k, v, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, QK_BF16, PV_BF16, B, Hq, Hkv, Sq, Skv,
                          mode, 1, 1, threshold_scale_factor, nullptr, nullptr, nullptr, skip_counts, lse, err, st);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (qk_dtype == DIT_QK_NVFP4) {
+    // NVFP4 Q/K + FP8 V: V as in QK16PV8; Q/K codes, block scales and the two tensor scales
+    float* v_scale = reinterpret_cast<float*>(ws + L.v_scale);
+    float* gs = reinterpret_cast<float*>(ws + L.gs);
+    cudaError_t e = launch_v_stats(v, B, Hkv, Skv, reinterpret_cast<float*>(ws + L.pmax), v_scale,
+                                   (mode & DIT_MODE_V_PER_TENSOR) != 0, st);
+    if (e == cudaSuccess) e = launch_quant_v(v, B, Hkv, Skv, v_scale, ws + L.v_codes, st);
+    if (e == cudaSuccess)
+      e = launch_nvfp4_quant(q, k, B, Hq, Hkv, Sq, Skv, ws + L.q_codes, ws + L.k_codes, ws + L.q_scale,
+                             ws + L.k_scale, gs, gs + 1, st);
+    if (e != cudaSuccess) return from_cuda(e);
+    return run_attention(ws + L.q_codes, ws + L.k_codes, ws + L.v_codes, out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
+                         QK_NVF4, PV_E4M3, B, Hq, Hkv, Sq, Skv, mode, 1, 1, threshold_scale_factor, nullptr, nullptr,
+                         v_scale, skip_counts, lse, err, st, 0, 0, ws + L.q_scale, ws + L.k_scale, gs, gs + 1);
+  }
   if (qk_dtype == DIT_QK_MXFP8) {
     // MXFP8 Q/K + FP8 V: V scales and codes as in QK16PV8, Q/K codes with their E8M0 block scales
     float* v_scale = reinterpret_cast<float*>(ws + L.v_scale);
@@ -467,8 +495,8 @@ dit_status fwd_quantized_impl(const void* q_codes, const void* k_codes, const vo
                               void* stream, void* workspace, size_t workspace_bytes, int32_t* skip_counts,
                               float* lse) {
   if (!valid_shape(B, Hq, Hkv, Sq, Skv) || !(mode & DIT_MODE_SAGE) || qk_dtype == DIT_QK_MXFP8 ||
-      !valid_mode(mode, qk_dtype, q_block, k_block, threshold_scale_factor))
-    return DIT_E_INVALID_ARG;  // MXFP8 operands go through dit_attn_fwd_mxfp8
+      qk_dtype == DIT_QK_NVFP4 || !valid_mode(mode, qk_dtype, q_block, k_block, threshold_scale_factor))
+    return DIT_E_INVALID_ARG;  // MXFP8 / NVFP4 operands go through dit_attn_fwd_mxfp8 / dit_attn_fwd_nvfp4
   if (B == 0 || Sq == 0) return DIT_OK;
   const bool qk16 = (qk_dtype == DIT_QK_BF16);  // QK16PV8: q_codes / k_codes are the BF16 Q / K, no Q/K scales
   const void* ptrs[] = {q_codes, k_codes, v_codes, v_scale, out};
@@ -572,6 +600,48 @@ dit_status dit_attn_fwd_mxfp8(const void* q_codes, const void* k_codes, const vo
   return run_attention(q_codes, k_codes, v_codes, out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, QK_MXF8, PV_E4M3, B, Hq,
                        Hkv, Sq, Skv, mode, 1, 1, threshold_scale_factor, nullptr, nullptr, v_scale, skip_counts, lse,
                        err, static_cast<cudaStream_t>(stream), 0, 0, q_sf, k_sf);
+}
+
+dit_status nvfp4_quantize_qk(const void* q, const void* k, int B, int Hq, int Hkv, int Sq, int Skv, void* q_codes,
+                            void* k_codes, uint8_t* q_sf, uint8_t* k_sf, float* q_scale, float* k_scale,
+                            void* stream) {
+  if (!valid_shape(B, Hq, Hkv, Sq, Skv)) return DIT_E_INVALID_ARG;
+  if (B == 0) return DIT_OK;
+  if (!k || !k_codes || !k_sf || !k_scale || !aligned16(k) || !aligned16(k_codes) ||
+      (reinterpret_cast<uintptr_t>(k_sf) & 7u) || (reinterpret_cast<uintptr_t>(k_scale) & 3u))
+    return DIT_E_INVALID_ARG;
+  if (Sq > 0 && (!q || !q_codes || !q_sf || !q_scale || !aligned16(q) || !aligned16(q_codes) ||
+                 (reinterpret_cast<uintptr_t>(q_sf) & 7u) || (reinterpret_cast<uintptr_t>(q_scale) & 3u)))
+    return DIT_E_INVALID_ARG;
+  int* err = nullptr;
+  const dit_status ds = prepare_device(&err);
+  if (ds != DIT_OK) return ds;
+  return from_cuda(launch_nvfp4_quant(Sq > 0 ? q : nullptr, k, B, Hq, Hkv, Sq, Skv, q_codes, k_codes, q_sf, k_sf,
+                                      q_scale, k_scale, static_cast<cudaStream_t>(stream)));
+}
+
+dit_status dit_attn_fwd_nvfp4(const void* q_codes, const void* k_codes, const void* v_codes, const uint8_t* q_sf,
+                              const uint8_t* k_sf, const float* q_scale, const float* k_scale, const float* v_scale,
+                              void* out, float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int mode,
+                              float threshold_scale_factor, void* stream, int32_t* skip_counts) {
+  if (!valid_shape(B, Hq, Hkv, Sq, Skv) || !(mode & DIT_MODE_SAGE) ||
+      !valid_mode(mode, DIT_QK_NVFP4, 0, 0, threshold_scale_factor))
+    return DIT_E_INVALID_ARG;
+  if (B == 0 || Sq == 0) return DIT_OK;
+  const void* ptrs[] = {q_codes, k_codes, v_codes, q_sf, k_sf, q_scale, k_scale, v_scale, out};
+  for (const void* ptr : ptrs)
+    if (!ptr) return DIT_E_INVALID_ARG;
+  if (!aligned16(q_codes) || !aligned16(k_codes) || !aligned16(v_codes) || !aligned16(out) ||
+      !aligned16(skip_counts) || (reinterpret_cast<uintptr_t>(q_sf) & 7u) ||
+      (reinterpret_cast<uintptr_t>(k_sf) & 7u) || (reinterpret_cast<uintptr_t>(q_scale) & 3u) ||
+      (reinterpret_cast<uintptr_t>(k_scale) & 3u) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return DIT_E_INVALID_ARG;
+  int* err = nullptr;
+  const dit_status ds = prepare_device(&err);
+  if (ds != DIT_OK) return ds;
+  return run_attention(q_codes, k_codes, v_codes, out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, QK_NVF4, PV_E4M3, B, Hq,
+                       Hkv, Sq, Skv, mode, 1, 1, threshold_scale_factor, nullptr, nullptr, v_scale, skip_counts, lse,
+                       err, static_cast<cudaStream_t>(stream), 0, 0, q_sf, k_sf, q_scale, k_scale);
 }
 
 dit_status dit_attn_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* out_host, void* q,

@@ -14,7 +14,8 @@ constexpr int kQuantRows = 256;    // tokens per CTA in the quantizers
 
 // Storage formats of the Q/K operands of BMM1 and the V operand of BMM2.
 // QK_F16: INT8 codes held exactly as fp16. QK_MXF8: E4M3 codes with E8M0 scales per 32 channels.
-enum QKFormat { QK_BF16 = 0, QK_F16 = 1, QK_E4M3 = 2, QK_MXF8 = 3 };
+// QK_NVF4: E2M1 codes (two per byte) with E4M3 scales per 16 channels and a float32 tensor scale.
+enum QKFormat { QK_BF16 = 0, QK_F16 = 1, QK_E4M3 = 2, QK_MXF8 = 3, QK_NVF4 = 4 };
 enum PVFormat { PV_BF16 = 0, PV_E4M3 = 1 };
 
 // Output formats of the Q/K quantizer.
@@ -36,7 +37,9 @@ struct FmhaParams {
   int k_block, nkb;
   const float* v_scale;  // E4M3 V (SAGE, QK16PV8, MXFP8): [B, Hkv, 128]
   const uint8_t* q_sf;   // MXFP8: E8M0 bytes [B, Hq, Sq, 4] (byte c scales channels 32c .. 32c+31)
-  const uint8_t* k_sf;   // MXFP8: E8M0 bytes [B, Hkv, Skv, 4]
+  const uint8_t* k_sf;   // MXFP8: E8M0 bytes [B, Hkv, Skv, 4]; NVFP4: E4M3 bytes [.., 8] (16 channels each)
+  const float* q_gs;     // NVFP4: the Q and K tensor scales S (BMM1 is divided by S_Q * S_K)
+  const float* k_gs;
   int32_t* skip_counts;  // optional [B, Hq, n_q_tiles]
   float* lse;            // optional [B, Hq, Sq]: ln sum_j exp(s_ij) of each query row
   int* err;              // device error word
@@ -55,6 +58,8 @@ cudaError_t launch_fmha_sage_f8(bool skip, const CUtensorMap& tq, const CUtensor
                                 const CUtensorMap& to, const FmhaParams& p, cudaStream_t stream);
 cudaError_t launch_fmha_qk16pv8(bool skip, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const CUtensorMap& to, const FmhaParams& p, cudaStream_t stream);
+cudaError_t launch_fmha_nvfp4(bool skip, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const CUtensorMap& to, const FmhaParams& p, cudaStream_t stream);
 cudaError_t launch_fmha_mxfp8(bool skip, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const CUtensorMap& to, const FmhaParams& p, cudaStream_t stream);
 
@@ -74,6 +79,11 @@ cudaError_t launch_quant_kv(const void* k, const void* v, int B, int Hkv, int Sk
                             cudaStream_t stream);
 // MXFP8 codes of a [B, S, H, 128] BF16 tensor and its E8M0 scale bytes [B, H, S, 4].
 cudaError_t launch_mx_quant(const void* x, int B, int S, int H, void* codes, uint8_t* sf, cudaStream_t stream);
+// NVFP4 codes (packed [B, S, H, 64]), E4M3 block-scale bytes [B, H, S, 8] and the float32 tensor scales
+// of Q and K (q may be skipped with Sq == 0).
+cudaError_t launch_nvfp4_quant(const void* q, const void* k, int B, int Hq, int Hkv, int Sq, int Skv, void* q_codes,
+                               void* k_codes, uint8_t* q_sf, uint8_t* k_sf, float* q_scale, float* k_scale,
+                               cudaStream_t stream);
 cudaError_t launch_widen_i8(const int8_t* codes, size_t n, void* out_f16, cudaStream_t stream);
 cudaError_t launch_zero_i32(int32_t* p, size_t n, cudaStream_t stream);
 

@@ -1,5 +1,5 @@
 // Fused attention forward kernel for sm_103a (template; instantiated by fmha_dense.cu,
-// fmha_sage_i8.cu, fmha_sage_f8.cu, fmha_qk16pv8.cu and fmha_mxfp8.cu): TMA-staged Q/K/V tiles, tcgen05 MMAs
+// fmha_sage_i8.cu, fmha_sage_f8.cu, fmha_qk16pv8.cu, fmha_mxfp8.cu and fmha_nvfp4.cu): TMA-staged Q/K/V tiles, tcgen05 MMAs
 // accumulating S = Q K^T and O += P V in tensor memory, online softmax with exp2, optional SAGE
 // dequantization, P re-quantization to FP8 (SAGE and QK16PV8), and the Skip-Softmax tile test.
 //
@@ -13,8 +13,8 @@
 //                BMM2 O_i += P_i V_j (V is MN-major, so no transpose). Warp 2 also allocates the 512
 //                tensor-memory columns (S0 | S1 | O0 | O1) at the start and frees them at the end.
 //   warp 3       stages the V scales (E4M3 V) and, in SAGE, the K-block scales of each KV tile; in
-//                MXFP8 the E8M0 block scales of Q and of each K tile, which the issuers copy into
-//                tensor memory for the block-scaled BMM1.
+//                MXFP8 and NVFP4 the block scales of Q and of each K tile, which the issuers copy
+//                into tensor memory for the block-scaled BMM1.
 //   warps 4-19   four softmax warpgroups: Q tile i = g / 2 and column half h = g % 2 for group g.
 //                A thread owns one row (= TMEM lane) and 64 of its 128 columns; the two halves
 //                of a row exchange partial maxima through shared memory. Halving the columns per
@@ -26,7 +26,7 @@
 // E4M3 P (SAGE and QK16PV8, 16 KB per tile): P goes to a shared-memory buffer and BMM2 is an SS MMA. S is free
 // as soon as the softmax has loaded it, so the issuer computes S_i(j+1) while the softmax works on
 // S_i(j); a per-tile barrier (o_done) returns P's buffer and O to the softmax after each BMM2.
-// MXFP8: the block-scaled MMA reads its scale factors from tensor memory, and S0 | S1 | O0 | O1 leave
+// MXFP8 / NVFP4: the block-scaled MMA reads its scale factors from tensor memory, and S0 | S1 | O0 | O1 leave
 // no room, so the two tiles share one S buffer (S | O0 | O1 | scale factors): BMM1s alternate
 // between the tiles, each issued once the other tile's softmax has loaded the previous S. The
 // softmax groups then run about one BMM1 apart, and each S still lands before its softmax needs it.
@@ -65,20 +65,23 @@ constexpr int kSlots = 4;  // ring of K/V tiles: K_j in slot 2j mod 4, V_j in sl
 // buffers for the E4M3 P of the two query tiles, which BMM2 reads from shared memory.
 template <int QKF, int PVF>
 struct SmemLayout {
-  static constexpr uint32_t kKTile = 128u * 128u * ((QKF == QK_E4M3 || QKF == QK_MXF8) ? 1u : 2u);
+  static constexpr bool kNV = (QKF == QK_NVF4);
+  static constexpr uint32_t kKTile = kNV ? 128u * 64u : 128u * 128u * ((QKF == QK_E4M3 || QKF == QK_MXF8) ? 1u : 2u);
+  // block-scaled Q/K: one 32 x 16-byte scale matrix per 32-bit scale word of a row (MXFP8 1, NVFP4 2)
+  static constexpr uint32_t kSfWords = kNV ? 2u : 1u;
   static constexpr uint32_t kVTile = 128u * 128u * (PVF == PV_E4M3 ? 1u : 2u);
   static constexpr bool kPInSmem = (PVF == PV_E4M3);
   static constexpr uint32_t kQOff = 0;
   static constexpr uint32_t kKOff = 2 * 32768;
   static constexpr uint32_t kVOff = kKOff + 2 * kKTile;
   static constexpr uint32_t kPOff = kVOff + 2 * kVTile;
-  // 4 x 128 floats (SAGE K-block scales), or 4 x 512 bytes of K tiles' E8M0 scales (MXFP8)
+  // 4 x 128 floats (SAGE K-block scales), or 4 x kSfWords x 512 bytes of K tiles' block scales
   static constexpr uint32_t kKsOff = kPOff + (kPInSmem ? 2 * 16384 : 0);
-  static constexpr uint32_t kVsOff = kKsOff + kSlots * 512;                // 128 floats
+  static constexpr uint32_t kVsOff = kKsOff + kSlots * 512 * kSfWords;     // 128 floats
   static constexpr uint32_t kXmaxOff = kVsOff + 512;        // [tile][half][parity][128] partial maxima
   static constexpr uint32_t kXlOff = kXmaxOff + 2 * 2 * 2 * 512;  // [tile][half][128] partial row sums
-  static constexpr uint32_t kSfaOff = kXlOff + 2 * 2 * 512;  // MXFP8: the Q tiles' E8M0 scales, 2 x 512 bytes
-  static constexpr uint32_t kBarOff = kSfaOff + (QKF == QK_MXF8 ? 2 * 512 : 0);
+  static constexpr uint32_t kSfaOff = kXlOff + 2 * 2 * 512;  // block-scaled: the Q tiles' scales, 2 x kSfWords x 512 B
+  static constexpr uint32_t kBarOff = kSfaOff + ((QKF == QK_MXF8 || kNV) ? 2 * 512 * kSfWords : 0);
   static constexpr uint32_t kSmemBytes = kBarOff + 512 + 1024;     // + alignment slack
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
@@ -98,7 +101,7 @@ struct Bars {
   uint64_t drain[2];
   uint64_t s_free[2];   // SAGE: the tile's softmax has loaded S (BMM1 of the next KV tile may overwrite it)
   uint64_t o_done[2];   // SAGE: BMM2 of the tile's latest KV tile is complete (P buffer free, O stable)
-  uint64_t sfa_full;    // MXFP8: the Q tiles' scale factors are in shared memory
+  uint64_t sfa_full;    // MXFP8 / NVFP4: the Q tiles' scale factors are in shared memory
   uint32_t tmem_base;
   int abort_flag;
   int skip_flag[2];
@@ -118,16 +121,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const FmhaParams p) {
   constexpr bool kQKScaled = (QKF == QK_F16 || QKF == QK_E4M3);  // Q/K codes with token-block scales (SAGE)
   constexpr bool kMX = (QKF == QK_MXF8);         // block-scaled MXFP8 Q/K (scales applied inside BMM1)
+  constexpr bool kNV = (QKF == QK_NVF4);         // block-scaled NVFP4 Q/K (and a tensor scale per Q and K)
+  constexpr bool kBS = kMX || kNV;
   constexpr bool kPV8 = (PVF == PV_E4M3);        // E4M3 P and V with per-channel V scales (SAGE, QK16PV8, MXFP8)
-  constexpr int kQKBytes = (QKF == QK_E4M3 || kMX) ? 1 : 2;
+  constexpr int kQKBytes = (QKF == QK_E4M3 || kBS) ? 1 : 2;  // NVFP4: two codes per byte, one 64-byte box per row
   constexpr int kPVBytes = (PVF == PV_E4M3) ? 1 : 2;
-  constexpr uint32_t kQTileBytes = 128u * 128u * kQKBytes;
+  constexpr uint32_t kQTileBytes = kNV ? 128u * 64u : 128u * 128u * kQKBytes;
   constexpr uint32_t kVTileBytes = 128u * 128u * kPVBytes;
   constexpr int kMma1Kind = (QKF == QK_E4M3) ? KIND_F8F6F4 : KIND_F16;
   constexpr int kMma2Kind = (PVF == PV_E4M3) ? KIND_F8F6F4 : KIND_F16;
   constexpr int kK1Steps = (kQKBytes == 1) ? 4 : 8;  // K = 128 in steps of 32 (8-bit) or 16
-  // tensor-memory columns: S and O of tile i; MXFP8 adds 4 columns of Q scales and 4 of K scales per tile
-  constexpr uint32_t kColS1 = kMX ? 0 : 128, kColO0 = kMX ? 128 : 256, kColSfa = 384, kColSfb = 392;
+  // tensor-memory columns: S and O of tile i; block-scaled Q/K add, per tile, 4 columns of Q scales and
+  // 4 of K scales per 32-bit scale word of a row
+  constexpr uint32_t kSfWords = kNV ? 2u : 1u;
+  constexpr uint32_t kColS1 = kBS ? 0 : 128, kColO0 = kBS ? 128 : 256;
+  constexpr uint32_t kColSfa = 384, kColSfb = 384 + 8 * kSfWords;
   constexpr int kK2Steps = (PVF == PV_E4M3) ? 4 : 8;
   constexpr uint32_t kIdesc1 = (QKF == QK_BF16)  ? make_idesc(1, 1, 0, 0, 128, 128)
                                : (QKF == QK_F16) ? make_idesc(0, 0, 0, 0, 128, 128)
@@ -159,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->kv_full[s], 1);
       mbar_init(&bars->kv_empty[s], 2);  // one commit from each MMA issuer
       mbar_init(&bars->ks_full[s], 32);
-      mbar_init(&bars->ks_empty[s], kMX ? 2 : 16);  // SAGE: one arrival per softmax warp; MXFP8: per issuer
+      mbar_init(&bars->ks_empty[s], kBS ? 2 : 16);  // SAGE: one arrival per softmax warp; block-scaled: per issuer
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
@@ -249,12 +257,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok && leader) record_timeout(p, bars);
     tc_fence_after();
     const uint32_t sbase = smem_u32(smem);
-    const uint64_t aq = make_sdesc_sw128(sbase + L::kQOff + i * 32768, 16, 1024);
-    const uint64_t dk0 = make_sdesc_sw128(sbase + L::kKOff, 16, 1024);
+    // Q/K operands: 128-byte rows with the 128-byte swizzle; NVFP4's 64-byte rows with the 64-byte one
+    const uint64_t aq = kNV ? make_sdesc_sw64(sbase + L::kQOff + i * 32768, 16, 512)
+                            : make_sdesc_sw128(sbase + L::kQOff + i * 32768, 16, 1024);
+    const uint64_t dk0 = kNV ? make_sdesc_sw64(sbase + L::kKOff, 16, 512) : make_sdesc_sw128(sbase + L::kKOff, 16, 1024);
     const uint64_t dv0 = make_sdesc_sw128(sbase + L::kVOff, kPVBytes == 2 ? 16384 : 8192, 1024);
     const uint32_t d_s = tbase + kColS1 * i;
     const uint32_t d_o = tbase + kColO0 + 128 * i;
-    const uint32_t t_sfa = tbase + kColSfa + 4 * i, t_sfb = tbase + kColSfb + 4 * i;  // MXFP8 scale factors
+    const uint32_t t_sfa = tbase + kColSfa + 4 * kSfWords * i;  // block-scaled: this tile's Q scale words
+    const uint32_t t_sfb = tbase + kColSfb + 4 * kSfWords * i;  // and its copy of the K tile's
     volatile int* skip_flag = bars->skip_flag;
     auto wait = [&](uint64_t* bar, int parity) {
       return __all_sync(0xffffffffu, mbar_wait_bounded(bar, (uint32_t)parity, budget, abort_flag));
@@ -271,6 +282,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < 4; ++kk)
           mma_mxf8_if(leader, d_s, aq + (uint64_t)((kk * 32) >> 4), bk + (uint64_t)((kk * 32) >> 4),
                       make_idesc_mxf8(128, 128, kk), t_sfa, t_sfb, kk > 0 ? 1u : 0u);
+      } else if constexpr (kNV) {
+        // two 64-wide K slices (32 bytes of packed codes each), each with its own scale word per row
+        // (the four E4M3 scales of its 16-channel blocks) in its own four columns
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk)
+          tmem_cp_32x128b_x4_if(leader, t_sfb + 4 * kk,
+                                make_sdesc_rows16(sbase + L::kKsOff + (j & 3) * 1024 + kk * 512));
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk)
+          mma_nvf4_if(leader, d_s, aq + (uint64_t)((kk * 32) >> 4), bk + (uint64_t)((kk * 32) >> 4),
+                      make_idesc_nvf4(128, 128), t_sfa + 4 * kk, t_sfb + 4 * kk, kk > 0 ? 1u : 0u);
       } else {
 #pragma unroll
         for (int kk = 0; kk < kK1Steps; ++kk) {
@@ -280,14 +302,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mma_commit_if(leader, &bars->s_full[i]);
       mma_commit_if(leader, &bars->kv_empty[(2 * j) & 3]);
-      if constexpr (kMX) mma_commit_if(leader, &bars->ks_empty[j & 3]);  // the scales' slot
+      if constexpr (kBS) mma_commit_if(leader, &bars->ks_empty[j & 3]);  // the scales' slot
     };
     // May S_i(j) be written? With a buffer per tile: once this tile's softmax has loaded S_i(j-1).
     // MXFP8 (one S for both tiles, BMM1s in the order Q0 Q1 Q0 Q1 ...): once the other tile's
     // softmax has loaded the S computed just before, which also orders every earlier BMM1 of this
     // issuer (and its reads of the scale columns) before the new one.
     auto s_writable = [&](int j) -> bool {
-      if constexpr (kMX) {
+      if constexpr (kBS) {
         return (i == 0) ? (j == 0 || wait(&bars->s_free[1], (j - 1) & 1)) : wait(&bars->s_free[0], j & 1);
       } else {
         return j == 0 || wait(&bars->s_free[i], (j - 1) & 1);
@@ -296,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto k_ready = [&](int j) -> bool {  // K_j staged (and, in MXFP8, its scales)
       const int tk = 2 * j;
       bool r = wait(&bars->kv_full[tk & 3], (tk >> 2) & 1);
-      if constexpr (kMX) r = r && wait(&bars->ks_full[j & 3], (j >> 2) & 1);
+      if constexpr (kBS) r = r && wait(&bars->ks_full[j & 3], (j >> 2) & 1);
       return r;
     };
     if constexpr (L::kPInSmem) {
@@ -305,12 +327,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // BMM2 is an SS MMA (P K-major, V MN-major); o_done tells the softmax when P's buffer and O
       // are free again.
       const uint64_t ap = make_sdesc_sw128(sbase + L::kPOff + i * 16384, 16, 1024);
-      if constexpr (kMX) {
+      if constexpr (kBS) {
         // this Q tile's scale words, once, ahead of every MMA that reads them
         if (ok) ok = wait(&bars->sfa_full, 0);
         if (ok) {
           tc_fence_after();
-          tmem_cp_32x128b_x4_if(leader, t_sfa, make_sdesc_rows16(sbase + L::kSfaOff + i * 512));
+#pragma unroll
+          for (uint32_t w = 0; w < kSfWords; ++w)
+            tmem_cp_32x128b_x4_if(leader, t_sfa + 4 * w,
+                                  make_sdesc_rows16(sbase + L::kSfaOff + (i * kSfWords + w) * 512));
         }
       }
       if (ok) ok = s_writable(0) && k_ready(0);
@@ -384,35 +409,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int e = 0; e < 4; ++e) s_vs[lane * 4 + e] = vs[lane * 4 + e];
       mbar_arrive(&bars->vs_full);
     }
-    if constexpr (kMX) {
-      // E8M0 scale words (4 bytes per row: channels 32c .. 32c+31 in byte c) of the two Q tiles once,
-      // then of every K tile through the ring. A 128-row tile's words go to a 32 x 16-byte matrix
-      // whose row l holds the words of rows l, l+32, l+64, l+96: the tensor-memory copy puts them in
-      // columns 0-3 of lane l of each lane quarter, where the MMA reads row 32c + l from column c.
-      // Rows past the end get 0 (their codes are zero, as TMA fills them).
-      const uint32_t* qsf = reinterpret_cast<const uint32_t*>(p.q_sf) + ((size_t)b * p.Hq + hq) * p.Sq;
+    if constexpr (kBS) {
+      // Block-scale words of the two Q tiles once, then of every K tile through the ring. A row has
+      // W = kSfWords 32-bit words (MXFP8: 4 E8M0 bytes for channels 32c..; NVFP4: 8 E4M3 bytes for
+      // channels 16c.., word w covering the MMA's K slice w). Each word of a 128-row tile goes to a
+      // 32 x 16-byte matrix whose row l holds that word of rows l, l+32, l+64, l+96: the tensor-memory
+      // copy puts them in columns 0-3 of lane l of each lane quarter, where the MMA reads row 32c + l
+      // from column c. Rows past the end get 0 (their codes are zero, as TMA fills them).
+      constexpr int W = (int)kSfWords;
+      auto load_words = [&](const uint32_t* base, int row, int nrows, uint32_t* w) {
+        if (row < nrows) {
+          if constexpr (W == 2) {
+            const uint2 u = __ldg(reinterpret_cast<const uint2*>(base) + row);
+            w[0] = u.x;
+            w[1] = u.y;
+          } else {
+            w[0] = __ldg(base + row);
+          }
+        } else {
+#pragma unroll
+          for (int ww = 0; ww < W; ++ww) w[ww] = 0u;
+        }
+      };
+      const uint32_t* qsf = reinterpret_cast<const uint32_t*>(p.q_sf) + ((size_t)b * p.Hq + hq) * p.Sq * W;
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
-        uint32_t w[4];
+        uint32_t w[4][W];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int row = q0 + 128 * t + 32 * c + lane;
-          w[c] = row < p.Sq ? __ldg(qsf + row) : 0u;
-        }
-        *reinterpret_cast<uint4*>(smem + L::kSfaOff + t * 512 + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int c = 0; c < 4; ++c) load_words(qsf, q0 + 128 * t + 32 * c + lane, p.Sq, w[c]);
+#pragma unroll
+        for (int ww = 0; ww < W; ++ww)
+          *reinterpret_cast<uint4*>(smem + L::kSfaOff + (t * W + ww) * 512 + lane * 16) =
+              make_uint4(w[0][ww], w[1][ww], w[2][ww], w[3][ww]);
       }
       fence_proxy_async_smem();
       mbar_arrive(&bars->sfa_full);
-      const uint32_t* ksf = reinterpret_cast<const uint32_t*>(p.k_sf) + ((size_t)b * p.Hkv + hkv) * p.Skv;
-      auto load_tile = [&](int j, uint32_t* w) {
+      const uint32_t* ksf = reinterpret_cast<const uint32_t*>(p.k_sf) + ((size_t)b * p.Hkv + hkv) * p.Skv * W;
+      auto load_tile = [&](int j, uint32_t (*w)[L::kSfWords]) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int key = 128 * j + 32 * c + lane;
-          w[c] = (j < nt && key < p.Skv) ? __ldg(ksf + key) : 0u;
-        }
+        for (int c = 0; c < 4; ++c) load_words(ksf, 128 * j + 32 * c + lane, j < nt ? p.Skv : 0, w[c]);
       };
-      constexpr int kAhead = 4;
-      uint32_t pre[kAhead][4];
+      constexpr int kAhead = (W == 2) ? 2 : 4;
+      uint32_t pre[kAhead][4][W];
 #pragma unroll
       for (int d = 0; d < kAhead; ++d) load_tile(d, pre[d]);
       for (int j = 0; j < nt; ++j) {
@@ -422,14 +460,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) record_timeout(p, bars);
           break;
         }
-        *reinterpret_cast<uint4*>(smem + L::kKsOff + e * 512 + lane * 16) =
-            make_uint4(pre[0][0], pre[0][1], pre[0][2], pre[0][3]);
+#pragma unroll
+        for (int ww = 0; ww < W; ++ww)
+          *reinterpret_cast<uint4*>(smem + L::kKsOff + (e * W + ww) * 512 + lane * 16) =
+              make_uint4(pre[0][0][ww], pre[0][1][ww], pre[0][2][ww], pre[0][3][ww]);
         fence_proxy_async_smem();
         mbar_arrive(&bars->ks_full[e]);
 #pragma unroll
         for (int d = 0; d + 1 < kAhead; ++d)
 #pragma unroll
-          for (int c = 0; c < 4; ++c) pre[d][c] = pre[d + 1][c];
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int ww = 0; ww < W; ++ww) pre[d][c][ww] = pre[d + 1][c][ww];
         load_tile(j + kAhead, pre[kAhead - 1]);
       }
     }
@@ -487,6 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* xmax = reinterpret_cast<float*>(smem + L::kXmaxOff);
     float* xl = reinterpret_cast<float*>(smem + L::kXlOff);
     float c = p.c_scale;
+    if constexpr (kNV) c = c / (__ldg(p.q_gs) * __ldg(p.k_gs));  // BMM1 carries both tensor scales
     if constexpr (kQKScaled) {
       const float qs = row_valid ? __ldg(p.q_scale + ((size_t)b * p.Hq + hq) * p.nqb + qrow / p.q_block) : 0.0f;
       c = qs * p.c_scale;

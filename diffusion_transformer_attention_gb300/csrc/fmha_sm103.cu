@@ -1,6 +1,6 @@
 // Attention-kernel dispatch: picks the instantiation for the operand formats, the K scale block
 // size and Skip-Softmax. The instantiations live in fmha_dense.cu, fmha_sage_i8.cu, fmha_sage_f8.cu
-// fmha_qk16pv8.cu and fmha_mxfp8.cu so that they compile in parallel.
+// fmha_qk16pv8.cu, fmha_mxfp8.cu and fmha_nvfp4.cu so that they compile in parallel.
 #include "ditattn_internal.h"
 
 namespace ditattn {
@@ -12,6 +12,7 @@ cudaError_t launch_fmha(int qk_format, int pv_format, bool skip, const CUtensorM
   if (qk_format == QK_E4M3 && pv_format == PV_E4M3) return launch_fmha_sage_f8(skip, tq, tk, tv, to, p, stream);
   if (qk_format == QK_BF16 && pv_format == PV_E4M3) return launch_fmha_qk16pv8(skip, tq, tk, tv, to, p, stream);
   if (qk_format == QK_MXF8 && pv_format == PV_E4M3) return launch_fmha_mxfp8(skip, tq, tk, tv, to, p, stream);
+  if (qk_format == QK_NVF4 && pv_format == PV_E4M3) return launch_fmha_nvfp4(skip, tq, tk, tv, to, p, stream);
   return cudaErrorInvalidValue;
 }
 

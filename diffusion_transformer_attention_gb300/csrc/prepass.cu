@@ -375,6 +375,96 @@ __global__ void __launch_bounds__(256) mx_quant_kernel(const uint4* __restrict__
   }
 }
 
+// ------------------------------------------------------------------ NVFP4 quantizer
+// NVFP4 ("VisualGen Quantized Attention" names NVFP4 Q/K with blocks of 16 along the head dimension;
+// the format is NVIDIA's two-level one): FP4 E2M1 elements, an unsigned E4M3 scale per 16 channels
+// of a token, and a float32 tensor scale S = 2688 / amax_T (2688 = 448 * 6). Per block:
+// byte = E4M3(float32(amax_b / 6) * S); elements E2M1(float32(x * float32(S / d_b))) with d_b the
+// decoded byte (zero codes when d_b = 0). Divisions are IEEE (__fdiv_rn), products single roundings.
+
+// max |x| over a whole tensor, as float32 bits, folded into *amax_bits with atomicMax (float32 bits of
+// non-negative values order like the values). *amax_bits must start at 0.
+__global__ void __launch_bounds__(256) absmax_kernel(const uint4* __restrict__ x, long long nvec,
+                                                     unsigned* __restrict__ amax_bits) {
+  float a = 0.0f;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += (long long)gridDim.x * blockDim.x) {
+    float f[8];
+    bf16x8_to_f32(ld_stream_v4(x + i), f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) a = fmaxf(a, fabsf(f[e]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+  __shared__ float red[8];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) a = fmaxf(a, red[w]);
+    atomicMax(amax_bits, __float_as_uint(a));
+  }
+}
+
+__device__ __forceinline__ float nvfp4_tensor_scale(unsigned amax_bits) {
+  const float amax = __uint_as_float(amax_bits);
+  return amax > 0.0f ? __fdiv_rn(2688.0f, amax) : 1.0f;
+}
+
+// value of a non-negative E4M3 byte (bias 7, 3 mantissa bits; exponent field 0 = subnormal, step 2^-9)
+__device__ __forceinline__ float e4m3_byte_value(uint32_t b) {
+  const uint32_t ex = (b >> 3) & 15u, m = b & 7u;
+  return ex == 0 ? (float)m * 0x1p-9f : __uint_as_float(((ex + 120u) << 23) | (m << 20));
+}
+
+// two E2M1 codes in one byte: `lo` in bits 0-3, `hi` in bits 4-7 (round to nearest even, saturating)
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n cvt.u32.u8 %0, t;\n}" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two consecutive lanes hold one block (8 channels each, one 16-byte load) and exchange its max
+// with one shuffle; the loop runs per warp so every shuffle has all 32 lanes.
+__global__ void __launch_bounds__(256) nvfp4_quant_kernel(const uint4* __restrict__ x, int S, int H, long long nvec,
+                                                          const unsigned* __restrict__ amax_bits,
+                                                          uint32_t* __restrict__ codes, uint8_t* __restrict__ sf) {
+  const int lane = threadIdx.x & 31;
+  const float scale = nvfp4_tensor_scale(*amax_bits);
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long wb = (long long)blockIdx.x * blockDim.x + (threadIdx.x & ~31); wb < nvec; wb += stride) {
+    const long long i = wb + lane;  // 16-byte vector: row i / 16 = (b * S + s) * H + h, block (i / 2) % 8
+    const bool valid = i < nvec;
+    uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+    if (valid) raw = ld_stream_v4(x + i);
+    float f[8];
+    bf16x8_to_f32(raw, f);
+    float a = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) a = fmaxf(a, fabsf(f[e]));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+    const uint32_t byte = e4m3x2(__fmul_rn(__fdiv_rn(a, 6.0f), scale), 0.0f) & 0xFFu;
+    const float d = e4m3_byte_value(byte);
+    const float enc = d > 0.0f ? __fdiv_rn(scale, d) : 0.0f;
+    uint32_t w = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) w |= e2m1x2(__fmul_rn(f[2 * e], enc), __fmul_rn(f[2 * e + 1], enc)) << (8 * e);
+    if (valid) {
+      codes[i] = w;
+      if ((lane & 1) == 0) {
+        const long long row = i >> 4, t = row / H, s = t % S, b = t / S, h = row % H;
+        sf[((b * H + h) * S + s) * 8 + ((i >> 1) & 7)] = (uint8_t)byte;
+      }
+    }
+  }
+}
+
+// tensor scales from the two maxima, in place (after every quantizer launch has read them)
+__global__ void nvfp4_scales_kernel(unsigned* q_amax_bits, unsigned* k_amax_bits) {
+  if (threadIdx.x == 0) {
+    if (q_amax_bits != nullptr) *reinterpret_cast<float*>(q_amax_bits) = nvfp4_tensor_scale(*q_amax_bits);
+    *reinterpret_cast<float*>(k_amax_bits) = nvfp4_tensor_scale(*k_amax_bits);
+  }
+}
+
 __global__ void widen_i8_kernel(const int8_t* __restrict__ in, size_t n8, __half* __restrict__ out) {
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
     const uint2 w = *reinterpret_cast<const uint2*>(in + i * 8);
@@ -495,6 +585,28 @@ cudaError_t launch_mx_quant(const void* x, int B, int S, int H, void* codes, uin
   if (nvec == 0) return cudaSuccess;
   mx_quant_kernel<<<grid_for(nvec, 256), 256, 0, stream>>>(static_cast<const uint4*>(x), S, H, nvec,
                                                             static_cast<uint2*>(codes), sf);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_nvfp4_quant(const void* q, const void* k, int B, int Hq, int Hkv, int Sq, int Skv, void* q_codes,
+                               void* k_codes, uint8_t* q_sf, uint8_t* k_sf, float* q_scale, float* k_scale,
+                               cudaStream_t stream) {
+  // q_scale / k_scale first hold the tensors' max |x| (float bits, accumulated from 0), then S
+  const long long nq = (long long)B * Sq * Hq * (kHeadDim / 8), nk = (long long)B * Skv * Hkv * (kHeadDim / 8);
+  unsigned* qa = reinterpret_cast<unsigned*>(q_scale);
+  unsigned* ka = reinterpret_cast<unsigned*>(k_scale);
+  cudaError_t e = cudaSuccess;
+  if (nq > 0) e = cudaMemsetAsync(qa, 0, sizeof(unsigned), stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ka, 0, sizeof(unsigned), stream);
+  if (e != cudaSuccess) return e;
+  if (nq > 0) absmax_kernel<<<grid_for(nq, 256), 256, 0, stream>>>(static_cast<const uint4*>(q), nq, qa);
+  absmax_kernel<<<grid_for(nk, 256), 256, 0, stream>>>(static_cast<const uint4*>(k), nk, ka);
+  if (nq > 0)
+    nvfp4_quant_kernel<<<grid_for(nq, 256), 256, 0, stream>>>(static_cast<const uint4*>(q), Sq, Hq, nq, qa,
+                                                              static_cast<uint32_t*>(q_codes), q_sf);
+  nvfp4_quant_kernel<<<grid_for(nk, 256), 256, 0, stream>>>(static_cast<const uint4*>(k), Skv, Hkv, nk, ka,
+                                                            static_cast<uint32_t*>(k_codes), k_sf);
+  nvfp4_scales_kernel<<<1, 32, 0, stream>>>(nq > 0 ? qa : nullptr, ka);
   return cudaGetLastError();
 }
 

@@ -284,10 +284,23 @@ __host__ __device__ constexpr uint32_t make_idesc_mxf8(uint32_t M, uint32_t N, u
   return (sf_id << 4) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) | (sf_id << 29);
 }
 
+// Instruction descriptor of the block-scaled kind::mxf4nvf4 MMA (scale_vec::4X) with E2M1 A and B
+// (K-major, two codes per byte), f32 D and E4M3 scale factors (bit 23 clear); each MMA reads one
+// whole scale word per row (four 16-wide blocks of its 64-wide K slice), so both scale ids are 0.
+__host__ __device__ constexpr uint32_t make_idesc_nvf4(uint32_t M, uint32_t N) {
+  return (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
 // Shared-memory matrix descriptor with 128-byte swizzling. `lbo`/`sbo` in bytes.
 __device__ __forceinline__ uint64_t make_sdesc_sw128(uint32_t smem_addr, uint32_t lbo, uint32_t sbo) {
   return (uint64_t)((smem_addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Shared-memory matrix descriptor with 64-byte swizzling (64-byte rows, 8-row atoms of 512 bytes).
+__device__ __forceinline__ uint64_t make_sdesc_sw64(uint32_t smem_addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((smem_addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (4ull << 61);
 }
 
 // Shared-memory matrix descriptor without swizzling for rows of 16 bytes stored one after another
@@ -315,6 +328,17 @@ __device__ __forceinline__ void mma_mxf8_if(uint32_t pred, uint32_t d, uint64_t 
   asm volatile(
       "{\n .reg .pred p, q;\n setp.ne.b32 p, %6, 0;\n setp.ne.b32 q, %7, 0;\n"
       " @q tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc), "r"(pred)
+      : "memory");
+}
+
+// D[tmem] (+)= (A * sfA) (B * sfB)^T with packed E2M1 A/B in shared memory and their E4M3 block
+// scales in tensor memory (one 32-bit word per row: four blocks of 16 along this MMA's K = 64).
+__device__ __forceinline__ void mma_nvf4_if(uint32_t pred, uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                            uint32_t sfa, uint32_t sfb, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.b32 p, %6, 0;\n setp.ne.b32 q, %7, 0;\n"
+      " @q tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(d),
       "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc), "r"(pred)
       : "memory");
 }

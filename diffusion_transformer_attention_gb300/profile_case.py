@@ -30,6 +30,7 @@ MODES = {
     "skip_sage_int8": (dit.MODE_SAGE | dit.MODE_SKIP, "int8"),
     "qk16pv8": (dit.MODE_SAGE | dit.MODE_V_PER_TENSOR, "bf16"),
     "mxfp8": (dit.MODE_SAGE, "mxfp8"),
+    "nvfp4": (dit.MODE_SAGE, "nvfp4"),
 }
 
 
@@ -51,7 +52,7 @@ def main():
                     help="run only the SAGE quantize prepass (sage_quantize_qkv) for a quantized --mode")
     args = ap.parse_args()
     mode, dt = MODES[args.mode]
-    if dt in ("bf16", "mxfp8") and mode & dit.MODE_SAGE:  # QK16PV8 and MXFP8 have no token blocks
+    if dt in ("bf16", "mxfp8", "nvfp4") and mode & dit.MODE_SAGE:  # these recipes have no token blocks
         args.q_block = args.k_block = 0
     grid = tuple(int(x) for x in args.grid.split(",")) if args.grid else ()
     S = args.S if not grid else grid[0] * grid[1] * grid[2]
@@ -59,10 +60,10 @@ def main():
     q, k, v = workloads.generate(w, seed=0, device="cuda")
     if args.prepass:
         if dt == "bf16":
-            raise SystemExit("--prepass needs a SAGE --mode with int8, fp8 or mxfp8 Q/K")
+            raise SystemExit("--prepass needs a SAGE --mode with int8, fp8, mxfp8 or nvfp4 Q/K")
         for _ in range(args.warmup + args.launches):
-            if dt == "mxfp8":
-                dit.mx_quantize_qk(q, k)
+            if dt in ("mxfp8", "nvfp4"):
+                (dit.mx_quantize_qk if dt == "mxfp8" else dit.nvfp4_quantize_qk)(q, k)
                 dit.sage_quantize_v(v)
             else:
                 dit.sage_quantize_qkv(q, k, v, qk_dtype=dt, q_block=args.q_block, k_block=args.k_block)

@@ -23,6 +23,11 @@
  *          fixed blocks of 32 elements, q/k block sizes 0, v_block_size 0 or 1). The scale rule is
  *          the OCP Microscaling v1.0 conversion: exponent floor(log2 amax) - 8, clamped to
  *          [-127, 127]; elements round to nearest even and saturate at 448. K is not smoothed.
+ *          With qk_dtype DIT_QK_NVFP4, SAGE is the NVFP4 Q/K + FP8 V recipe (same section: blocks
+ *          of 16): Q and K become FP4 E2M1 codes (two per byte) with one E4M3 scale per 16 channels
+ *          of each token, applied inside BMM1 by the block-scaled tensor-core MMA, and one float32
+ *          scale per Q and K tensor, S = 2688 / max |x| over the tensor (NVIDIA's two-level NVFP4
+ *          format); V is FP8 as in QK16PV8. K is not smoothed.
  *   SKIP   Skip-Softmax: a 128-column KV tile's exp and P.V work is skipped for a 128-row Q
  *          tile when every valid row has exp(m_tile - m_run) < threshold, with
  *          threshold = threshold_scale_factor / Skv ("SAGE + Skip-Softmax -- API Design & Test
@@ -64,22 +69,23 @@ typedef enum dit_status {
 } dit_status;
 
 /* Mode bits (or-able): DIT_MODE_SAGE | DIT_MODE_SKIP is SAGE with Skip-Softmax.
- * DIT_MODE_V_PER_TENSOR is valid only with DIT_MODE_SAGE and DIT_QK_BF16 (QK16PV8) or DIT_QK_MXFP8: V gets one
+ * DIT_MODE_V_PER_TENSOR is valid only with DIT_MODE_SAGE and DIT_QK_BF16 (QK16PV8), DIT_QK_MXFP8 or
+ * DIT_QK_NVFP4: V gets one
  * tensor-wide scale, max |V| over the whole [B, Skv, Hkv, 128] tensor / 448 (v_block_size 0);
  * without it V is scaled per (batch, kv head, channel) (v_block_size 1). */
 enum { DIT_MODE_DENSE = 0, DIT_MODE_SAGE = 1, DIT_MODE_SKIP = 2, DIT_MODE_V_PER_TENSOR = 4 };
 
 /* Q/K element type. DENSE uses BF16; SAGE takes INT8 or FP8 E4M3 ("TRTLLM Attention" user guide,
- * SAGE table: dtype_qk in {int8, fp8_e4m3}), BF16 for QK16PV8, or MXFP8 ("VisualGen Quantized
- * Attention", quant_attention_config table: qk_dtype "mxfp8"). */
-enum { DIT_QK_BF16 = 0, DIT_QK_INT8 = 1, DIT_QK_FP8_E4M3 = 2, DIT_QK_MXFP8 = 3 };
+ * SAGE table: dtype_qk in {int8, fp8_e4m3}), BF16 for QK16PV8, MXFP8 or NVFP4 ("VisualGen
+ * Quantized Attention", quant_attention_config table: qk_dtype "mxfp8", "nvfp4"). */
+enum { DIT_QK_BF16 = 0, DIT_QK_INT8 = 1, DIT_QK_FP8_E4M3 = 2, DIT_QK_MXFP8 = 3, DIT_QK_NVFP4 = 4 };
 
 /* Rows and columns of one attention tile; skip counts are kept per 128-row Q tile. */
 enum { DIT_HEAD_DIM = 128, DIT_TILE = 128 };
 
 /* Version of this interface (2: QK16PV8, DIT_MODE_V_PER_TENSOR, sage_quantize_v, the LSE outputs,
  * sage_quantize_qkv_with_mean and dit_attn_fwd_host; 3: DIT_QK_MXFP8, mx_quantize_qk and
- * dit_attn_fwd_mxfp8). */
+ * dit_attn_fwd_mxfp8; 4: DIT_QK_NVFP4, nvfp4_quantize_qk and dit_attn_fwd_nvfp4). */
 int dit_abi_version(void);
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -88,8 +94,8 @@ const char* dit_status_string(dit_status status);
 /*
  * Bytes of device workspace dit_attn_fwd needs for these arguments: 0 for DENSE (with or without
  * SKIP), otherwise room for the quantized codes, their scales and the K-mean / V-absmax partials
- * (QK16PV8: the V codes, V scales and V-absmax partials only; MXFP8: Q/K codes and scale bytes,
- * V codes, V scales and V-absmax partials).
+ * (QK16PV8: the V codes, V scales and V-absmax partials only; MXFP8 and NVFP4: Q/K codes and
+ * scale bytes (NVFP4 also the two tensor scales), V codes, V scales and V-absmax partials).
  * Returns 0 for arguments dit_attn_fwd would reject.
  */
 size_t dit_attn_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int mode, int qk_dtype, int q_block,
@@ -102,11 +108,11 @@ size_t dit_attn_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int mod
  *   k, v       device bf16 [B, Skv, Hkv, 128]
  *   out        device bf16 [B, Sq, Hq, 128], written completely
  *   mode       DIT_MODE_* bits
- *   qk_dtype   DIT_QK_BF16 without SAGE; DIT_QK_INT8, DIT_QK_FP8_E4M3, (QK16PV8) DIT_QK_BF16 or
- *              DIT_QK_MXFP8 with SAGE
+ *   qk_dtype   DIT_QK_BF16 without SAGE; DIT_QK_INT8, DIT_QK_FP8_E4M3, (QK16PV8) DIT_QK_BF16,
+ *              DIT_QK_MXFP8 or DIT_QK_NVFP4 with SAGE
  *   q_block, k_block   SAGE with INT8/FP8: tokens per Q / K scale block, each in {1, 4, 16}
- *              ("TRTLLM Attention" user guide, SAGE table); QK16PV8 and MXFP8: both must be 0;
- *              ignored without SAGE
+ *              ("TRTLLM Attention" user guide, SAGE table); QK16PV8, MXFP8 and NVFP4: both must be
+ *              0; ignored without SAGE
  *   threshold_scale_factor   with SKIP: finite and >= 0, threshold = factor / Skv (0 never
  *              skips and gives the same output as the mode without SKIP); ignored without SKIP
  *   workspace  device scratch of at least dit_attn_workspace_bytes(...) bytes, 256-byte
@@ -129,8 +135,8 @@ dit_status dit_attn_fwd(const void* q, const void* k, const void* v, void* out, 
  *   lse   device float [B, Hq, Sq], 4-byte aligned, not NULL: ln sum_j exp(s_ij) over the row's
  *         logits s_ij as the mode computes them (softmax scale applied; SAGE: from the codes and
  *         scales of the K-smoothed K, so lower by q_i . mean / sqrt(128) than for the raw K;
- *         MXFP8: from the dequantized Q and K, no smoothing; with SKIP only the KV tiles that were
- *         not skipped contribute)
+ *         MXFP8 and NVFP4: from the dequantized Q and K, no smoothing; with SKIP only the KV tiles
+ *         that were not skipped contribute)
  * All other arguments, results and errors are those of dit_attn_fwd.
  */
 dit_status dit_attn_fwd_lse(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
@@ -259,7 +265,8 @@ size_t dit_attn_quantized_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk
  * mode must include DIT_MODE_SAGE; the other arguments are as for dit_attn_fwd. For QK16PV8
  * (qk_dtype DIT_QK_BF16, q_block = k_block = 0) q_codes and k_codes are the BF16 Q and K,
  * q_scale and k_scale are unused (may be NULL), and v_codes / v_scale come from sage_quantize_v.
- * MXFP8 operands go through dit_attn_fwd_mxfp8 (qk_dtype DIT_QK_MXFP8 is rejected here).
+ * MXFP8 and NVFP4 operands go through dit_attn_fwd_mxfp8 / dit_attn_fwd_nvfp4 (those qk_dtypes
+ * are rejected here).
  */
 dit_status dit_attn_fwd_quantized(const void* q_codes, const void* k_codes, const void* v_codes,
                                   const float* q_scale, const float* k_scale, const float* v_scale, void* out, int B,
@@ -312,6 +319,38 @@ dit_status dit_attn_fwd_mxfp8(const void* q_codes, const void* k_codes, const vo
                               const uint8_t* k_sf, const float* v_scale, void* out, float* lse, int B, int Hq,
                               int Hkv, int Sq, int Skv, int mode, float threshold_scale_factor, void* stream,
                               int32_t* skip_counts);
+
+/*
+ * The NVFP4 Q/K prepass alone ("VisualGen Quantized Attention", section "MXFP8 and NVFP4 in the
+ * CUTEDSL and FlashInfer backends": Q/K in fixed blocks of 16 elements); V goes through
+ * sage_quantize_v. Per tensor, S = 2688 / amax_T (amax_T = max |x| over the whole Q, resp. K
+ * tensor; 1 if it is 0), a float32 division. Per token, head and block of 16 channels 16c..16c+15:
+ * scale byte = E4M3(float32(amax_b / 6) * S) (round to nearest even, saturating), and elements
+ * E2M1(float32(x * float32(S / d_b))) with d_b the byte's value (round to nearest even, saturating
+ * at 6; zero codes when d_b = 0). Dequantized: x ~ code * d_b / S.
+ *
+ *   q, k       device bf16 [B, Sq, Hq, 128] / [B, Skv, Hkv, 128]; q may be NULL when Sq == 0
+ *   q_codes    device [B, Sq, Hq, 64]: E2M1 codes, channel 2i in bits 0-3 and 2i+1 in bits 4-7 of
+ *              byte i (16-byte aligned)
+ *   k_codes    device [B, Skv, Hkv, 64], likewise
+ *   q_sf       device uint8 [B, Hq, Sq, 8]: E4M3 block-scale bytes (8-byte aligned)
+ *   k_sf       device uint8 [B, Hkv, Skv, 8]
+ *   q_scale, k_scale   device float, one each: the tensor scales S (used as scratch during the call)
+ * The codes, bytes and scales are those the NVFP4 path of dit_attn_fwd computes, bit for bit.
+ */
+dit_status nvfp4_quantize_qk(const void* q, const void* k, int B, int Hq, int Hkv, int Sq, int Skv, void* q_codes,
+                             void* k_codes, uint8_t* q_sf, uint8_t* k_sf, float* q_scale, float* k_scale,
+                             void* stream);
+
+/*
+ * Attention over NVFP4 Q/K (from nvfp4_quantize_qk) and FP8 V (from sage_quantize_v): BMM1 applies
+ * the E4M3 block scales inside the block-scaled MMA and divides by q_scale * k_scale; the rest is the
+ * QK16PV8 path. Other arguments, results and errors as for dit_attn_fwd_mxfp8.
+ */
+dit_status dit_attn_fwd_nvfp4(const void* q_codes, const void* k_codes, const void* v_codes, const uint8_t* q_sf,
+                              const uint8_t* k_sf, const float* q_scale, const float* k_scale, const float* v_scale,
+                              void* out, float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int mode,
+                              float threshold_scale_factor, void* stream, int32_t* skip_counts);
 
 /*
  * Synchronizes `stream`, then reports and clears the device error word: DIT_OK, or

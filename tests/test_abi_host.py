@@ -50,7 +50,7 @@ def test_status_strings(lib):
     assert dit.dit_status_string(0) == "ok"
     for s in range(6):
         assert dit.dit_status_string(s)
-    assert lib.dit_abi_version() == 3
+    assert lib.dit_abi_version() == 4
 
 
 FAKE = ctypes.c_void_p(1 << 20)           # a 16-byte aligned, never-dereferenced address
@@ -74,7 +74,8 @@ def _fwd(lib, q=FAKE, B=1, Hq=4, Hkv=2, Sq=256, Skv=256, mode=0, qk=0, qb=1, kb=
     dict(mode=1, qk=0),                     # QK16PV8 with Q/K block sizes
     dict(mode=1, qk=3),                     # MXFP8 with token-block sizes (its blocks are its own)
     dict(mode=1, qk=3, qb=0, kb=16), dict(mode=0, qk=3, qb=0, kb=0),  # MXFP8 blocks; MXFP8 without SAGE
-    dict(mode=1, qk=4, qb=0, kb=0),         # no such dtype
+    dict(mode=1, qk=4), dict(mode=0, qk=4, qb=0, kb=0),  # NVFP4 with token blocks; NVFP4 without SAGE
+    dict(mode=1, qk=5, qb=0, kb=0),         # no such dtype
     dict(mode=1, qk=1, qb=2), dict(mode=1, qk=2, kb=8), dict(mode=1, qk=1, kb=0),
     dict(mode=2, factor=-1.0), dict(mode=2, factor=float("nan")), dict(mode=3, qk=1, factor=float("inf")),
     dict(q=MISALIGNED), dict(q=None),
@@ -125,7 +126,7 @@ def _recipes():
 def test_every_printed_recipe_is_accepted(lib, recipe):
     _, dt, qb, kb, vb = recipe
     qk = dit.QK_DTYPES[dt]
-    if dt in ("bf16", "mxfp8"):  # QK16PV8, MXFP8: one tensor-wide V scale (v_block 0) or one per channel (1)
+    if dt in ("bf16", "mxfp8", "nvfp4"):  # one tensor-wide V scale (v_block 0) or one per channel (1)
         assert vb in (0, 1)
         mode = dit.MODE_SAGE | (dit.MODE_V_PER_TENSOR if vb == 0 else 0)
     else:
@@ -160,6 +161,9 @@ def test_workspace_layout_size():
     mx = dit.dit_attn_workspace_bytes(B, Hq, Hkv, S, S, 1, "mxfp8", 0, 0)
     assert 3 * n + 2 * n // 32 <= mx < 3 * n + 2 * n // 32 + 16 * 2**20
     assert dit.dit_attn_workspace_bytes(B, Hq, Hkv, S, S, 5, "mxfp8", 0, 0) == mx
+    # NVFP4: half-byte Q/K codes, 1-byte V codes, 8 scale bytes per token and head for Q and K
+    nv = dit.dit_attn_workspace_bytes(B, Hq, Hkv, S, S, 1, "nvfp4", 0, 0)
+    assert 2 * n + 2 * n // 16 <= nv < 2 * n + 2 * n // 16 + 16 * 2**20
 
 
 def test_v_prepass_arguments_rejected_on_host(lib):
@@ -195,14 +199,15 @@ def test_host_pipeline_rejects_bad_arguments(lib):
 
 def test_sage_prepasses_reject_dtypes_without_token_blocks(lib):
     ws = lib.sage_quantize_workspace_bytes(1, 2, 256)
-    for qk in (0, 3):  # BF16 and MXFP8 have no SAGE token blocks to quantize with
+    for qk in (0, 3, 4):  # BF16, MXFP8 and NVFP4 have no SAGE token blocks to quantize with
         assert lib.sage_quantize_qkv(FAKE, FAKE, FAKE, 1, 4, 2, 256, 256, qk, 0, 0, FAKE, FAKE, FAKE, FAKE, FAKE,
                                      FAKE, FAKE, FAKE, ws, None) == INVALID
         assert lib.sage_quantize_qkv_with_mean(FAKE, FAKE, FAKE, FAKE, 1, 4, 2, 256, 256, qk, 0, 0, FAKE, FAKE, FAKE,
                                                FAKE, FAKE, FAKE, FAKE, ws, None) == INVALID
-    # MXFP8 operands have their own attention entry point
-    assert lib.dit_attn_fwd_quantized(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 2, 256, 256, 1, 3, 0, 0, 0.0,
-                                      None, None, 0, None) == INVALID
+    # MXFP8 and NVFP4 operands have their own attention entry points
+    for qk in (3, 4):
+        assert lib.dit_attn_fwd_quantized(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 2, 256, 256, 1, qk, 0, 0,
+                                          0.0, None, None, 0, None) == INVALID
 
 
 def test_mxfp8_entry_points_reject_bad_arguments(lib):
@@ -235,3 +240,32 @@ def test_mxfp8_entry_points_reject_bad_arguments(lib):
     assert lib.mx_quantize_qk(FAKE, FAKE, 0, 4, 2, 256, 256, FAKE, FAKE, FAKE, FAKE, None) == 0
     assert lib.dit_attn_fwd_mxfp8(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 1, 4, 2, 0, 256, 1, 0.0, None,
                                   None) == 0
+
+
+def test_nvfp4_entry_points_reject_bad_arguments(lib):
+    ODD4 = ctypes.c_void_p((1 << 20) + 4)   # 4- but not 8-byte aligned
+    ODD2 = ctypes.c_void_p((1 << 20) + 2)
+
+    def quant(q=FAKE, qsf=FAKE, ksf=FAKE, gs=FAKE, Sq=256, Hq=4):
+        return lib.nvfp4_quantize_qk(q, FAKE, 1, Hq, 2, Sq, 256, FAKE, FAKE, qsf, ksf, gs, FAKE, None)
+    assert quant(Hq=5) == INVALID
+    assert quant(q=None) == INVALID
+    assert quant(qsf=ODD4) == INVALID       # the 8 scale bytes of a row are read as one 8-byte word
+    assert quant(ksf=ODD4) == INVALID
+    assert quant(gs=ODD2) == INVALID
+    assert quant(gs=None) == INVALID
+
+    def fwd(mode=1, qsf=FAKE, gs=FAKE, lse=None, factor=0.0):
+        return lib.dit_attn_fwd_nvfp4(FAKE, FAKE, FAKE, qsf, FAKE, gs, FAKE, FAKE, FAKE, lse, 1, 4, 2, 256, 256, mode,
+                                      factor, None, None)
+    assert fwd(mode=0) == INVALID
+    assert fwd(mode=3, factor=float("nan")) == INVALID
+    assert fwd(qsf=ODD4) == INVALID
+    assert fwd(gs=None) == INVALID
+    assert fwd(lse=ODD2) == INVALID
+    if not torch.cuda.is_available():
+        assert fwd() == UNSUPPORTED
+        assert fwd(mode=7, factor=1.0) == UNSUPPORTED   # SAGE | SKIP | V per tensor
+        assert quant() == UNSUPPORTED
+        assert quant(Sq=0, q=None, qsf=None, gs=None) == UNSUPPORTED
+    assert lib.nvfp4_quantize_qk(FAKE, FAKE, 0, 4, 2, 256, 256, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None) == 0

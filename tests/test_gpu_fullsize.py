@@ -175,3 +175,23 @@ def test_dit_mxfp8_32k_prepass_bit_exact_and_sampled_tiles():
     for b, h, t in case.sample_tiles():
         o, _, rows = oatt.attention_q_tile(case.inp, b, h, t, mode="mxfp8", quant=want)
         assert _rel(_np(out[b, rows, h]), o) <= SAGE_REL, (b, h, t)
+
+
+def test_dit_nvfp4_32k_prepass_bit_exact_and_sampled_tiles():
+    # NVFP4 Q/K + per-channel FP8 V (the CUTEDSL recipe's block sizes (0, 0, 1)) on the DiT inputs
+    from oracle import nvfp4_quant
+    case = _case("dit_nvfp4_32k")
+    want = nvfp4_quant.nvfp4_qk_quantize(case.inp["q"], case.inp["k"], case.inp["v"], per_tensor=False)
+    got = dit.nvfp4_quantize_qk(case.gpu[0], case.gpu[1])
+    torch.cuda.synchronize()
+    for name in ["q_sf", "k_sf", "q_codes", "k_codes"]:
+        bad = np.count_nonzero(got[name].cpu().numpy() != want[name])
+        assert bad == 0, f"{name}: {bad} differ"
+    for name in ["q_gs", "k_gs"]:
+        assert np.array_equal(got[name].cpu().numpy().view(np.uint32), np.array([want[name]]).view(np.uint32)), name
+    del got
+    out = dit.dit_attn_fwd(*case.gpu, mode=dit.MODE_SAGE, qk_dtype="nvfp4", q_block=0, k_block=0)
+    dit.dit_attn_check_errors()
+    for b, h, t in case.sample_tiles():
+        o, _, rows = oatt.attention_q_tile(case.inp, b, h, t, mode="nvfp4", quant=want)
+        assert _rel(_np(out[b, rows, h]), o) <= SAGE_REL, (b, h, t)

@@ -1,0 +1,189 @@
+"""GPU parity of NVFP4 Q/K + FP8 V through the C-ABI, against the CPU oracle ("VisualGen Quantized
+Attention", section "MXFP8 and NVFP4 in the CUTEDSL and FlashInfer backends": Q/K in fixed blocks
+of 16 elements, V in FP8 per channel or with one tensor-wide scale).
+
+Bars: packed Q/K codes, E4M3 block-scale bytes and the float32 tensor scales bit-exact; output
+rel-L2 <= 1e-2 against the quantization-emulating oracle (the SAGE bar: BMM1 differs from the
+oracle only in float32 summation order, P is re-quantized the same way); LSE within 2e-3 per row;
+skipped-tile counts within 0.5% of the oracle's (at least one tile of slack).
+
+The block scales reach the tensor cores through tensor memory, one scale word per row for each of
+the MMA's two 64-wide K slices; the scaled-rows test gives every row and every 16-channel block of
+Q and K its own magnitude, so any row, block, word or byte read from the wrong place, or a swapped
+nibble order, moves the result far outside the bar.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import diffusion_transformer_attention_gb300 as dit
+import workloads
+from oracle import attention as oatt
+from oracle import nvfp4_quant
+
+pytestmark = pytest.mark.gpu
+
+REL, LSE_ABS = 1e-2, 2e-3
+
+
+def _np(t):
+    return t.float().cpu().numpy()
+
+
+def _rel(a, b):
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+def _inputs(w, seed):
+    q, k, v = workloads.generate(w, seed)
+    return (q.cuda(), k.cuda(), v.cuda()), dict(q=_np(q), k=_np(k), v=_np(v))
+
+
+def _mode(per_tensor, skip=False):
+    return dit.MODE_SAGE | (dit.MODE_V_PER_TENSOR if per_tensor else 0) | (dit.MODE_SKIP if skip else 0)
+
+
+def _reference(inp, per_tensor, factor=None):
+    quant = nvfp4_quant.nvfp4_qk_quantize(inp["q"], inp["k"], inp["v"], per_tensor)
+    B, Sq, Hq = inp["q"].shape[:3]
+    nqt = math.ceil(Sq / 128)
+    out = np.zeros(inp["q"].shape)
+    lse = np.zeros((B, Hq, Sq))
+    counts = np.zeros((B, Hq, nqt), np.int64)
+    for b in range(B):
+        for h in range(Hq):
+            for t in range(nqt):
+                o, n, rows, l = oatt.attention_q_tile(inp, b, h, t, mode="nvfp4", factor=factor, quant=quant,
+                                                      with_lse=True)
+                out[b, rows, h] = o
+                lse[b, h, rows] = l
+                counts[b, h, t] = n
+    return out, lse, counts
+
+
+def _scaled_rows(B, S, H, seed, span=9):
+    """bf16 values with a power of two per (token, head, 16-channel block) in 2^-span .. 2^span."""
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(B, S, H, 128, generator=g)
+    e = torch.randint(-span, span + 1, (B, S, H, 8), generator=g).float()
+    return (x * torch.exp2(e).repeat_interleave(16, dim=3)).bfloat16()
+
+
+def _check_quant(got, x, name):
+    codes, sf, S = nvfp4_quant.nvfp4_quantize(x)
+    assert np.array_equal(got[name + "_gs"].cpu().numpy().view(np.uint32), np.array([S]).view(np.uint32)), name
+    assert np.array_equal(got[name + "_sf"].cpu().numpy(), sf), name
+    g = got[name + "_codes"].cpu().numpy()
+    bad = np.count_nonzero(g != codes)
+    assert bad == 0, f"{name}: {bad} of {g.size} code bytes differ"
+
+
+@pytest.mark.parametrize("shape,kind", [((2, 4, 2, 300, 333), "koffset"), ((1, 2, 2, 129, 1000), "outlier"),
+                                        ((3, 2, 1, 5, 1), "iid")])
+def test_nvfp4_prepass_bit_exact(shape, kind):
+    B, Hq, Hkv, Sq, Skv = shape
+    (q, k, v), inp = _inputs(workloads.Workload("nq", B, Hq, Hkv, Sq, Skv, kind=kind), seed=41)
+    got = dit.nvfp4_quantize_qk(q, k)
+    torch.cuda.synchronize()
+    _check_quant(got, inp["q"], "q")
+    _check_quant(got, inp["k"], "k")
+
+
+def test_nvfp4_prepass_extreme_blocks_bit_exact():
+    # zero blocks, ties of E2M1 rounding, blocks far below the tensor max (subnormal E4M3 scales and
+    # zero scales), negative zeros, mixed with normal ones
+    x = _scaled_rows(1, 64, 3, seed=42).float()
+    x[0, 0] = 0.0
+    x[0, 1, :, :16] = 2.0 ** -20
+    x[0, 2, :, 16:32] = torch.tensor([6.0, 5.0, 3.5, 2.5, 1.75, 1.25, 0.75, 0.25] * 2)
+    x[0, 3, :, 32:48] = -0.0
+    x[0, 4, :, 48:64] = torch.linspace(-3, 3, 16)
+    x[0, 5, 0, 5] = 0.0
+    x = x.bfloat16()
+    got = dit.nvfp4_quantize_qk(x.cuda(), x.cuda())
+    torch.cuda.synchronize()
+    _check_quant(got, x.float().numpy(), "q")
+    _check_quant(got, x.float().numpy(), "k")
+
+
+@pytest.mark.parametrize("per_tensor", [True, False])
+@pytest.mark.parametrize("shape,kind", [
+    ((1, 2, 2, 256, 256), "iid"),        # one CTA per head
+    ((2, 4, 2, 300, 400), "koffset"),    # GQA, ragged Q and KV tails
+    ((1, 3, 1, 130, 1000), "outlier"),   # MQA, cross-attention shape, outlier channels (distinct block scales)
+    ((1, 1, 1, 1, 1), "iid"),            # a single query and key
+])
+def test_attention_matches_oracle(per_tensor, shape, kind):
+    B, Hq, Hkv, Sq, Skv = shape
+    (q, k, v), inp = _inputs(workloads.Workload("na", B, Hq, Hkv, Sq, Skv, kind=kind), seed=43)
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full((B, Hq, Sq), float("nan"), dtype=torch.float32, device="cuda")
+    counts = torch.full((B, Hq, math.ceil(Sq / 128)), -1, dtype=torch.int32, device="cuda")
+    dit.dit_attn_fwd(q, k, v, out, mode=_mode(per_tensor), qk_dtype="nvfp4", q_block=0, k_block=0,
+                     skip_counts=counts, lse=lse)
+    dit.dit_attn_check_errors()
+    got = _np(out)
+    want, want_lse, _ = _reference(inp, per_tensor)
+    assert np.isfinite(got).all()
+    assert _rel(got, want) <= REL
+    assert np.abs(lse.cpu().numpy() - want_lse).max() <= LSE_ABS
+    assert (counts == 0).all()
+
+
+def test_scaled_rows_and_blocks_match_oracle():
+    B, Hq, Hkv, Sq, Skv = 1, 2, 1, 256, 384
+    q, k = _scaled_rows(B, Sq, Hq, seed=44, span=3), _scaled_rows(B, Skv, Hkv, seed=45, span=3)
+    v = torch.randn(B, Skv, Hkv, 128, generator=torch.Generator().manual_seed(46)).bfloat16()
+    inp = dict(q=_np(q), k=_np(k), v=_np(v))
+    out = dit.dit_attn_fwd(q.cuda(), k.cuda(), v.cuda(), mode=_mode(False), qk_dtype="nvfp4", q_block=0, k_block=0)
+    dit.dit_attn_check_errors()
+    want, _, _ = _reference(inp, False)
+    assert _rel(_np(out), want) <= REL
+
+
+VIDEO_SMALL = workloads.Workload("v", 1, 2, 2, 3 * 16 * 24, 3 * 16 * 24, kind="video", grid=(3, 16, 24))
+
+
+@pytest.mark.parametrize("factor", [0.0, 50.0, 400.0])
+def test_skip_matches_oracle(factor):
+    w = VIDEO_SMALL
+    (q, k, v), inp = _inputs(w, seed=47)
+    nqt = math.ceil(w.Sq / 128)
+    counts = torch.full((w.B, w.Hq, nqt), -1, dtype=torch.int32, device="cuda")
+    out = dit.dit_attn_fwd(q, k, v, mode=_mode(False, skip=True), qk_dtype="nvfp4", q_block=0, k_block=0,
+                           threshold_scale_factor=factor, skip_counts=counts)
+    dit.dit_attn_check_errors()
+    want, _, wcounts = _reference(inp, False, factor=factor)
+    gc = counts.cpu().numpy()
+    assert (gc >= 0).all()
+    assert abs(int(gc.sum()) - int(wcounts.sum())) <= max(1, 0.005 * wcounts.sum())
+    assert _rel(_np(out), want) <= REL
+    if factor == 0.0:
+        assert gc.sum() == 0
+    else:
+        assert gc.sum() > 0
+
+
+def test_skip_factor_zero_is_bit_identical_to_no_skip():
+    (q, k, v), _ = _inputs(VIDEO_SMALL, seed=48)
+    a = dit.dit_attn_fwd(q, k, v, mode=_mode(True), qk_dtype="nvfp4", q_block=0, k_block=0)
+    b = dit.dit_attn_fwd(q, k, v, mode=_mode(True, skip=True), qk_dtype="nvfp4", q_block=0, k_block=0,
+                         threshold_scale_factor=0.0)
+    assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("per_tensor", [True, False])
+def test_separate_entries_equal_the_fused_path(per_tensor):
+    (q, k, v), _ = _inputs(workloads.Workload("ns", 1, 4, 2, 260, 390, kind="outlier"), seed=49)
+    lse_a = torch.empty((1, 4, 260), dtype=torch.float32, device="cuda")
+    lse_b = torch.empty_like(lse_a)
+    fused = dit.dit_attn_fwd(q, k, v, mode=_mode(per_tensor), qk_dtype="nvfp4", q_block=0, k_block=0, lse=lse_a)
+    quant = dit.nvfp4_quantize_qk(q, k)
+    quant.update(dit.sage_quantize_v(v, per_tensor=per_tensor))
+    sep = dit.dit_attn_fwd_nvfp4(quant, torch.empty_like(q), mode=dit.MODE_SAGE, lse=lse_b)
+    dit.dit_attn_check_errors()
+    assert torch.equal(fused, sep)
+    assert torch.equal(lse_a, lse_b)
