@@ -104,7 +104,7 @@ struct Bars {
   uint64_t sfa_full;    // MXFP8 / NVFP4: the Q tiles' scale factors are in shared memory
   uint32_t tmem_base;
   int abort_flag;
-  int skip_flag[2];
+  int skip_flag[2][2];  // [Q tile][KV tile parity]: 1 when that KV tile was skipped
 };
 static_assert(sizeof(Bars) <= 512, "barrier block too large");
 
@@ -183,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->o_done[i], 1);
     }
     bars->abort_flag = 0;
-    bars->skip_flag[0] = bars->skip_flag[1] = 0;
+    bars->skip_flag[0][0] = bars->skip_flag[0][1] = bars->skip_flag[1][0] = bars->skip_flag[1][1] = 0;
     fence_mbar_init();
   }
   if (warp == 2) {
@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t d_o = tbase + kColO0 + 128 * i;
     const uint32_t t_sfa = tbase + kColSfa + 4 * kSfWords * i;  // block-scaled: this tile's Q scale words
     const uint32_t t_sfb = tbase + kColSfb + 4 * kSfWords * i;  // and its copy of the K tile's
-    volatile int* skip_flag = bars->skip_flag;
+    volatile int (*skip_flag)[2] = bars->skip_flag;
     auto wait = [&](uint64_t* bar, int parity) {
       return __all_sync(0xffffffffu, mbar_wait_bounded(bar, (uint32_t)parity, budget, abort_flag));
     };
@@ -354,14 +354,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = wait(&bars->kv_full[tv & 3], (tv >> 2) & 1) && wait(&bars->p_full[i], j & 1);
         if (!ok) break;
         tc_fence_after();
-        if (!SKIP || skip_flag[i] == 0) {
+        if (!SKIP || skip_flag[i][j & 1] == 0) {
+          // (the first KV tile is never skipped, so O is initialized by BMM2 of tile 0)
           const uint64_t bv = dv0 + (uint64_t)(((j & 1) * L::kVTile) >> 4);
 #pragma unroll
           for (int kk = 0; kk < kK2Steps; ++kk)
             mma_ss_if<kMma2Kind>(leader, d_o, ap + (uint64_t)((kk * 32) >> 4), bv + (uint64_t)((kk * 4096) >> 4),
                                  kIdesc2, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit_if(leader, &bars->o_done[i]);  // one phase per BMM2
         }
-        mma_commit_if(leader, &bars->o_done[i]);
         mma_commit_if(leader, &bars->kv_empty[tv & 3]);
       }
     } else {
@@ -377,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
         }
         tc_fence_after();
-        if (j >= 1 && (!SKIP || skip_flag[i] == 0)) {
+        if (j >= 1 && (!SKIP || skip_flag[i][0] == 0)) {
           const uint64_t bv = dv0 + (uint64_t)((((j - 1) & 1) * L::kVTile) >> 4);
 #pragma unroll
           for (int kk = 0; kk < kK2Steps; ++kk) {
@@ -537,9 +538,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_ex = -INFINITY, m_ref = -INFINITY, l = 0.0f;
     int nskip = 0;
     bool ok = true;
-    volatile int* skip_flag = bars->skip_flag;
+    volatile int (*skip_flag)[2] = bars->skip_flag;
+    int n_pv = 0;  // E4M3 P: BMM2s issued so far for this tile (o_done completes once per BMM2)
+    // Exponent weight per column group (log2 units): the row constant c, times the K block scale in
+    // SAGE. KB >= 4 folds the block scale into the weight; KB == 1 multiplies first.
+    constexpr int kGroups = (kQKScaled && KB >= 4) ? 64 / KB : 1;
 
     for (int j = 0; j < nt; ++j) {
+      float wg[kGroups];
+      if constexpr (kQKScaled && KB >= 4) {
+        // the block weights do not depend on S: read them (and return the scales' slot) before
+        // waiting for S, so that their wait and loads overlap the BMM1
+        if (ok) {
+          const int e = j & 3;
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->ks_full[e], (j >> 2) & 1, budget, abort_flag));
+          if (!ok) {
+            if (lane == 0) record_timeout(p, bars);
+          } else {
+            const float4* ks4 = reinterpret_cast<const float4*>(s_ks + e * 128 + (64 / KB) * h);
+#pragma unroll
+            for (int q4 = 0; q4 < kGroups / 4; ++q4) {
+              const float4 k4 = ks4[q4];
+              wg[4 * q4 + 0] = k4.x * c;
+              wg[4 * q4 + 1] = k4.y * c;
+              wg[4 * q4 + 2] = k4.z * c;
+              wg[4 * q4 + 3] = k4.w * c;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->ks_empty[e]);
+          }
+        }
+      }
       if (ok) {
         ok = mbar_wait_bounded(&bars->s_full[i], j & 1, budget, abort_flag);
         ok = __all_sync(0xffffffffu, ok);
@@ -573,12 +602,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < 64; ++k)
           if (k >= nvalid) s[k] = -INFINITY;
       }
-      // Exponent weight per column group (log2 units): the row constant c, times the K block
-      // scale in SAGE. KB >= 4 folds the block scale into the weight; KB == 1 multiplies first.
-      constexpr int kGroups = (kQKScaled && KB >= 4) ? 64 / KB : 1;
-      float wg[kGroups];
       float mh;  // this half's max of the weighted logits
-      if constexpr (kQKScaled) {
+      if constexpr (kQKScaled && KB == 1) {
+        // per-column scales: multiply S by them first (64 values, not held across the wait for S)
         const int e = j & 3;
         bool ks_ok = mbar_wait_bounded(&bars->ks_full[e], (j >> 2) & 1, budget, abort_flag);
         ks_ok = __all_sync(0xffffffffu, ks_ok);
@@ -586,30 +612,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) record_timeout(p, bars);
           ok = false;
         }
-        const float* ks = s_ks + e * 128 + (64 / KB) * h;  // this half's block scales
-        if constexpr (KB == 1) {
-          const float2* ks2 = reinterpret_cast<const float2*>(ks);
+        const float2* ks2 = reinterpret_cast<const float2*>(s_ks + e * 128 + 64 * h);  // this half's scales
 #pragma unroll
-          for (int k = 0; k < 32; ++k) s2[k] = __fmul2_rn(s2[k], ks2[k]);
-          wg[0] = c;
-          mh = rowmax64(s) * c;
-        } else {
-          mh = -INFINITY;
-          const float4* ks4 = reinterpret_cast<const float4*>(ks);
-#pragma unroll
-          for (int q4 = 0; q4 < kGroups / 4; ++q4) {
-            const float4 k4 = ks4[q4];
-            wg[4 * q4 + 0] = k4.x * c;
-            wg[4 * q4 + 1] = k4.y * c;
-            wg[4 * q4 + 2] = k4.z * c;
-            wg[4 * q4 + 3] = k4.w * c;
-          }
-#pragma unroll
-          for (int q = 0; q < kGroups; ++q)
-            mh = fmaxf(mh, groupmax<KB>(s + q * KB) * wg[q]);  // a NaN from -inf * 0 is ignored
-        }
+        for (int k = 0; k < 32; ++k) s2[k] = __fmul2_rn(s2[k], ks2[k]);
+        wg[0] = c;
+        mh = rowmax64(s) * c;
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->ks_empty[e]);
+      } else if constexpr (kQKScaled) {
+        mh = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < kGroups; ++q)
+          mh = fmaxf(mh, groupmax<KB>(s + q * KB) * wg[q]);  // a NaN from -inf * 0 is ignored
       } else {
         wg[0] = c;
         mh = rowmax64(s) * c;  // -inf when this half has no valid column
@@ -626,19 +640,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_sync(tile_bar, 256);
       }
       if constexpr (L::kPInSmem) {
-        // BMM2 of the previous KV tile must be complete before P's buffer, O or the skip flag
-        // (which that BMM2's issue read) change. Waiting on every tile keeps the waits in step with
-        // the barrier's phases.
-        if (j > 0 && ok) {
-          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->o_done[i], (j - 1) & 1, budget, abort_flag));
+        // The previous BMM2 must be complete before P's buffer or O change. o_done completes once
+        // per BMM2, so the wait before the n-th P is on phase n - 1: that phase is the only one
+        // outstanding (the one before was waited for, the next needs this P), so its parity is
+        // unambiguous. A skipped tile writes neither and does not wait.
+        if (!skip_tile && n_pv > 0 && ok) {
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->o_done[i], (n_pv - 1) & 1, budget, abort_flag));
           if (!ok && lane == 0) record_timeout(p, bars);
         }
         if (!ok) continue;
       }
       if (skip_tile) {
+        // With P in shared memory the flag has a slot per KV-tile parity: the issuer reads tile j's
+        // slot before it issues the BMM1 of tile j + 2, so this tile's write cannot overtake that
+        // read. With TMEM P the issuer reads the flag before the BMM1 of tile j + 1: one slot.
         ++nskip;
-        if (r == 0 && h == 0) skip_flag[i] = 1;
-        tc_fence_before();
+        if (r == 0 && h == 0) skip_flag[i][L::kPInSmem ? (j & 1) : 0] = 1;
+        // TMEM P: the issuer's next BMM1 overwrites the S just loaded (with P in shared memory, S
+        // was already released after its load)
+        if constexpr (!L::kPInSmem) tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->p_full[i]);
         continue;
@@ -737,8 +757,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_st_wait();
       if constexpr (SKIP) {
-        if (r == 0 && h == 0) skip_flag[i] = 0;
+        if (r == 0 && h == 0) skip_flag[i][L::kPInSmem ? (j & 1) : 0] = 0;
       }
+      ++n_pv;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->p_full[i]);

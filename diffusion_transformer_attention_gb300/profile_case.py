@@ -31,6 +31,7 @@ MODES = {
     "qk16pv8": (dit.MODE_SAGE | dit.MODE_V_PER_TENSOR, "bf16"),
     "mxfp8": (dit.MODE_SAGE, "mxfp8"),
     "nvfp4": (dit.MODE_SAGE, "nvfp4"),
+    "skip_mxfp8": (dit.MODE_SAGE | dit.MODE_SKIP, "mxfp8"),
 }
 
 
