@@ -120,6 +120,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                     const FmhaParams p) {
   constexpr bool kQKScaled = (QKF == QK_F16 || QKF == QK_E4M3);  // Q/K codes with token-block scales (SAGE)
+  // SAGE with Skip-Softmax: the softmax waits for the previous BMM2 only before writing P, so skipped
+  // tiles skip that wait (measured faster there; the other instantiations keep a wait on every tile,
+  // which measured faster for them). o_done then completes once per BMM2, and the skip flag needs a
+  // slot per KV-tile parity.
+  constexpr bool kLazyPv = SKIP && kQKScaled;
   constexpr bool kMX = (QKF == QK_MXF8);         // block-scaled MXFP8 Q/K (scales applied inside BMM1)
   constexpr bool kNV = (QKF == QK_NVF4);         // block-scaled NVFP4 Q/K (and a tensor scale per Q and K)
   constexpr bool kBS = kMX || kNV;
@@ -354,15 +359,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = wait(&bars->kv_full[tv & 3], (tv >> 2) & 1) && wait(&bars->p_full[i], j & 1);
         if (!ok) break;
         tc_fence_after();
-        if (!SKIP || skip_flag[i][j & 1] == 0) {
+        const bool skipped = SKIP && skip_flag[i][kLazyPv ? (j & 1) : 0] != 0;
+        if (!skipped) {
           // (the first KV tile is never skipped, so O is initialized by BMM2 of tile 0)
           const uint64_t bv = dv0 + (uint64_t)(((j & 1) * L::kVTile) >> 4);
 #pragma unroll
           for (int kk = 0; kk < kK2Steps; ++kk)
             mma_ss_if<kMma2Kind>(leader, d_o, ap + (uint64_t)((kk * 32) >> 4), bv + (uint64_t)((kk * 4096) >> 4),
                                  kIdesc2, (j > 0 || kk > 0) ? 1u : 0u);
-          mma_commit_if(leader, &bars->o_done[i]);  // one phase per BMM2
         }
+        // o_done: one phase per BMM2 (kLazyPv) or per KV tile
+        if (!kLazyPv || !skipped) mma_commit_if(leader, &bars->o_done[i]);
         mma_commit_if(leader, &bars->kv_empty[tv & 3]);
       }
     } else {
@@ -546,29 +553,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     for (int j = 0; j < nt; ++j) {
       float wg[kGroups];
-      if constexpr (kQKScaled && KB >= 4) {
-        // the block weights do not depend on S: read them (and return the scales' slot) before
-        // waiting for S, so that their wait and loads overlap the BMM1
-        if (ok) {
-          const int e = j & 3;
-          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->ks_full[e], (j >> 2) & 1, budget, abort_flag));
-          if (!ok) {
-            if (lane == 0) record_timeout(p, bars);
-          } else {
-            const float4* ks4 = reinterpret_cast<const float4*>(s_ks + e * 128 + (64 / KB) * h);
-#pragma unroll
-            for (int q4 = 0; q4 < kGroups / 4; ++q4) {
-              const float4 k4 = ks4[q4];
-              wg[4 * q4 + 0] = k4.x * c;
-              wg[4 * q4 + 1] = k4.y * c;
-              wg[4 * q4 + 2] = k4.z * c;
-              wg[4 * q4 + 3] = k4.w * c;
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->ks_empty[e]);
-          }
-        }
-      }
       if (ok) {
         ok = mbar_wait_bounded(&bars->s_full[i], j & 1, budget, abort_flag);
         ok = __all_sync(0xffffffffu, ok);
@@ -620,10 +604,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->ks_empty[e]);
       } else if constexpr (kQKScaled) {
+        const int e = j & 3;
+        bool ks_ok = mbar_wait_bounded(&bars->ks_full[e], (j >> 2) & 1, budget, abort_flag);
+        ks_ok = __all_sync(0xffffffffu, ks_ok);
+        if (!ks_ok) {
+          if (lane == 0) record_timeout(p, bars);
+          ok = false;
+        }
+        const float4* ks4 = reinterpret_cast<const float4*>(s_ks + e * 128 + (64 / KB) * h);  // this half's scales
+#pragma unroll
+        for (int q4 = 0; q4 < kGroups / 4; ++q4) {
+          const float4 k4 = ks4[q4];
+          wg[4 * q4 + 0] = k4.x * c;
+          wg[4 * q4 + 1] = k4.y * c;
+          wg[4 * q4 + 2] = k4.z * c;
+          wg[4 * q4 + 3] = k4.w * c;
+        }
         mh = -INFINITY;
 #pragma unroll
         for (int q = 0; q < kGroups; ++q)
           mh = fmaxf(mh, groupmax<KB>(s + q * KB) * wg[q]);  // a NaN from -inf * 0 is ignored
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->ks_empty[e]);
       } else {
         wg[0] = c;
         mh = rowmax64(s) * c;  // -inf when this half has no valid column
@@ -640,25 +642,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_sync(tile_bar, 256);
       }
       if constexpr (L::kPInSmem) {
-        // The previous BMM2 must be complete before P's buffer or O change. o_done completes once
-        // per BMM2, so the wait before the n-th P is on phase n - 1: that phase is the only one
-        // outstanding (the one before was waited for, the next needs this P), so its parity is
-        // unambiguous. A skipped tile writes neither and does not wait.
-        if (!skip_tile && n_pv > 0 && ok) {
-          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->o_done[i], (n_pv - 1) & 1, budget, abort_flag));
-          if (!ok && lane == 0) record_timeout(p, bars);
+        // The previous BMM2 must be complete before P's buffer, O or the skip flag change.
+        // kLazyPv: o_done completes once per BMM2, so the wait before the n-th P is on phase n - 1:
+        // that phase is the only one outstanding (the one before was waited for, the next needs this
+        // P), so its parity is unambiguous; a skipped tile writes neither P nor O and does not wait.
+        // Otherwise o_done completes once per KV tile and is waited for on every tile, which keeps
+        // the waits in step with its phases.
+        if constexpr (kLazyPv) {
+          if (!skip_tile && n_pv > 0 && ok) {
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->o_done[i], (n_pv - 1) & 1, budget, abort_flag));
+            if (!ok && lane == 0) record_timeout(p, bars);
+          }
+        } else {
+          if (j > 0 && ok) {
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->o_done[i], (j - 1) & 1, budget, abort_flag));
+            if (!ok && lane == 0) record_timeout(p, bars);
+          }
         }
         if (!ok) continue;
       }
       if (skip_tile) {
-        // With P in shared memory the flag has a slot per KV-tile parity: the issuer reads tile j's
-        // slot before it issues the BMM1 of tile j + 2, so this tile's write cannot overtake that
-        // read. With TMEM P the issuer reads the flag before the BMM1 of tile j + 1: one slot.
+        // kLazyPv: the flag has a slot per KV-tile parity; the issuer reads tile j's slot before it
+        // issues the BMM1 of tile j + 2, so this tile's write cannot overtake that read. Otherwise the
+        // wait on the previous BMM2 (or, with TMEM P, the issuer's order) already orders them: one slot.
         ++nskip;
-        if (r == 0 && h == 0) skip_flag[i][L::kPInSmem ? (j & 1) : 0] = 1;
+        if (r == 0 && h == 0) skip_flag[i][kLazyPv ? (j & 1) : 0] = 1;
         // TMEM P: the issuer's next BMM1 overwrites the S just loaded (with P in shared memory, S
         // was already released after its load)
-        if constexpr (!L::kPInSmem) tc_fence_before();
+        if constexpr (!kLazyPv) tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->p_full[i]);
         continue;
@@ -757,7 +768,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_st_wait();
       if constexpr (SKIP) {
-        if (r == 0 && h == 0) skip_flag[i][L::kPInSmem ? (j & 1) : 0] = 0;
+        if (r == 0 && h == 0) skip_flag[i][kLazyPv ? (j & 1) : 0] = 0;
       }
       ++n_pv;
       tc_fence_before();
