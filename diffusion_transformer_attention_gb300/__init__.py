@@ -54,6 +54,7 @@ SIGNATURES = {
     "nvfp4_quantize_qk": (_c_int, [_vp, _vp] + [_c_int] * 5 + [_vp] * 7),
     "dit_attn_fwd_nvfp4": (_c_int, [_vp] * 10 + [_c_int] * 6 + [_c_float, _vp, _vp]),
     "dit_attn_check_errors": (_c_int, [_vp]),
+    "dit_selftest_withheld_loads": (_c_int, [_vp] * 5 + [_c_int] * 6 + [ctypes.c_ulonglong, _vp]),
 }
 
 
@@ -331,6 +332,16 @@ def dit_attn_fwd_nvfp4(quant: dict, out, *, mode=MODE_SAGE, threshold_scale_fact
                                    float(threshold_scale_factor), _stream(stream), _ptr(skip_counts))
     _check(st, "dit_attn_fwd_nvfp4")
     return out
+
+
+def dit_selftest_withheld_loads(q, k, v, out, *, v_scale=None, wait_budget_ns=20_000_000, stream=None):
+    """Launch the attention kernel with its loads withheld and a short wait budget (a test of the
+    timeout path): the next ``dit_attn_check_errors`` raises with DIT_E_TIMEOUT. ``v`` holds E4M3 codes
+    (uint8) when ``v_scale`` is given (the QK16PV8 kernel), else BF16 (the dense kernel)."""
+    B, Hq, Hkv, Sq, Skv = _shape(q, k)
+    st = _lib().dit_selftest_withheld_loads(_ptr(q), _ptr(k), _ptr(v), _ptr(v_scale), _ptr(out), B, Hq, Hkv, Sq, Skv,
+                                            0 if v_scale is None else 1, int(wait_budget_ns), _stream(stream))
+    _check(st, "dit_selftest_withheld_loads")
 
 
 def dit_attn_check_errors(stream=None):

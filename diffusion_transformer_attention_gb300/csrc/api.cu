@@ -222,7 +222,8 @@ dit_status run_attention(const void* q, const void* k, const void* v, void* out,
                          const float* k_scale, const float* v_scale, int32_t* skip_counts, float* lse,
                          int* err, cudaStream_t stream, int q_hstride = 0, int kv_hstride = 0,
                          const uint8_t* q_sf = nullptr, const uint8_t* k_sf = nullptr,
-                         const float* q_gs = nullptr, const float* k_gs = nullptr) {
+                         const float* q_gs = nullptr, const float* k_gs = nullptr,
+                         unsigned long long wait_budget_ns = kWaitBudgetNs, int withhold_loads = 0) {
   // q_hstride / kv_hstride: head counts of the full tensors' rows when q, k, v, out are head slices
   if (q_hstride == 0) q_hstride = Hq;
   if (kv_hstride == 0) kv_hstride = Hkv;
@@ -254,7 +255,8 @@ dit_status run_attention(const void* q, const void* k, const void* v, void* out,
   p.skip_counts = skip_counts;
   p.lse = lse;
   p.err = err;
-  p.wait_budget_ns = kWaitBudgetNs;
+  p.wait_budget_ns = wait_budget_ns;
+  p.withhold_loads = withhold_loads;
   return from_cuda(launch_fmha(qk_format, pv_format, skip, tq, tk, tv, to, p, stream));
 }
 
@@ -713,6 +715,24 @@ dit_status dit_attn_fwd_host(const void* q_host, const void* k_host, const void*
   if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev->done, 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev->aux_done, 0);
   return from_cuda(e);
+}
+
+dit_status dit_selftest_withheld_loads(const void* q, const void* k, const void* v, const float* v_scale, void* out,
+                                      int B, int Hq, int Hkv, int Sq, int Skv, int e4m3_v,
+                                      unsigned long long wait_budget_ns, void* stream) {
+  if (!valid_shape(B, Hq, Hkv, Sq, Skv) || B == 0 || Sq == 0 || (e4m3_v != 0 && e4m3_v != 1) ||
+      wait_budget_ns < 1000000ull || wait_budget_ns > 10000000000ull)
+    return DIT_E_INVALID_ARG;
+  if (!q || !k || !v || !out || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      (e4m3_v && !v_scale))
+    return DIT_E_INVALID_ARG;
+  int* err = nullptr;
+  const dit_status ds = prepare_device(&err);
+  if (ds != DIT_OK) return ds;
+  return run_attention(q, k, v, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, QK_BF16, e4m3_v ? PV_E4M3 : PV_BF16, B, Hq,
+                       Hkv, Sq, Skv, e4m3_v ? DIT_MODE_SAGE : DIT_MODE_DENSE, 1, 1, 0.0f, nullptr, nullptr,
+                       e4m3_v ? v_scale : nullptr, nullptr, nullptr, err, static_cast<cudaStream_t>(stream), 0, 0,
+                       nullptr, nullptr, nullptr, nullptr, wait_budget_ns, 1);
 }
 
 dit_status dit_attn_check_errors(void* stream) {

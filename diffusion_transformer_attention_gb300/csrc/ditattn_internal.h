@@ -44,6 +44,7 @@ struct FmhaParams {
   float* lse;            // optional [B, Hq, Sq]: ln sum_j exp(s_ij) of each query row
   int* err;              // device error word
   unsigned long long wait_budget_ns;
+  int withhold_loads;    // self-test only: the producer issues no copy, so the first waits run out
 };
 
 // Attention kernel launcher (fmha_sm103.cu). Tensor maps describe q, k, v, out as 4-D

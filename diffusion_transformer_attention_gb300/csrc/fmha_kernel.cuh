@@ -206,7 +206,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   regs_dec<kRegsWG0>();
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    // (withhold_loads: a self-test of the timeout path; no copy is issued, so nothing is in flight
+    // when the other roles' bounded waits run out and they leave)
+    if (lane == 0 && !p.withhold_loads) {
       const uint64_t pol_q = l2_policy_evict_first();
       const uint64_t pol_kv = l2_policy_evict_last();
       int issued[kSlots] = {0, 0, 0, 0};

@@ -353,6 +353,22 @@ dit_status dit_attn_fwd_nvfp4(const void* q_codes, const void* k_codes, const vo
                               float threshold_scale_factor, void* stream, int32_t* skip_counts);
 
 /*
+ * Self-test of the timeout path: launches the attention kernel (dense, or with e4m3_v = 1 the
+ * QK16PV8 kernel, whose V is E4M3 codes with scales v_scale [B, Hkv, 128]) with every wait bounded by
+ * wait_budget_ns and with its loads withheld: no copy into the kernel is ever issued, so the first
+ * waits of the other roles run out, the kernel records DIT_E_TIMEOUT, every role leaves its loop and
+ * the kernel exits with nothing in flight. `out` is not written. Returns DIT_OK once launched; the
+ * following dit_attn_check_errors reports DIT_E_TIMEOUT (and clears it), and the device stays usable.
+ *
+ *   q, k, v, out   device buffers with the layouts of dit_attn_fwd (v: 1 byte per element if e4m3_v)
+ *   wait_budget_ns 1 ms .. 10 s
+ * B and Sq must be > 0.
+ */
+dit_status dit_selftest_withheld_loads(const void* q, const void* k, const void* v, const float* v_scale, void* out,
+                                      int B, int Hq, int Hkv, int Sq, int Skv, int e4m3_v,
+                                      unsigned long long wait_budget_ns, void* stream);
+
+/*
  * Synchronizes `stream`, then reports and clears the device error word: DIT_OK, or
  * DIT_E_TIMEOUT if a kernel since the last check gave up waiting, or DIT_E_CUDA if the
  * synchronization itself failed.

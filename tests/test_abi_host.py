@@ -269,3 +269,16 @@ def test_nvfp4_entry_points_reject_bad_arguments(lib):
         assert quant() == UNSUPPORTED
         assert quant(Sq=0, q=None, qsf=None, gs=None) == UNSUPPORTED
     assert lib.nvfp4_quantize_qk(FAKE, FAKE, 0, 4, 2, 256, 256, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None) == 0
+
+
+def test_withheld_loads_selftest_rejects_bad_arguments(lib):
+    def call(budget=20_000_000, B=1, Sq=256, e4m3=0, vs=None, q=FAKE):
+        return lib.dit_selftest_withheld_loads(q, FAKE, FAKE, vs, FAKE, B, 4, 2, Sq, 256, e4m3, budget, None)
+    assert call(budget=999_999) == INVALID          # below 1 ms
+    assert call(budget=10_000_000_001) == INVALID   # above 10 s
+    assert call(B=0) == INVALID and call(Sq=0) == INVALID
+    assert call(e4m3=2) == INVALID
+    assert call(e4m3=1, vs=None) == INVALID         # E4M3 V needs its scales
+    assert call(q=MISALIGNED) == INVALID
+    if not torch.cuda.is_available():
+        assert call() == UNSUPPORTED
