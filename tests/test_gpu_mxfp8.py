@@ -183,3 +183,59 @@ def test_separate_entries_equal_the_fused_path(per_tensor):
     dit.dit_attn_check_errors()
     assert torch.equal(fused, sep)
     assert torch.equal(lse_a, lse_b)
+
+
+def test_skip_counts_monotone_in_factor():
+    # for thr < 1 a skipped tile never holds the running max, so the skipped set only grows with the factor
+    (q, k, v), _ = _inputs(VIDEO_SMALL, seed=60)
+    prev = -1
+    for factor in [0.0, 1.0, 10.0, 100.0, 1000.0]:
+        counts = torch.zeros((1, 2, math.ceil(VIDEO_SMALL.Sq / 128)), dtype=torch.int32, device="cuda")
+        dit.dit_attn_fwd(q, k, v, mode=_mode(False, skip=True), qk_dtype="mxfp8", q_block=0, k_block=0,
+                         threshold_scale_factor=factor, skip_counts=counts)
+        total = int(counts.sum())
+        assert total >= prev
+        prev = total
+    dit.dit_attn_check_errors()
+    assert prev > 0
+
+
+def test_kv_shards_merge_with_the_lse():
+    # MXFP8 scales each token on its own, so KV shards need no shared statistic: the merge of the shards'
+    # (O, LSE) matches the oracle's merge of the same shards
+    w = workloads.Workload("mm", 1, 2, 2, 260, 1000, kind="koffset")
+    (q, k, v), inp = _inputs(w, seed=61)
+    cuts = (0, 384, 1000)
+    parts, oracle_parts = [], []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        ks, vs = k[:, a:b].contiguous(), v[:, a:b].contiguous()
+        lse = torch.empty((1, 2, 260), dtype=torch.float32, device="cuda")
+        out = dit.dit_attn_fwd(q, ks, vs, mode=_mode(False), qk_dtype="mxfp8", q_block=0, k_block=0, lse=lse)
+        parts.append((out.float(), lse))
+        sh = dict(q=inp["q"], k=inp["k"][:, a:b], v=inp["v"][:, a:b])
+        o_sh, l_sh, _ = _reference(sh, False)
+        oracle_parts.append((torch.from_numpy(o_sh), torch.from_numpy(l_sh)))
+    dit.dit_attn_check_errors()
+
+    def merge(ps):
+        lses = torch.stack([l for _, l in ps])
+        wgt = torch.softmax(lses, dim=0).permute(0, 1, 3, 2)
+        return sum(wgt[i][..., None] * o for i, (o, _) in enumerate(ps))
+    got = merge([(o.cpu(), l.cpu()) for o, l in parts]).numpy()
+    want = merge(oracle_parts).numpy()
+    assert _rel(got, want) <= REL
+
+
+def test_mx_prepass_near_bf16_max_bit_exact():
+    # blocks near the top of bfloat16 (the largest E8M0 bytes) next to ordinary and tiny ones
+    x = _scaled_rows(1, 64, 2, seed=64).float()
+    x[0, 0, :, :32] = 3.0e38
+    x[0, 1, :, 32:64] = -2.0 ** 127
+    x[0, 2, :, 64:96] *= 2.0 ** -120
+    x = x.bfloat16()
+    got = dit.mx_quantize_qk(x.cuda(), x.cuda())
+    torch.cuda.synchronize()
+    codes, sf = mx_quant.mx_quantize(x.float().numpy())
+    for name in ("q", "k"):
+        assert np.array_equal(got[name + "_sf"].cpu().numpy(), sf)
+        assert np.array_equal(got[name + "_codes"].cpu().numpy(), codes)

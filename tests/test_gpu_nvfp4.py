@@ -187,3 +187,32 @@ def test_separate_entries_equal_the_fused_path(per_tensor):
     dit.dit_attn_check_errors()
     assert torch.equal(fused, sep)
     assert torch.equal(lse_a, lse_b)
+
+
+def test_skip_counts_monotone_in_factor():
+    # for thr < 1 a skipped tile never holds the running max, so the skipped set only grows with the factor
+    (q, k, v), _ = _inputs(VIDEO_SMALL, seed=62)
+    prev = -1
+    for factor in [0.0, 1.0, 10.0, 100.0, 1000.0]:
+        counts = torch.zeros((1, 2, math.ceil(VIDEO_SMALL.Sq / 128)), dtype=torch.int32, device="cuda")
+        dit.dit_attn_fwd(q, k, v, mode=_mode(False, skip=True), qk_dtype="nvfp4", q_block=0, k_block=0,
+                         threshold_scale_factor=factor, skip_counts=counts)
+        total = int(counts.sum())
+        assert total >= prev
+        prev = total
+    dit.dit_attn_check_errors()
+    assert prev > 0
+
+
+def test_nvfp4_prepass_near_bf16_max_bit_exact():
+    # a tensor whose maximum is near the top of bfloat16 (tensor scale ~1e-35) with blocks far below it,
+    # whose scale bytes underflow to zero
+    x = _scaled_rows(1, 64, 2, seed=63).float()
+    x[0, 0, 0, 0] = 3.0e38
+    x[0, 1, :, :16] = -2.5e38
+    x[0, 2] *= 1e-30
+    x = x.bfloat16()
+    got = dit.nvfp4_quantize_qk(x.cuda(), x.cuda())
+    torch.cuda.synchronize()
+    _check_quant(got, x.float().numpy(), "q")
+    _check_quant(got, x.float().numpy(), "k")
