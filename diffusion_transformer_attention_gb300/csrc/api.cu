@@ -256,7 +256,7 @@ dit_status run_attention(const void* q, const void* k, const void* v, void* out,
   p.lse = lse;
   p.err = err;
   p.wait_budget_ns = wait_budget_ns;
-  p.withhold_loads = withhold_loads;
+  if (withhold_loads) return from_cuda(launch_fmha_withheld(pv_format, tq, tk, tv, to, p, stream));
   return from_cuda(launch_fmha(qk_format, pv_format, skip, tq, tk, tv, to, p, stream));
 }
 

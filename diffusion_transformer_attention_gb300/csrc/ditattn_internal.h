@@ -44,13 +44,19 @@ struct FmhaParams {
   float* lse;            // optional [B, Hq, Sq]: ln sum_j exp(s_ij) of each query row
   int* err;              // device error word
   unsigned long long wait_budget_ns;
-  int withhold_loads;    // self-test only: the producer issues no copy, so the first waits run out
 };
 
 // Attention kernel launcher (fmha_sm103.cu). Tensor maps describe q, k, v, out as 4-D
 // {128, S, H, B} tensors with 128-byte swizzled boxes.
 cudaError_t launch_fmha(int qk_format, int pv_format, bool skip, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                         const CUtensorMap& tm_v, const CUtensorMap& tm_o, const FmhaParams& p, cudaStream_t stream);
+// The timeout-path self-test: the dense (PV_BF16) or QK16PV8 (PV_E4M3) kernel with its loads withheld.
+cudaError_t launch_fmha_withheld(int pv_format, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                 const CUtensorMap& to, const FmhaParams& p, cudaStream_t stream);
+cudaError_t launch_fmha_withheld_dense(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                       const CUtensorMap& to, const FmhaParams& p, cudaStream_t stream);
+cudaError_t launch_fmha_withheld_qk16pv8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                         const CUtensorMap& to, const FmhaParams& p, cudaStream_t stream);
 cudaError_t launch_fmha_dense(bool skip, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const CUtensorMap& to, const FmhaParams& p, cudaStream_t stream);
 cudaError_t launch_fmha_sage_i8(bool skip, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -114,7 +114,10 @@ __device__ __forceinline__ void record_timeout(const FmhaParams& p, Bars* bars) 
 }
 
 
-template <int QKF, int PVF, int KB, bool SKIP>
+// WITHHOLD (a self-test of the timeout path, its own instantiation so that the production kernels'
+// code is unaffected): the producer issues no copy, so nothing is in flight when the other roles'
+// bounded waits run out and they leave.
+template <int QKF, int PVF, int KB, bool SKIP, bool WITHHOLD = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fmha_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -206,9 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   regs_dec<kRegsWG0>();
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    // (withhold_loads: a self-test of the timeout path; no copy is issued, so nothing is in flight
-    // when the other roles' bounded waits run out and they leave)
-    if (lane == 0 && !p.withhold_loads) {
+    if (lane == 0 && !WITHHOLD) {
       const uint64_t pol_q = l2_policy_evict_first();
       const uint64_t pol_kv = l2_policy_evict_last();
       int issued[kSlots] = {0, 0, 0, 0};
@@ -848,7 +849,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int QKF, int PVF, int KB, bool SKIP>
+template <int QKF, int PVF, int KB, bool SKIP, bool WITHHOLD = false>
 cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                        const FmhaParams& p, cudaStream_t stream) {
   static bool attr_set[64] = {};
@@ -859,16 +860,16 @@ cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
     // The register hand-over in the kernel (setmaxnreg) assumes exactly kLaunchRegs per thread at
     // launch; with fewer, the softmax warpgroups' increase could never be granted.
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, fmha_fwd_kernel<QKF, PVF, KB, SKIP>);
+    e = cudaFuncGetAttributes(&fa, fmha_fwd_kernel<QKF, PVF, KB, SKIP, WITHHOLD>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidKernelImage;
-    e = cudaFuncSetAttribute(fmha_fwd_kernel<QKF, PVF, KB, SKIP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(fmha_fwd_kernel<QKF, PVF, KB, SKIP, WITHHOLD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SmemLayout<QKF, PVF>::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   const dim3 grid((p.Sq + 255) / 256, p.Hq, p.B);
-  fmha_fwd_kernel<QKF, PVF, KB, SKIP><<<grid, kThreads, SmemLayout<QKF, PVF>::kSmemBytes, stream>>>(tq, tk, tv, to, p);
+  fmha_fwd_kernel<QKF, PVF, KB, SKIP, WITHHOLD><<<grid, kThreads, SmemLayout<QKF, PVF>::kSmemBytes, stream>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 

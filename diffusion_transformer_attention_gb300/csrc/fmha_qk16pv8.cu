@@ -11,4 +11,10 @@ cudaError_t launch_fmha_qk16pv8(bool skip, const CUtensorMap& tq, const CUtensor
               : launch_one<QK_BF16, PV_E4M3, 0, false>(tq, tk, tv, to, p, stream);
 }
 
+// the QK16PV8 kernel of the timeout-path self-test (loads withheld)
+cudaError_t launch_fmha_withheld_qk16pv8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                         const CUtensorMap& to, const FmhaParams& p, cudaStream_t stream) {
+  return launch_one<QK_BF16, PV_E4M3, 0, false, true>(tq, tk, tv, to, p, stream);
+}
+
 }  // namespace ditattn

@@ -16,4 +16,11 @@ cudaError_t launch_fmha(int qk_format, int pv_format, bool skip, const CUtensorM
   return cudaErrorInvalidValue;
 }
 
+cudaError_t launch_fmha_withheld(int pv_format, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                 const CUtensorMap& to, const FmhaParams& p, cudaStream_t stream) {
+  if (pv_format == PV_BF16) return launch_fmha_withheld_dense(tq, tk, tv, to, p, stream);
+  if (pv_format == PV_E4M3) return launch_fmha_withheld_qk16pv8(tq, tk, tv, to, p, stream);
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace ditattn
