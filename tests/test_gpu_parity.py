@@ -191,6 +191,24 @@ def test_skip_matches_oracle(sage, factor):
         assert gc.sum() == 0
 
 
+@pytest.mark.parametrize("dtype,qb,kb", [("fp8_e4m3", 1, 4), ("int8", 4, 1), ("fp8_e4m3", 16, 16), ("int8", 1, 1)])
+def test_sage_skip_other_formats_and_blocks(dtype, qb, kb):
+    # SAGE with Skip-Softmax waits for the previous BMM2 only before writing P: every K-block size and
+    # both code types run that path
+    w = VIDEO_SMALL
+    (q, k, v), inp = _inputs(w, seed=10)
+    nqt = math.ceil(w.Sq / 128)
+    counts = torch.full((w.B, w.Hq, nqt), -1, dtype=torch.int32, device="cuda")
+    out = dit.dit_attn_fwd(*_gpu(q, k, v), mode=dit.MODE_SKIP | dit.MODE_SAGE, qk_dtype=dtype, q_block=qb, k_block=kb,
+                           threshold_scale_factor=50.0, skip_counts=counts)
+    dit.dit_attn_check_errors()
+    want, wcounts = _sage_reference(inp, w, dtype, qb, kb, factor=50.0)
+    gc = counts.cpu().numpy()
+    assert abs(int(gc.sum()) - int(wcounts.sum())) <= max(1, 0.005 * wcounts.sum())
+    assert wcounts.sum() > 0
+    assert _rel(_np(out), want) <= SAGE_REL
+
+
 @pytest.mark.parametrize("sage", [False, True])
 def test_skip_factor_zero_is_bit_identical_to_no_skip(sage):
     (q, k, v), _ = _inputs(VIDEO_SMALL, seed=8)
