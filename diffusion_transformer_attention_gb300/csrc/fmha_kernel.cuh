@@ -1,7 +1,8 @@
 // Fused attention forward kernel for sm_103a (template; instantiated by fmha_dense.cu,
-// fmha_sage_i8.cu, fmha_sage_f8.cu, fmha_qk16pv8.cu, fmha_mxfp8.cu and fmha_nvfp4.cu): TMA-staged Q/K/V tiles, tcgen05 MMAs
-// accumulating S = Q K^T and O += P V in tensor memory, online softmax with exp2, optional SAGE
-// dequantization, P re-quantization to FP8 (SAGE and QK16PV8), and the Skip-Softmax tile test.
+// fmha_sage_i8.cu, fmha_sage_f8.cu, fmha_qk16pv8.cu, fmha_mxfp8.cu and fmha_nvfp4.cu): TMA-staged
+// Q/K/V tiles, tcgen05 MMAs accumulating S = Q K^T and O += P V in tensor memory (block-scaled for
+// MXFP8 / NVFP4 Q/K), online softmax with exp2, optional SAGE dequantization, P re-quantization to
+// FP8 (every recipe with E4M3 V), the Skip-Softmax tile test and the optional LSE output.
 //
 // The method is fixed by the pages ("TRTLLM Attention" user guide: dense BF16, SAGE, Skip-Softmax;
 // "SAGE + Skip-Softmax -- API Design & Test Plan", Part 1 §4: bmm1/bmm2 scales and
@@ -23,9 +24,10 @@
 // BMM2 reads P from tensor memory (TS). The issuer runs O_i += P_i(j-1) V_{j-1}, S_i = Q_i K_j^T as
 // soon as P_i(j-1) is ready, so while one tile's softmax turns S into P, the tensor cores work on
 // the other tile.
-// E4M3 P (SAGE and QK16PV8, 16 KB per tile): P goes to a shared-memory buffer and BMM2 is an SS MMA. S is free
-// as soon as the softmax has loaded it, so the issuer computes S_i(j+1) while the softmax works on
-// S_i(j); a per-tile barrier (o_done) returns P's buffer and O to the softmax after each BMM2.
+// E4M3 P (SAGE, QK16PV8, MXFP8, NVFP4; 16 KB per tile): P goes to a shared-memory buffer and BMM2 is
+// an SS MMA. S is free as soon as the softmax has loaded it, so the issuer computes S_i(j+1) while
+// the softmax works on S_i(j); a per-tile barrier (o_done) returns P's buffer and O to the softmax
+// after each BMM2 (SAGE with Skip-Softmax: only before the next P; see kLazyPv).
 // MXFP8 / NVFP4: the block-scaled MMA reads its scale factors from tensor memory, and S0 | S1 | O0 | O1 leave
 // no room, so the two tiles share one S buffer (S | O0 | O1 | scale factors): BMM1s alternate
 // between the tiles, each issued once the other tile's softmax has loaded the previous S. The
@@ -34,8 +36,8 @@
 // Numerics: logits are kept in log2 units (scaled by softmax_scale * log2 e). With BF16 P, O is
 // rescaled lazily (only when the running max grows by more than 8, P then stays below 2^8); with
 // E4M3 P it is rescaled eagerly so P = exp2(s - m_run) lies in [0, 1] and P * 448 re-quantizes on
-// the same grid as the definition. The row sum uses the unquantized P. Skip-Softmax compares the tile max against
-// the exact running max.
+// the same grid as the definition. The row sum uses the unquantized P. Skip-Softmax compares the
+// tile max against the exact running max.
 //
 // Every wait is bounded; on expiry the kernel records a timeout in the device error word, tells
 // the other roles to stop, drains its own copies and MMAs, frees tensor memory and exits. Named
@@ -549,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int nskip = 0;
     bool ok = true;
     volatile int (*skip_flag)[2] = bars->skip_flag;
-    int n_pv = 0;  // E4M3 P: BMM2s issued so far for this tile (o_done completes once per BMM2)
+    int n_pv = 0;  // kLazyPv: BMM2s issued so far for this tile (o_done completes once per BMM2)
     // Exponent weight per column group (log2 units): the row constant c, times the K block scale in
     // SAGE. KB >= 4 folds the block scale into the weight; KB == 1 multiplies first.
     constexpr int kGroups = (kQKScaled && KB >= 4) ? 64 / KB : 1;
