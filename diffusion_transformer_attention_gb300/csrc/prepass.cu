@@ -37,15 +37,6 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   return r;
 }
 
-// Cached in L2 but not L1: for rows read twice in a row (the second read hits L2).
-__device__ __forceinline__ uint4 ld_l2_v4(const void* p) {
-  uint4 r;
-  asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-}
-
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -68,84 +59,146 @@ __device__ __forceinline__ float quotient(float x, float scale, bool fast, float
   return (scale == 0.0f) ? 0.0f : __fdiv_rn(x, scale);
 }
 
-__device__ __forceinline__ int int8_code(float q) {
-  int c = __float2int_rn(q);  // round half to even
-  return max(-127, min(127, c));
+// INT8 codes without the conversion unit. Adding 1.5 * 2^23 to a float32 of magnitude <= 2^22
+// rounds it to an integer, half to even (the sum's unit in the last place is 1), and leaves that
+// integer n in the low mantissa bits: the sum's bits are 0x4B400000 + n. The quotient is clamped
+// to [-127, 127] first, which gives the same code as clamping the rounded value.
+constexpr float kRoundInt = 12582912.0f;  // 1.5 * 2^23
+__device__ __forceinline__ uint32_t int8_round_bits(float q) {
+  return __float_as_uint(__fadd_rn(fminf(fmaxf(q, -127.0f), 127.0f), kRoundInt));
+}
+
+// Four INT8 codes, `a` in the low byte (the low byte of the rounded sum is n's two's complement).
+__device__ __forceinline__ uint32_t int8_codes4(float a, float b, float c, float d) {
+  return __byte_perm(__byte_perm(int8_round_bits(a), int8_round_bits(b), 0x0040),
+                     __byte_perm(int8_round_bits(c), int8_round_bits(d), 0x0040), 0x5410);
+}
+
+// Two INT8 codes held exactly as fp16, `lo` in bits 0-15 (a zero code is +0).
+__device__ __forceinline__ uint32_t int8_code_f16x2(float lo, float hi) {
+  const __half2 h2 = __floats2half2_rn(__fsub_rn(__uint_as_float(int8_round_bits(lo)), kRoundInt),
+                                       __fsub_rn(__uint_as_float(int8_round_bits(hi)), kRoundInt));
+  return *reinterpret_cast<const uint32_t*>(&h2);
 }
 
 // ------------------------------------------------------------------ K mean / V absmax
-// Exact float32 sums of K by exponent bin. A bf16 value has 8 significant bits; 64 values whose
-// float32 exponent fields lie in one 10-wide window [lo, lo + 10) sum to a multiple of
-// 2^(lo - 134) below 2^(lo - 111), i.e. within 23 bits, so a float32 accumulator per window adds
-// them without rounding. Five windows cover |x| in [2^-32, 2^18); anything else that is not zero
-// (including subnormals) is added in float64 directly. GB300's float64 rate is low, so this
-// moves the per-element work to the float32 pipes and leaves a few float64 additions per thread.
+// Exact float32 sums of K by exponent bin. A bf16 value whose float32 exponent field E lies in
+// a 10-wide window [lo, lo + 10) is M * 2^(E - 134) with M < 256, i.e. a multiple of
+// u = 2^(lo - 134) below 255 * 2^9 u; 128 such values sum to less than 2^24 u, so a float32
+// accumulator per window adds them without rounding. Five windows cover |x| in [2^-32, 2^18);
+// anything else that is not zero (including subnormals) is added in float64. GB300's float64 rate
+// is low, so this moves the per-element work to the float32 pipes; the float64 additions run only
+// in CTAs that meet such a value, in a second pass over their tokens.
 constexpr int kBinLo = 127 - 32, kBinWidth = 10, kBins = 5;
+constexpr int kStatsBatch = 8;  // token rows a lane loads before it adds them (loads in flight)
+
+// Offset of the exponent field from the first window: below kBins * kBinWidth inside the windows,
+// larger otherwise (zero and subnormals wrap around).
+__device__ __forceinline__ unsigned bin_offset(float x) {
+  return ((__float_as_uint(x) >> 23) & 0xFFu) - (unsigned)kBinLo;
+}
+
+__device__ __forceinline__ uint2 ld_stream_v2(const void* p) {
+  uint2 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ void bf16x4_to_f32(const uint2& u, float* f) {
+  f[0] = __uint_as_float(u.x << 16);
+  f[1] = __uint_as_float(u.x & 0xFFFF0000u);
+  f[2] = __uint_as_float(u.y << 16);
+  f[3] = __uint_as_float(u.y & 0xFFFF0000u);
+}
 
 // Pass 1: each CTA reduces kStatsChunk tokens of one (batch, kv head): sums of K (WITH_K) and
-// float32 max |V| per channel. Thread t handles channels 8*(t%16).. and tokens t/16 + 16i (64
-// tokens: the bins above are exact for 64 values). Each thread's sum is the exact sum of its 64
-// values rounded once to float64 (its bins are added smallest first); the 16 partial rows are
-// then combined in a fixed order, so the result is deterministic.
+// float32 max |V| per channel. A warp reads whole 256-byte rows: lane l handles channels 4l..4l+3,
+// warp w tokens w + 8i (128 tokens: the bins above are exact for 128 values). Each lane's sum is
+// the exact sum of its in-window values (bins added smallest first in float64) plus the float64
+// sum, in token order, of the rest; the 8 warps' partial rows are then combined in a fixed order,
+// so the result is deterministic.
 template <bool WITH_K>
 __global__ void __launch_bounds__(256) kv_stats_partial_kernel(const __nv_bfloat16* __restrict__ k,
                                                                const __nv_bfloat16* __restrict__ v, int Skv, int Hkv,
                                                                int nchunk, double* __restrict__ psum,
                                                                float* __restrict__ pmax) {
-  __shared__ double ssum[16][kHeadDim];
-  __shared__ float smax[16][kHeadDim];
-  static_assert(kStatsChunk == 1024, "64 tokens per thread: the exponent bins are exact for 64 values");
+  constexpr int kWarps = 8, kTokens = kStatsChunk / kWarps;
+  static_assert(kTokens == 128, "128 tokens per lane: the exponent bins are exact for 128 values");
+  __shared__ double ssum[kWarps][kHeadDim];
+  __shared__ float smax[kWarps][kHeadDim];
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int cg = threadIdx.x & 15, tr = threadIdx.x >> 4;
-  double s[8];
-  float m[8];
-  float acc[8][kBins];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  float m[4];
+  float acc[4][kBins];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    s[e] = 0.0;
+  for (int e = 0; e < 4; ++e) {
     m[e] = 0.0f;
 #pragma unroll
-    for (int k = 0; k < kBins; ++k) acc[e][k] = 0.0f;
+    for (int i = 0; i < kBins; ++i) acc[e][i] = 0.0f;
   }
-  const int j0 = chunk * kStatsChunk;
-  const int j1 = min(Skv, j0 + kStatsChunk);
-#pragma unroll 4
-  for (int j = j0 + tr; j < j1; j += 16) {
-    const size_t off = (((size_t)b * Skv + j) * Hkv + h) * kHeadDim + cg * 8;
-    float kf[8], vf[8];
-    if constexpr (WITH_K) bf16x8_to_f32(ld_stream_v4(k + off), kf);
-    bf16x8_to_f32(ld_stream_v4(v + off), vf);
+  bool wide = false;  // a nonzero K value outside the windows
+  const int j0 = chunk * kStatsChunk + w;
+  const int jn = min(Skv, chunk * kStatsChunk + kStatsChunk);
+  const size_t row0 = (((size_t)b * Skv + j0) * Hkv + h) * kHeadDim + lane * 4;
+  const size_t step = (size_t)kWarps * Hkv * kHeadDim;  // 8 tokens
+  for (int i0 = 0; i0 < kTokens && j0 + kWarps * i0 < jn; i0 += kStatsBatch) {
+    uint2 kr[kStatsBatch], vr[kStatsBatch];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      if constexpr (WITH_K) {
-        const float x = kf[e];
-        const unsigned d = ((__float_as_uint(x) >> 23) & 0xFFu) - (unsigned)kBinLo;  // wraps below the window
-        if (d < (unsigned)(kBins * kBinWidth)) {
-          const unsigned bin = (d * 205u) >> 11;  // d / 10 for d < 50
-#pragma unroll
-          for (int k = 0; k < kBins; ++k) acc[e][k] += (bin == (unsigned)k) ? x : 0.0f;
-        } else if (x != 0.0f) {
-          s[e] += (double)x;
-        }
+    for (int u = 0; u < kStatsBatch; ++u) {
+      kr[u] = vr[u] = make_uint2(0u, 0u);  // zero rows past the end add nothing
+      if (j0 + kWarps * (i0 + u) < jn) {
+        const size_t off = row0 + (size_t)(i0 + u) * step;
+        if constexpr (WITH_K) kr[u] = ld_stream_v2(k + off);
+        vr[u] = ld_stream_v2(v + off);
       }
-      m[e] = fmaxf(m[e], fabsf(vf[e]));
+    }
+#pragma unroll
+    for (int u = 0; u < kStatsBatch; ++u) {
+      float kf[4], vf[4];
+      bf16x4_to_f32(kr[u], kf);
+      bf16x4_to_f32(vr[u], vf);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if constexpr (WITH_K) {
+          const float x = kf[e];
+          const unsigned d = bin_offset(x);
+          if (d < (unsigned)(kBins * kBinWidth)) {
+            const unsigned bin = (d * 205u) >> 11;  // d / 10 for d < 50
+#pragma unroll
+            for (int i = 0; i < kBins; ++i) acc[e][i] += (bin == (unsigned)i) ? x : 0.0f;
+          } else {
+            wide |= x != 0.0f;
+          }
+        }
+        m[e] = fmaxf(m[e], fabsf(vf[e]));
+      }
+    }
+  }
+  double s[4] = {0.0, 0.0, 0.0, 0.0};
+  if (WITH_K && __syncthreads_or(wide)) {  // rare: add the out-of-window values in float64, in token order
+    for (int i = 0; i < kTokens && j0 + kWarps * i < jn; ++i) {
+      float kf[4];
+      bf16x4_to_f32(ld_stream_v2(k + row0 + (size_t)i * step), kf);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (bin_offset(kf[e]) >= (unsigned)(kBins * kBinWidth) && kf[e] != 0.0f) s[e] += (double)kf[e];
     }
   }
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
+  for (int e = 0; e < 4; ++e) {
     if constexpr (WITH_K) {
       double t = (double)acc[e][0];
 #pragma unroll
-      for (int k = 1; k < kBins; ++k) t += (double)acc[e][k];
-      ssum[tr][cg * 8 + e] = t + s[e];
+      for (int i = 1; i < kBins; ++i) t += (double)acc[e][i];
+      ssum[w][lane * 4 + e] = t + s[e];
     }
-    smax[tr][cg * 8 + e] = m[e];
+    smax[w][lane * 4 + e] = m[e];
   }
   __syncthreads();
   if (threadIdx.x < kHeadDim) {
     double a = 0.0;
     float mx = 0.0f;
-    for (int r = 0; r < 16; ++r) {
+    for (int r = 0; r < kWarps; ++r) {
       a += ssum[r][threadIdx.x];
       mx = fmaxf(mx, smax[r][threadIdx.x]);
     }
@@ -214,19 +267,28 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const __nv_bfloat16* __res
     fast[e] = scale_in_fast_range(vs[e]);
     rcp[e] = fast[e] ? __frcp_rn(vs[e]) : 0.0f;
   }
-  const int j0 = chunk * kQuantRows;
-  const int j1 = min(Skv, j0 + kQuantRows);
-#pragma unroll 4
-  for (int j = j0 + tr; j < j1; j += 16) {
-    const size_t off = (((size_t)b * Skv + j) * Hkv + h) * kHeadDim + cg * 8;
-    float vf[8];
-    bf16x8_to_f32(ld_stream_v4(v + off), vf);
+  constexpr int kBatch = 8;  // rows loaded before any is converted
+  const int j0 = chunk * kQuantRows + tr;
+  const int jn = min(Skv, chunk * kQuantRows + kQuantRows);
+  const size_t row0 = (((size_t)b * Skv + j0) * Hkv + h) * kHeadDim + cg * 8;
+  const size_t step = (size_t)16 * Hkv * kHeadDim;  // 16 tokens
+  for (int i0 = 0; i0 < kQuantRows / 16 && j0 + 16 * i0 < jn; i0 += kBatch) {
+    uint4 raw[kBatch];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) vf[e] = quotient(vf[e], vs[e], fast[e], rcp[e]);
-    uint2 w;
-    w.x = e4m3x2(vf[0], vf[1]) | (e4m3x2(vf[2], vf[3]) << 16);
-    w.y = e4m3x2(vf[4], vf[5]) | (e4m3x2(vf[6], vf[7]) << 16);
-    *reinterpret_cast<uint2*>(v_codes + off) = w;
+    for (int u = 0; u < kBatch; ++u)
+      if (j0 + 16 * (i0 + u) < jn) raw[u] = ld_stream_v4(v + row0 + (size_t)(i0 + u) * step);
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      if (j0 + 16 * (i0 + u) >= jn) break;
+      float vf[8];
+      bf16x8_to_f32(raw[u], vf);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) vf[e] = quotient(vf[e], vs[e], fast[e], rcp[e]);
+      uint2 w;
+      w.x = e4m3x2(vf[0], vf[1]) | (e4m3x2(vf[2], vf[3]) << 16);
+      w.y = e4m3x2(vf[4], vf[5]) | (e4m3x2(vf[6], vf[7]) << 16);
+      *reinterpret_cast<uint2*>(v_codes + row0 + (size_t)(i0 + u) * step) = w;
+    }
   }
 }
 
@@ -234,17 +296,20 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const __nv_bfloat16* __res
 // A CTA covers kQuantRows consecutive tokens of one (batch, head), in warp units of ROWS =
 // max(QB, 2) tokens: two rows per iteration, 16 lanes per row (16-byte loads). For QB == 1 each
 // half-warp is its own block; otherwise the whole unit is one block. SMOOTH subtracts the K mean.
-// Blocks of 8 or more rows take two passes over their rows (the block max, then the codes, the
-// second reading from L2) instead of holding every row in registers, which keeps occupancy up.
+// A warp takes NU of its units at a time and loads all their rows (8 per lane, held as raw bf16)
+// before it reduces any block, so that enough loads are in flight; the codes are then computed from
+// the held rows.
 template <int QB, int OUT, bool SMOOTH>
 __global__ void __launch_bounds__(256) quant_tokens_kernel(const __nv_bfloat16* __restrict__ x, int S, int H,
                                                            const float* __restrict__ mean, void* __restrict__ codes,
                                                            float* __restrict__ scales, int nblk) {
   constexpr int ROWS = QB < 2 ? 2 : QB;
-  constexpr int IT = ROWS / 2;
+  constexpr int IT = ROWS / 2;               // rows per lane in a unit
   constexpr int UNITS = kQuantRows / ROWS;  // warp units per CTA
+  constexpr int PER_WARP = UNITS / 8;
+  constexpr int NU = IT >= 8 ? 1 : 8 / IT;  // units loaded together
   constexpr float QMAX = (OUT == CODE_E4M3) ? 448.0f : 127.0f;
-  static_assert(kQuantRows % 16 == 0, "whole blocks per CTA");
+  static_assert(kQuantRows % 16 == 0 && PER_WARP % NU == 0, "whole blocks per CTA, whole batches per warp");
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int half = lane >> 4, cg = lane & 15;
@@ -255,80 +320,76 @@ __global__ void __launch_bounds__(256) quant_tokens_kernel(const __nv_bfloat16* 
     mu[0] = m0.x; mu[1] = m0.y; mu[2] = m0.z; mu[3] = m0.w;
     mu[4] = m1.x; mu[5] = m1.y; mu[6] = m1.z; mu[7] = m1.w;
   }
-#pragma unroll 2
-  for (int u = warp; u < UNITS; u += 8) {
-    const int rb = chunk * UNITS + u;  // block of rows (a whole warp unit) within this (b, h)
-    if (rb * ROWS >= S) break;
-    constexpr bool kTwoPass = IT >= 4;
-    constexpr int KEEP = kTwoPass ? 1 : IT;  // rows held in registers between the passes
-    float val[KEEP][8];
-    float amax = 0.0f;
-    auto load_row = [&](int it, float* out) {  // smoothed values of this lane's 8 channels of a row
-      const int row = rb * ROWS + 2 * it + half;
-      if (row < S) {
-        const size_t off = (((size_t)b * S + row) * H + h) * kHeadDim + cg * 8;
-        bf16x8_to_f32(kTwoPass ? ld_l2_v4(x + off) : ld_stream_v4(x + off), out);
+  auto values = [&](const uint4& raw, float* out) {  // smoothed values of this lane's 8 channels of a row
+    bf16x8_to_f32(raw, out);
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          if constexpr (SMOOTH) out[e] = __fsub_rn(out[e], mu[e]);
-      } else {
+    for (int e = 0; e < 8; ++e)
+      if constexpr (SMOOTH) out[e] = __fsub_rn(out[e], mu[e]);
+  };
+  auto row_offset = [&](int row) { return (((size_t)b * S + row) * H + h) * kHeadDim + cg * 8; };
+  for (int t0 = 0; t0 < PER_WARP; t0 += NU) {
+    if ((chunk * UNITS + warp + 8 * t0) * ROWS >= S) break;  // later units start later still
+    uint4 raw[NU][IT];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) out[e] = 0.0f;
+    for (int n = 0; n < NU; ++n) {
+      const int rb = chunk * UNITS + warp + 8 * (t0 + n);
+#pragma unroll
+      for (int it = 0; it < IT; ++it) {
+        const int row = rb * ROWS + 2 * it + half;
+        raw[n][it] = row < S ? ld_stream_v4(x + row_offset(row)) : make_uint4(0u, 0u, 0u, 0u);
       }
-    };
-#pragma unroll
-    for (int it = 0; it < IT; ++it) {
-      float* vrow = val[kTwoPass ? 0 : it];
-      load_row(it, vrow);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(vrow[e]));
     }
-    // block absmax: over 16 lanes (QB == 1, one row per half-warp) or the whole warp
 #pragma unroll
-    for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    if constexpr (QB > 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
-    const float scale = __fdiv_rn(amax, QMAX);
-    const bool fast = scale_in_fast_range(scale);
-    const float rcp = fast ? __frcp_rn(scale) : 0.0f;
+    for (int n = 0; n < NU; ++n) {
+      const int rb = chunk * UNITS + warp + 8 * (t0 + n);  // block of rows (a whole warp unit) within this (b, h)
+      if (rb * ROWS >= S) break;                          // the same for every lane of the warp
+      float amax = 0.0f;
 #pragma unroll
-    for (int it = 0; it < IT; ++it) {
-      const int row = rb * ROWS + 2 * it + half;
-      if (row >= S) continue;
-      const size_t off = (((size_t)b * S + row) * H + h) * kHeadDim + cg * 8;
-      float* vrow = val[kTwoPass ? 0 : it];
-      if constexpr (kTwoPass) load_row(it, vrow);  // the second pass reads the rows again (from L2)
-      float q[8];
+      for (int it = 0; it < IT; ++it) {
+        if (rb * ROWS + 2 * it + half >= S) continue;
+        float f[8];
+        values(raw[n][it], f);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) q[e] = quotient(vrow[e], scale, fast, rcp);
-      if constexpr (OUT == CODE_E4M3) {
-        uint2 w;
-        w.x = e4m3x2(q[0], q[1]) | (e4m3x2(q[2], q[3]) << 16);
-        w.y = e4m3x2(q[4], q[5]) | (e4m3x2(q[6], q[7]) << 16);
-        *reinterpret_cast<uint2*>(static_cast<uint8_t*>(codes) + off) = w;
-      } else if constexpr (OUT == CODE_I8) {
-        uint2 w;
-        w.x = (uint32_t)(int8_code(q[0]) & 0xFF) | ((uint32_t)(int8_code(q[1]) & 0xFF) << 8) |
-              ((uint32_t)(int8_code(q[2]) & 0xFF) << 16) | ((uint32_t)(int8_code(q[3]) & 0xFF) << 24);
-        w.y = (uint32_t)(int8_code(q[4]) & 0xFF) | ((uint32_t)(int8_code(q[5]) & 0xFF) << 8) |
-              ((uint32_t)(int8_code(q[6]) & 0xFF) << 16) | ((uint32_t)(int8_code(q[7]) & 0xFF) << 24);
-        *reinterpret_cast<uint2*>(static_cast<uint8_t*>(codes) + off) = w;
-      } else {  // CODE_I8_AS_F16: the same integer codes, held exactly in fp16
-        uint32_t w[4];
+        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
+      }
+      // block absmax: over 16 lanes (QB == 1, one row per half-warp) or the whole warp
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const __half lo = __int2half_rn(int8_code(q[2 * e]));
-          const __half hi = __int2half_rn(int8_code(q[2 * e + 1]));
-          w[e] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+      for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      if constexpr (QB > 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
+      const float scale = __fdiv_rn(amax, QMAX);
+      const bool fast = scale_in_fast_range(scale);
+      const float rcp = fast ? __frcp_rn(scale) : 0.0f;
+#pragma unroll
+      for (int it = 0; it < IT; ++it) {
+        const int row = rb * ROWS + 2 * it + half;
+        if (row >= S) continue;
+        const size_t off = row_offset(row);
+        float q[8];
+        values(raw[n][it], q);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) q[e] = quotient(q[e], scale, fast, rcp);
+        if constexpr (OUT == CODE_E4M3) {
+          uint2 w;
+          w.x = e4m3x2(q[0], q[1]) | (e4m3x2(q[2], q[3]) << 16);
+          w.y = e4m3x2(q[4], q[5]) | (e4m3x2(q[6], q[7]) << 16);
+          *reinterpret_cast<uint2*>(static_cast<uint8_t*>(codes) + off) = w;
+        } else if constexpr (OUT == CODE_I8) {
+          const uint2 w = make_uint2(int8_codes4(q[0], q[1], q[2], q[3]), int8_codes4(q[4], q[5], q[6], q[7]));
+          *reinterpret_cast<uint2*>(static_cast<uint8_t*>(codes) + off) = w;
+        } else {  // CODE_I8_AS_F16: the same integer codes, held exactly in fp16
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) w[e] = int8_code_f16x2(q[2 * e], q[2 * e + 1]);
+          *reinterpret_cast<uint4*>(static_cast<__half*>(codes) + off) = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        *reinterpret_cast<uint4*>(static_cast<__half*>(codes) + off) = make_uint4(w[0], w[1], w[2], w[3]);
       }
-    }
-    // scales: one per block; for QB == 1 lane 0 and lane 16 each own a row (= a block)
-    if (QB == 1) {
-      const int row = rb * 2 + half;
-      if (cg == 0 && row < S) scales[((size_t)b * H + h) * nblk + row] = scale;
-    } else if (lane == 0) {
-      scales[((size_t)b * H + h) * nblk + rb] = scale;
+      // scales: one per block; for QB == 1 lane 0 and lane 16 each own a row (= a block)
+      if (QB == 1) {
+        const int row = rb * 2 + half;
+        if (cg == 0 && row < S) scales[((size_t)b * H + h) * nblk + row] = scale;
+      } else if (lane == 0) {
+        scales[((size_t)b * H + h) * nblk + rb] = scale;
+      }
     }
   }
 }

@@ -77,6 +77,43 @@ def test_prepass_is_deterministic():
         assert torch.equal(a[name], b[name]), name
 
 
+def _wide_range_k(Skv, seed=21):
+    """K (float32 values of bf16) whose channels leave the statistics pass's float32 exponent
+    windows [2^-32, 2^18): huge values among normal ones, tiny ones, bf16 subnormals, and values on
+    both sides of each window edge. Each channel's values span few enough bits that its float64
+    sum is exact."""
+    rng = np.random.default_rng(seed)
+    k = rng.standard_normal((1, Skv, 2, 128)).astype(np.float32)
+    n = len(k[0, ::97, 0, 0])
+    k[0, ::97, 0, 0] = rng.choice([-1.0, 1.0], n) * 2.0 ** rng.uniform(18, 24, n)  # above the top window
+    k[0, :, 0, 1] *= np.float32(2.0 ** -40)                                          # below the bottom one
+    k[0, :, 1, 2] = rng.integers(-127, 128, Skv) * np.float32(2.0 ** -133)           # subnormal
+    k[0, :, 1, 3] = rng.choice([2.0 ** -32, -(2.0 ** -33), 1.5 * 2.0 ** -31], Skv)  # the bottom edge
+    k[0, :, 1, 4] = rng.choice([2.0 ** 18, -(2.0 ** 18 - 2.0 ** 10), 2.0 ** 17], Skv)  # the top edge
+    k[0, Skv // 2:, 1, 5] = 0.0
+    return torch.from_numpy(k).bfloat16()
+
+
+@pytest.mark.parametrize("dtype", ["int8", "fp8_e4m3"])
+@pytest.mark.parametrize("Skv", [2053, 3000])
+def test_prepass_k_outside_the_exponent_windows(dtype, Skv):
+    rng = np.random.default_rng(22)
+    k = _wide_range_k(Skv)
+    q = torch.from_numpy(rng.standard_normal((1, 200, 2, 128)).astype(np.float32)).bfloat16()
+    v = torch.from_numpy(rng.standard_normal((1, Skv, 2, 128)).astype(np.float32)).bfloat16()
+    inp = dict(q=_np(q), k=_np(k), v=_np(v))
+    want = sage_quant.sage_quantize(inp["q"], inp["k"], inp["v"], dtype, 1, 16)
+    for h, c in [(0, 0), (0, 1), (1, 2), (1, 3), (1, 4), (1, 5)]:  # the premise: one correct mean
+        assert np.float32(math.fsum(inp["k"][0, :, h, c].astype(np.float64)) / Skv) == want["k_mean"][0, h, c]
+    got = dit.sage_quantize_qkv(*_gpu(q, k, v), qk_dtype=dtype, q_block=1, k_block=16)
+    torch.cuda.synchronize()
+    for name in ["k_mean", "v_scale", "q_scale", "k_scale"]:
+        assert np.array_equal(got[name].cpu().numpy().view(np.uint32), want[name].view(np.uint32)), name
+    for name in ["q_codes", "k_codes", "v_codes"]:
+        bad = np.count_nonzero(got[name].cpu().numpy().view(np.uint8) != want[name].view(np.uint8))
+        assert bad == 0, f"{name}: {bad} codes differ"
+
+
 # ---------------------------------------------------------------- dense BF16
 @pytest.mark.parametrize("shape", [
     (1, 2, 2, 256, 256),        # the tiny workload: one CTA per head
