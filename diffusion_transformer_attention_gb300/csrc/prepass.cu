@@ -22,6 +22,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstring>
 
 #include "ditattn_internal.h"
 #include "quant_math.cuh"
@@ -104,6 +105,12 @@ __device__ __forceinline__ uint2 ld_stream_v2(const void* p) {
   return r;
 }
 
+__device__ __forceinline__ __nv_bfloat162 u32_as_bf162(uint32_t u) {
+  __nv_bfloat162 r;
+  memcpy(&r, &u, sizeof(r));
+  return r;
+}
+
 __device__ __forceinline__ void bf16x4_to_f32(const uint2& u, float* f) {
   f[0] = __uint_as_float(u.x << 16);
   f[1] = __uint_as_float(u.x & 0xFFFF0000u);
@@ -128,14 +135,12 @@ __global__ void __launch_bounds__(256) kv_stats_partial_kernel(const __nv_bfloat
   __shared__ float smax[kWarps][kHeadDim];
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  float m[4];
+  __nv_bfloat162 m2[2] = {u32_as_bf162(0u), u32_as_bf162(0u)};  // channel pairs (4l, 4l+1), (4l+2, 4l+3)
   float acc[4][kBins];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    m[e] = 0.0f;
+  for (int e = 0; e < 4; ++e)
 #pragma unroll
     for (int i = 0; i < kBins; ++i) acc[e][i] = 0.0f;
-  }
   bool wide = false;  // a nonzero K value outside the windows
   const int j0 = chunk * kStatsChunk + w;
   const int jn = min(Skv, chunk * kStatsChunk + kStatsChunk);
@@ -154,26 +159,25 @@ __global__ void __launch_bounds__(256) kv_stats_partial_kernel(const __nv_bfloat
     }
 #pragma unroll
     for (int u = 0; u < kStatsBatch; ++u) {
-      float kf[4], vf[4];
-      bf16x4_to_f32(kr[u], kf);
-      bf16x4_to_f32(vr[u], vf);
+      if constexpr (WITH_K) {
+        float kf[4];
+        bf16x4_to_f32(kr[u], kf);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if constexpr (WITH_K) {
+        for (int e = 0; e < 4; ++e) {
           const float x = kf[e];
-          const unsigned d = bin_offset(x);
-          if (d < (unsigned)(kBins * kBinWidth)) {
-            const unsigned bin = (d * 205u) >> 11;  // d / 10 for d < 50
+          // window index d / 10 for d < 50, kBins (no accumulator) outside the windows
+          const unsigned bin = (min(bin_offset(x), (unsigned)(kBins * kBinWidth)) * 205u) >> 11;
 #pragma unroll
-            for (int i = 0; i < kBins; ++i) acc[e][i] += (bin == (unsigned)i) ? x : 0.0f;
-          } else {
-            wide |= x != 0.0f;
-          }
+          for (int i = 0; i < kBins; ++i) acc[e][i] += (bin == (unsigned)i) ? x : 0.0f;
+          wide |= (bin == (unsigned)kBins) && x != 0.0f;
         }
-        m[e] = fmaxf(m[e], fabsf(vf[e]));
       }
+      // max |V| on bf16 pairs (exact: a max only selects)
+      m2[0] = __hmax2(m2[0], __habs2(u32_as_bf162(vr[u].x)));
+      m2[1] = __hmax2(m2[1], __habs2(u32_as_bf162(vr[u].y)));
     }
   }
+  const float m[4] = {__low2float(m2[0]), __high2float(m2[0]), __low2float(m2[1]), __high2float(m2[1])};
   double s[4] = {0.0, 0.0, 0.0, 0.0};
   if (WITH_K && __syncthreads_or(wide)) {  // rare: add the out-of-window values in float64, in token order
     for (int i = 0; i < kTokens && j0 + kWarps * i < jn; ++i) {
@@ -296,9 +300,9 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const __nv_bfloat16* __res
 // A CTA covers kQuantRows consecutive tokens of one (batch, head), in warp units of ROWS =
 // max(QB, 2) tokens: two rows per iteration, 16 lanes per row (16-byte loads). For QB == 1 each
 // half-warp is its own block; otherwise the whole unit is one block. SMOOTH subtracts the K mean.
-// A warp takes NU of its units at a time and loads all their rows (8 per lane, held as raw bf16)
-// before it reduces any block, so that enough loads are in flight; the codes are then computed from
-// the held rows.
+// A warp takes NU of its units at a time (two units of one or two rows per lane, or one unit of
+// eight) and loads all their rows, held as raw bf16, before it reduces any block; the codes are
+// then computed from the held rows, so a 16-row block is read once.
 template <int QB, int OUT, bool SMOOTH>
 __global__ void __launch_bounds__(256) quant_tokens_kernel(const __nv_bfloat16* __restrict__ x, int S, int H,
                                                            const float* __restrict__ mean, void* __restrict__ codes,
@@ -307,7 +311,7 @@ __global__ void __launch_bounds__(256) quant_tokens_kernel(const __nv_bfloat16* 
   constexpr int IT = ROWS / 2;               // rows per lane in a unit
   constexpr int UNITS = kQuantRows / ROWS;  // warp units per CTA
   constexpr int PER_WARP = UNITS / 8;
-  constexpr int NU = IT >= 8 ? 1 : 8 / IT;  // units loaded together
+  constexpr int NU = IT >= 8 ? 1 : 2;      // units loaded together
   constexpr float QMAX = (OUT == CODE_E4M3) ? 448.0f : 127.0f;
   static_assert(kQuantRows % 16 == 0 && PER_WARP % NU == 0, "whole blocks per CTA, whole batches per warp");
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
