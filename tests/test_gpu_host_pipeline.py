@@ -28,7 +28,7 @@ def _run(w, chunks, mode=dit.MODE_DENSE, factor=0.0, same_stream=False, seed=90)
 
 
 @pytest.mark.parametrize("shape", [(1, 4, 2, 300, 520), (2, 8, 8, 256, 256), (1, 6, 3, 130, 1000)])
-@pytest.mark.parametrize("chunks", [1, 2, 3])
+@pytest.mark.parametrize("chunks", [1, 2, 3, 4, 6, 8])
 def test_pipelined_host_call_equals_device_call(shape, chunks):
     B, Hq, Hkv, Sq, Skv = shape
     if chunks > Hkv:
