@@ -11,6 +11,7 @@ from oracle import formats, sage_quant
 from . import test_oracle_attention as TA
 from . import test_oracle_formats as TF
 from . import test_oracle_quant as TQ
+from . import test_oracle_sage_lossless as TL
 
 
 def _fails(fn, *args):
@@ -213,3 +214,21 @@ def test_per_head_tensor_scale_is_caught(monkeypatch):
 def test_missing_tensor_scale_is_caught(monkeypatch):
     monkeypatch.setattr(nvfp4_quant, "tensor_scale", lambda x: np.float32(1.0))
     _fails(TN.test_hand_derived_blocks)
+
+
+def test_sage_dropped_k_scale_is_caught(monkeypatch):
+    good = att.sage_scores
+    monkeypatch.setattr(att, "sage_scores", lambda qc, kc, qs, ks, dt: good(qc, kc, qs, np.ones_like(ks), dt))
+    _fails(TL.test_sage_equals_qk16pv8_when_quantization_is_lossless, "int8", 1, 16)
+
+
+def test_sage_k_scale_of_the_next_block_is_caught(monkeypatch):
+    good = att.sage_scores
+    monkeypatch.setattr(att, "sage_scores", lambda qc, kc, qs, ks, dt: good(qc, kc, qs, np.roll(ks, -16), dt))
+    _fails(TL.test_sage_equals_qk16pv8_when_quantization_is_lossless, "fp8_e4m3", 1, 16)
+
+
+def test_sage_q_scale_of_the_previous_row_is_caught(monkeypatch):
+    good = att.sage_scores
+    monkeypatch.setattr(att, "sage_scores", lambda qc, kc, qs, ks, dt: good(qc, kc, np.roll(qs, 1), ks, dt))
+    _fails(TL.test_sage_equals_qk16pv8_when_quantization_is_lossless, "int8", 4, 4)
