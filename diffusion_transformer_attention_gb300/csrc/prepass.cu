@@ -14,9 +14,10 @@
 //     zero codes. The quotients x / scale are computed from the scale's correctly rounded
 //     reciprocal with one remainder correction (quant_math.cuh), which gives the same codes.
 //
-// Access pattern: a row of one head is 128 bf16 = 256 contiguous bytes; 16 lanes read it with
-// 16-byte vector loads, so a warp covers two rows per instruction. Results are written with
-// 8-byte (codes) or 16-byte (widened codes) stores at the same positions.
+// Access pattern: a row of one head is 128 bf16 = 256 contiguous bytes. The quantizers read it with
+// 16 lanes and 16-byte vector loads (a warp covers two rows per instruction) and write codes with
+// 8-byte (or, widened, 16-byte) stores at the same positions; the statistics pass reads it with a
+// whole warp and 8-byte loads. Each thread issues several rows' loads before it uses any of them.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -255,7 +256,8 @@ __global__ void __launch_bounds__(1024) v_scale_tensor_kernel(float* __restrict_
 
 // E4M3 codes of V / v_scale[b, h, c] (V alone, for QK16PV8): the same arithmetic as the V part of
 // the token-block quantizer. A CTA covers kQuantRows tokens of one (batch, kv head); thread t
-// keeps channels 8*(t%16).. (and their scales' reciprocals) over tokens t/16 + 16i.
+// keeps channels 8*(t%16).. (and their scales' reciprocals) over tokens t/16 + 16i, loading eight rows
+// before it converts any.
 __global__ void __launch_bounds__(256) quant_v_kernel(const __nv_bfloat16* __restrict__ v, int Hkv, int Skv,
                                                       const float* __restrict__ v_scale,
                                                       uint8_t* __restrict__ v_codes) {
