@@ -1,6 +1,8 @@
 """GPU: dit_attn_fwd_host (inputs and output in pinned host memory, copies overlapped with the
 kernels over groups of kv heads) writes exactly dit_attn_fwd's output, bit for bit, for any number
-of groups, with the three streams distinct or the same, and with Skip-Softmax."""
+of groups (equal ones, and the ramp of 1, 2, 4, ..., 1 kv heads), with the three streams distinct or the
+same, with page-locked or pageable host buffers (the first and last transfers by a copy kernel or by
+the copy engines), and with Skip-Softmax."""
 
 import pytest
 import torch
@@ -11,10 +13,13 @@ import workloads
 pytestmark = pytest.mark.gpu
 
 
-def _run(w, chunks, mode=dit.MODE_DENSE, factor=0.0, same_stream=False, seed=90):
+def _run(w, chunks, mode=dit.MODE_DENSE, factor=0.0, same_stream=False, seed=90, pinned=(True, True)):
+    """pinned: (inputs, output) in page-locked memory; pageable buffers take the copy engines only."""
     q, k, v = workloads.generate(w, seed=seed)
-    hq, hk, hv = (t.pin_memory() for t in (q, k, v))
-    hout = torch.full(q.shape, float("nan"), dtype=q.dtype).pin_memory()
+    hq, hk, hv = (t.pin_memory() if pinned[0] else t.clone() for t in (q, k, v))
+    hout = torch.full(q.shape, float("nan"), dtype=q.dtype)
+    if pinned[1]:
+        hout = hout.pin_memory()
     dq, dk, dv = (torch.empty_like(t, device="cuda") for t in (q, k, v))
     dout = torch.empty_like(dq)
     s = torch.cuda.current_stream()
@@ -27,8 +32,9 @@ def _run(w, chunks, mode=dit.MODE_DENSE, factor=0.0, same_stream=False, seed=90)
     return hout, want
 
 
-@pytest.mark.parametrize("shape", [(1, 4, 2, 300, 520), (2, 8, 8, 256, 256), (1, 6, 3, 130, 1000)])
-@pytest.mark.parametrize("chunks", [1, 2, 3, 4, 6, 8])
+@pytest.mark.parametrize("shape", [(1, 4, 2, 300, 520), (2, 8, 8, 256, 256), (1, 6, 3, 130, 1000),
+                                   (1, 24, 12, 200, 300)])  # 12 kv heads: 5 and 8 groups ramp as 1, 2, 4, ..., 1
+@pytest.mark.parametrize("chunks", [1, 2, 3, 4, 5, 6, 8])
 def test_pipelined_host_call_equals_device_call(shape, chunks):
     B, Hq, Hkv, Sq, Skv = shape
     if chunks > Hkv:
@@ -45,4 +51,12 @@ def test_one_stream_for_everything():
 def test_skip_softmax_through_the_host_call():
     w = workloads.Workload("v", 1, 2, 2, 3 * 16 * 24, 3 * 16 * 24, kind="video", grid=(3, 16, 24))
     got, want = _run(w, 2, mode=dit.MODE_SKIP, factor=50.0)
+    assert torch.equal(got, want)
+
+
+@pytest.mark.parametrize("pinned", [(False, False), (True, False), (False, True)])
+def test_pageable_buffers_take_the_copy_engines(pinned):
+    # the first group's inputs and the last group's output go through a copy kernel only when the host
+    # buffer is page-locked; pageable ones (either side) must give the same result through cudaMemcpy2D
+    got, want = _run(workloads.Workload("h", 1, 24, 12, 200, 300, kind="koffset"), 5, pinned=pinned)
     assert torch.equal(got, want)
