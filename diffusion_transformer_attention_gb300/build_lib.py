@@ -20,7 +20,8 @@ CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libditattn.so")
 SOURCES = ["api.cu", "prepass.cu", "fmha_sm103.cu", "fmha_dense.cu", "fmha_sage_i8.cu", "fmha_sage_f8.cu",
-           "fmha_qk16pv8.cu", "fmha_mxfp8.cu", "fmha_nvfp4.cu", "noalloc.cu"]
+           "fmha_qk16pv8.cu", "fmha_mxfp8.cu", "fmha_nvfp4.cu", "noalloc.cu",
+           "host_copy.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

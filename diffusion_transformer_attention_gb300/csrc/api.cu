@@ -260,6 +260,50 @@ dit_status run_attention(const void* q, const void* k, const void* v, void* out,
   return from_cuda(launch_fmha(qk_format, pv_format, skip, tq, tk, tv, to, p, stream));
 }
 
+// Group boundaries for dit_attn_fwd_host: group c holds kv heads [bounds[c], bounds[c + 1]). Only the
+// first group's input copies and the last group's output copy have no kernel to hide behind, so with
+// five or more groups and enough kv heads the groups ramp up as 1, 2 and 4 kv heads (each group's
+// inputs arrive while the one before computes: the host link moves a head's Q, K and V several times
+// faster than the kernel consumes it), the middle groups split the rest evenly and the last group holds
+// one kv head. Otherwise the groups are (nearly) equal.
+void host_chunk_bounds(int Hkv, int chunks, int* bounds) {
+  if (chunks >= 5 && Hkv - 8 >= chunks - 4) {
+    const int mid = chunks - 4, rest = Hkv - 8;  // groups 3 .. chunks - 2 share heads [7, Hkv - 1)
+    bounds[0] = 0;
+    bounds[1] = 1;
+    bounds[2] = 3;
+    for (int c = 0; c <= mid; ++c) bounds[3 + c] = 7 + (int)((long long)rest * c / mid);
+    bounds[chunks] = Hkv;
+  } else {
+    for (int c = 0; c <= chunks; ++c) bounds[c] = (int)((long long)Hkv * c / chunks);
+  }
+}
+
+// The device address of the host range [p, p + bytes) when all of it is page-locked host memory mapped
+// for the current device (both ends are, with device addresses bytes - 1 apart) and 16-byte aligned;
+// nullptr otherwise (pageable memory, another device's mapping), in which case the caller keeps the
+// copy engines.
+void* pinned_device_view(const void* p, size_t bytes) {
+  if (p == nullptr || bytes == 0 || !aligned16(p)) return nullptr;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  cudaPointerAttributes a{}, z{};
+  const void* last = static_cast<const uint8_t*>(p) + (bytes - 1);
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess || cudaPointerGetAttributes(&z, last) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (a.type != cudaMemoryTypeHost || z.type != cudaMemoryTypeHost || a.device != dev || z.device != dev ||
+      a.devicePointer == nullptr || z.devicePointer == nullptr)
+    return nullptr;
+  const uintptr_t d0 = reinterpret_cast<uintptr_t>(a.devicePointer), d1 = reinterpret_cast<uintptr_t>(z.devicePointer);
+  if (d1 < d0 || d1 - d0 != bytes - 1 || (d0 & 15u) != 0) return nullptr;
+  return a.devicePointer;
+}
+
 }  // namespace
 
 extern "C" {
@@ -673,19 +717,40 @@ dit_status dit_attn_fwd_host(const void* q_host, const void* k_host, const void*
   if (e == cudaSuccess) e = cudaStreamWaitEvent(hs, ev->start, 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(ds2, ev->start, 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(ev->aux, ev->start, 0);
-  // chunk c covers kv heads [Hkv*c/chunks, Hkv*(c+1)/chunks) and their query heads
-  auto kv0 = [&](int c) { return (int)((long long)Hkv * c / chunks); };
+  // chunk c covers kv heads [bounds[c], bounds[c + 1]) and their query heads
+  int bounds[kMaxHostChunks + 1];
+  host_chunk_bounds(Hkv, chunks, bounds);
+  auto kv0 = [&](int c) { return bounds[c]; };
+  // The first group's inputs and the last group's output are copied by SM kernels when the host
+  // buffers are page-locked (no attention kernel runs at those times); everything else by the copy
+  // engines, overlapped with the attention.
+  const size_t q_bytes = (size_t)B * Sq * Hq * row, kv_bytes = (size_t)B * Skv * Hkv * row;
+  const void* qh_dev = pinned_device_view(q_host, q_bytes);
+  const void* kh_dev = pinned_device_view(k_host, kv_bytes);
+  const void* vh_dev = pinned_device_view(v_host, kv_bytes);
+  void* oh_dev = pinned_device_view(out_host, q_bytes);
   for (int c = 0; c < chunks && e == cudaSuccess; ++c) {
     const int hk0 = kv0(c), hkc = kv0(c + 1) - hk0, hq0 = hk0 * group, hqc = hkc * group;
     const size_t qo = hq0 * row, ko = hk0 * row;
-    e = cudaMemcpy2DAsync(static_cast<uint8_t*>(q) + qo, Hq * row, static_cast<const uint8_t*>(q_host) + qo, Hq * row,
-                          hqc * row, (size_t)B * Sq, cudaMemcpyHostToDevice, hs);
-    if (e == cudaSuccess)
-      e = cudaMemcpy2DAsync(static_cast<uint8_t*>(k) + ko, Hkv * row, static_cast<const uint8_t*>(k_host) + ko,
-                            Hkv * row, hkc * row, (size_t)B * Skv, cudaMemcpyHostToDevice, hs);
-    if (e == cudaSuccess)
-      e = cudaMemcpy2DAsync(static_cast<uint8_t*>(v) + ko, Hkv * row, static_cast<const uint8_t*>(v_host) + ko,
-                            Hkv * row, hkc * row, (size_t)B * Skv, cudaMemcpyHostToDevice, hs);
+    if (c == 0 && qh_dev != nullptr && kh_dev != nullptr && vh_dev != nullptr) {
+      e = launch_copy_rows(static_cast<const uint8_t*>(qh_dev) + qo, Hq * row, static_cast<uint8_t*>(q) + qo, Hq * row,
+                           hqc * row, (size_t)B * Sq, hs);
+      if (e == cudaSuccess)
+        e = launch_copy_rows(static_cast<const uint8_t*>(kh_dev) + ko, Hkv * row, static_cast<uint8_t*>(k) + ko,
+                             Hkv * row, hkc * row, (size_t)B * Skv, hs);
+      if (e == cudaSuccess)
+        e = launch_copy_rows(static_cast<const uint8_t*>(vh_dev) + ko, Hkv * row, static_cast<uint8_t*>(v) + ko,
+                             Hkv * row, hkc * row, (size_t)B * Skv, hs);
+    } else {
+      e = cudaMemcpy2DAsync(static_cast<uint8_t*>(q) + qo, Hq * row, static_cast<const uint8_t*>(q_host) + qo,
+                            Hq * row, hqc * row, (size_t)B * Sq, cudaMemcpyHostToDevice, hs);
+      if (e == cudaSuccess)
+        e = cudaMemcpy2DAsync(static_cast<uint8_t*>(k) + ko, Hkv * row, static_cast<const uint8_t*>(k_host) + ko,
+                              Hkv * row, hkc * row, (size_t)B * Skv, cudaMemcpyHostToDevice, hs);
+      if (e == cudaSuccess)
+        e = cudaMemcpy2DAsync(static_cast<uint8_t*>(v) + ko, Hkv * row, static_cast<const uint8_t*>(v_host) + ko,
+                              Hkv * row, hkc * row, (size_t)B * Skv, cudaMemcpyHostToDevice, hs);
+    }
     if (e == cudaSuccess) e = cudaEventRecord(ev->in[c], hs);
   }
   for (int c = 0; c < chunks && e == cudaSuccess; ++c) {
@@ -705,9 +770,15 @@ dit_status dit_attn_fwd_host(const void* q_host, const void* k_host, const void*
     const int hk0 = kv0(c), hkc = kv0(c + 1) - hk0, hq0 = hk0 * group, hqc = hkc * group;
     const size_t qo = hq0 * row;
     e = cudaStreamWaitEvent(ds2, ev->comp[c], 0);
-    if (e == cudaSuccess)
+    if (e != cudaSuccess) break;
+    if (c == chunks - 1 && oh_dev != nullptr) {
+      // d2h_stream has waited for every group's kernel by now, so no attention kernel is running
+      e = launch_copy_rows(static_cast<const uint8_t*>(out) + qo, Hq * row, static_cast<uint8_t*>(oh_dev) + qo, Hq * row,
+                           hqc * row, (size_t)B * Sq, ds2);
+    } else {
       e = cudaMemcpy2DAsync(static_cast<uint8_t*>(out_host) + qo, Hq * row, static_cast<const uint8_t*>(out) + qo,
                             Hq * row, hqc * row, (size_t)B * Sq, cudaMemcpyDeviceToHost, ds2);
+    }
   }
   // completion (the last output byte on the host, and all kernels) is signalled on the compute stream
   if (e == cudaSuccess) e = cudaEventRecord(ev->done, ds2);

@@ -93,6 +93,10 @@ cudaError_t launch_nvfp4_quant(const void* q, const void* k, int B, int Hq, int 
                                cudaStream_t stream);
 cudaError_t launch_widen_i8(const int8_t* codes, size_t n, void* out_f16, cudaStream_t stream);
 cudaError_t launch_zero_i32(int32_t* p, size_t n, cudaStream_t stream);
+// SM-driven copy of `rows` rows of `width` bytes (src/dst pitches in bytes; addresses, pitches and
+// width multiples of 16); either side may be the device mapping of page-locked host memory.
+cudaError_t launch_copy_rows(const void* src, size_t src_pitch, void* dst, size_t dst_pitch, size_t width,
+                             size_t rows, cudaStream_t stream);
 
 inline int stats_chunks(int Skv) { return (Skv + kStatsChunk - 1) / kStatsChunk; }
 

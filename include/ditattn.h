@@ -149,10 +149,15 @@ dit_status dit_attn_fwd_lse(const void* q, const void* k, const void* v, void* o
  * with the attention. The pages have no counterpart; this serves callers whose Q, K, V live on the
  * host (for example a step that offloads activations), so that the copies hide behind the kernels.
  *
- * The kv heads are split into `chunks` groups of (nearly) equal size, each with its query heads. Every
- * group's Q, K and V head slices are copied in on h2d_stream, its attention runs on compute_stream once
- * they have arrived, and its output slice is copied back on d2h_stream once it is done: group g+1's
- * inputs and group g-1's output move while group g computes. The result equals dit_attn_fwd's bit for bit.
+ * The kv heads are split into `chunks` groups, each with its query heads. Every group's Q, K and V head
+ * slices are copied in on h2d_stream, its attention runs on compute_stream once they have arrived, and
+ * its output slice is copied back on d2h_stream once it is done: group g+1's inputs and group g-1's
+ * output move while group g computes. Only the first group's inputs and the last group's output are
+ * not hidden, so with chunks >= 5 and Hkv - 8 >= chunks - 4 the groups hold 1, 2 and 4 kv heads, then
+ * equal shares of the rest, and 1 kv head last; otherwise they are (nearly) equal. Those two transfers
+ * are made by a copy kernel when the host buffer is page-locked memory mapped for the device (its SM
+ * loads and stores reach the host link's rate for narrow head slices, the copy engines do not), and
+ * by the copy engines otherwise. The result equals dit_attn_fwd's bit for bit.
  *
  *   q_host, k_host, v_host, out_host   host buffers with the layouts of dit_attn_fwd (pinned memory
  *              for the copies to be asynchronous); out_host is written completely

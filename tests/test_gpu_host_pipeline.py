@@ -1,7 +1,8 @@
 """GPU: dit_attn_fwd_host (inputs and output in pinned host memory, copies overlapped with the
 kernels over groups of kv heads) writes exactly dit_attn_fwd's output, bit for bit, for any number
-of groups, with the three streams distinct or the same, with page-locked or pageable host buffers, and
-with Skip-Softmax."""
+of groups (equal ones, and the ramp of 1, 2, 4, ..., 1 kv heads), with the three streams distinct or the
+same, with page-locked or pageable host buffers (the first and last transfers by a copy kernel or by
+the copy engines), and with Skip-Softmax."""
 
 import pytest
 import torch
@@ -32,7 +33,7 @@ def _run(w, chunks, mode=dit.MODE_DENSE, factor=0.0, same_stream=False, seed=90,
 
 
 @pytest.mark.parametrize("shape", [(1, 4, 2, 300, 520), (2, 8, 8, 256, 256), (1, 6, 3, 130, 1000),
-                                   (1, 24, 12, 200, 300)])
+                                   (1, 24, 12, 200, 300)])  # 12 kv heads: 5 and 8 groups ramp as 1, 2, 4, ..., 1
 @pytest.mark.parametrize("chunks", [1, 2, 3, 4, 5, 6, 8])
 def test_pipelined_host_call_equals_device_call(shape, chunks):
     B, Hq, Hkv, Sq, Skv = shape
@@ -54,7 +55,8 @@ def test_skip_softmax_through_the_host_call():
 
 
 @pytest.mark.parametrize("pinned", [(False, False), (True, False), (False, True)])
-def test_pageable_host_buffers(pinned):
-    # pageable inputs or output (the copies are then synchronous for the host) give the same result
+def test_pageable_buffers_take_the_copy_engines(pinned):
+    # the first group's inputs and the last group's output go through a copy kernel only when the host
+    # buffer is page-locked; pageable ones (either side) must give the same result through cudaMemcpy2D
     got, want = _run(workloads.Workload("h", 1, 24, 12, 200, 300, kind="koffset"), 5, pinned=pinned)
     assert torch.equal(got, want)
