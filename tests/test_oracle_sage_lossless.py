@@ -11,7 +11,8 @@ zero tail block), so every channel mean is exactly 0 and smoothing subtracts not
 dequantized logits are then the exact logits, and SAGE's output, LSE and V codes must equal
 QK16PV8's (per-channel V) to float64 rounding. A dropped dequantization scale, a block index off by
 one or a neighbouring row's scale breaks the equality (tests/test_oracle_mutations.py
-plants those). Smoothing itself is pinned by the K-mean and smoothing-invariance tests.
+plants those). Smoothing itself is pinned by the K-mean and smoothing-invariance tests. With
+Skip-Softmax the skipped tiles must match too (the decisions use the same exact logits).
 """
 
 import numpy as np
@@ -46,6 +47,11 @@ def _on_grid(rng, dtype, B, S, H, block):
 @pytest.mark.parametrize("dtype,qb,kb", [("int8", 1, 16), ("int8", 4, 4), ("int8", 16, 1), ("fp8_e4m3", 1, 16),
                                          ("fp8_e4m3", 4, 1), ("fp8_e4m3", 16, 4)])
 def test_sage_equals_qk16pv8_when_quantization_is_lossless(dtype, qb, kb):
+    _compare(dtype, qb, kb, None)
+
+
+def _compare(dtype, qb, kb, factor):
+    """Asserts SAGE == QK16PV8 on lossless inputs; returns the number of skipped tiles."""
     rng = np.random.default_rng(40 + qb * 3 + kb)
     B, Hq, Hkv, Sq, half, tail = 2, 4, 2, 200, 144, 5  # GQA, a ragged Q tile, a zero K tail block
     q = _on_grid(rng, dtype, B, Sq, Hq, qb)
@@ -61,11 +67,25 @@ def test_sage_equals_qk16pv8_when_quantization_is_lossless(dtype, qb, kb):
     assert np.array_equal(formats.code_values(sq["q_codes"], dtype) *
                           np.repeat(sq["q_scale"].transpose(0, 2, 1), qb, axis=1)[:, :Sq, :, None], q)
     assert np.array_equal(sq["v_codes"], ref["v_codes"]) and np.array_equal(sq["v_scale"], ref["v_scale"])
+    skipped = 0
     for b in range(B):
         for h in range(Hq):
             for t in range(2):
-                o1, _, rows, l1 = att.attention_q_tile(inp, b, h, t, mode="sage", qk_dtype=dtype, q_block=qb,
-                                                       k_block=kb, quant=sq, with_lse=True)
-                o2, _, _, l2 = att.attention_q_tile(inp, b, h, t, mode="qk16pv8", quant=ref, with_lse=True)
+                o1, n1, rows, l1 = att.attention_q_tile(inp, b, h, t, mode="sage", qk_dtype=dtype, q_block=qb,
+                                                        k_block=kb, quant=sq, with_lse=True, factor=factor)
+                o2, n2, _, l2 = att.attention_q_tile(inp, b, h, t, mode="qk16pv8", quant=ref, with_lse=True,
+                                                     factor=factor)
+                assert n1 == n2
                 assert np.max(np.abs(o1 - o2)) <= 1e-12 * max(1.0, np.max(np.abs(o2)))
                 assert np.max(np.abs(l1 - l2)) <= 1e-12
+                skipped += n1
+    return skipped
+
+
+@pytest.mark.parametrize("factor", [0.0, 50.0, 3000.0])
+def test_sage_skip_equals_qk16pv8_skip_when_quantization_is_lossless(factor):
+    # Skip-Softmax decides on the scaled logits, which are the same exact values here: the same tiles
+    # must be skipped and the outputs must agree (factor 3000 gives a threshold above 1: many skips)
+    n = _compare("int8", 1, 16, factor) + _compare("fp8_e4m3", 4, 1, factor)
+    if factor == 3000.0:
+        assert n > 0
