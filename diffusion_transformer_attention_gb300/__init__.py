@@ -213,8 +213,31 @@ def sage_quantize_qkv(q, k, v, *, qk_dtype="int8", q_block=1, k_block=16, stream
 def sage_quantize_qkv_noalloc(q, k, v, out: dict, *, qk_dtype="int8", q_block=1, k_block=16, stream=None):
     """``sage_quantize_qkv`` into caller-provided outputs, with the scratch the library keeps in
     its own fixed 32 MiB device array (for callers that cannot allocate at call time). ``out``
-    holds preallocated tensors with the keys and shapes ``sage_quantize_qkv`` returns."""
+    holds preallocated tensors with the keys and shapes ``sage_quantize_qkv`` returns; each is
+    checked (shape, dtype, device, contiguity) before the call, since the kernels write through
+    their raw pointers."""
     B, Hq, Hkv, Sq, Skv = _shape(q, k)
+    if tuple(v.shape) != tuple(k.shape):
+        raise ValueError("v must have k's shape [B, Skv, Hkv, 128]")
+    if q_block not in (1, 4, 16) or k_block not in (1, 4, 16):
+        raise ValueError("q_block and k_block must be 1, 4 or 16")
+    code_t = torch.int8 if _qk(qk_dtype) == QK_INT8 else torch.uint8
+    want = dict(
+        q_codes=(tuple(q.shape), code_t),
+        k_codes=(tuple(k.shape), code_t),
+        v_codes=(tuple(v.shape), torch.uint8),
+        q_scale=((B, Hq, math.ceil(Sq / q_block)), torch.float32),
+        k_scale=((B, Hkv, math.ceil(Skv / k_block)), torch.float32),
+        v_scale=((B, Hkv, HEAD_DIM), torch.float32),
+        k_mean=((B, Hkv, HEAD_DIM), torch.float32),
+    )
+    for name, (shape, dtype) in want.items():
+        t = out.get(name)
+        if t is None:
+            raise ValueError(f"out[{name!r}] is missing")
+        if tuple(t.shape) != shape or t.dtype != dtype or t.device != q.device or not t.is_contiguous():
+            raise ValueError(f"out[{name!r}] must be a contiguous {dtype} tensor of shape {shape} on {q.device}, "
+                             f"got {t.dtype} {tuple(t.shape)} on {t.device}")
     st = _lib().sage_quantize_qkv_noalloc(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Sq, Skv, _qk(qk_dtype), q_block,
                                           k_block, _ptr(out["q_codes"]), _ptr(out["k_codes"]),
                                           _ptr(out["v_codes"]), _ptr(out["q_scale"]), _ptr(out["k_scale"]),

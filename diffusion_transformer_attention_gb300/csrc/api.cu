@@ -9,6 +9,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "../../include/ditattn.h"
 #include "ditattn_internal.h"
@@ -22,43 +23,9 @@ constexpr unsigned long long kWaitBudgetNs = 4000000000ull;  // far beyond any l
 
 __device__ int g_device_error = 0;
 
-bool is_block(int x) { return x == 1 || x == 4 || x == 16; }
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
-
-// Shapes shared by every entry point. Empty problems (B == 0 or Sq == 0) are valid no-ops.
-bool valid_shape(int B, int Hq, int Hkv, int Sq, int Skv) {
-  if (B < 0 || Sq < 0 || Hq < 1 || Hkv < 1 || Skv < 1) return false;
-  if (Hq % Hkv != 0) return false;
-  if (Hq > 65535 || B > 65535) return false;  // grid y / z limits
-  // every element index must fit the 64-bit offsets and TMA's 2^40-byte stride limit
-  const double q_bytes = (double)B * Sq * Hq * kHeadDim * 2.0;
-  const double kv_bytes = (double)B * Skv * Hkv * kHeadDim * 2.0;
-  return q_bytes < 1e12 && kv_bytes < 1e12;
-}
-
-bool valid_mode(int mode, int qk_dtype, int q_block, int k_block, float factor) {
-  if (mode < 0 || mode > (DIT_MODE_SAGE | DIT_MODE_SKIP | DIT_MODE_V_PER_TENSOR)) return false;
-  if (mode & DIT_MODE_SAGE) {
-    if (qk_dtype == DIT_QK_BF16 || qk_dtype == DIT_QK_MXFP8 || qk_dtype == DIT_QK_NVFP4) {
-      // QK16PV8: Q/K stay BF16; MXFP8 / NVFP4: Q/K carry their own blocks of 32 / 16 channels. Either way
-      // the token-block sizes are 0 (the pages' block sizes (0, 0, v)); V per channel or per tensor.
-      if (q_block != 0 || k_block != 0) return false;
-    } else {
-      if (qk_dtype != DIT_QK_INT8 && qk_dtype != DIT_QK_FP8_E4M3) return false;
-      if (!is_block(q_block) || !is_block(k_block)) return false;
-      if (mode & DIT_MODE_V_PER_TENSOR) return false;  // the SAGE recipes scale V per channel
-    }
-  } else {
-    if (qk_dtype != DIT_QK_BF16) return false;       // a quantized dtype without SAGE is contradictory
-    if (mode & DIT_MODE_V_PER_TENSOR) return false;  // V is not quantized without SAGE
-  }
-  if (mode & DIT_MODE_SKIP) {
-    if (!std::isfinite(factor) || factor < 0.0f) return false;
-  }
-  return true;
-}
 
 struct SageLayout {
   size_t q_codes, k_codes, v_codes, q_scale, k_scale, v_scale, k_mean, psum, pmax, gs, total;
@@ -178,10 +145,9 @@ bool encode_map(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int esi
 // stream and `aux`, so each kernel's last partial wave of CTAs overlaps the next one's first.
 constexpr int kMaxHostChunks = 64;
 struct HostEvents {
-  bool ready = false;
   bool ok = false;
   cudaStream_t aux;
-  cudaEvent_t start, done, aux_done, in[kMaxHostChunks], comp[kMaxHostChunks];
+  cudaEvent_t start, done, aux_done, h2d_done, in[kMaxHostChunks], comp[kMaxHostChunks];
 };
 HostEvents g_host_events[64];
 std::mutex g_host_mu;
@@ -194,19 +160,38 @@ HostEvents* host_events() {
   }
   std::lock_guard<std::mutex> lock(g_host_mu);
   HostEvents& h = g_host_events[dev];
-  if (!h.ready) {
-    h.ready = true;
-    bool ok = cudaStreamCreateWithFlags(&h.aux, cudaStreamNonBlocking) == cudaSuccess &&
-              cudaEventCreateWithFlags(&h.start, cudaEventDisableTiming) == cudaSuccess &&
-              cudaEventCreateWithFlags(&h.done, cudaEventDisableTiming) == cudaSuccess &&
-              cudaEventCreateWithFlags(&h.aux_done, cudaEventDisableTiming) == cudaSuccess;
-    for (int i = 0; ok && i < kMaxHostChunks; ++i)
-      ok = cudaEventCreateWithFlags(&h.in[i], cudaEventDisableTiming) == cudaSuccess &&
-           cudaEventCreateWithFlags(&h.comp[i], cudaEventDisableTiming) == cudaSuccess;
-    if (!ok) cudaGetLastError();
-    h.ok = ok;
+  if (h.ok) return &h;
+  // Only a complete set is kept; a failed attempt releases what it created and is retried on the
+  // next call (a transient failure, e.g. out of memory, is not cached).
+  HostEvents n;
+  std::vector<cudaEvent_t> made;
+  bool aux_made = cudaStreamCreateWithFlags(&n.aux, cudaStreamNonBlocking) == cudaSuccess;
+  bool ok = aux_made;
+  auto make = [&](cudaEvent_t* e) {
+    if (ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess) {
+      made.push_back(*e);
+    } else {
+      ok = false;
+    }
+  };
+  make(&n.start);
+  make(&n.done);
+  make(&n.aux_done);
+  make(&n.h2d_done);
+  for (int i = 0; i < kMaxHostChunks; ++i) {
+    make(&n.in[i]);
+    make(&n.comp[i]);
   }
-  return h.ok ? &h : nullptr;
+  if (!ok) {
+    cudaGetLastError();
+    for (cudaEvent_t e : made) cudaEventDestroy(e);
+    if (aux_made) cudaStreamDestroy(n.aux);
+    cudaGetLastError();
+    return nullptr;
+  }
+  n.ok = true;
+  h = n;
+  return &h;
 }
 
 dit_status from_cuda(cudaError_t e) {
@@ -305,6 +290,45 @@ void* pinned_device_view(const void* p, size_t bytes) {
 }
 
 }  // namespace
+
+namespace ditattn {
+
+bool is_block(int x) { return x == 1 || x == 4 || x == 16; }
+
+// Shapes shared by every entry point. Empty problems (B == 0 or Sq == 0) are valid no-ops.
+bool valid_shape(int B, int Hq, int Hkv, int Sq, int Skv) {
+  if (B < 0 || Sq < 0 || Hq < 1 || Hkv < 1 || Skv < 1) return false;
+  if (Hq % Hkv != 0) return false;
+  if (Hq > 65535 || B > 65535) return false;  // grid y / z limits
+  // every element index must fit the 64-bit offsets and TMA's 2^40-byte stride limit
+  const double q_bytes = (double)B * Sq * Hq * kHeadDim * 2.0;
+  const double kv_bytes = (double)B * Skv * Hkv * kHeadDim * 2.0;
+  return q_bytes < 1e12 && kv_bytes < 1e12;
+}
+
+bool valid_mode(int mode, int qk_dtype, int q_block, int k_block, float factor) {
+  if (mode < 0 || mode > (DIT_MODE_SAGE | DIT_MODE_SKIP | DIT_MODE_V_PER_TENSOR)) return false;
+  if (mode & DIT_MODE_SAGE) {
+    if (qk_dtype == DIT_QK_BF16 || qk_dtype == DIT_QK_MXFP8 || qk_dtype == DIT_QK_NVFP4) {
+      // QK16PV8: Q/K stay BF16; MXFP8 / NVFP4: Q/K carry their own blocks of 32 / 16 channels. Either way
+      // the token-block sizes are 0 (the pages' block sizes (0, 0, v)); V per channel or per tensor.
+      if (q_block != 0 || k_block != 0) return false;
+    } else {
+      if (qk_dtype != DIT_QK_INT8 && qk_dtype != DIT_QK_FP8_E4M3) return false;
+      if (!is_block(q_block) || !is_block(k_block)) return false;
+      if (mode & DIT_MODE_V_PER_TENSOR) return false;  // the SAGE recipes scale V per channel
+    }
+  } else {
+    if (qk_dtype != DIT_QK_BF16) return false;       // a quantized dtype without SAGE is contradictory
+    if (mode & DIT_MODE_V_PER_TENSOR) return false;  // V is not quantized without SAGE
+  }
+  if (mode & DIT_MODE_SKIP) {
+    if (!std::isfinite(factor) || factor < 0.0f) return false;
+  }
+  return true;
+}
+
+}  // namespace ditattn
 
 extern "C" {
 
@@ -753,6 +777,7 @@ dit_status dit_attn_fwd_host(const void* q_host, const void* k_host, const void*
     }
     if (e == cudaSuccess) e = cudaEventRecord(ev->in[c], hs);
   }
+  dit_status failed = DIT_OK;  // a group's launch that failed (its copies are still joined below)
   for (int c = 0; c < chunks && e == cudaSuccess; ++c) {
     const int hk0 = kv0(c), hkc = kv0(c + 1) - hk0, hq0 = hk0 * group, hqc = hkc * group;
     cudaStream_t ks = (c & 1) ? ev->aux : cs;
@@ -763,9 +788,34 @@ dit_status dit_attn_fwd_host(const void* q_host, const void* k_host, const void*
         static_cast<uint8_t*>(v) + hk0 * row, static_cast<uint8_t*>(out) + hq0 * row, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
         2, QK_BF16, PV_BF16, B, hqc, hkc, Sq, Skv, mode, 1, 1, threshold_scale_factor, nullptr, nullptr, nullptr,
         nullptr, nullptr, err, ks, Hq, Hkv);
-    if (st != DIT_OK) return st;
+    if (st != DIT_OK) {
+      failed = st;
+      break;
+    }
     e = cudaEventRecord(ev->comp[c], ks);
   }
+  // On a failure nothing more is queued. The copies and kernels already queued on the copy streams
+  // and on `aux` are joined back to the compute stream, so that once it drains the caller may reuse
+  // or free every buffer; if even that cannot be queued, this waits for them.
+  auto fail_joined = [&](dit_status ret) {
+    cudaGetLastError();
+    const bool joined = cudaEventRecord(ev->h2d_done, hs) == cudaSuccess &&
+                        cudaEventRecord(ev->done, ds2) == cudaSuccess &&
+                        cudaEventRecord(ev->aux_done, ev->aux) == cudaSuccess &&
+                        cudaStreamWaitEvent(cs, ev->h2d_done, 0) == cudaSuccess &&
+                        cudaStreamWaitEvent(cs, ev->done, 0) == cudaSuccess &&
+                        cudaStreamWaitEvent(cs, ev->aux_done, 0) == cudaSuccess;
+    if (!joined) {
+      cudaGetLastError();
+      cudaStreamSynchronize(hs);
+      cudaStreamSynchronize(ds2);
+      cudaStreamSynchronize(ev->aux);
+      cudaGetLastError();
+    }
+    return ret;
+  };
+  if (failed != DIT_OK) return fail_joined(failed);
+  if (e != cudaSuccess) return fail_joined(DIT_E_CUDA);
   for (int c = 0; c < chunks && e == cudaSuccess; ++c) {
     const int hk0 = kv0(c), hkc = kv0(c + 1) - hk0, hq0 = hk0 * group, hqc = hkc * group;
     const size_t qo = hq0 * row;
@@ -780,12 +830,14 @@ dit_status dit_attn_fwd_host(const void* q_host, const void* k_host, const void*
                             Hq * row, hqc * row, (size_t)B * Sq, cudaMemcpyDeviceToHost, ds2);
     }
   }
+  if (e != cudaSuccess) return fail_joined(DIT_E_CUDA);
   // completion (the last output byte on the host, and all kernels) is signalled on the compute stream
-  if (e == cudaSuccess) e = cudaEventRecord(ev->done, ds2);
+  e = cudaEventRecord(ev->done, ds2);
   if (e == cudaSuccess) e = cudaEventRecord(ev->aux_done, ev->aux);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev->done, 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev->aux_done, 0);
-  return from_cuda(e);
+  if (e != cudaSuccess) return fail_joined(DIT_E_CUDA);
+  return DIT_OK;
 }
 
 dit_status dit_selftest_withheld_loads(const void* q, const void* k, const void* v, const float* v_scale, void* out,

@@ -98,6 +98,14 @@ cudaError_t launch_zero_i32(int32_t* p, size_t n, cudaStream_t stream);
 cudaError_t launch_copy_rows(const void* src, size_t src_pitch, void* dst, size_t dst_pitch, size_t width,
                              size_t rows, cudaStream_t stream);
 
+// Argument checks shared by the entry points (api.cu). valid_shape: B, Sq >= 0; Hq, Hkv, Skv >= 1;
+// Hq a multiple of Hkv; grid limits; every tensor under 1e12 bytes. valid_mode: the mode bits, Q/K
+// dtype and token-block sizes form a recipe the library implements, and a Skip-Softmax factor is
+// finite and non-negative.
+bool is_block(int x);
+bool valid_shape(int B, int Hq, int Hkv, int Sq, int Skv);
+bool valid_mode(int mode, int qk_dtype, int q_block, int k_block, float factor);
+
 inline int stats_chunks(int Skv) { return (Skv + kStatsChunk - 1) / kStatsChunk; }
 
 }  // namespace ditattn

@@ -46,8 +46,10 @@
 #pragma once
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "ditattn_internal.h"
 #include "fmha_common.cuh"
@@ -854,11 +856,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int QKF, int PVF, int KB, bool SKIP, bool WITHHOLD = false>
 cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                        const FmhaParams& p, cudaStream_t stream) {
-  static bool attr_set[64] = {};
+  // set once per device and instantiation; host threads may launch concurrently
+  static std::atomic<bool> attr_set[64];
+  static std::mutex attr_mu;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 64 && !attr_set[dev]) {
+  if (dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev].load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(attr_mu);
     // The register hand-over in the kernel (setmaxnreg) assumes exactly kLaunchRegs per thread at
     // launch; with fewer, the softmax warpgroups' increase could never be granted.
     cudaFuncAttributes fa;
@@ -868,7 +874,7 @@ cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
     e = cudaFuncSetAttribute(fmha_fwd_kernel<QKF, PVF, KB, SKIP, WITHHOLD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SmemLayout<QKF, PVF>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   const dim3 grid((p.Sq + 255) / 256, p.Hq, p.B);
   fmha_fwd_kernel<QKF, PVF, KB, SKIP, WITHHOLD><<<grid, kThreads, SmemLayout<QKF, PVF>::kSmemBytes, stream>>>(tq, tk, tv, to, p);

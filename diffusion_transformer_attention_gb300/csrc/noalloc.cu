@@ -26,13 +26,10 @@ constexpr size_t kScratchBytes = size_t(32) << 20;  // 32 MiB
 static __device__ __align__(256) uint8_t g_prepass_scratch[kScratchBytes];
 
 // Device address of g_prepass_scratch, looked up once per device. In host code the array's
-// name only stands in for the symbol; it is not a device address.
-struct ScratchAddr {
-  bool ready = false;
-  bool ok = false;
-  uint8_t* ptr = nullptr;
-};
-ScratchAddr g_addr[64];
+// name only stands in for the symbol; it is not a device address. Only a successful lookup is
+// cached: a failure (for example, no room to load the module that holds the array) is reported
+// and tried again on the next call.
+uint8_t* g_addr[64];
 std::mutex g_addr_mu;
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -44,25 +41,22 @@ dit_status scratch_for_current_device(uint8_t** out) {
     return DIT_E_UNSUPPORTED;
   }
   std::lock_guard<std::mutex> lock(g_addr_mu);
-  ScratchAddr& a = g_addr[dev];
-  if (!a.ready) {
-    a.ready = true;
+  if (g_addr[dev] == nullptr) {
     cudaDeviceProp prop;
     if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
       cudaGetLastError();
-      return DIT_E_UNSUPPORTED;
+      return DIT_E_CUDA;
     }
     if (!(prop.major == 10 && prop.minor == 3)) return DIT_E_UNSUPPORTED;
+    // With lazy module loading this is the call that loads the module and so reserves the array.
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_prepass_scratch) != cudaSuccess || p == nullptr) {
       cudaGetLastError();
       return DIT_E_CUDA;
     }
-    a.ptr = static_cast<uint8_t*>(p);
-    a.ok = true;
+    g_addr[dev] = static_cast<uint8_t*>(p);
   }
-  if (!a.ok) return DIT_E_UNSUPPORTED;
-  *out = a.ptr;
+  *out = g_addr[dev];
   return DIT_OK;
 }
 
@@ -76,19 +70,19 @@ dit_status sage_quantize_qkv_noalloc(const void* q, const void* k, const void* v
                                      int Skv, int qk_dtype, int q_block, int k_block, void* q_codes, void* k_codes,
                                      void* v_codes, float* q_scale, float* k_scale, float* v_scale, float* k_mean,
                                      void* stream) {
-  if (B < 0 || Sq < 0 || Hq < 1 || Hkv < 1 || Skv < 1 || Hq % Hkv != 0 || Hq > 65535 || B > 65535)
+  // The same argument checks as sage_quantize_qkv, in an order that launches nothing for a problem
+  // too large for the fixed scratch whatever its pointers are.
+  if (!valid_shape(B, Hq, Hkv, Sq, Skv) || (qk_dtype != DIT_QK_INT8 && qk_dtype != DIT_QK_FP8_E4M3) ||
+      !valid_mode(DIT_MODE_SAGE, qk_dtype, q_block, k_block, 0.0f))
     return DIT_E_INVALID_ARG;
-  if (qk_dtype != DIT_QK_INT8 && qk_dtype != DIT_QK_FP8_E4M3) return DIT_E_INVALID_ARG;
-  const auto is_block = [](int x) { return x == 1 || x == 4 || x == 16; };
-  if (!is_block(q_block) || !is_block(k_block)) return DIT_E_INVALID_ARG;
   if (B == 0) return DIT_OK;
+  const size_t n = (size_t)B * Hkv * stats_chunks(Skv) * kHeadDim;
+  const size_t sum_bytes = round256(n * 8);
+  if (sum_bytes + round256(n * 4) > kScratchBytes) return DIT_E_WORKSPACE;  // beyond the fixed scratch
   const void* ptrs[] = {k, v, k_codes, v_codes, k_scale, v_scale, k_mean};
   for (const void* ptr : ptrs)
     if (!ptr || !aligned16(ptr)) return DIT_E_INVALID_ARG;
   if (Sq > 0 && (!q || !q_codes || !q_scale || !aligned16(q) || !aligned16(q_codes))) return DIT_E_INVALID_ARG;
-  const size_t n = (size_t)B * Hkv * stats_chunks(Skv) * kHeadDim;
-  const size_t sum_bytes = round256(n * 8);
-  if (sum_bytes + round256(n * 4) > kScratchBytes) return DIT_E_WORKSPACE;  // beyond the fixed scratch
   uint8_t* scratch = nullptr;
   const dit_status ds = scratch_for_current_device(&scratch);
   if (ds != DIT_OK) return ds;

@@ -234,8 +234,13 @@ dit_status sage_quantize_qkv_with_mean(const void* q, const void* k, const void*
  * larger problems return DIT_E_WORKSPACE (e.g. B * Hkv = 40 allows Skv up to about 550,000).
  * Nothing here calls cudaMalloc, cudaFree or any allocating routine.
  *
- * The first call on each device looks up the array's device address (a one-time set-up); make
- * that first call before any stream capture. Every call shares the one array and the kernels
+ * The first call on each device looks up the array's device address (a one-time set-up). With
+ * CUDA's lazy module loading that lookup is also what loads the library's module and so reserves
+ * the 32 MiB on that device: make the first call before the host framework claims its memory
+ * pool, and before any stream capture. A failed lookup (e.g. no room left to reserve the array)
+ * returns DIT_E_CUDA and is tried again on the next call; it is not remembered. Arguments are
+ * checked first, and a problem too large for the array returns DIT_E_WORKSPACE before any
+ * pointer is looked at or anything is launched. Every call shares the one array and the kernels
  * write each scratch value before reading it, so nothing needs clearing between calls; but two
  * calls whose kernels overlap on the GPU (e.g. on different streams) race on it.
  */

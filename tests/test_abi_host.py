@@ -282,3 +282,21 @@ def test_withheld_loads_selftest_rejects_bad_arguments(lib):
     assert call(q=MISALIGNED) == INVALID
     if not torch.cuda.is_available():
         assert call() == UNSUPPORTED
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch_before_any_pointer(lib):
+    # B * Hkv * ceil(Skv / 1024) chunks of 128 channels at 12 bytes each (about 77 MB here) exceed the
+    # 32 MiB array. The size check comes before the pointer checks and any CUDA call: with null
+    # pointers the call returns DIT_E_WORKSPACE, and a regression would return DIT_E_INVALID_ARG.
+    st = lib.sage_quantize_qkv_noalloc(None, None, None, 1, 64, 64, 1, 800_000, 1, 1, 16,
+                                       None, None, None, None, None, None, None, None)
+    assert st == WORKSPACE
+    # a problem that fits reaches the pointer checks, and null pointers are refused there
+    st = lib.sage_quantize_qkv_noalloc(None, None, None, 1, 8, 8, 1, 4096, 1, 1, 16,
+                                       None, None, None, None, None, None, None, None)
+    assert st == INVALID
+    # the shared shape and recipe checks come first
+    assert lib.sage_quantize_qkv_noalloc(None, None, None, 1, 6, 4, 1, 4096, 1, 1, 16, None, None, None, None,
+                                         None, None, None, None) == INVALID
+    assert lib.sage_quantize_qkv_noalloc(None, None, None, 1, 8, 8, 1, 4096, 0, 0, 0, None, None, None, None,
+                                         None, None, None, None) == INVALID

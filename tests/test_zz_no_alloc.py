@@ -4,12 +4,10 @@ where cudaMalloc's possible device-wide synchronization is not allowed). It keep
 a fixed device array inside the library instead of taking a workspace.
 
 Checks, through the C-ABI: two calls in a row (different shapes, so stale scratch from the first
-call would show) give exactly the codes and scales of the regular entry point, and a problem too
-large for the fixed scratch is rejected with DIT_E_WORKSPACE before anything is launched.
+call would show) give exactly the codes and scales of the regular entry point. (The rejection of a
+problem too large for the fixed scratch needs no GPU: tests/test_abi_host.py.)
 This file is collected last on purpose.
 """
-
-import ctypes
 
 import numpy as np
 import pytest
@@ -19,8 +17,6 @@ import diffusion_transformer_attention_gb300 as dit
 import workloads
 
 pytestmark = pytest.mark.gpu
-
-DIT_E_WORKSPACE = 5
 
 
 def _outputs_like(ref: dict) -> dict:
@@ -44,13 +40,3 @@ def test_noalloc_matches_regular_entry_point_twice(dtype):
             b = got[name].cpu().numpy()
             assert np.array_equal(a.view(np.uint8), b.view(np.uint8)), (w.name, name)
 
-
-def test_noalloc_rejects_problems_beyond_its_scratch():
-    t = torch.zeros(256, dtype=torch.uint8, device="cuda")
-    p = ctypes.c_void_p(t.data_ptr())
-    lib = dit.library()
-    # B * Hkv * ceil(Skv / 1024) chunks of 128 channels at 12 bytes each (about 77 MB here) exceed
-    # 32 MiB; the size check returns before any launch, so the small placeholder buffers are never
-    # touched.
-    st = lib.sage_quantize_qkv_noalloc(p, p, p, 1, 64, 64, 1, 800_000, 1, 1, 16, p, p, p, p, p, p, p, None)
-    assert st == DIT_E_WORKSPACE
