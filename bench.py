@@ -64,27 +64,78 @@ def peaks():
 
 # ------------------------------------------------------------------ clocks during the timed region
 class ClockSampler:
+    """Samples the SM clock, power and clock-event reasons of one GPU while the timed region runs.
+
+    Reads NVML (libnvidia-ml, through ctypes) every 10 ms from a thread, so even a region of a few
+    hundred milliseconds gets tens of samples; falls back to ``nvidia-smi -lms 200``. Only queries:
+    no clock, power or other setting is touched."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clock-event reason bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
 
-    def __init__(self, gpu_index):
-        self.idx = gpu_index
+    def __init__(self, gpu_uuid, period_s: float = 0.01):
+        self.uuid = gpu_uuid
+        self.period = period_s
+        self.rows = []          # (sm_mhz, power_w, reason_bits)
+        self.max_mhz = None
         self.proc = None
         self.file = None
+        self.thread = None
+        self.stop = None
+        self.nvml = None
+
+    def _nvml_open(self):
+        import ctypes
+        import ctypes.util
+        name = ctypes.util.find_library("nvidia-ml") or "libnvidia-ml.so.1"
+        lib = ctypes.CDLL(name)
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByUUID(self.uuid.encode(), ctypes.byref(h)) != 0:
+            raise OSError("no NVML handle for this GPU")
+        get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:  # 1 = NVML_CLOCK_SM
+            self.max_mhz = float(mx.value)
+        self.nvml = (lib, h, get_reasons)
+
+    def _nvml_loop(self):
+        import ctypes
+        lib, h, get_reasons = self.nvml
+        mhz, mw, rb = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop.is_set():
+            if (lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0 and
+                    lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw)) == 0 and get_reasons(h, ctypes.byref(rb)) == 0):
+                self.rows.append((float(mhz.value), mw.value / 1000.0, int(rb.value)))
+            self.stop.wait(self.period)
 
     def __enter__(self):
+        import threading
         try:
-            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
-                                         stdout=self.file, stderr=subprocess.DEVNULL)
-        except OSError:
-            self.proc = None
-        time.sleep(0.3)
+            self._nvml_open()
+            self.stop = threading.Event()
+            self.thread = threading.Thread(target=self._nvml_loop, daemon=True)
+            self.thread.start()
+        except (OSError, AttributeError):
+            self.nvml = None
+            try:
+                self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+                self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.uuid), f"--query-gpu={self.FIELDS}",
+                                              "--format=csv,noheader,nounits", "-lms", "200"],
+                                             stdout=self.file, stderr=subprocess.DEVNULL)
+            except OSError:
+                self.proc = None
+            time.sleep(0.3)
         return self
 
     def __exit__(self, *exc):
+        if self.thread is not None:
+            self.stop.set()
+            self.thread.join(timeout=5)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -93,6 +144,13 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
+        if self.nvml is not None:
+            load = [r for r in self.rows if r[1] > 300] or self.rows  # samples under load
+            if not load:
+                return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no samples"], "source": "nvml"}
+            reasons = sorted({name for _, _, bits in load for bit, name in self.REASONS.items() if bits & bit})
+            return {"sm_mhz": statistics.median(r[0] for r in load), "sm_max_mhz": self.max_mhz,
+                    "reasons": reasons, "samples": len(load), "source": "nvml, 10 ms"}
         if self.proc is None or self.file is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         rows = []
@@ -119,7 +177,7 @@ class ClockSampler:
                 if val.lower().startswith("active"):
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(rows[0][2]),
-                "reasons": sorted(reasons), "samples": len(load)}
+                "reasons": sorted(reasons), "samples": len(load), "source": "nvidia-smi, 200 ms"}
 
 
 # ------------------------------------------------------------------ distributed helpers
@@ -159,23 +217,70 @@ def aggregate_value(flop_per_step: float, steps: int, elapsed_ms: float, world: 
 
 
 # ------------------------------------------------------------------ CPU oracle sample
+def blas_threads():
+    """Threads of the BLAS NumPy calls (threadpoolctl when installed, else the bundled OpenBLAS's own
+    query through its loaded library), or None when neither is available."""
+    try:
+        import threadpoolctl
+        n = [i["num_threads"] for i in threadpoolctl.threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:  # noqa: BLE001 - optional dependency, any failure means "unknown"
+        pass
+    import ctypes
+    np.ones((2, 2)) @ np.ones((2, 2))  # make sure the BLAS library is loaded
+    try:
+        with open("/proc/self/maps") as f:
+            paths = sorted({ln.split()[-1] for ln in f if "blas" in ln.lower() and ".so" in ln})
+    except OSError:
+        return None
+    for path in paths:
+        try:
+            lib = ctypes.CDLL(path)
+        except OSError:
+            continue
+        for sym in ("scipy_openblas_get_num_threads64_", "openblas_get_num_threads64_", "openblas_get_num_threads"):
+            fn = getattr(lib, sym, None)
+            if fn is not None:
+                return int(fn())
+    return None
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
 def oracle_sample(w: workloads.Workload, budget_s: float = 15.0, max_tiles: int = 64, warmup: int = 0,
-                  steps: int | None = None):
+                  steps: int | None = None, factor: float | None = None):
     """Time the CPU oracle on whole 128-row query tiles of one head of the workload's recipe.
 
     One sample (a "step") is one query tile against all Skv keys. With ``steps`` given, runs
     ``warmup`` untimed tiles and then exactly ``steps`` timed tiles; otherwise runs tiles until
-    ``budget_s`` seconds or ``max_tiles``. Returns (dense-equiv TFLOP/s, seconds per tile, tiles,
-    threads, description)."""
+    ``budget_s`` seconds or ``max_tiles`` (at least two). Quantized recipes first run the oracle's
+    quantizer over the whole head (timed separately). Returns a dict: dense-equiv TFLOP/s of the
+    sampled tiles, seconds per tile, tiles, the quantizer's seconds for the head, threads,
+    description."""
     from oracle import attention as oatt
-    from oracle import sage_quant
+    from oracle import mx_quant, nvfp4_quant, sage_quant
     one = w.scaled(B=1, Hq=1, Hkv=1)
     q, k, v = workloads.generate(one, seed=0)
     inp = dict(q=q.float().numpy(), k=k.float().numpy(), v=v.float().numpy())
+    t0 = time.perf_counter()
     quant = None
     if w.mode == "sage":
         quant = sage_quant.sage_quantize(inp["q"], inp["k"], inp["v"], w.qk_dtype, w.q_block, w.k_block)
-    factor = w.factors[len(w.factors) // 2] if w.factors else None
+    elif w.mode == "qk16pv8":
+        quant = sage_quant.qk16pv8_quantize(inp["v"], True)
+    elif w.mode == "mxfp8":
+        quant = mx_quant.mxfp8_quantize(inp["q"], inp["k"], inp["v"], False)
+    elif w.mode == "nvfp4":
+        quant = nvfp4_quant.nvfp4_qk_quantize(inp["q"], inp["k"], inp["v"], False)
+    quant_s = time.perf_counter() - t0
+    if factor is None and w.factors:
+        factor = w.factors[len(w.factors) // 2]
     ntiles = math.ceil(w.Sq / 128)
     order = np.random.default_rng(0).permutation(ntiles)
 
@@ -186,18 +291,30 @@ def oracle_sample(w: workloads.Workload, budget_s: float = 15.0, max_tiles: int 
         tile(n)
     t0 = time.perf_counter()
     tiles = 0
-    while (tiles < steps) if steps is not None else (tiles < max_tiles and time.perf_counter() - t0 < budget_s):
+    while (tiles < steps) if steps is not None else \
+            (tiles < 2 or (tiles < max_tiles and time.perf_counter() - t0 < budget_s)):
         tile(warmup + tiles)
         tiles += 1
     dt = time.perf_counter() - t0
     flop = 4.0 * tiles * 128 * w.Skv * 128
-    try:
-        threads = len(os.sched_getaffinity(0))
-    except AttributeError:
-        threads = os.cpu_count()
     desc = (f"{tiles} query tiles x 128 rows of one head against all {w.Skv} keys, float64 NumPy "
-            f"({w.name} recipe)")
-    return flop / dt / 1e12, dt / max(tiles, 1), tiles, threads, desc
+            f"({w.name} recipe" + (f", factor {factor:g}" if factor is not None else "") + ")")
+    return {"tflops": flop / dt / 1e12, "s_per_tile": dt / max(tiles, 1), "tiles": tiles, "quant_s": quant_s,
+            "threads": host_cores(), "desc": desc}
+
+
+def oracle_config_baseline(w: workloads.Workload, budget_s: float, factor: float | None = None) -> dict:
+    """The oracle on a bounded sample of a large workload: its quantizer over one head and whole query
+    tiles of that head, timed on the host cores, with the full call's time extrapolated from them
+    (quantizer time x the elements of all heads, attention time x all query tiles of all heads)."""
+    r = oracle_sample(w, budget_s=budget_s, max_tiles=16, factor=factor)
+    heads_q = w.B * w.Hq
+    elems_full = w.B * (w.Sq * w.Hq + 2 * w.Skv * w.Hkv)
+    elems_one = w.Sq + 2 * w.Skv
+    full_s = r["quant_s"] * elems_full / elems_one + r["s_per_tile"] * heads_q * math.ceil(w.Sq / 128)
+    return {"tflops": round(r["tflops"], 5), "tiles": r["tiles"], "s_per_tile": round(r["s_per_tile"], 3),
+            "quant_s_one_head": round(r["quant_s"], 3), "full_call_s_extrapolated": round(full_s, 1),
+            "full_call_tflops_extrapolated": round(w.dense_equiv_flop / full_s / 1e12, 5)}
 
 
 def dense_kernel_traffic():
@@ -241,136 +358,142 @@ def time_steps(fn, steps, warmup, world, stream):
     return e0.elapsed_time(e1)  # ms on this rank
 
 
-def run_modes(dit, steps, warmup, world, stream, peak16, hbm_gbs):
-    """The other workloads. Each quantized one is timed as one call of the whole path (prepass +
-    attention), and also in its two halves through the split entry points: the prepass alone
-    (against the measured HBM bandwidth: it is memory-bound) and the attention over
-    precomputed codes (against the tensor peak of its operand types)."""
-    res = {}
+def _r(x, nd=3):
+    return None if x is None else round(float(x), nd)
+
+
+def run_recipe(dit, name, steps, warmup, world, stream, peak, hbm_gbs):
+    """One quantized workload on the DiT / GQA inputs: the whole call (prepass + attention) through
+    dit_attn_fwd, then its two halves through the split entry points: the prepass alone (against the
+    measured HBM bandwidth: it is memory-bound) and the attention over precomputed codes (against
+    the tensor peak of its operand types)."""
+    w = workloads.WORKLOADS[name]
+    q, k, v = workloads.generate(w, seed=1, device="cuda")
+    qk16, mx, nv = w.mode == "qk16pv8", w.mode == "mxfp8", w.mode == "nvfp4"
+    mode = dit.MODE_SAGE | (dit.MODE_V_PER_TENSOR if qk16 else 0)
+    ws = torch.empty(dit.dit_attn_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, mode, w.qk_dtype,
+                                                  w.q_block, w.k_block), dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(q)
+
+    def step():
+        dit.dit_attn_fwd(q, k, v, out, mode=mode, qk_dtype=w.qk_dtype, q_block=w.q_block,
+                         k_block=w.k_block, workspace=ws, stream=stream)
+    ms = max_over_ranks(time_steps(step, steps, warmup, world, stream), world) / steps
+    tf = w.dense_equiv_flop / (ms * 1e-3) / 1e12
+    bq, bkv = q.numel() * 2, k.numel() * 2
+    # algorithmic prepass bytes (inputs read as often as the passes need them, codes and scales written)
+    if qk16:
+        pre = lambda: dit.sage_quantize_v(v, per_tensor=True, stream=stream)  # noqa: E731
+        pre_bytes = 2 * bkv + bkv // 2                                        # V twice, 1-byte V codes
+    elif nv:
+        def pre():
+            res = dit.nvfp4_quantize_qk(q, k, stream=stream)
+            res.update(dit.sage_quantize_v(v, per_tensor=False, stream=stream))
+            return res
+        # Q, K, V twice; half-byte Q/K codes, 1-byte V codes, 8 scale bytes per 128 Q/K elements
+        pre_bytes = 2 * bq + 4 * bkv + (bq + bkv) // 4 + bkv // 2 + (bq + bkv) // 32
+    elif mx:
+        def pre():
+            res = dit.mx_quantize_qk(q, k, stream=stream)
+            res.update(dit.sage_quantize_v(v, per_tensor=False, stream=stream))
+            return res
+        # Q, K once, V twice; 1-byte Q/K/V codes, 4 scale bytes per 128 Q/K elements
+        pre_bytes = bq + 3 * bkv + (bq + 2 * bkv) // 2 + (bq + bkv) // 64
+    else:
+        pre = lambda: dit.sage_quantize_qkv(q, k, v, qk_dtype=w.qk_dtype, q_block=w.q_block,  # noqa: E731
+                                            k_block=w.k_block, stream=stream)
+        pre_bytes = bq + 4 * bkv + (bq + 2 * bkv) // 2                        # K, V twice, Q once; 1-byte codes
+    quant = pre()
+    if qk16:
+        quant.update(q_codes=q, k_codes=k)
+    pre_ms = max_over_ranks(time_steps(pre, steps, warmup, world, stream), world) / steps
+
+    def attn():
+        if mx:
+            dit.dit_attn_fwd_mxfp8(quant, out, mode=mode, stream=stream)
+        elif nv:
+            dit.dit_attn_fwd_nvfp4(quant, out, mode=mode, stream=stream)
+        else:
+            dit.dit_attn_fwd_quantized(quant, out, mode=mode, qk_dtype=w.qk_dtype, q_block=w.q_block,
+                                       k_block=w.k_block, stream=stream)
+    attn_ms = max_over_ranks(time_steps(attn, steps, warmup, world, stream), world) / steps
+    atf = w.dense_equiv_flop / (attn_ms * 1e-3) / 1e12
+    pre_gbs = pre_bytes / (pre_ms * 1e-3) / 1e9
+    del q, k, v, ws, out, quant
+    return {"ms": _r(ms), "tflops": _r(tf, 1), "frac": _r(tf / peak), "peak": _r(peak, 1),
+            "pre_ms": _r(pre_ms), "pre_gbs": _r(pre_gbs, 1), "pre_frac_hbm": _r(pre_gbs / hbm_gbs),
+            "pre_bytes": int(pre_bytes), "attn_ms": _r(attn_ms), "attn_tflops": _r(atf, 1), "attn_frac": _r(atf / peak)}
+
+
+def skip_sweep(dit, q, k, v, out, counts, w, factors, steps, warmup, world, stream, dense_ms, *, mode, dt, qb, kb):
+    """Time one Skip-Softmax recipe over the threshold factors on the video inputs; returns compact
+    lists (factor, skipped fraction, ms, speedup against dense BF16 on the same inputs)."""
+    nqt, nkt = math.ceil(w.Sq / 128), math.ceil(w.Skv / 128)
+    need = dit.dit_attn_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, mode & ~dit.MODE_SKIP, dt, qb, kb)
+    ws = torch.empty(max(1, need), dtype=torch.uint8, device="cuda") if need > 0 else None
+    res = {"f": [], "skip": [], "ms": [], "x": []}
+    for factor in factors:
+        def step():
+            dit.dit_attn_fwd(q, k, v, out, mode=mode, qk_dtype=dt, q_block=qb, k_block=kb,
+                             threshold_scale_factor=factor, workspace=ws, skip_counts=counts, stream=stream)
+        ms = max_over_ranks(time_steps(step, steps, warmup, world, stream), world) / steps
+        frac = float(counts.sum().item()) / (w.B * w.Hq * nqt * nkt)
+        res["f"].append(factor)
+        res["skip"].append(_r(frac, 4))
+        res["ms"].append(_r(ms, 2))
+        res["x"].append(_r(dense_ms / ms))
+    return res
+
+
+def run_modes(dit, steps, warmup, world, stream, peak16, hbm_gbs, cpu: bool):
+    """The other workloads, in the order the line prints them: the other Q/K formats on the DiT
+    inputs, the Skip-Softmax sweeps with FP8-rate BMM1s, then SAGE INT8 on the DiT inputs, SAGE FP8
+    with GQA, and the Skip-Softmax curve on the video grid (SAGE INT8, and BF16 without SAGE), each
+    against its own instruction peak and, on rank 0, beside the oracle timed on a bounded sample."""
     peak8 = 2.0 * peak16                               # FP8 dense = 2 x BF16 (nominal ratio)
     peak_mix = 2.0 * peak16 * peak8 / (peak16 + peak8)  # BMM1 on 16-bit operands, BMM2 on FP8
     peak4 = 4.0 * peak16                               # FP4 dense = 4 x BF16 (nominal ratio)
     peak_nv = 2.0 * peak4 * peak8 / (peak4 + peak8)     # BMM1 on FP4, BMM2 on FP8
-    table = [("dit_sage_int8_32k", peak_mix, "BMM1 f16 + BMM2 e4m3 harmonic peak"),
-             ("gqa_sage_fp8_16k", peak8, "2 x measured bf16 (e4m3 nominal ratio)"),
-             ("dit_qk16pv8_32k", peak_mix, "BMM1 bf16 + BMM2 e4m3 harmonic peak"),
-             ("dit_mxfp8_32k", peak8, "2 x measured bf16 (e4m3 nominal ratio; BMM1 block-scaled)"),
-             ("dit_nvfp4_32k", peak_nv, "BMM1 fp4 (4 x bf16) + BMM2 e4m3 (2 x bf16) harmonic peak")]
-    for name, peak, peak_desc in table:
-        w = workloads.WORKLOADS[name]
-        q, k, v = workloads.generate(w, seed=1, device="cuda")
-        qk16, mx, nv = w.mode == "qk16pv8", w.mode == "mxfp8", w.mode == "nvfp4"
-        mode = dit.MODE_SAGE | (dit.MODE_V_PER_TENSOR if qk16 else 0)
-        ws = torch.empty(dit.dit_attn_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, mode, w.qk_dtype,
-                                                      w.q_block, w.k_block), dtype=torch.uint8, device="cuda")
-        out = torch.empty_like(q)
-
-        def step():
-            dit.dit_attn_fwd(q, k, v, out, mode=mode, qk_dtype=w.qk_dtype, q_block=w.q_block,
-                             k_block=w.k_block, workspace=ws, stream=stream)
-        ms = max_over_ranks(time_steps(step, steps, warmup, world, stream), world) / steps
-        tf = w.dense_equiv_flop / (ms * 1e-3) / 1e12
-        entry = {"ms": round(ms, 3), "tflops": round(tf, 1), "peak_tflops": round(peak, 1),
-                 "frac": round(tf / peak, 3), "peak": peak_desc,
-                 "launches_per_step": 4 if qk16 else 6 if mx else 9 if nv else 5}
-        # the two halves, through the split entry points
-        bq, bkv = q.numel() * 2, k.numel() * 2
-        if qk16:
-            pre = lambda: dit.sage_quantize_v(v, per_tensor=True, stream=stream)  # noqa: E731
-            # V read twice (absmax, then codes), 1-byte codes written
-            pre_bytes, pre_desc = 2 * bkv + bkv // 2, "V read twice, 1-byte V codes written"
-        elif nv:
-            def pre():
-                res = dit.nvfp4_quantize_qk(q, k, stream=stream)
-                res.update(dit.sage_quantize_v(v, per_tensor=False, stream=stream))
-                return res
-            # Q, K read twice (tensor max, then codes), V twice; half-byte Q/K codes, 1-byte V codes and
-            # 8 scale bytes per 128 Q/K elements written
-            pre_bytes = 2 * bq + 4 * bkv + (bq + bkv) // 4 + bkv // 2 + (bq + bkv) // 32
-            pre_desc = "Q, K, V read twice, half-byte Q/K codes, 1-byte V codes and E4M3 block scales written"
-        elif mx:
-            def pre():
-                res = dit.mx_quantize_qk(q, k, stream=stream)
-                res.update(dit.sage_quantize_v(v, per_tensor=False, stream=stream))
-                return res
-            # Q, K read once and V twice; 1-byte Q/K/V codes and 4 scale bytes per 128 Q/K elements written
-            pre_bytes = bq + 3 * bkv + (bq + 2 * bkv) // 2 + (bq + bkv) // 64
-            pre_desc = "Q, K read once, V twice, 1-byte Q/K/V codes and E8M0 bytes written"
-        else:
-            pre = lambda: dit.sage_quantize_qkv(q, k, v, qk_dtype=w.qk_dtype, q_block=w.q_block,  # noqa: E731
-                                                k_block=w.k_block, stream=stream)
-            # K, V read in the stats pass and again with Q in the code pass; 1-byte codes written
-            pre_bytes = bq + 4 * bkv + (bq + 2 * bkv) // 2
-            pre_desc = "K, V read twice, Q once, 1-byte Q/K/V codes written"
-        quant = pre()
-        if qk16:
-            quant.update(q_codes=q, k_codes=k)
-        pre_ms = max_over_ranks(time_steps(pre, steps, warmup, world, stream), world) / steps
-
-        def attn():
-            if mx:
-                dit.dit_attn_fwd_mxfp8(quant, out, mode=mode, stream=stream)
-            elif nv:
-                dit.dit_attn_fwd_nvfp4(quant, out, mode=mode, stream=stream)
-            else:
-                dit.dit_attn_fwd_quantized(quant, out, mode=mode, qk_dtype=w.qk_dtype, q_block=w.q_block,
-                                           k_block=w.k_block, stream=stream)
-        attn_ms = max_over_ranks(time_steps(attn, steps, warmup, world, stream), world) / steps
-        atf = w.dense_equiv_flop / (attn_ms * 1e-3) / 1e12
-        entry["prepass"] = {"ms": round(pre_ms, 3), "gbs": round(pre_bytes / (pre_ms * 1e-3) / 1e9, 1),
-                            "frac_hbm": round(pre_bytes / (pre_ms * 1e-3) / 1e9 / hbm_gbs, 3),
-                            "bytes": int(pre_bytes), "bytes_desc": pre_desc}
-        entry["attention"] = {"ms": round(attn_ms, 3), "tflops": round(atf, 1), "frac": round(atf / peak, 3),
-                              "note": "INT8 codes are widened to fp16 inside this call" if w.qk_dtype == "int8"
-                              else "the attention kernel alone"}
-        res[name] = entry
-        del q, k, v, ws, out, quant
-    # Skip-Softmax sweep on the video grid, against dense BF16 on the same shape
+    res = {"peaks": {"bf16": _r(peak16, 1), "f16_e4m3": _r(peak_mix, 1), "e4m3": _r(peak8, 1),
+                     "fp4_e4m3": _r(peak_nv, 1)}}
+    res["recipes"] = {label: run_recipe(dit, name, steps, warmup, world, stream, peak, hbm_gbs)
+                      for label, name, peak in [("qk16pv8", "dit_qk16pv8_32k", peak_mix),
+                                                ("mxfp8", "dit_mxfp8_32k", peak8),
+                                                ("nvfp4", "dit_nvfp4_32k", peak_nv)]}
+    # the video inputs, shared by every sweep
     w = workloads.WORKLOADS["video_skip_int8_75600"]
     q, k, v = workloads.generate(w, seed=1, device="cuda")
     out = torch.empty_like(q)
-    nqt = math.ceil(w.Sq / 128)
-    counts = torch.zeros((w.B, w.Hq, nqt), dtype=torch.int32, device="cuda")
-    ws = torch.empty(dit.dit_attn_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, dit.MODE_SAGE, w.qk_dtype,
-                                                  w.q_block, w.k_block), dtype=torch.uint8, device="cuda")
-    s = max(2, steps // 4)
+    counts = torch.zeros((w.B, w.Hq, math.ceil(w.Sq / 128)), dtype=torch.int32, device="cuda")
+    s, wu = max(2, steps // 4), min(warmup, 3)
 
     def dense():
         dit.dit_attn_fwd(q, k, v, out, stream=stream)
-    dense_ms = max_over_ranks(time_steps(dense, s, min(warmup, 3), world, stream), world) / s
-    sweep = {}
-    nkt = math.ceil(w.Skv / 128)
-    for factor in w.factors:
-        def step():
-            dit.dit_attn_fwd(q, k, v, out, mode=dit.MODE_SAGE | dit.MODE_SKIP, qk_dtype=w.qk_dtype,
-                             q_block=w.q_block, k_block=w.k_block, threshold_scale_factor=factor, workspace=ws,
-                             skip_counts=counts, stream=stream)
-        ms = max_over_ranks(time_steps(step, s, min(warmup, 3), world, stream), world) / s
-        frac = float(counts.sum().item()) / (w.B * w.Hq * nqt * nkt)
-        sweep[str(factor)] = {"ms": round(ms, 3), "skip_fraction": round(frac, 4),
-                              "speedup_vs_dense_bf16": round(dense_ms / ms, 3),
-                              "dense_equiv_tflops": round(w.dense_equiv_flop / (ms * 1e-3) / 1e12, 1)}
-    # The same inputs and sweep points with Q/K formats whose BMM1 runs at the FP8 (or FP4) rate: a skipped
-    # tile still costs its BMM1, so the INT8 codes' 16-bit BMM1 caps the INT8 sweep's speedup
-    fast = {}
-    for label, dt, qb, kb in [("sage_fp8_1_16", "fp8_e4m3", 1, 16), ("mxfp8", "mxfp8", 0, 0),
-                              ("nvfp4", "nvfp4", 0, 0)]:
-        ws2 = torch.empty(max(1, dit.dit_attn_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, dit.MODE_SAGE, dt, qb, kb)),
-                          dtype=torch.uint8, device="cuda")
-        pts = {}
-        for factor in (0.0, 50.0, 3200.0):
-            def step2():
-                dit.dit_attn_fwd(q, k, v, out, mode=dit.MODE_SAGE | dit.MODE_SKIP, qk_dtype=dt, q_block=qb, k_block=kb,
-                                 threshold_scale_factor=factor, workspace=ws2, skip_counts=counts, stream=stream)
-            ms = max_over_ranks(time_steps(step2, s, min(warmup, 3), world, stream), world) / s
-            frac = float(counts.sum().item()) / (w.B * w.Hq * nqt * nkt)
-            pts[str(factor)] = {"ms": round(ms, 3), "skip_fraction": round(frac, 4),
-                                "speedup_vs_dense_bf16": round(dense_ms / ms, 3)}
-        fast[label] = pts
-        del ws2
-    res["video_skip_int8_75600"] = {"dense_bf16_ms": round(dense_ms, 3),
-                                    "dense_bf16_tflops": round(w.dense_equiv_flop / (dense_ms * 1e-3) / 1e12, 1),
-                                    "sweep": sweep, "fp8_rate_bmm1_sweeps": fast}
+    dense_ms = max_over_ranks(time_steps(dense, s, wu, world, stream), world) / s
+    sk = dit.MODE_SAGE | dit.MODE_SKIP
+    # Q/K formats whose BMM1 runs at the FP8 (or FP4) rate: a skipped tile still costs its BMM1, so the
+    # INT8 codes' 16-bit BMM1 caps the INT8 curve's speedup
+    short = (0.0, 2.0, 50.0, 3200.0)
+    res["video_fp8_rate_bmm1"] = {
+        label: skip_sweep(dit, q, k, v, out, counts, w, short, s, wu, world, stream, dense_ms, mode=sk, dt=dt, qb=qb, kb=kb)
+        for label, dt, qb, kb in [("sage_fp8_1_16", "fp8_e4m3", 1, 16), ("mxfp8", "mxfp8", 0, 0),
+                                  ("nvfp4", "nvfp4", 0, 0)]}
+    curve = skip_sweep(dit, q, k, v, out, counts, w, w.factors, s, wu, world, stream, dense_ms, mode=sk,
+                       dt=w.qk_dtype, qb=w.q_block, kb=w.k_block)
+    bf16 = skip_sweep(dit, q, k, v, out, counts, w, w.factors, s, wu, world, stream, dense_ms,
+                      mode=dit.MODE_SKIP, dt="bf16", qb=1, kb=1)
+    del q, k, v, out, counts
+    torch.cuda.empty_cache()
+    for label, name, peak in [("dit_sage_int8_32k", "dit_sage_int8_32k", peak_mix),
+                              ("gqa_sage_fp8_16k", "gqa_sage_fp8_16k", peak8)]:
+        res[label] = run_recipe(dit, name, steps, warmup, world, stream, peak, hbm_gbs)
+        if cpu:
+            res[label]["cpu"] = oracle_config_baseline(workloads.WORKLOADS[name], budget_s=4.0)
+    vid = {"dense_bf16_ms": _r(dense_ms), "dense_bf16_tflops": _r(w.dense_equiv_flop / (dense_ms * 1e-3) / 1e12, 1),
+           "bf16_skip": bf16, "sage_int8_1_16_skip": curve}
+    if cpu:
+        vid["cpu"] = oracle_config_baseline(w, budget_s=4.0, factor=50.0)
+    res["video_skip_int8_75600"] = vid
     return res
 
 
@@ -395,13 +518,14 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        tf, per_tile, tiles, threads, desc = oracle_sample(w, warmup=warmup, steps=args.steps)
+        r = oracle_sample(w, warmup=warmup, steps=args.steps)
+        tf = r["tflops"]
         line = {"metric": METRIC, "value": round(tf, 6), "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
-                "warmup": warmup, "ms_per_step": round(per_tile * 1e3, 3), "higher_is_better": True,
+                "warmup": warmup, "ms_per_step": round(r["s_per_tile"] * 1e3, 3), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
                 "impl": "reference",
-                "cpu_baseline": {"value": round(tf, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                                 "sample": desc},
+                "cpu_baseline": {"value": round(tf, 6), "unit": "TFLOP/s", "cores": r["threads"], "kind": "oracle",
+                                 "blas_threads": blas_threads(), "sample": r["desc"]},
                 "e2e": {"value": round(tf, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
@@ -460,14 +584,16 @@ def main():
     if not args.no_modes:
         del q, k, v, out
         torch.cuda.empty_cache()
-        modes = run_modes(dit, args.steps, warmup, world, stream, peak16, hbm)
+        modes = run_modes(dit, args.steps, warmup, world, stream, peak16, hbm,
+                          cpu=(rank == 0 and not args.no_cpu_baseline))
 
     if rank != 0:
         return
     cpu = None
     if not args.no_cpu_baseline:
-        tf, _, tiles, threads, desc = oracle_sample(w)
-        cpu = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc}
+        r = oracle_sample(w, budget_s=10.0)
+        cpu = {"value": round(r["tflops"], 6), "unit": "TFLOP/s", "cores": r["threads"], "kind": "oracle",
+               "blas_threads": blas_threads(), "sample": r["desc"]}
     traffic = dense_kernel_traffic()
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -475,6 +601,12 @@ def main():
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) Q/V, K + per-channel offset)",
         "config": config,
         "pct_of_peak": round(100.0 * kernel_tflops / peak16, 1),
+        # the same rate over the nominal BF16 tensor rate at the SM clock sampled during the timed region
+        # (M128 N128 K16 in 64 clocks = 8192 FLOP per clock per SM): a clock-independent duty estimate,
+        # since the measured cuBLAS peak ran at a lower, power-capped clock
+        "tensor_duty_at_clock": (round(kernel_tflops * 1e12 / (8192.0 * props.multi_processor_count *
+                                                             clocks["sm_mhz"] * 1e6), 3)
+                                 if clocks.get("sm_mhz") else None),
         "roofline": {"bound": "tensor", "achieved": round(kernel_tflops, 1), "peak": peak16, "unit": "TFLOP/s",
                      "frac": round(kernel_tflops / peak16, 3), "traffic": traffic,
                      "peak_source": f"{peak_src} dense bf16 burst (MEASURED_PEAKS.json bf16_tflops)",

@@ -327,11 +327,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         return j == 0 || wait(&bars->s_free[i], (j - 1) & 1);
       }
     };
-    auto k_ready = [&](int j) -> bool {  // K_j staged (and, in MXFP8, its scales)
+    auto k_ready = [&](int j) -> bool {  // K_j staged (and, in MXFP8 / NVFP4, its scales)
       const int tk = 2 * j;
-      bool r = wait(&bars->kv_full[tk & 3], (tk >> 2) & 1);
-      if constexpr (kBS) r = r && wait(&bars->ks_full[j & 3], (j >> 2) & 1);
-      return r;
+      if constexpr (kBS) {
+        return __all_sync(0xffffffffu, mbar_wait2_bounded(&bars->kv_full[tk & 3], (tk >> 2) & 1, &bars->ks_full[j & 3],
+                                                          (j >> 2) & 1, budget, abort_flag));
+      } else {
+        return wait(&bars->kv_full[tk & 3], (tk >> 2) & 1);
+      }
     };
     if constexpr (L::kPInSmem) {
       // E4M3 P in shared memory: BMM1 of the next KV tile overwrites S as soon as the softmax has
@@ -561,7 +564,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < nt; ++j) {
       float wg[kGroups];
       if (ok) {
-        ok = mbar_wait_bounded(&bars->s_full[i], j & 1, budget, abort_flag);
+        // S_i(j), and in SAGE the K-block scales of tile j (both tested at once, so the two waits'
+        // latencies overlap)
+        if constexpr (kQKScaled) {
+          ok = mbar_wait2_bounded(&bars->s_full[i], j & 1, &bars->ks_full[j & 3], (j >> 2) & 1, budget, abort_flag);
+        } else {
+          ok = mbar_wait_bounded(&bars->s_full[i], j & 1, budget, abort_flag);
+        }
         ok = __all_sync(0xffffffffu, ok);
         if (!ok && lane == 0) record_timeout(p, bars);
       }
@@ -577,8 +586,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       float2 s2[32];
       float* s = reinterpret_cast<float*>(s2);
-      tmem_ld32(t_s, s);
-      tmem_ld32(t_s + 32, s + 32);
+      // S into registers. tcgen05.ld.red also returns each load's max over its columns: one load per
+      // K block of 16 tokens in SAGE (the block's max, weighted by its scale below), one load of all
+      // 64 columns without K-block scales. K blocks of 4 or 1 token use plain loads and take their
+      // maxima below (sixteen 4-column loads measured slower than two plain ones and the max tree).
+      constexpr bool kLdMax = !kQKScaled || KB == 16;
+      constexpr int kLoads = (kQKScaled && KB == 16) ? 4 : 1;
+      constexpr int kCols = 64 / kLoads;
+      float gmax[kLoads];
+      if constexpr (!kLdMax) {
+        tmem_ld32(t_s, s);
+        tmem_ld32(t_s + 32, s + 32);
+      } else {
+#pragma unroll
+        for (int q = 0; q < kLoads; ++q) {
+          if constexpr (kCols == 64) tmem_ldmax64(t_s, s, gmax[0]);
+          else tmem_ldmax16(t_s + 16 * q, s + 16 * q, gmax[q]);
+        }
+      }
       tmem_ld_wait();
       if constexpr (L::kPInSmem) {
         // S is in registers: the issuer may compute the next tile's S into the same columns
@@ -589,20 +614,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nvalid = min(64, p.Skv - 128 * j - 64 * h);  // may be <= 0 for the upper half
       const bool tail = nvalid < 64;
       if (tail) {
+        // the last KV tile: columns past Skv hold the products with TMA's zero fill; mask them (and
+        // take the loads' maxima over the valid columns only)
 #pragma unroll
         for (int k = 0; k < 64; ++k)
           if (k >= nvalid) s[k] = -INFINITY;
+        if constexpr (kLdMax) {
+#pragma unroll
+          for (int q = 0; q < kLoads; ++q) {
+            float m = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < kCols; ++k) m = fmaxf(m, s[kCols * q + k]);
+            gmax[q] = m;
+          }
+        }
       }
       float mh;  // this half's max of the weighted logits
       if constexpr (kQKScaled && KB == 1) {
         // per-column scales: multiply S by them first (64 values, not held across the wait for S)
         const int e = j & 3;
-        bool ks_ok = mbar_wait_bounded(&bars->ks_full[e], (j >> 2) & 1, budget, abort_flag);
-        ks_ok = __all_sync(0xffffffffu, ks_ok);
-        if (!ks_ok) {
-          if (lane == 0) record_timeout(p, bars);
-          ok = false;
-        }
         const float2* ks2 = reinterpret_cast<const float2*>(s_ks + e * 128 + 64 * h);  // this half's scales
 #pragma unroll
         for (int k = 0; k < 32; ++k) s2[k] = __fmul2_rn(s2[k], ks2[k]);
@@ -612,12 +642,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&bars->ks_empty[e]);
       } else if constexpr (kQKScaled) {
         const int e = j & 3;
-        bool ks_ok = mbar_wait_bounded(&bars->ks_full[e], (j >> 2) & 1, budget, abort_flag);
-        ks_ok = __all_sync(0xffffffffu, ks_ok);
-        if (!ks_ok) {
-          if (lane == 0) record_timeout(p, bars);
-          ok = false;
-        }
         const float4* ks4 = reinterpret_cast<const float4*>(s_ks + e * 128 + (64 / KB) * h);  // this half's scales
 #pragma unroll
         for (int q4 = 0; q4 < kGroups / 4; ++q4) {
@@ -629,13 +653,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mh = -INFINITY;
 #pragma unroll
-        for (int q = 0; q < kGroups; ++q)
-          mh = fmaxf(mh, groupmax<KB>(s + q * KB) * wg[q]);  // a NaN from -inf * 0 is ignored
+        for (int q = 0; q < kGroups; ++q) {
+          const float gm = kLdMax ? gmax[q] : groupmax<KB>(s + q * KB);
+          mh = fmaxf(mh, gm * wg[q]);  // a NaN from -inf * 0 is ignored
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->ks_empty[e]);
       } else {
         wg[0] = c;
-        mh = rowmax64(s) * c;  // -inf when this half has no valid column
+        mh = gmax[0] * c;  // -inf when this half has no valid column
       }
       // Publish this half's max; one barrier over both halves of the tile then orders the exchange
       // and, with Skip-Softmax, carries the vote. A row's full max is below the threshold exactly

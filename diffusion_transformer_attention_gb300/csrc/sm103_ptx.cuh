@@ -72,6 +72,18 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// Wait for two phases (of two barriers). Both are first tested back to back, so when both have
+// completed (the common case) the two tests' latencies overlap; otherwise each is waited for in
+// turn, bounded as above.
+__device__ __forceinline__ bool mbar_wait2_bounded(uint64_t* bar_a, uint32_t parity_a, uint64_t* bar_b,
+                                                   uint32_t parity_b, uint64_t budget_ns, const volatile int* abort) {
+  const bool a = mbar_try_wait(bar_a, parity_a);
+  const bool b = mbar_try_wait(bar_b, parity_b);
+  if (a && b) return true;
+  return (a || mbar_wait_bounded(bar_a, parity_a, budget_ns, abort)) &&
+         (b || mbar_wait_bounded(bar_b, parity_b, budget_ns, abort));
+}
+
 // ---------------------------------------------------------------- TMA (bulk tensor copies)
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -357,6 +369,45 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
         "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
 }
+// tcgen05.ld.red (sm_103a): the same 32x32b load of N consecutive columns, which also returns the
+// maximum of the N values each thread loads (its row's max over those columns; NaN operands are
+// ignored). Both the values and the max are ready after tmem_ld_wait().
+#define DITATTN_R4(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3])
+__device__ __forceinline__ void tmem_ldmax32(uint32_t taddr, float* v, float& m) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, %32, [%33];"
+      : DITATTN_R4(0), DITATTN_R4(4), DITATTN_R4(8), DITATTN_R4(12), DITATTN_R4(16), DITATTN_R4(20),
+        DITATTN_R4(24), DITATTN_R4(28), "=f"(m)
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ldmax64(uint32_t taddr, float* v, float& m) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x64.max.f32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,"
+      "%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, %64, [%65];"
+      : DITATTN_R4(0), DITATTN_R4(4), DITATTN_R4(8), DITATTN_R4(12), DITATTN_R4(16), DITATTN_R4(20),
+        DITATTN_R4(24), DITATTN_R4(28), DITATTN_R4(32), DITATTN_R4(36), DITATTN_R4(40), DITATTN_R4(44),
+        DITATTN_R4(48), DITATTN_R4(52), DITATTN_R4(56), DITATTN_R4(60), "=f"(m)
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ldmax16(uint32_t taddr, float* v, float& m) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x16.max.f32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15},"
+      " %16, [%17];"
+      : DITATTN_R4(0), DITATTN_R4(4), DITATTN_R4(8), DITATTN_R4(12), "=f"(m)
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ldmax4(uint32_t taddr, float* v, float& m) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  asm volatile("tcgen05.ld.red.sync.aligned.32x32b.x4.max.f32 {%0,%1,%2,%3}, %4, [%5];"
+               : DITATTN_R4(0), "=f"(m)
+               : "r"(taddr));
+}
+#undef DITATTN_R4
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
