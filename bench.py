@@ -427,18 +427,17 @@ def run_recipe(dit, name, steps, warmup, world, stream, peak, hbm_gbs):
 
 def skip_sweep(dit, q, k, v, out, counts, w, factors, steps, warmup, world, stream, dense_ms, *, mode, dt, qb, kb):
     """Time one Skip-Softmax recipe over the threshold factors on the video inputs; returns compact
-    lists (factor, skipped fraction, ms, speedup against dense BF16 on the same inputs)."""
+    lists, one entry per factor: skipped fraction, ms, speedup against dense BF16 on the same inputs."""
     nqt, nkt = math.ceil(w.Sq / 128), math.ceil(w.Skv / 128)
     need = dit.dit_attn_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, mode & ~dit.MODE_SKIP, dt, qb, kb)
     ws = torch.empty(max(1, need), dtype=torch.uint8, device="cuda") if need > 0 else None
-    res = {"f": [], "skip": [], "ms": [], "x": []}
+    res = {"skip": [], "ms": [], "x": []}
     for factor in factors:
         def step():
             dit.dit_attn_fwd(q, k, v, out, mode=mode, qk_dtype=dt, q_block=qb, k_block=kb,
                              threshold_scale_factor=factor, workspace=ws, skip_counts=counts, stream=stream)
         ms = max_over_ranks(time_steps(step, steps, warmup, world, stream), world) / steps
         frac = float(counts.sum().item()) / (w.B * w.Hq * nqt * nkt)
-        res["f"].append(factor)
         res["skip"].append(_r(frac, 4))
         res["ms"].append(_r(ms, 2))
         res["x"].append(_r(dense_ms / ms))
@@ -474,10 +473,11 @@ def run_modes(dit, steps, warmup, world, stream, peak16, hbm_gbs, cpu: bool):
     # Q/K formats whose BMM1 runs at the FP8 (or FP4) rate: a skipped tile still costs its BMM1, so the
     # INT8 codes' 16-bit BMM1 caps the INT8 curve's speedup
     short = (0.0, 2.0, 50.0, 3200.0)
-    res["video_fp8_rate_bmm1"] = {
+    res["video_fp8_rate_bmm1"] = {"f": list(short)}
+    res["video_fp8_rate_bmm1"].update({
         label: skip_sweep(dit, q, k, v, out, counts, w, short, s, wu, world, stream, dense_ms, mode=sk, dt=dt, qb=qb, kb=kb)
         for label, dt, qb, kb in [("sage_fp8_1_16", "fp8_e4m3", 1, 16), ("mxfp8", "mxfp8", 0, 0),
-                                  ("nvfp4", "nvfp4", 0, 0)]}
+                                  ("nvfp4", "nvfp4", 0, 0)]})
     curve = skip_sweep(dit, q, k, v, out, counts, w, w.factors, s, wu, world, stream, dense_ms, mode=sk,
                        dt=w.qk_dtype, qb=w.q_block, kb=w.k_block)
     bf16 = skip_sweep(dit, q, k, v, out, counts, w, w.factors, s, wu, world, stream, dense_ms,
@@ -490,7 +490,7 @@ def run_modes(dit, steps, warmup, world, stream, peak16, hbm_gbs, cpu: bool):
         if cpu:
             res[label]["cpu"] = oracle_config_baseline(workloads.WORKLOADS[name], budget_s=4.0)
     vid = {"dense_bf16_ms": _r(dense_ms), "dense_bf16_tflops": _r(w.dense_equiv_flop / (dense_ms * 1e-3) / 1e12, 1),
-           "bf16_skip": bf16, "sage_int8_1_16_skip": curve}
+           "f": list(w.factors), "bf16_skip": bf16, "sage_int8_1_16_skip": curve}
     if cpu:
         vid["cpu"] = oracle_config_baseline(w, budget_s=4.0, factor=50.0)
     res["video_skip_int8_75600"] = vid

@@ -74,7 +74,8 @@ WORKLOADS = {
     "dit_nvfp4_32k": Workload("dit_nvfp4_32k", 1, 40, 40, 32768, 32768, kind="koffset", mode="nvfp4",
                               qk_dtype="nvfp4", q_block=0, k_block=0),
     "video_skip_int8_75600": Workload("video_skip_int8_75600", 1, 40, 40, 75600, 75600, kind="video", mode="sage",
-                                      qk_dtype="int8", q_block=1, k_block=16, factors=(0.0, 50.0, 200.0, 800.0, 3200.0),
+                                      qk_dtype="int8", q_block=1, k_block=16,
+                                      factors=(0.0, 1.0, 2.0, 5.0, 20.0, 50.0, 200.0, 800.0, 3200.0),
                                       grid=VIDEO_GRID),
 }
 
