@@ -32,6 +32,18 @@ __device__ __forceinline__ float rowmax64(const float* s) {
   return max3f(max3f(a[0], a[1], a[2]), max3f(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
 }
 
+// Max of 128 values with eight independent accumulators.
+__device__ __forceinline__ float rowmax128(const float* s) {
+  float a[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) a[j] = fmaxf(s[2 * j], s[2 * j + 1]);
+#pragma unroll
+  for (int k = 16; k < 128; k += 16)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) a[j] = max3f(a[j], s[k + 2 * j], s[k + 2 * j + 1]);
+  return max3f(max3f(a[0], a[1], a[2]), max3f(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
+}
+
 // Max of one K-scale group of G consecutive columns.
 template <int G>
 __device__ __forceinline__ float groupmax(const float* s) {

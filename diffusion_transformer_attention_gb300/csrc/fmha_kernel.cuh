@@ -8,7 +8,7 @@
 // "SAGE + Skip-Softmax -- API Design & Test Plan", Part 1 §4: bmm1/bmm2 scales and
 // threshold = factor / seqlen). The pages give no kernel design; this one is built for GB300:
 //
-// CTA = 2 query tiles of 128 rows of one (batch, query head); 640 threads in 20 warps.
+// CTA = 2 query tiles of 128 rows of one (batch, query head); 640 or 384 threads (Parts below).
 //   warp 0       TMA producer: Q0, Q1 once, then K_j / V_j into two K and two V buffers.
 //   warps 1, 2   MMA issuers, one per Q tile (one elected lane each): BMM1 S_i = Q_i K_j^T (SS),
 //                BMM2 O_i += P_i V_j (V is MN-major, so no transpose). Warp 2 also allocates the 512
@@ -16,12 +16,13 @@
 //   warp 3       stages the V scales (E4M3 V) and, in SAGE, the K-block scales of each KV tile; in
 //                MXFP8 and NVFP4 the block scales of Q and of each K tile, which the issuers copy
 //                into tensor memory for the block-scaled BMM1.
-//   warps 4-19   four softmax warpgroups: Q tile i = g / 2 and column half h = g % 2 for group g.
-//                A thread owns one row (= TMEM lane) and 64 of its 128 columns; the two halves
-//                of a row exchange partial maxima through shared memory. Halving the columns per
-//                thread halves the softmax latency, which is what bounds the pipeline.
-// Dense (BF16 P): each half writes its packed P over the first columns of its own half of S, and
-// BMM2 reads P from tensor memory (TS). The issuer runs O_i += P_i(j-1) V_{j-1}, S_i = Q_i K_j^T as
+//   warps 4-     softmax warpgroups: two per Q tile (a thread owns one row = TMEM lane and 64 of its
+//                128 columns; the halves exchange their maxima through shared memory, and one
+//                named barrier per tile orders that exchange and carries the Skip-Softmax vote), or
+//                one per Q tile (a thread owns the whole row: no exchange, and the per-tile costs
+//                are paid once per 128 scores). Which one is a property of the recipe (Parts).
+// Dense (BF16 P): each softmax part writes its packed P over the first columns of its own part of
+// S, and BMM2 reads P from tensor memory (TS). The issuer runs O_i += P_i(j-1) V_{j-1}, S_i = Q_i K_j^T as
 // soon as P_i(j-1) is ready, so while one tile's softmax turns S into P, the tensor cores work on
 // the other tile.
 // E4M3 P (SAGE, QK16PV8, MXFP8, NVFP4; 16 KB per tile): P goes to a shared-memory buffer and BMM2 is
@@ -58,10 +59,22 @@
 namespace ditattn {
 namespace {
 
-constexpr int kThreads = 640;
-constexpr int kLaunchRegs = 96;                  // 65536 / 640, rounded down to a multiple of 8
-constexpr int kRegsWG0 = 64, kRegsSoftmax = 104;  // 128 * 64 + 512 * 104 == 640 * 96
-static_assert(128 * kRegsWG0 + 512 * kRegsSoftmax <= kThreads * kLaunchRegs, "register hand-over must fit");
+// Softmax warpgroups per Q tile and the launch shape they imply. Two (each thread holds 64 of a row's
+// 128 columns, the two halves exchange the row max through shared memory) for dense BF16 and SAGE
+// INT8 / FP8; one (each thread holds the whole row) for the E4M3-P recipes whose softmax has no
+// K-block scales (QK16PV8, MXFP8, NVFP4). Each measured faster for its recipes on GB300.
+template <int QKF, int PVF>
+struct Parts {
+  static constexpr int kNH = (PVF == PV_E4M3 && (QKF == QK_BF16 || QKF == QK_MXF8 || QKF == QK_NVF4)) ? 1 : 2;
+  static constexpr int kThreads = 128 + 256 * kNH;
+  // launched at 65536 / kThreads registers (rounded down to a multiple of 8); warpgroup 0 (producer,
+  // MMA issuers, scale stager) hands registers to the softmax warpgroups
+  static constexpr int kLaunchRegs = kNH == 1 ? 168 : 96;
+  static constexpr int kRegsWG0 = kNH == 1 ? 72 : 64;
+  static constexpr int kRegsSoftmax = kNH == 1 ? 216 : 104;
+  static_assert(128 * kRegsWG0 + 256 * kNH * kRegsSoftmax <= kThreads * kLaunchRegs, "register hand-over must fit");
+  static_assert(kThreads * kLaunchRegs <= 65536, "one CTA per SM");
+};
 constexpr int kSlots = 4;  // ring of K/V tiles: K_j in slot 2j mod 4, V_j in slot 2j+1 mod 4
 
 // Shared-memory layout for operand formats QKF / PVF. Two Q buffers of 32 KB (also the output
@@ -109,6 +122,15 @@ struct Bars {
   uint32_t tmem_base;
   int abort_flag;
   int skip_flag[2][2];  // [Q tile][KV tile parity]: 1 when that KV tile was skipped
+  // SAGE with Skip-Softmax hands P of odd KV tiles to the issuer through p_full_odd (even tiles through
+  // p_full): the softmax waits there only for the previous kept tile's BMM2, so over skipped tiles it
+  // can run ahead of the issuer, and with one barrier it could complete tile j (skipped) and tile j + 1
+  // (kept) while the issuer still waited for V_j; the issuer's parity test would then wait for tile
+  // j + 2, which needs a BMM1 only the issuer can issue. With a barrier per KV-tile parity a barrier's
+  // next phase is tile j + 2 itself, whose S needs that BMM1, so no phase completes twice before the
+  // issuer tests it. (Every other path waits for the previous BMM2, or has the issuer's order, before
+  // the next P, so one barrier per tile serves it.)
+  uint64_t p_full_odd[2];
 };
 static_assert(sizeof(Bars) <= 512, "barrier block too large");
 
@@ -122,7 +144,7 @@ __device__ __forceinline__ void record_timeout(const FmhaParams& p, Bars* bars) 
 // code is unaffected): the producer issues no copy, so nothing is in flight when the other roles'
 // bounded waits run out and they leave.
 template <int QKF, int PVF, int KB, bool SKIP, bool WITHHOLD = false>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Parts<QKF, PVF>::kThreads, 1)
     fmha_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                     const FmhaParams p) {
@@ -155,12 +177,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kIdesc2 = (PVF == PV_BF16) ? make_idesc(1, 1, 0, 1, 128, 128) : make_idesc(0, 0, 0, 1, 128, 128);
 
   using L = SmemLayout<QKF, PVF>;
+  using P = Parts<QKF, PVF>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + L::kBarOff);
   float* s_ks = reinterpret_cast<float*>(smem + L::kKsOff);
   float* s_vs = reinterpret_cast<float*>(smem + L::kVsOff);
   const volatile int* abort_flag = &bars->abort_flag;
+  // the barrier that hands P of KV tile j of Q tile i to the issuer, and the parity of that phase
+  auto p_full_bar = [&](int i, int j) { return (kLazyPv && (j & 1)) ? &bars->p_full_odd[i] : &bars->p_full[i]; };
+  auto p_full_par = [&](int j) -> uint32_t { return kLazyPv ? (uint32_t)((j >> 1) & 1) : (uint32_t)(j & 1); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hq = blockIdx.y, b = blockIdx.z;
@@ -179,11 +205,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->kv_full[s], 1);
       mbar_init(&bars->kv_empty[s], 2);  // one commit from each MMA issuer
       mbar_init(&bars->ks_full[s], 32);
-      mbar_init(&bars->ks_empty[s], kBS ? 2 : 16);  // SAGE: one arrival per softmax warp; block-scaled: per issuer
+      mbar_init(&bars->ks_empty[s], kBS ? 2 : 8 * P::kNH);  // SAGE: one arrival per softmax warp; block-scaled: per issuer
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->p_full[i], 8);     // one arrival per softmax warp of the tile
+      mbar_init(&bars->p_full[i], 4 * P::kNH);  // one arrival per softmax warp of the tile
+      if constexpr (kLazyPv) mbar_init(&bars->p_full_odd[i], 4 * P::kNH);
       mbar_init(&bars->o_full[i], 1);
     }
     mbar_init(&bars->vs_full, 32);
@@ -191,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->drain[0], 1);
     mbar_init(&bars->drain[1], 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars->s_free[i], 8);  // one arrival per softmax warp of the tile
+      mbar_init(&bars->s_free[i], 4 * P::kNH);  // one arrival per softmax warp of the tile
       mbar_init(&bars->o_done[i], 1);
     }
     bars->abort_flag = 0;
@@ -210,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Launched at 96 registers per thread: warpgroup 0 (producer, MMA, allocator, scale stager)
   // hands registers to the four softmax warpgroups, which hold 64 scores per thread.
   if (warp < 4) {
-  regs_dec<kRegsWG0>();
+  regs_dec<P::kRegsWG0>();
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && !WITHHOLD) {
@@ -366,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           bmm1(j + 1);
         }
         const int tv = 2 * j + 1;
-        ok = wait(&bars->kv_full[tv & 3], (tv >> 2) & 1) && wait(&bars->p_full[i], j & 1);
+        ok = wait(&bars->kv_full[tv & 3], (tv >> 2) & 1) && wait(p_full_bar(i, j), p_full_par(j));
         if (!ok) break;
         tc_fence_after();
         const bool skipped = SKIP && skip_flag[i][kLazyPv ? (j & 1) : 0] != 0;
@@ -391,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
         }
         if (j >= 1) {
-          ok = wait(&bars->kv_full[tv & 3], (tv >> 2) & 1) && wait(&bars->p_full[i], (j - 1) & 1);
+          ok = wait(&bars->kv_full[tv & 3], (tv >> 2) & 1) && wait(p_full_bar(i, j - 1), p_full_par(j - 1));
           if (!ok) break;
         }
         tc_fence_after();
@@ -400,8 +427,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kK2Steps; ++kk) {
             const uint32_t off = (kPVBytes == 2) ? kk * 2048 : kk * 4096;
-            // K columns 0..63 come from the P piece in S columns 0.., 64..127 from S columns 64..
-            const uint32_t pa = d_s + ((kk < kK2Steps / 2) ? 8 * kk : 64 + 8 * (kk - kK2Steps / 2));
+            // P (bf16, two values per column) sits in the first 64 / kNH columns of each softmax part's
+            // region of S (part h at columns 128 h / kNH): K step kk reads 8 columns
+            constexpr int kPerPart = kK2Steps / P::kNH;
+            const uint32_t pa = d_s + (kk / kPerPart) * (128 / P::kNH) + 8 * (kk % kPerPart);
             mma_ts_if<kMma2Kind>(leader, d_o, pa, bv + (off >> 4), kIdesc2, (j > 1 || kk > 0) ? 1u : 0u);
           }
         }
@@ -531,343 +560,715 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   } else {
-    // ------------------------------------------------------------ softmax groups
-    regs_inc<kRegsSoftmax>();
-    const int g = (warp - 4) >> 2;                 // softmax warpgroup 0..3
-    const int i = g >> 1;                          // Q tile within the CTA
-    const int h = g & 1;                           // column half: S/O columns 64h .. 64h+63
-    const int r = ((warp & 3) << 5) + lane;        // row within the tile == TMEM lane
-    const uint32_t lane_base = (uint32_t)((warp & 3) << 5) << 16;
-    const uint32_t t_s = tbase + lane_base + kColS1 * i + 64 * h;
-    const uint32_t t_o = tbase + lane_base + kColO0 + 128 * i + 64 * h;
-    const int qrow = q0 + 128 * i + r;
-    const bool row_valid = qrow < p.Sq;
-    const uint32_t tile_bar = 1 + i;               // the 256 threads of this Q tile
-    const uint32_t group_bar = 3 + g;              // the 128 threads of this warpgroup
-    float* xmax = reinterpret_cast<float*>(smem + L::kXmaxOff);
-    float* xl = reinterpret_cast<float*>(smem + L::kXlOff);
-    float c = p.c_scale;
-    if constexpr (kNV) c = c / (__ldg(p.q_gs) * __ldg(p.k_gs));  // BMM1 carries both tensor scales
-    if constexpr (kQKScaled) {
-      const float qs = row_valid ? __ldg(p.q_scale + ((size_t)b * p.Hq + hq) * p.nqb + qrow / p.q_block) : 0.0f;
-      c = qs * p.c_scale;
-    }
-    float m_ex = -INFINITY, m_ref = -INFINITY, l = 0.0f;
-    int nskip = 0;
-    bool ok = true;
-    volatile int (*skip_flag)[2] = bars->skip_flag;
-    int n_pv = 0;  // kLazyPv: BMM2s issued so far for this tile (o_done completes once per BMM2)
-    // Exponent weight per column group (log2 units): the row constant c, times the K block scale in
-    // SAGE. KB >= 4 folds the block scale into the weight; KB == 1 multiplies first.
-    constexpr int kGroups = (kQKScaled && KB >= 4) ? 64 / KB : 1;
-
-    for (int j = 0; j < nt; ++j) {
-      float wg[kGroups];
-      if (ok) {
-        // S_i(j), and in SAGE the K-block scales of tile j (both tested at once, so the two waits'
-        // latencies overlap)
-        if constexpr (kQKScaled) {
-          ok = mbar_wait2_bounded(&bars->s_full[i], j & 1, &bars->ks_full[j & 3], (j >> 2) & 1, budget, abort_flag);
-        } else {
-          ok = mbar_wait_bounded(&bars->s_full[i], j & 1, budget, abort_flag);
-        }
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok && lane == 0) record_timeout(p, bars);
+    if constexpr (P::kNH == 2) {
+      // ------------------------------------------------------------ softmax groups
+      regs_inc<P::kRegsSoftmax>();
+      const int g = (warp - 4) >> 2;                 // softmax warpgroup 0..3
+      const int i = g >> 1;                          // Q tile within the CTA
+      const int h = g & 1;                           // column half: S/O columns 64h .. 64h+63
+      const int r = ((warp & 3) << 5) + lane;        // row within the tile == TMEM lane
+      const uint32_t lane_base = (uint32_t)((warp & 3) << 5) << 16;
+      const uint32_t t_s = tbase + lane_base + kColS1 * i + 64 * h;
+      const uint32_t t_o = tbase + lane_base + kColO0 + 128 * i + 64 * h;
+      const int qrow = q0 + 128 * i + r;
+      const bool row_valid = qrow < p.Sq;
+      const uint32_t tile_bar = 1 + i;               // the 256 threads of this Q tile
+      const uint32_t group_bar = 3 + g;              // the 128 threads of this warpgroup
+      float* xmax = reinterpret_cast<float*>(smem + L::kXmaxOff);
+      float* xl = reinterpret_cast<float*>(smem + L::kXlOff);
+      float c = p.c_scale;
+      if constexpr (kNV) c = c / (__ldg(p.q_gs) * __ldg(p.k_gs));  // BMM1 carries both tensor scales
+      if constexpr (kQKScaled) {
+        const float qs = row_valid ? __ldg(p.q_scale + ((size_t)b * p.Hq + hq) * p.nqb + qrow / p.q_block) : 0.0f;
+        c = qs * p.c_scale;
       }
-      if (!ok) {
-        // keep this tile's named barrier in step with the peer half
+      float m_ex = -INFINITY, m_ref = -INFINITY, l = 0.0f;
+      int nskip = 0;
+      bool ok = true;
+      volatile int (*skip_flag)[2] = bars->skip_flag;
+      int n_pv = 0;  // kLazyPv: BMM2s issued so far for this tile (o_done completes once per BMM2)
+      // Exponent weight per column group (log2 units): the row constant c, times the K block scale in
+      // SAGE. KB >= 4 folds the block scale into the weight; KB == 1 multiplies first.
+      constexpr int kGroups = (kQKScaled && KB >= 4) ? 64 / KB : 1;
+
+      for (int j = 0; j < nt; ++j) {
+        float wg[kGroups];
+        if (ok) {
+          // S_i(j), and in SAGE the K-block scales of tile j (both tested at once, so the two waits'
+          // latencies overlap)
+          if constexpr (kQKScaled) {
+            ok = mbar_wait2_bounded(&bars->s_full[i], j & 1, &bars->ks_full[j & 3], (j >> 2) & 1, budget, abort_flag);
+          } else {
+            ok = mbar_wait_bounded(&bars->s_full[i], j & 1, budget, abort_flag);
+          }
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok && lane == 0) record_timeout(p, bars);
+        }
+        if (!ok) {
+          // keep this tile's named barrier in step with the peer half
+          if (SKIP && j > 0) {
+            named_bar_and(tile_bar, 256, true);
+          } else {
+            named_bar_sync(tile_bar, 256);
+          }
+          continue;
+        }
+        tc_fence_after();
+        float2 s2[32];
+        float* s = reinterpret_cast<float*>(s2);
+        // S into registers. tcgen05.ld.red also returns each load's max over its columns: one load per
+        // K block of 16 tokens in SAGE (the block's max, weighted by its scale below), one load of all
+        // 64 columns without K-block scales. K blocks of 4 or 1 token use plain loads and take their
+        // maxima below (sixteen 4-column loads measured slower than two plain ones and the max tree).
+        constexpr bool kLdMax = !kQKScaled || KB == 16;
+        constexpr int kLoads = (kQKScaled && KB == 16) ? 4 : 1;
+        constexpr int kCols = 64 / kLoads;
+        float gmax[kLoads];
+        if constexpr (!kLdMax) {
+          tmem_ld32(t_s, s);
+          tmem_ld32(t_s + 32, s + 32);
+        } else {
+#pragma unroll
+          for (int q = 0; q < kLoads; ++q) {
+            if constexpr (kCols == 64) tmem_ldmax64(t_s, s, gmax[0]);
+            else tmem_ldmax16(t_s + 16 * q, s + 16 * q, gmax[q]);
+          }
+        }
+        tmem_ld_wait();
+        if constexpr (L::kPInSmem) {
+          // S is in registers: the issuer may compute the next tile's S into the same columns
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->s_free[i]);
+        }
+        const int nvalid = min(64, p.Skv - 128 * j - 64 * h);  // may be <= 0 for the upper half
+        const bool tail = nvalid < 64;
+        if (tail) {
+          // the last KV tile: columns past Skv hold the products with TMA's zero fill; mask them (and
+          // take the loads' maxima over the valid columns only)
+#pragma unroll
+          for (int k = 0; k < 64; ++k)
+            if (k >= nvalid) s[k] = -INFINITY;
+          if constexpr (kLdMax) {
+#pragma unroll
+            for (int q = 0; q < kLoads; ++q) {
+              float m = -INFINITY;
+#pragma unroll
+              for (int k = 0; k < kCols; ++k) m = fmaxf(m, s[kCols * q + k]);
+              gmax[q] = m;
+            }
+          }
+        }
+        float mh;  // this half's max of the weighted logits
+        if constexpr (kQKScaled && KB == 1) {
+          // per-column scales: multiply S by them first (64 values, not held across the wait for S)
+          const int e = j & 3;
+          const float2* ks2 = reinterpret_cast<const float2*>(s_ks + e * 128 + 64 * h);  // this half's scales
+#pragma unroll
+          for (int k = 0; k < 32; ++k) s2[k] = __fmul2_rn(s2[k], ks2[k]);
+          wg[0] = c;
+          mh = rowmax64(s) * c;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->ks_empty[e]);
+        } else if constexpr (kQKScaled) {
+          const int e = j & 3;
+          const float4* ks4 = reinterpret_cast<const float4*>(s_ks + e * 128 + (64 / KB) * h);  // this half's scales
+#pragma unroll
+          for (int q4 = 0; q4 < kGroups / 4; ++q4) {
+            const float4 k4 = ks4[q4];
+            wg[4 * q4 + 0] = k4.x * c;
+            wg[4 * q4 + 1] = k4.y * c;
+            wg[4 * q4 + 2] = k4.z * c;
+            wg[4 * q4 + 3] = k4.w * c;
+          }
+          mh = -INFINITY;
+#pragma unroll
+          for (int q = 0; q < kGroups; ++q) {
+            const float gm = kLdMax ? gmax[q] : groupmax<KB>(s + q * KB);
+            mh = fmaxf(mh, gm * wg[q]);  // a NaN from -inf * 0 is ignored
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->ks_empty[e]);
+        } else {
+          wg[0] = c;
+          mh = gmax[0] * c;  // -inf when this half has no valid column
+        }
+        // Publish this half's max; one barrier over both halves of the tile then orders the exchange
+        // and, with Skip-Softmax, carries the vote. A row's full max is below the threshold exactly
+        // when both halves' maxima are, so each half votes on its own max.
+        xmax[((i * 2 + h) * 2 + (j & 1)) * 128 + r] = mh;
+        bool skip_tile = false;
         if (SKIP && j > 0) {
-          named_bar_and(tile_bar, 256, true);
+          const bool vote = !row_valid || !ok || (mh - m_ex < p.log2_thr);
+          skip_tile = named_bar_and(tile_bar, 256, vote);
         } else {
           named_bar_sync(tile_bar, 256);
         }
-        continue;
-      }
-      tc_fence_after();
-      float2 s2[32];
-      float* s = reinterpret_cast<float*>(s2);
-      // S into registers. tcgen05.ld.red also returns each load's max over its columns: one load per
-      // K block of 16 tokens in SAGE (the block's max, weighted by its scale below), one load of all
-      // 64 columns without K-block scales. K blocks of 4 or 1 token use plain loads and take their
-      // maxima below (sixteen 4-column loads measured slower than two plain ones and the max tree).
-      constexpr bool kLdMax = !kQKScaled || KB == 16;
-      constexpr int kLoads = (kQKScaled && KB == 16) ? 4 : 1;
-      constexpr int kCols = 64 / kLoads;
-      float gmax[kLoads];
-      if constexpr (!kLdMax) {
-        tmem_ld32(t_s, s);
-        tmem_ld32(t_s + 32, s + 32);
-      } else {
-#pragma unroll
-        for (int q = 0; q < kLoads; ++q) {
-          if constexpr (kCols == 64) tmem_ldmax64(t_s, s, gmax[0]);
-          else tmem_ldmax16(t_s + 16 * q, s + 16 * q, gmax[q]);
-        }
-      }
-      tmem_ld_wait();
-      if constexpr (L::kPInSmem) {
-        // S is in registers: the issuer may compute the next tile's S into the same columns
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->s_free[i]);
-      }
-      const int nvalid = min(64, p.Skv - 128 * j - 64 * h);  // may be <= 0 for the upper half
-      const bool tail = nvalid < 64;
-      if (tail) {
-        // the last KV tile: columns past Skv hold the products with TMA's zero fill; mask them (and
-        // take the loads' maxima over the valid columns only)
-#pragma unroll
-        for (int k = 0; k < 64; ++k)
-          if (k >= nvalid) s[k] = -INFINITY;
-        if constexpr (kLdMax) {
-#pragma unroll
-          for (int q = 0; q < kLoads; ++q) {
-            float m = -INFINITY;
-#pragma unroll
-            for (int k = 0; k < kCols; ++k) m = fmaxf(m, s[kCols * q + k]);
-            gmax[q] = m;
+        if constexpr (L::kPInSmem) {
+          // The previous BMM2 must be complete before P's buffer, O or the skip flag change.
+          // kLazyPv: o_done completes once per BMM2, so the wait before the n-th P is on phase n - 1:
+          // that phase is the only one outstanding (the one before was waited for, the next needs this
+          // P), so its parity is unambiguous; a skipped tile writes neither P nor O and does not wait.
+          // Otherwise o_done completes once per KV tile and is waited for on every tile, which keeps
+          // the waits in step with its phases.
+          if constexpr (kLazyPv) {
+            if (!skip_tile && n_pv > 0 && ok) {
+              ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->o_done[i], (n_pv - 1) & 1, budget, abort_flag));
+              if (!ok && lane == 0) record_timeout(p, bars);
+            }
+          } else {
+            if (j > 0 && ok) {
+              ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->o_done[i], (j - 1) & 1, budget, abort_flag));
+              if (!ok && lane == 0) record_timeout(p, bars);
+            }
           }
+          if (!ok) continue;
         }
-      }
-      float mh;  // this half's max of the weighted logits
-      if constexpr (kQKScaled && KB == 1) {
-        // per-column scales: multiply S by them first (64 values, not held across the wait for S)
-        const int e = j & 3;
-        const float2* ks2 = reinterpret_cast<const float2*>(s_ks + e * 128 + 64 * h);  // this half's scales
-#pragma unroll
-        for (int k = 0; k < 32; ++k) s2[k] = __fmul2_rn(s2[k], ks2[k]);
-        wg[0] = c;
-        mh = rowmax64(s) * c;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->ks_empty[e]);
-      } else if constexpr (kQKScaled) {
-        const int e = j & 3;
-        const float4* ks4 = reinterpret_cast<const float4*>(s_ks + e * 128 + (64 / KB) * h);  // this half's scales
-#pragma unroll
-        for (int q4 = 0; q4 < kGroups / 4; ++q4) {
-          const float4 k4 = ks4[q4];
-          wg[4 * q4 + 0] = k4.x * c;
-          wg[4 * q4 + 1] = k4.y * c;
-          wg[4 * q4 + 2] = k4.z * c;
-          wg[4 * q4 + 3] = k4.w * c;
+        if (skip_tile) {
+          // kLazyPv: the flag has a slot per KV-tile parity; the issuer reads tile j's slot before it
+          // issues the BMM1 of tile j + 2, so this tile's write cannot overtake that read. Otherwise the
+          // wait on the previous BMM2 (or, with TMEM P, the issuer's order) already orders them: one slot.
+          ++nskip;
+          if (r == 0 && h == 0) skip_flag[i][kLazyPv ? (j & 1) : 0] = 1;
+          // TMEM P: the issuer's next BMM1 overwrites the S just loaded (with P in shared memory, S
+          // was already released after its load)
+          if constexpr (!kLazyPv) tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(p_full_bar(i, j));
+          continue;
         }
-        mh = -INFINITY;
-#pragma unroll
-        for (int q = 0; q < kGroups; ++q) {
-          const float gm = kLdMax ? gmax[q] : groupmax<KB>(s + q * KB);
-          mh = fmaxf(mh, gm * wg[q]);  // a NaN from -inf * 0 is ignored
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->ks_empty[e]);
-      } else {
-        wg[0] = c;
-        mh = gmax[0] * c;  // -inf when this half has no valid column
-      }
-      // Publish this half's max; one barrier over both halves of the tile then orders the exchange
-      // and, with Skip-Softmax, carries the vote. A row's full max is below the threshold exactly
-      // when both halves' maxima are, so each half votes on its own max.
-      xmax[((i * 2 + h) * 2 + (j & 1)) * 128 + r] = mh;
-      bool skip_tile = false;
-      if (SKIP && j > 0) {
-        const bool vote = !row_valid || !ok || (mh - m_ex < p.log2_thr);
-        skip_tile = named_bar_and(tile_bar, 256, vote);
-      } else {
-        named_bar_sync(tile_bar, 256);
-      }
-      if constexpr (L::kPInSmem) {
-        // The previous BMM2 must be complete before P's buffer, O or the skip flag change.
-        // kLazyPv: o_done completes once per BMM2, so the wait before the n-th P is on phase n - 1:
-        // that phase is the only one outstanding (the one before was waited for, the next needs this
-        // P), so its parity is unambiguous; a skipped tile writes neither P nor O and does not wait.
-        // Otherwise o_done completes once per KV tile and is waited for on every tile, which keeps
-        // the waits in step with its phases.
-        if constexpr (kLazyPv) {
-          if (!skip_tile && n_pv > 0 && ok) {
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->o_done[i], (n_pv - 1) & 1, budget, abort_flag));
-            if (!ok && lane == 0) record_timeout(p, bars);
-          }
-        } else {
-          if (j > 0 && ok) {
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->o_done[i], (j - 1) & 1, budget, abort_flag));
-            if (!ok && lane == 0) record_timeout(p, bars);
-          }
-        }
+        const float mo = xmax[((i * 2 + (h ^ 1)) * 2 + (j & 1)) * 128 + r];
+        const float mt = fmaxf(mh, mo);  // identical on both halves: max is exact
         if (!ok) continue;
-      }
-      if (skip_tile) {
-        // kLazyPv: the flag has a slot per KV-tile parity; the issuer reads tile j's slot before it
-        // issues the BMM1 of tile j + 2, so this tile's write cannot overtake that read. Otherwise the
-        // wait on the previous BMM2 (or, with TMEM P, the issuer's order) already orders them: one slot.
-        ++nskip;
-        if (r == 0 && h == 0) skip_flag[i][kLazyPv ? (j & 1) : 0] = 1;
-        // TMEM P: the issuer's next BMM1 overwrites the S just loaded (with P in shared memory, S
-        // was already released after its load)
-        if constexpr (!kLazyPv) tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->p_full[i]);
-        continue;
-      }
-      const float mo = xmax[((i * 2 + (h ^ 1)) * 2 + (j & 1)) * 128 + r];
-      const float mt = fmaxf(mh, mo);  // identical on both halves: max is exact
-      if (!ok) continue;
-      const float m_new = fmaxf(m_ex, mt);
-      bool need;
-      float alpha = 1.0f;
-      if constexpr (kPV8) {
-        need = m_new > m_ref;
-        if (need) alpha = ex2_approx(m_ref - m_new);
-        m_ref = m_new;
-      } else {
-        need = (m_new - m_ref) > kLazyRescale;
-        if (need) {
-          alpha = ex2_approx(m_ref - m_new);
+        const float m_new = fmaxf(m_ex, mt);
+        bool need;
+        float alpha = 1.0f;
+        if constexpr (kPV8) {
+          need = m_new > m_ref;
+          if (need) alpha = ex2_approx(m_ref - m_new);
           m_ref = m_new;
-        }
-      }
-      m_ex = m_new;
-      l *= alpha;
-      // exponentials (two columns per packed FMA) and this half's row sum
-      const float bias = kPV8 ? (m_ref - kLog2_448) : m_ref;
-      const float2 nb = make_float2(-bias, -bias);
-#pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const float w = wg[kGroups == 1 ? 0 : (2 * k) / (kGroups == 1 ? 64 : KB)];
-        const float2 t = __ffma2_rn(s2[k], make_float2(w, w), nb);
-        s2[k].x = ex2_approx(t.x);
-        s2[k].y = ex2_approx(t.y);
-      }
-      if constexpr (kQKScaled) {
-        // masked columns hold -inf; with a zero weight (zero scale) that gives NaN, so clear them
-        if (tail) {
-#pragma unroll
-          for (int k = 0; k < 64; ++k)
-            if (k >= nvalid) s[k] = 0.f;
-        }
-      }
-      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-      for (int k = 0; k < 32; ++k) acc[k & 3] = __fadd2_rn(acc[k & 3], s2[k]);
-      l += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
-      if constexpr (PVF == PV_BF16) {
-        // P over the first columns of this half of S
-        uint32_t w[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) w[k] = pack_bf16x2(s[2 * k], s[2 * k + 1]);
-        tmem_st32(t_s, w);
-      } else {
-        // E4M3 P into the tile's shared-memory buffer, laid out as a K-major operand with the
-        // 128-byte swizzle: row r's 16-byte chunk ch sits at (r/8)*1024 + (r%8)*128 + (ch ^ r%8)*16.
-        // This half holds chunks 4h .. 4h+3 (columns 64h .. 64h+63).
-        uint32_t w[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k)
-          w[k] = pack_e4m3x4(s[4 * k], s[4 * k + 1], s[4 * k + 2], s[4 * k + 3]);
-        uint8_t* prow = smem + L::kPOff + i * 16384 + (r >> 3) * 1024 + (r & 7) * 128;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int ch = 4 * h + q;
-          *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) =
-              make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-        }
-        fence_proxy_async_smem();  // visible to the tensor cores' reads
-      }
-      // O rescale for this half (after P, when the scores are no longer held in registers; still
-      // before the arrive that lets the MMA accumulate into O)
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
-        const float2 a2 = make_float2(alpha, alpha);
-        if constexpr (kQKScaled && KB >= 16) {
-          // frequent (every new running max): all 64 columns with one wait. Measured faster with
-          // K blocks of 16; with finer blocks the two-round form below is faster.
-          float2 o[32];
-          tmem_ld32(t_o, reinterpret_cast<float*>(o));
-          tmem_ld32(t_o + 32, reinterpret_cast<float*>(o + 16));
-          tmem_ld_wait();
-#pragma unroll
-          for (int k = 0; k < 32; ++k) o[k] = __fmul2_rn(o[k], a2);
-          tmem_st32(t_o, reinterpret_cast<const uint32_t*>(o));
-          tmem_st32(t_o + 32, reinterpret_cast<const uint32_t*>(o + 16));
         } else {
-          // two rounds of 32 columns keep register pressure low
-#pragma unroll 1
-          for (int cc = 0; cc < 2; ++cc) {
-            float2 o[16];
-            tmem_ld32(t_o + 32 * cc, reinterpret_cast<float*>(o));
+          need = (m_new - m_ref) > kLazyRescale;
+          if (need) {
+            alpha = ex2_approx(m_ref - m_new);
+            m_ref = m_new;
+          }
+        }
+        m_ex = m_new;
+        l *= alpha;
+        // exponentials (two columns per packed FMA) and this half's row sum
+        const float bias = kPV8 ? (m_ref - kLog2_448) : m_ref;
+        const float2 nb = make_float2(-bias, -bias);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float w = wg[kGroups == 1 ? 0 : (2 * k) / (kGroups == 1 ? 64 : KB)];
+          const float2 t = __ffma2_rn(s2[k], make_float2(w, w), nb);
+          s2[k].x = ex2_approx(t.x);
+          s2[k].y = ex2_approx(t.y);
+        }
+        if constexpr (kQKScaled) {
+          // masked columns hold -inf; with a zero weight (zero scale) that gives NaN, so clear them
+          if (tail) {
+#pragma unroll
+            for (int k = 0; k < 64; ++k)
+              if (k >= nvalid) s[k] = 0.f;
+          }
+        }
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int k = 0; k < 32; ++k) acc[k & 3] = __fadd2_rn(acc[k & 3], s2[k]);
+        l += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
+        if constexpr (PVF == PV_BF16) {
+          // P over the first columns of this half of S
+          uint32_t w[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) w[k] = pack_bf16x2(s[2 * k], s[2 * k + 1]);
+          tmem_st32(t_s, w);
+        } else {
+          // E4M3 P into the tile's shared-memory buffer, laid out as a K-major operand with the
+          // 128-byte swizzle: row r's 16-byte chunk ch sits at (r/8)*1024 + (r%8)*128 + (ch ^ r%8)*16.
+          // This half holds chunks 4h .. 4h+3 (columns 64h .. 64h+63).
+          uint32_t w[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            w[k] = pack_e4m3x4(s[4 * k], s[4 * k + 1], s[4 * k + 2], s[4 * k + 3]);
+          uint8_t* prow = smem + L::kPOff + i * 16384 + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int ch = 4 * h + q;
+            *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) =
+                make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+          }
+          fence_proxy_async_smem();  // visible to the tensor cores' reads
+        }
+        // O rescale for this half (after P, when the scores are no longer held in registers; still
+        // before the arrive that lets the MMA accumulate into O)
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+          const float2 a2 = make_float2(alpha, alpha);
+          if constexpr (kQKScaled && KB >= 16) {
+            // frequent (every new running max): all 64 columns with one wait. Measured faster with
+            // K blocks of 16; with finer blocks the two-round form below is faster.
+            float2 o[32];
+            tmem_ld32(t_o, reinterpret_cast<float*>(o));
+            tmem_ld32(t_o + 32, reinterpret_cast<float*>(o + 16));
             tmem_ld_wait();
 #pragma unroll
-            for (int k = 0; k < 16; ++k) o[k] = __fmul2_rn(o[k], a2);
-            tmem_st32(t_o + 32 * cc, reinterpret_cast<const uint32_t*>(o));
-          }
-        }
-      }
-      tmem_st_wait();
-      if constexpr (SKIP) {
-        if (r == 0 && h == 0) skip_flag[i][kLazyPv ? (j & 1) : 0] = 0;
-      }
-      ++n_pv;
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[i]);
-    }
-
-    // ------------------------------------------------------------ epilogue: O / l -> bf16 -> TMA store
-    xl[(i * 2 + h) * 128 + r] = l;
-    named_bar_sync(tile_bar, 256);
-    const float l_row = xl[(i * 2 + 0) * 128 + r] + xl[(i * 2 + 1) * 128 + r];
-    if (p.lse != nullptr && h == 0 && row_valid && ok) {
-      // ln sum_j exp(s_j) = ln 2 * (m_ref + log2 l), with l relative to m_ref (and carrying P's 448
-      // with E4M3 P); only the kept KV tiles contribute under Skip-Softmax, as to the output
-      const float l_true = kPV8 ? l_row * (1.0f / 448.0f) : l_row;
-      p.lse[((size_t)b * p.Hq + hq) * p.Sq + qrow] = 0.69314718055994531f * (m_ref + log2f(l_true));
-    }
-    if (ok) {
-      ok = mbar_wait_bounded(&bars->o_full[i], 0, budget, abort_flag);
-      if constexpr (kPV8) ok = ok && mbar_wait_bounded(&bars->vs_full, 0, budget, abort_flag);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok && lane == 0) record_timeout(p, bars);
-    }
-    // Stage O in this tile's own Q buffer (32 KB reserved per tile): only this tile's issuer reads
-    // it, and all of that issuer's MMAs are complete once O is final. (The K/V ring may still be
-    // read by the other tile's issuer.)
-    uint8_t* stage = smem + L::kQOff + i * 32768 + h * 16384;
-    if (ok) {
-      tc_fence_after();
-      const float inv_l = 1.0f / l_row;
+            for (int k = 0; k < 32; ++k) o[k] = __fmul2_rn(o[k], a2);
+            tmem_st32(t_o, reinterpret_cast<const uint32_t*>(o));
+            tmem_st32(t_o + 32, reinterpret_cast<const uint32_t*>(o + 16));
+          } else {
+            // two rounds of 32 columns keep register pressure low
 #pragma unroll 1
-      for (int cc = 0; cc < 2; ++cc) {
-        float o[32];
-        tmem_ld32(t_o + 32 * cc, o);
-        tmem_ld_wait();
-        uint32_t w[16];
+            for (int cc = 0; cc < 2; ++cc) {
+              float2 o[16];
+              tmem_ld32(t_o + 32 * cc, reinterpret_cast<float*>(o));
+              tmem_ld_wait();
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          float a0 = o[2 * k] * inv_l, a1 = o[2 * k + 1] * inv_l;
-          if constexpr (kPV8) {
-            a0 *= s_vs[64 * h + 32 * cc + 2 * k];
-            a1 *= s_vs[64 * h + 32 * cc + 2 * k + 1];
+              for (int k = 0; k < 16; ++k) o[k] = __fmul2_rn(o[k], a2);
+              tmem_st32(t_o + 32 * cc, reinterpret_cast<const uint32_t*>(o));
+            }
           }
-          w[k] = pack_bf16x2(a0, a1);
         }
-        // 128-byte swizzled staging of this half (columns 64h..64h+63): 16-byte chunk ch of row r
-        // sits at r*128 + ((ch ^ (r & 7)) * 16).
-        uint8_t* rowp = stage + r * 128;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int ch = cc * 4 + q;
-          *reinterpret_cast<uint4*>(rowp + ((ch ^ (r & 7)) << 4)) =
-              make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+        tmem_st_wait();
+        if constexpr (SKIP) {
+          if (r == 0 && h == 0) skip_flag[i][kLazyPv ? (j & 1) : 0] = 0;
         }
+        ++n_pv;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full_bar(i, j));
       }
-      fence_proxy_async_smem();
-    }
-    const bool all_ok = named_bar_and(group_bar, 128, ok);
-    if (all_ok && r == 0) {
-      tma_store_4d(&tm_o, stage, 64 * h, q0 + 128 * i, hq, b);
-      tma_store_commit();
-      tma_store_wait_all0();
-    }
-    if (r == 0 && h == 0 && p.skip_counts != nullptr) {
-      const int qt = 2 * blockIdx.x + i;
-      if (qt < p.n_q_tiles) p.skip_counts[((size_t)b * p.Hq + hq) * p.n_q_tiles + qt] = nskip;
+
+      // ------------------------------------------------------------ epilogue: O / l -> bf16 -> TMA store
+      xl[(i * 2 + h) * 128 + r] = l;
+      named_bar_sync(tile_bar, 256);
+      const float l_row = xl[(i * 2 + 0) * 128 + r] + xl[(i * 2 + 1) * 128 + r];
+      if (p.lse != nullptr && h == 0 && row_valid && ok) {
+        // ln sum_j exp(s_j) = ln 2 * (m_ref + log2 l), with l relative to m_ref (and carrying P's 448
+        // with E4M3 P); only the kept KV tiles contribute under Skip-Softmax, as to the output
+        const float l_true = kPV8 ? l_row * (1.0f / 448.0f) : l_row;
+        p.lse[((size_t)b * p.Hq + hq) * p.Sq + qrow] = 0.69314718055994531f * (m_ref + log2f(l_true));
+      }
+      if (ok) {
+        ok = mbar_wait_bounded(&bars->o_full[i], 0, budget, abort_flag);
+        if constexpr (kPV8) ok = ok && mbar_wait_bounded(&bars->vs_full, 0, budget, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok && lane == 0) record_timeout(p, bars);
+      }
+      // Stage O in this tile's own Q buffer (32 KB reserved per tile): only this tile's issuer reads
+      // it, and all of that issuer's MMAs are complete once O is final. (The K/V ring may still be
+      // read by the other tile's issuer.)
+      uint8_t* stage = smem + L::kQOff + i * 32768 + h * 16384;
+      if (ok) {
+        tc_fence_after();
+        const float inv_l = 1.0f / l_row;
+#pragma unroll 1
+        for (int cc = 0; cc < 2; ++cc) {
+          float o[32];
+          tmem_ld32(t_o + 32 * cc, o);
+          tmem_ld_wait();
+          uint32_t w[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            float a0 = o[2 * k] * inv_l, a1 = o[2 * k + 1] * inv_l;
+            if constexpr (kPV8) {
+              a0 *= s_vs[64 * h + 32 * cc + 2 * k];
+              a1 *= s_vs[64 * h + 32 * cc + 2 * k + 1];
+            }
+            w[k] = pack_bf16x2(a0, a1);
+          }
+          // 128-byte swizzled staging of this half (columns 64h..64h+63): 16-byte chunk ch of row r
+          // sits at r*128 + ((ch ^ (r & 7)) * 16).
+          uint8_t* rowp = stage + r * 128;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int ch = cc * 4 + q;
+            *reinterpret_cast<uint4*>(rowp + ((ch ^ (r & 7)) << 4)) =
+                make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+          }
+        }
+        fence_proxy_async_smem();
+      }
+      const bool all_ok = named_bar_and(group_bar, 128, ok);
+      if (all_ok && r == 0) {
+        tma_store_4d(&tm_o, stage, 64 * h, q0 + 128 * i, hq, b);
+        tma_store_commit();
+        tma_store_wait_all0();
+      }
+      if (r == 0 && h == 0 && p.skip_counts != nullptr) {
+        const int qt = 2 * blockIdx.x + i;
+        if (qt < p.n_q_tiles) p.skip_counts[((size_t)b * p.Hq + hq) * p.n_q_tiles + qt] = nskip;
+      }
+    } else {
+      // ------------------------------------------------------------ softmax warpgroups
+      regs_inc<P::kRegsSoftmax>();
+      constexpr int NH = P::kNH;                     // softmax warpgroups per Q tile
+      constexpr int NC = 128 / NH;                   // columns of S per thread
+      const int g = (warp - 4) >> 2;                 // softmax warpgroup
+      const int i = g / NH;                          // Q tile within the CTA
+      const int h = g % NH;                          // column part: S/O columns NC*h .. NC*h + NC-1
+      const int r = ((warp & 3) << 5) + lane;        // row within the tile == TMEM lane
+      const uint32_t lane_base = (uint32_t)((warp & 3) << 5) << 16;
+      const uint32_t t_s = tbase + lane_base + kColS1 * i + NC * h;
+      const uint32_t t_o = tbase + lane_base + kColO0 + 128 * i + NC * h;
+      const int qrow = q0 + 128 * i + r;
+      const bool row_valid = qrow < p.Sq;
+      const uint32_t tile_bar = 1 + i;               // the 128 * NH threads of this Q tile
+      const uint32_t group_bar = 3 + g;              // the 128 threads of this warpgroup
+      const uint32_t s_base = smem_u32(smem);
+      float* xmax = reinterpret_cast<float*>(smem + L::kXmaxOff);  // [tile][part][parity][128] partial maxima
+      float* xl = reinterpret_cast<float*>(smem + L::kXlOff);      // [tile][part][128] partial row sums
+      float c = p.c_scale;
+      if constexpr (kNV) c = c / (__ldg(p.q_gs) * __ldg(p.k_gs));  // BMM1 carries both tensor scales
+      if constexpr (kQKScaled) {
+        const float qs = row_valid ? __ldg(p.q_scale + ((size_t)b * p.Hq + hq) * p.nqb + qrow / p.q_block) : 0.0f;
+        c = qs * p.c_scale;
+      }
+      float m_ex = -INFINITY, m_ref = -INFINITY, l = 0.0f;
+      int nskip = 0;
+      bool ok = true;
+      volatile int (*skip_flag)[2] = bars->skip_flag;
+      int n_pv = 0;  // kLazyPv: BMM2s issued so far for this tile (o_done completes once per BMM2)
+      // Exponent weight per group of columns that share a K-block scale (log2 units): the row constant
+      // c, times the block scale in SAGE. KB >= 4 folds the block scale into the weight; KB == 1
+      // multiplies S by the column scales first.
+      constexpr int kGroups = (kQKScaled && KB >= 4) ? NC / KB : 1;
+      // S into registers. tcgen05.ld.red also returns each load's max over its columns: one load per
+      // K block of 16 tokens in SAGE (the block's max, weighted by its scale below), loads of 64
+      // columns without K-block scales. K blocks of 4 or 1 token use plain loads and take their maxima
+      // below (4-column loads measured slower than plain ones and the max tree).
+      constexpr bool kLdMax = !kQKScaled || KB == 16;
+      constexpr int kLoads = (kQKScaled && KB == 16) ? NC / 16 : NC / 64;
+      constexpr int kCols = NC / kLoads;
+      // E4M3 P: this row's 128 bytes in the tile's P buffer (a K-major operand with the 128-byte
+      // swizzle): 16-byte chunk ch (columns 16ch .. 16ch+15) of row r sits at
+      // (r/8)*1024 + (r%8)*128 + (ch ^ r%8)*16.
+      uint8_t* const p_row = smem + L::kPOff + i * 16384 + (r >> 3) * 1024 + (r & 7) * 128;
+      const uint32_t sw = (uint32_t)(r & 7);
+
+      for (int j = 0; j < nt; ++j) {
+        if (ok) {
+          // S_i(j), and in SAGE the K-block scales of tile j (both tested at once, so the two waits'
+          // latencies overlap)
+          if constexpr (kQKScaled) {
+            ok = mbar_wait2_bounded(&bars->s_full[i], j & 1, &bars->ks_full[j & 3], (j >> 2) & 1, budget, abort_flag);
+          } else {
+            ok = mbar_wait_bounded(&bars->s_full[i], j & 1, budget, abort_flag);
+          }
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok && lane == 0) record_timeout(p, bars);
+        }
+        if (!ok) {
+          // keep this tile's named barrier in step with the other warps
+          if (SKIP && j > 0) {
+            named_bar_and(tile_bar, 128 * NH, true);
+          } else if (NH == 2) {
+            named_bar_sync(tile_bar, 128 * NH);
+          }
+          continue;
+        }
+        tc_fence_after();
+        float2 s2[NC / 2];
+        float* s = reinterpret_cast<float*>(s2);
+        float gmax[kLoads];
+        if constexpr (!kLdMax) {
+#pragma unroll
+          for (int q = 0; q < NC / 32; ++q) tmem_ld32(t_s + 32 * q, s + 32 * q);
+        } else if constexpr (kCols == 16) {
+#pragma unroll
+          for (int q = 0; q < kLoads; ++q) tmem_ldmax16(t_s + 16 * q, s + 16 * q, gmax[q]);
+        } else {
+#pragma unroll
+          for (int q = 0; q < kLoads; ++q) tmem_ldmax64(t_s + 64 * q, s + 64 * q, gmax[q]);
+        }
+        tmem_ld_wait();
+        if constexpr (L::kPInSmem) {
+          // S is in registers: the issuer may compute the next tile's S into the same columns
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->s_free[i]);
+        }
+        const int nvalid = min(NC, p.Skv - 128 * j - NC * h);  // may be <= 0 for the upper part
+        const bool tail = nvalid < NC;
+        if (tail) {
+          // the last KV tile: columns past Skv hold the products with TMA's zero fill; mask them (and
+          // take the loads' maxima over the valid columns only)
+#pragma unroll
+          for (int k = 0; k < NC; ++k)
+            if (k >= nvalid) s[k] = -INFINITY;
+          if constexpr (kLdMax) {
+#pragma unroll
+            for (int q = 0; q < kLoads; ++q) {
+              float m = -INFINITY;
+#pragma unroll
+              for (int k = 0; k < kCols; ++k) m = fmaxf(m, s[kCols * q + k]);
+              gmax[q] = m;
+            }
+          }
+        }
+        float wg[kGroups];
+        float mh;  // this part's max of the row's weighted logits
+        if constexpr (kQKScaled && KB == 1) {
+          // per-column scales: multiply S by them first
+          const int e = j & 3;
+          const uint32_t ks = s_base + L::kKsOff + e * 512 + NC * h * 4;  // this part's scales
+#pragma unroll
+          for (int q = 0; q < NC / 4; ++q) {
+            const float4 k4 = lds128f(ks + 16 * q);
+            s2[2 * q] = __fmul2_rn(s2[2 * q], make_float2(k4.x, k4.y));
+            s2[2 * q + 1] = __fmul2_rn(s2[2 * q + 1], make_float2(k4.z, k4.w));
+          }
+          wg[0] = c;
+          mh = (NC == 128 ? rowmax128(s) : rowmax64(s)) * c;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->ks_empty[e]);
+        } else if constexpr (kQKScaled) {
+          const int e = j & 3;
+          const uint32_t ks = s_base + L::kKsOff + e * 512 + kGroups * h * 4;  // this part's scales
+#pragma unroll
+          for (int q4 = 0; q4 < kGroups / 4; ++q4) {
+            const float4 k4 = lds128f(ks + 16 * q4);
+            wg[4 * q4 + 0] = k4.x * c;
+            wg[4 * q4 + 1] = k4.y * c;
+            wg[4 * q4 + 2] = k4.z * c;
+            wg[4 * q4 + 3] = k4.w * c;
+          }
+          mh = -INFINITY;
+#pragma unroll
+          for (int q = 0; q < kGroups; ++q) {
+            const float gm = kLdMax ? gmax[q] : groupmax<KB>(s + q * KB);
+            mh = fmaxf(mh, gm * wg[q]);  // a NaN from -inf * 0 is ignored
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->ks_empty[e]);
+        } else {
+          wg[0] = c;
+          mh = gmax[0];
+#pragma unroll
+          for (int q = 1; q < kLoads; ++q) mh = fmaxf(mh, gmax[q]);
+          mh *= c;  // -inf when this part has no valid column
+        }
+        // With two parts, each publishes its max and one barrier over the tile orders the exchange.
+        // Skip-Softmax: the tile is skipped when every row's max is below the threshold (padded rows do
+        // not vote; a row's max is below it exactly when every part's is, so each part votes on its
+        // own); the barrier over the tile carries the vote.
+        if constexpr (NH == 2) xmax[((i * 2 + h) * 2 + (j & 1)) * 128 + r] = mh;
+        bool skip_tile = false;
+        if (SKIP && j > 0) {
+          const bool vote = !row_valid || (mh - m_ex < p.log2_thr);
+          skip_tile = named_bar_and(tile_bar, 128 * NH, vote);
+        } else if constexpr (NH == 2) {
+          named_bar_sync(tile_bar, 128 * NH);
+        }
+        if constexpr (L::kPInSmem) {
+          // The previous BMM2 must be complete before P's buffer, O or the skip flag change.
+          // kLazyPv: o_done completes once per BMM2, so the wait before the n-th P is on phase n - 1:
+          // that phase is the only one outstanding (the one before was waited for, the next needs this
+          // P), so its parity is unambiguous; a skipped tile writes neither P nor O and does not wait.
+          // Otherwise o_done completes once per KV tile and is waited for on every tile, which keeps
+          // the waits in step with its phases.
+          if constexpr (kLazyPv) {
+            if (!skip_tile && n_pv > 0) {
+              ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->o_done[i], (n_pv - 1) & 1, budget, abort_flag));
+              if (!ok && lane == 0) record_timeout(p, bars);
+            }
+          } else {
+            if (j > 0) {
+              ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->o_done[i], (j - 1) & 1, budget, abort_flag));
+              if (!ok && lane == 0) record_timeout(p, bars);
+            }
+          }
+          if (!ok) continue;
+        }
+        if (skip_tile) {
+          // kLazyPv: the flag has a slot per KV-tile parity; the issuer reads tile j's slot before it
+          // issues the BMM1 of tile j + 2, so this tile's write cannot overtake that read. Otherwise the
+          // wait on the previous BMM2 (or, with TMEM P, the issuer's order) already orders them: one slot.
+          ++nskip;
+          if (r == 0 && h == 0) skip_flag[i][kLazyPv ? (j & 1) : 0] = 1;
+          // TMEM P: the issuer's next BMM1 overwrites the S just loaded (with P in shared memory, S
+          // was already released after its load)
+          if constexpr (!kLazyPv) tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(p_full_bar(i, j));
+          continue;
+        }
+        float mt = mh;
+        if constexpr (NH == 2)  // identical on both parts: max is exact
+          mt = fmaxf(mh, xmax[((i * 2 + (h ^ 1)) * 2 + (j & 1)) * 128 + r]);
+        const float m_new = fmaxf(m_ex, mt);
+        bool need;
+        float alpha = 1.0f;
+        if constexpr (kPV8) {
+          need = m_new > m_ref;
+          if (need) alpha = ex2_approx(m_ref - m_new);
+          m_ref = m_new;
+        } else {
+          need = (m_new - m_ref) > kLazyRescale;
+          if (need) {
+            alpha = ex2_approx(m_ref - m_new);
+            m_ref = m_new;
+          }
+        }
+        m_ex = m_new;
+        l *= alpha;
+        // exponentials (two columns per packed FMA) and this part's row sum
+        const float bias = kPV8 ? (m_ref - kLog2_448) : m_ref;
+        const float2 nb = make_float2(-bias, -bias);
+#pragma unroll
+        for (int k = 0; k < NC / 2; ++k) {
+          const float w = wg[kGroups == 1 ? 0 : (2 * k) / (kGroups == 1 ? NC : KB)];
+          const float2 t = __ffma2_rn(s2[k], make_float2(w, w), nb);
+          s2[k].x = ex2_approx(t.x);
+          s2[k].y = ex2_approx(t.y);
+        }
+        if constexpr (kQKScaled) {
+          // masked columns hold -inf; with a zero weight (zero scale) that gives NaN, so clear them
+          if (tail) {
+#pragma unroll
+            for (int k = 0; k < NC; ++k)
+              if (k >= nvalid) s[k] = 0.f;
+          }
+        }
+        constexpr int kAcc = NC == 128 ? 8 : 4;  // independent packed partial sums
+        float2 acc[kAcc];
+#pragma unroll
+        for (int k = 0; k < kAcc; ++k) acc[k] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < NC / 2; ++k) acc[k % kAcc] = __fadd2_rn(acc[k % kAcc], s2[k]);
+#pragma unroll
+        for (int k = 0; k < kAcc - 4; ++k) acc[k] = __fadd2_rn(acc[k], acc[k + 4]);
+        l += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
+        if constexpr (PVF == PV_BF16) {
+          // P (two bf16 values per column) over the first NC / 2 columns of this part of S
+          uint32_t w[NC / 2];
+#pragma unroll
+          for (int k = 0; k < NC / 2; ++k) w[k] = pack_bf16x2(s[2 * k], s[2 * k + 1]);
+#pragma unroll
+          for (int q = 0; q < NC / 64; ++q) tmem_st32(t_s + 32 * q, w + 32 * q);
+        } else {
+          // E4M3 P into the tile's shared-memory buffer: this part's chunks (NC / 16 of 16 columns)
+#pragma unroll
+          for (int cq = 0; cq < NC / 16; ++cq) {
+            const uint32_t ch = (uint32_t)((NC / 16) * h + cq);
+            const float* x = s + 16 * cq;
+            *reinterpret_cast<uint4*>(p_row + ((ch ^ sw) << 4)) =
+                make_uint4(pack_e4m3x4(x[0], x[1], x[2], x[3]), pack_e4m3x4(x[4], x[5], x[6], x[7]),
+                           pack_e4m3x4(x[8], x[9], x[10], x[11]), pack_e4m3x4(x[12], x[13], x[14], x[15]));
+          }
+          fence_proxy_async_smem();  // visible to the tensor cores' reads
+        }
+        // O rescale for this part (after P, when the scores are no longer held in registers; still
+        // before the arrive that lets the MMA accumulate into O)
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+          const float2 a2 = make_float2(alpha, alpha);
+          if constexpr (NC == 128 || (kQKScaled && KB >= 16)) {
+            // rounds of 64 columns with one wait each (measured faster with K blocks of 16; with finer
+            // blocks and 64 columns per thread the rounds of 32 below are faster)
+#pragma unroll 1
+            for (int cc = 0; cc < NC / 64; ++cc) {
+              float2 o[32];
+              tmem_ld32(t_o + 64 * cc, reinterpret_cast<float*>(o));
+              tmem_ld32(t_o + 64 * cc + 32, reinterpret_cast<float*>(o + 16));
+              tmem_ld_wait();
+#pragma unroll
+              for (int k = 0; k < 32; ++k) o[k] = __fmul2_rn(o[k], a2);
+              tmem_st32(t_o + 64 * cc, reinterpret_cast<const uint32_t*>(o));
+              tmem_st32(t_o + 64 * cc + 32, reinterpret_cast<const uint32_t*>(o + 16));
+            }
+          } else {
+#pragma unroll 1
+            for (int cc = 0; cc < NC / 32; ++cc) {
+              float2 o[16];
+              tmem_ld32(t_o + 32 * cc, reinterpret_cast<float*>(o));
+              tmem_ld_wait();
+#pragma unroll
+              for (int k = 0; k < 16; ++k) o[k] = __fmul2_rn(o[k], a2);
+              tmem_st32(t_o + 32 * cc, reinterpret_cast<const uint32_t*>(o));
+            }
+          }
+        }
+        tmem_st_wait();
+        if constexpr (SKIP) {
+          if (r == 0 && h == 0) skip_flag[i][kLazyPv ? (j & 1) : 0] = 0;
+        }
+        ++n_pv;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full_bar(i, j));
+      }
+
+      // ------------------------------------------------------------ epilogue: O / l -> bf16 -> TMA store
+      float l_row = l;
+      if constexpr (NH == 2) {
+        xl[(i * 2 + h) * 128 + r] = l;
+        named_bar_sync(tile_bar, 128 * NH);
+        l_row = xl[(i * 2) * 128 + r] + xl[(i * 2 + 1) * 128 + r];
+      }
+      if (p.lse != nullptr && h == 0 && row_valid && ok) {
+        // ln sum_j exp(s_j) = ln 2 * (m_ref + log2 l), with l relative to m_ref (and carrying P's 448
+        // with E4M3 P); only the kept KV tiles contribute under Skip-Softmax, as to the output
+        const float l_true = kPV8 ? l_row * (1.0f / 448.0f) : l_row;
+        p.lse[((size_t)b * p.Hq + hq) * p.Sq + qrow] = 0.69314718055994531f * (m_ref + log2f(l_true));
+      }
+      if (ok) {
+        ok = mbar_wait_bounded(&bars->o_full[i], 0, budget, abort_flag);
+        if constexpr (kPV8) ok = ok && mbar_wait_bounded(&bars->vs_full, 0, budget, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok && lane == 0) record_timeout(p, bars);
+      }
+      // Stage O in this tile's own Q buffer (32 KB reserved per tile: two 128-byte-swizzled halves of 64
+      // columns, 16-byte chunk ch of row r at r*128 + (ch ^ r%8)*16): only this tile's issuer reads it,
+      // and all of that issuer's MMAs are complete once O is final. (The K/V ring may still be read by
+      // the other tile's issuer.)
+      const uint32_t stage = s_base + L::kQOff + i * 32768;
+      if (ok) {
+        tc_fence_after();
+        const float inv_l = 1.0f / l_row;
+#pragma unroll 1
+        for (int cc = 0; cc < NC / 32; ++cc) {
+          float o[32];
+          tmem_ld32(t_o + 32 * cc, o);
+          tmem_ld_wait();
+          const int gc = NC * h + 32 * cc;  // the first of these 32 columns within the row
+          uint32_t w[16];
+#pragma unroll
+          for (int k4 = 0; k4 < 8; ++k4) {
+            float a[4] = {o[4 * k4] * inv_l, o[4 * k4 + 1] * inv_l, o[4 * k4 + 2] * inv_l, o[4 * k4 + 3] * inv_l};
+            if constexpr (kPV8) {
+              const float4 vs = lds128f(s_base + L::kVsOff + (gc + 4 * k4) * 4);
+              a[0] *= vs.x;
+              a[1] *= vs.y;
+              a[2] *= vs.z;
+              a[3] *= vs.w;
+            }
+            w[2 * k4] = pack_bf16x2(a[0], a[1]);
+            w[2 * k4 + 1] = pack_bf16x2(a[2], a[3]);
+          }
+          const uint32_t rowp = stage + (gc >> 6) * 16384 + r * 128;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t ch = (uint32_t)(((gc & 63) >> 3) + q);
+            sts128(rowp + ((ch ^ sw) << 4), w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+          }
+        }
+        fence_proxy_async_smem();
+      }
+      const bool all_ok = named_bar_and(group_bar, 128, ok);
+      if (all_ok && r == 0) {
+        // this warpgroup's halves of 64 columns
+#pragma unroll
+        for (int hh = 0; hh < 2 / NH; ++hh) {
+          const int half = (2 / NH) * h + hh;
+          tma_store_4d(&tm_o, smem + L::kQOff + i * 32768 + half * 16384, 64 * half, q0 + 128 * i, hq, b);
+        }
+        tma_store_commit();
+        tma_store_wait_all0();
+      }
+      if (r == 0 && h == 0 && p.skip_counts != nullptr) {
+        const int qt = 2 * blockIdx.x + i;
+        if (qt < p.n_q_tiles) p.skip_counts[((size_t)b * p.Hq + hq) * p.n_q_tiles + qt] = nskip;
+      }
     }
   }
 
@@ -896,14 +1297,14 @@ cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
     cudaFuncAttributes fa;
     e = cudaFuncGetAttributes(&fa, fmha_fwd_kernel<QKF, PVF, KB, SKIP, WITHHOLD>);
     if (e != cudaSuccess) return e;
-    if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidKernelImage;
+    if (fa.numRegs != Parts<QKF, PVF>::kLaunchRegs) return cudaErrorInvalidKernelImage;
     e = cudaFuncSetAttribute(fmha_fwd_kernel<QKF, PVF, KB, SKIP, WITHHOLD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SmemLayout<QKF, PVF>::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set[dev].store(true, std::memory_order_release);
   }
   const dim3 grid((p.Sq + 255) / 256, p.Hq, p.B);
-  fmha_fwd_kernel<QKF, PVF, KB, SKIP, WITHHOLD><<<grid, kThreads, SmemLayout<QKF, PVF>::kSmemBytes, stream>>>(tq, tk, tv, to, p);
+  fmha_fwd_kernel<QKF, PVF, KB, SKIP, WITHHOLD><<<grid, Parts<QKF, PVF>::kThreads, SmemLayout<QKF, PVF>::kSmemBytes, stream>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 
