@@ -28,7 +28,9 @@
 // E4M3 P (SAGE, QK16PV8, MXFP8, NVFP4; 16 KB per tile): P goes to a shared-memory buffer and BMM2 is
 // an SS MMA. S is free as soon as the softmax has loaded it, so the issuer computes S_i(j+1) while
 // the softmax works on S_i(j); a per-tile barrier (o_done) returns P's buffer and O to the softmax
-// after each BMM2 (SAGE with Skip-Softmax: only before the next P; see kLazyPv).
+// after each BMM2. With 8- or 4-bit K tiles there is room for two P buffers per tile, and the
+// softmax then waits for the previous BMM2 only before it rescales O (kDblP); SAGE with
+// Skip-Softmax waits only before the next P (kLazyPv).
 // MXFP8 / NVFP4: the block-scaled MMA reads its scale factors from tensor memory, and S0 | S1 | O0 | O1 leave
 // no room, so the two tiles share one S buffer (S | O0 | O1 | scale factors): BMM1s alternate
 // between the tiles, each issued once the other tile's softmax has loaded the previous S. The
@@ -92,8 +94,11 @@ struct SmemLayout {
   static constexpr uint32_t kKOff = 2 * 32768;
   static constexpr uint32_t kVOff = kKOff + 2 * kKTile;
   static constexpr uint32_t kPOff = kVOff + 2 * kVTile;
+  // E4M3 P buffers per Q tile (16 KB each): two when the K tiles are 8- or 4-bit (the shared memory
+  // then has room), so that a tile's P never waits for the BMM2 that read the previous one
+  static constexpr uint32_t kPBufs = kPInSmem ? (kKTile <= 16384 ? 2u : 1u) : 0u;
   // 4 x 128 floats (SAGE K-block scales), or 4 x kSfWords x 512 bytes of K tiles' block scales
-  static constexpr uint32_t kKsOff = kPOff + (kPInSmem ? 2 * 16384 : 0);
+  static constexpr uint32_t kKsOff = kPOff + kPBufs * 2 * 16384;
   static constexpr uint32_t kVsOff = kKsOff + kSlots * 512 * kSfWords;     // 128 floats
   static constexpr uint32_t kXmaxOff = kVsOff + 512;        // [tile][half][parity][128] partial maxima
   static constexpr uint32_t kXlOff = kXmaxOff + 2 * 2 * 2 * 512;  // [tile][half][128] partial row sums
@@ -154,6 +159,15 @@ __global__ void __launch_bounds__(Parts<QKF, PVF>::kThreads, 1)
   // which measured faster for them). o_done then completes once per BMM2, and the skip flag needs a
   // slot per KV-tile parity.
   constexpr bool kLazyPv = SKIP && kQKScaled;
+  // Two P buffers per tile (L::kPBufs): the softmax writes its n-th P into buffer n % 2, which BMM2
+  // #(n-2) read; that BMM2 was issued before BMM1 of the current KV tile (the issuer issues BMM1(j+1)
+  // before BMM2(j), and its MMAs complete in order), so S's arrival already frees the buffer and the
+  // softmax waits for the previous BMM2 only before it rescales O. o_done then completes once per
+  // BMM2, as with kLazyPv.
+  constexpr bool kDblP = (SmemLayout<QKF, PVF>::kPBufs == 2);
+  // the softmax may run ahead of the issuer over several KV tiles: P is handed over through one
+  // barrier per KV-tile parity and the skip flag has a slot per parity (see p_full_odd)
+  constexpr bool kRunAhead = kLazyPv || kDblP;
   constexpr bool kMX = (QKF == QK_MXF8);         // block-scaled MXFP8 Q/K (scales applied inside BMM1)
   constexpr bool kNV = (QKF == QK_NVF4);         // block-scaled NVFP4 Q/K (and a tensor scale per Q and K)
   constexpr bool kBS = kMX || kNV;
@@ -185,8 +199,8 @@ __global__ void __launch_bounds__(Parts<QKF, PVF>::kThreads, 1)
   float* s_vs = reinterpret_cast<float*>(smem + L::kVsOff);
   const volatile int* abort_flag = &bars->abort_flag;
   // the barrier that hands P of KV tile j of Q tile i to the issuer, and the parity of that phase
-  auto p_full_bar = [&](int i, int j) { return (kLazyPv && (j & 1)) ? &bars->p_full_odd[i] : &bars->p_full[i]; };
-  auto p_full_par = [&](int j) -> uint32_t { return kLazyPv ? (uint32_t)((j >> 1) & 1) : (uint32_t)(j & 1); };
+  auto p_full_bar = [&](int i, int j) { return (kRunAhead && (j & 1)) ? &bars->p_full_odd[i] : &bars->p_full[i]; };
+  auto p_full_par = [&](int j) -> uint32_t { return kRunAhead ? (uint32_t)((j >> 1) & 1) : (uint32_t)(j & 1); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hq = blockIdx.y, b = blockIdx.z;
@@ -210,7 +224,7 @@ __global__ void __launch_bounds__(Parts<QKF, PVF>::kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->p_full[i], 4 * P::kNH);  // one arrival per softmax warp of the tile
-      if constexpr (kLazyPv) mbar_init(&bars->p_full_odd[i], 4 * P::kNH);
+      if constexpr (kRunAhead) mbar_init(&bars->p_full_odd[i], 4 * P::kNH);
       mbar_init(&bars->o_full[i], 1);
     }
     mbar_init(&bars->vs_full, 32);
@@ -368,7 +382,8 @@ __global__ void __launch_bounds__(Parts<QKF, PVF>::kThreads, 1)
       // loaded it, so each tile's S(j+1) is computed while its softmax turns S(j) into P(j).
       // BMM2 is an SS MMA (P K-major, V MN-major); o_done tells the softmax when P's buffer and O
       // are free again.
-      const uint64_t ap = make_sdesc_sw128(sbase + L::kPOff + i * 16384, 16, 1024);
+      const uint64_t ap = make_sdesc_sw128(sbase + L::kPOff + i * L::kPBufs * 16384, 16, 1024);
+      int n2 = 0;  // BMM2s issued so far (kDblP: BMM2 #n reads P buffer n % 2)
       if constexpr (kBS) {
         // this Q tile's scale words, once, ahead of every MMA that reads them
         if (ok) ok = wait(&bars->sfa_full, 0);
@@ -396,17 +411,19 @@ __global__ void __launch_bounds__(Parts<QKF, PVF>::kThreads, 1)
         ok = wait(&bars->kv_full[tv & 3], (tv >> 2) & 1) && wait(p_full_bar(i, j), p_full_par(j));
         if (!ok) break;
         tc_fence_after();
-        const bool skipped = SKIP && skip_flag[i][kLazyPv ? (j & 1) : 0] != 0;
+        const bool skipped = SKIP && skip_flag[i][kRunAhead ? (j & 1) : 0] != 0;
         if (!skipped) {
           // (the first KV tile is never skipped, so O is initialized by BMM2 of tile 0)
           const uint64_t bv = dv0 + (uint64_t)(((j & 1) * L::kVTile) >> 4);
+          const uint64_t ap_n = ap + (uint64_t)(((kDblP ? (n2 & 1) : 0) * 16384) >> 4);
+          ++n2;
 #pragma unroll
           for (int kk = 0; kk < kK2Steps; ++kk)
-            mma_ss_if<kMma2Kind>(leader, d_o, ap + (uint64_t)((kk * 32) >> 4), bv + (uint64_t)((kk * 4096) >> 4),
+            mma_ss_if<kMma2Kind>(leader, d_o, ap_n + (uint64_t)((kk * 32) >> 4), bv + (uint64_t)((kk * 4096) >> 4),
                                  kIdesc2, (j > 0 || kk > 0) ? 1u : 0u);
         }
         // o_done: one phase per BMM2 (kLazyPv) or per KV tile
-        if (!kLazyPv || !skipped) mma_commit_if(leader, &bars->o_done[i]);
+        if (!kRunAhead || !skipped) mma_commit_if(leader, &bars->o_done[i]);
         mma_commit_if(leader, &bars->kv_empty[tv & 3]);
       }
     } else {
@@ -711,7 +728,9 @@ __global__ void __launch_bounds__(Parts<QKF, PVF>::kThreads, 1)
           // P), so its parity is unambiguous; a skipped tile writes neither P nor O and does not wait.
           // Otherwise o_done completes once per KV tile and is waited for on every tile, which keeps
           // the waits in step with its phases.
-          if constexpr (kLazyPv) {
+          if constexpr (kDblP) {
+            // no wait here: the P buffer is free (see kDblP); O is waited for only before a rescale
+          } else if constexpr (kLazyPv) {
             if (!skip_tile && n_pv > 0 && ok) {
               ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->o_done[i], (n_pv - 1) & 1, budget, abort_flag));
               if (!ok && lane == 0) record_timeout(p, bars);
@@ -729,7 +748,7 @@ __global__ void __launch_bounds__(Parts<QKF, PVF>::kThreads, 1)
           // issues the BMM1 of tile j + 2, so this tile's write cannot overtake that read. Otherwise the
           // wait on the previous BMM2 (or, with TMEM P, the issuer's order) already orders them: one slot.
           ++nskip;
-          if (r == 0 && h == 0) skip_flag[i][kLazyPv ? (j & 1) : 0] = 1;
+          if (r == 0 && h == 0) skip_flag[i][kRunAhead ? (j & 1) : 0] = 1;
           // TMEM P: the issuer's next BMM1 overwrites the S just loaded (with P in shared memory, S
           // was already released after its load)
           if constexpr (!kLazyPv) tc_fence_before();
@@ -792,7 +811,7 @@ __global__ void __launch_bounds__(Parts<QKF, PVF>::kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 16; ++k)
             w[k] = pack_e4m3x4(s[4 * k], s[4 * k + 1], s[4 * k + 2], s[4 * k + 3]);
-          uint8_t* prow = smem + L::kPOff + i * 16384 + (r >> 3) * 1024 + (r & 7) * 128;
+          uint8_t* prow = smem + L::kPOff + (i * L::kPBufs + (kDblP ? (n_pv & 1) : 0)) * 16384 + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int ch = 4 * h + q;
@@ -804,6 +823,13 @@ __global__ void __launch_bounds__(Parts<QKF, PVF>::kThreads, 1)
         // O rescale for this half (after P, when the scores are no longer held in registers; still
         // before the arrive that lets the MMA accumulate into O)
         if (j > 0 && __any_sync(0xffffffffu, need)) {
+          if constexpr (kDblP) {
+            // O must not change while the previous BMM2 still accumulates into it
+            if (n_pv > 0) {
+              ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->o_done[i], (n_pv - 1) & 1, budget, abort_flag));
+              if (!ok && lane == 0) record_timeout(p, bars);
+            }
+          }
           const float2 a2 = make_float2(alpha, alpha);
           if constexpr (kQKScaled && KB >= 16) {
             // frequent (every new running max): all 64 columns with one wait. Measured faster with
@@ -828,10 +854,11 @@ __global__ void __launch_bounds__(Parts<QKF, PVF>::kThreads, 1)
               tmem_st32(t_o + 32 * cc, reinterpret_cast<const uint32_t*>(o));
             }
           }
+          if constexpr (kDblP) tmem_st_wait();  // the rescaled O is in tensor memory
         }
-        tmem_st_wait();
+        if constexpr (!kDblP) tmem_st_wait();
         if constexpr (SKIP) {
-          if (r == 0 && h == 0) skip_flag[i][kLazyPv ? (j & 1) : 0] = 0;
+          if (r == 0 && h == 0) skip_flag[i][kRunAhead ? (j & 1) : 0] = 0;
         }
         ++n_pv;
         tc_fence_before();
@@ -943,7 +970,7 @@ __global__ void __launch_bounds__(Parts<QKF, PVF>::kThreads, 1)
       // E4M3 P: this row's 128 bytes in the tile's P buffer (a K-major operand with the 128-byte
       // swizzle): 16-byte chunk ch (columns 16ch .. 16ch+15) of row r sits at
       // (r/8)*1024 + (r%8)*128 + (ch ^ r%8)*16.
-      uint8_t* const p_row = smem + L::kPOff + i * 16384 + (r >> 3) * 1024 + (r & 7) * 128;
+      uint8_t* const p_row0 = smem + L::kPOff + i * L::kPBufs * 16384 + (r >> 3) * 1024 + (r & 7) * 128;
       const uint32_t sw = (uint32_t)(r & 7);
 
       for (int j = 0; j < nt; ++j) {
@@ -1067,7 +1094,9 @@ __global__ void __launch_bounds__(Parts<QKF, PVF>::kThreads, 1)
           // P), so its parity is unambiguous; a skipped tile writes neither P nor O and does not wait.
           // Otherwise o_done completes once per KV tile and is waited for on every tile, which keeps
           // the waits in step with its phases.
-          if constexpr (kLazyPv) {
+          if constexpr (kDblP) {
+            // no wait here: the P buffer is free (see kDblP); O is waited for only before a rescale
+          } else if constexpr (kLazyPv) {
             if (!skip_tile && n_pv > 0) {
               ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->o_done[i], (n_pv - 1) & 1, budget, abort_flag));
               if (!ok && lane == 0) record_timeout(p, bars);
@@ -1085,7 +1114,7 @@ __global__ void __launch_bounds__(Parts<QKF, PVF>::kThreads, 1)
           // issues the BMM1 of tile j + 2, so this tile's write cannot overtake that read. Otherwise the
           // wait on the previous BMM2 (or, with TMEM P, the issuer's order) already orders them: one slot.
           ++nskip;
-          if (r == 0 && h == 0) skip_flag[i][kLazyPv ? (j & 1) : 0] = 1;
+          if (r == 0 && h == 0) skip_flag[i][kRunAhead ? (j & 1) : 0] = 1;
           // TMEM P: the issuer's next BMM1 overwrites the S just loaded (with P in shared memory, S
           // was already released after its load)
           if constexpr (!kLazyPv) tc_fence_before();
@@ -1152,7 +1181,7 @@ __global__ void __launch_bounds__(Parts<QKF, PVF>::kThreads, 1)
           for (int cq = 0; cq < NC / 16; ++cq) {
             const uint32_t ch = (uint32_t)((NC / 16) * h + cq);
             const float* x = s + 16 * cq;
-            *reinterpret_cast<uint4*>(p_row + ((ch ^ sw) << 4)) =
+            *reinterpret_cast<uint4*>(p_row0 + (kDblP ? (n_pv & 1) * 16384 : 0) + ((ch ^ sw) << 4)) =
                 make_uint4(pack_e4m3x4(x[0], x[1], x[2], x[3]), pack_e4m3x4(x[4], x[5], x[6], x[7]),
                            pack_e4m3x4(x[8], x[9], x[10], x[11]), pack_e4m3x4(x[12], x[13], x[14], x[15]));
           }
@@ -1161,6 +1190,13 @@ __global__ void __launch_bounds__(Parts<QKF, PVF>::kThreads, 1)
         // O rescale for this part (after P, when the scores are no longer held in registers; still
         // before the arrive that lets the MMA accumulate into O)
         if (j > 0 && __any_sync(0xffffffffu, need)) {
+          if constexpr (kDblP) {
+            // O must not change while the previous BMM2 still accumulates into it
+            if (n_pv > 0) {
+              ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->o_done[i], (n_pv - 1) & 1, budget, abort_flag));
+              if (!ok && lane == 0) record_timeout(p, bars);
+            }
+          }
           const float2 a2 = make_float2(alpha, alpha);
           if constexpr (NC == 128 || (kQKScaled && KB >= 16)) {
             // rounds of 64 columns with one wait each (measured faster with K blocks of 16; with finer
@@ -1187,10 +1223,11 @@ __global__ void __launch_bounds__(Parts<QKF, PVF>::kThreads, 1)
               tmem_st32(t_o + 32 * cc, reinterpret_cast<const uint32_t*>(o));
             }
           }
+          if constexpr (kDblP) tmem_st_wait();  // the rescaled O is in tensor memory
         }
-        tmem_st_wait();
+        if constexpr (!kDblP) tmem_st_wait();
         if constexpr (SKIP) {
-          if (r == 0 && h == 0) skip_flag[i][kLazyPv ? (j & 1) : 0] = 0;
+          if (r == 0 && h == 0) skip_flag[i][kRunAhead ? (j & 1) : 0] = 0;
         }
         ++n_pv;
         tc_fence_before();
