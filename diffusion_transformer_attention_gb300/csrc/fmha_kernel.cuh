@@ -64,11 +64,12 @@ namespace {
 
 // Softmax warpgroups per Q tile and the launch shape they imply. Two (each thread holds 64 of a row's
 // 128 columns, the two halves exchange the row max through shared memory) for dense BF16 and SAGE
-// INT8 / FP8; one (each thread holds the whole row) for the E4M3-P recipes whose softmax has no
-// K-block scales (QK16PV8, MXFP8, NVFP4). Each measured faster for its recipes on GB300.
+// INT8; one (each thread holds the whole row) for the other recipes, all with an E4M3 P (SAGE FP8,
+// QK16PV8, MXFP8, NVFP4). Each measured faster for its recipes on GB300 (with one warpgroup SAGE FP8
+// ran 15% faster, dense 15% and SAGE INT8 2% slower).
 template <int QKF, int PVF>
 struct Parts {
-  static constexpr int kNH = (PVF == PV_E4M3 && (QKF == QK_BF16 || QKF == QK_MXF8 || QKF == QK_NVF4)) ? 1 : 2;
+  static constexpr int kNH = (PVF == PV_E4M3 && QKF != QK_F16) ? 1 : 2;
   static constexpr int kThreads = 128 + 256 * kNH;
   // launched at 65536 / kThreads registers (rounded down to a multiple of 8); warpgroup 0 (producer,
   // MMA issuers, scale stager) hands registers to the softmax warpgroups
@@ -870,12 +871,9 @@ __global__ void __launch_bounds__(Parts<QKF, PVF>::kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(p_full_bar(i, j));
       };
-      if constexpr (QKF == QK_E4M3) {  // measured faster peeled for SAGE FP8 only
-        for (int j = 0; j + 1 < nt; ++j) kv_tile(j, std::integral_constant<int, 0>{});
-        if (nt > 0) kv_tile(nt - 1, std::integral_constant<int, 1>{});
-      } else {
-        for (int j = 0; j < nt; ++j) kv_tile(j, std::integral_constant<int, 1>{});
-      }
+      // dense and SAGE INT8: every tile keeps the run-time tail test (a peeled last tile measured no
+      // faster for SAGE INT8)
+      for (int j = 0; j < nt; ++j) kv_tile(j, std::integral_constant<int, 1>{});
 
       // ------------------------------------------------------------ epilogue: O / l -> bf16 -> TMA store
       xl[(i * 2 + h) * 128 + r] = l;
@@ -984,7 +982,11 @@ __global__ void __launch_bounds__(Parts<QKF, PVF>::kThreads, 1)
       uint8_t* const p_row0 = smem + L::kPOff + i * L::kPBufs * 16384 + (r >> 3) * 1024 + (r & 7) * 128;
       const uint32_t sw = (uint32_t)(r & 7);
 
-      for (int j = 0; j < nt; ++j) {
+      // One KV tile. kTailMode 0: the tile is full (the masking of columns past Skv is compiled out);
+      // 1: the tile may be the ragged last one (decided at run time). The masking code, present in the
+      // loop body, measured several percent slower on every tile, so the last tile runs its own copy.
+      auto kv_tile = [&](int j, auto tail_mode) {
+        constexpr int kTailMode = decltype(tail_mode)::value;
         if (ok) {
           // S_i(j), and in SAGE the K-block scales of tile j (both tested at once, so the two waits'
           // latencies overlap)
@@ -1003,7 +1005,7 @@ __global__ void __launch_bounds__(Parts<QKF, PVF>::kThreads, 1)
           } else if (NH == 2) {
             named_bar_sync(tile_bar, 128 * NH);
           }
-          continue;
+          return;
         }
         tc_fence_after();
         float2 s2[NC / 2];
@@ -1027,7 +1029,7 @@ __global__ void __launch_bounds__(Parts<QKF, PVF>::kThreads, 1)
           if (lane == 0) mbar_arrive(&bars->s_free[i]);
         }
         const int nvalid = min(NC, p.Skv - 128 * j - NC * h);  // may be <= 0 for the upper part
-        const bool tail = nvalid < NC;
+        const bool tail = kTailMode != 0 && nvalid < NC;
         if (tail) {
           // the last KV tile: columns past Skv hold the products with TMA's zero fill; mask them (and
           // take the loads' maxima over the valid columns only)
@@ -1118,7 +1120,7 @@ __global__ void __launch_bounds__(Parts<QKF, PVF>::kThreads, 1)
               if (!ok && lane == 0) record_timeout(p, bars);
             }
           }
-          if (!ok) continue;
+          if (!ok) return;
         }
         if (skip_tile) {
           // kLazyPv: the flag has a slot per KV-tile parity; the issuer reads tile j's slot before it
@@ -1131,7 +1133,7 @@ __global__ void __launch_bounds__(Parts<QKF, PVF>::kThreads, 1)
           if constexpr (!kLazyPv) tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(p_full_bar(i, j));
-          continue;
+          return;
         }
         float mt = mh;
         if constexpr (NH == 2)  // identical on both parts: max is exact
@@ -1244,6 +1246,12 @@ __global__ void __launch_bounds__(Parts<QKF, PVF>::kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(p_full_bar(i, j));
+      };
+      if constexpr (QKF == QK_E4M3) {  // measured faster peeled for SAGE FP8; QK16PV8 and MXFP8 spilled or slowed
+        for (int j = 0; j + 1 < nt; ++j) kv_tile(j, std::integral_constant<int, 0>{});
+        if (nt > 0) kv_tile(nt - 1, std::integral_constant<int, 1>{});
+      } else {
+        for (int j = 0; j < nt; ++j) kv_tile(j, std::integral_constant<int, 1>{});
       }
 
       // ------------------------------------------------------------ epilogue: O / l -> bf16 -> TMA store

@@ -1,6 +1,6 @@
 """Run one attention configuration a few times, for profiling under ncu.
 
-    python -m diffusion_transformer_attention_gb300.profile_case --mode dense --B 1 --H 16 --S 16384 \
+    python profile_case.py --mode dense --B 1 --H 16 --S 16384 \
         --warmup 1 --launches 2
 
 Inputs are drawn on the device with the DiT recipe (K with a per-channel offset; the video
@@ -15,7 +15,7 @@ import sys
 
 import torch
 
-ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
@@ -28,6 +28,7 @@ MODES = {
     "sage_fp8": (dit.MODE_SAGE, "fp8_e4m3"),
     "skip_dense": (dit.MODE_SKIP, "bf16"),
     "skip_sage_int8": (dit.MODE_SAGE | dit.MODE_SKIP, "int8"),
+    "skip_sage_fp8": (dit.MODE_SAGE | dit.MODE_SKIP, "fp8_e4m3"),
     "qk16pv8": (dit.MODE_SAGE | dit.MODE_V_PER_TENSOR, "bf16"),
     "mxfp8": (dit.MODE_SAGE, "mxfp8"),
     "nvfp4": (dit.MODE_SAGE, "nvfp4"),

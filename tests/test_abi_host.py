@@ -136,6 +136,16 @@ def test_every_printed_recipe_is_accepted(lib, recipe):
     assert lib.dit_attn_workspace_bytes(2, 32, 8, 1000, 1000, mode | dit.MODE_SKIP, qk, qb, kb) > 0
 
 
+def test_qk16pv8_with_per_channel_v_is_accepted(lib):
+    # not a printed recipe: the "Recipes" table of "VisualGen Quantized Attention" lists QK16PV8 only
+    # with blocks (0, 0, 0); its section on MXFP8 and NVFP4 says the CUTEDSL backend takes
+    # v_block_size 0 (one tensor-wide V scale) or 1 (one per head and channel), and the build reads
+    # that as holding for the CUTEDSL QK16PV8 kernel too (its V path is the same per-channel one SAGE uses)
+    qk = dit.QK_DTYPES["bf16"]
+    assert lib.dit_attn_workspace_bytes(2, 32, 8, 1000, 1000, dit.MODE_SAGE, qk, 0, 0) > 0
+    assert lib.dit_attn_workspace_bytes(2, 32, 8, 1000, 1000, dit.MODE_SAGE | dit.MODE_SKIP, qk, 0, 0) > 0
+
+
 @pytest.mark.parametrize("bad", [0, 2, 3, 8, 32])
 def test_block_sizes_outside_the_pages_set_are_rejected(lib, bad):
     assert lib.dit_attn_workspace_bytes(1, 4, 4, 512, 512, 1, 1, bad, 16) == 0
