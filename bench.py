@@ -489,6 +489,11 @@ def run_modes(dit, steps, warmup, world, stream, peak16, hbm_gbs, cpu: bool):
         res[label] = run_recipe(dit, name, steps, warmup, world, stream, peak, hbm_gbs)
         if cpu:
             res[label]["cpu"] = oracle_config_baseline(workloads.WORKLOADS[name], budget_s=4.0)
+    # INT8 codes run BMM1 at the fp16 tensor rate (there is no INT8 MMA on this part) and BMM2 at the
+    # E4M3 rate, half the BF16 time, and a skipped tile still costs its BMM1: at skipped fraction f the
+    # tensor time per tile is (1 + (1 - f) / 2) / 2 of dense BF16, so 2 / (1 + (1 - f) / 2) is the
+    # most Skip-Softmax with INT8 codes can gain over dense BF16 at equal tensor efficiency
+    curve["ceiling_x"] = [_r(2.0 / (1.0 + 0.5 * (1.0 - f))) for f in curve["skip"]]
     vid = {"dense_bf16_ms": _r(dense_ms), "dense_bf16_tflops": _r(w.dense_equiv_flop / (dense_ms * 1e-3) / 1e12, 1),
            "f": list(w.factors), "bf16_skip": bf16, "sage_int8_1_16_skip": curve}
     if cpu:

@@ -170,6 +170,10 @@ __global__ void __launch_bounds__(Parts<QKF, PVF>::kThreads, 1)
   // the softmax may run ahead of the issuer over several KV tiles: P is handed over through one
   // barrier per KV-tile parity and the skip flag has a slot per parity (see p_full_odd)
   constexpr bool kRunAhead = kLazyPv || kDblP;
+  // K tiles ahead: the producer loads K_{j+1} before V_j and the MMA issuer tests K_{j+1} before it
+  // waits for the softmax to release S. Measured faster for every instantiation but dense BF16 with
+  // Skip-Softmax, which keeps the K, V, K, V order.
+  constexpr bool kKAhead = !(SKIP && PVF == PV_BF16);
   constexpr bool kMX = (QKF == QK_MXF8);         // block-scaled MXFP8 Q/K (scales applied inside BMM1)
   constexpr bool kNV = (QKF == QK_NVF4);         // block-scaled NVFP4 Q/K (and a tensor scale per Q and K)
   constexpr bool kBS = kMX || kNV;
@@ -271,8 +275,22 @@ __global__ void __launch_bounds__(Parts<QKF, PVF>::kThreads, 1)
           tma_load_4d(dst, &tm_q, &bars->q_full, 0, q0 + 128 * i, hq, b, pol_q);
         }
       }
-      for (int j = 0; j < nt && ok; ++j) {
-        for (int kv = 0; kv < 2; ++kv) {
+      // kKAhead: K_0, then K_{j+1} before V_j. BMM1(j+1) needs its K tile before BMM2(j) needs V_j, and
+      // K_{j+1}'s buffer is freed first (by BMM1(j-1), which the issuer runs before BMM2(j-2), the last
+      // reader of V_j's buffer), so a V buffer still in use never holds back the next K tile.
+      // Otherwise K_j, V_j, K_{j+1}, ... Each slot receives its tiles in order either way.
+      for (int n = 0; n <= 2 * nt && ok; ++n) {
+        {
+          int j, kv;
+          if constexpr (kKAhead) {
+            j = (n == 0) ? 0 : ((n & 1) ? (n + 1) >> 1 : (n >> 1) - 1);
+            kv = (n == 0) ? 0 : ((n & 1) ? 0 : 1);
+            if (kv == 0 && j >= nt) continue;  // no K_{j+1} after the last tile
+          } else {
+            if (n == 2 * nt) break;
+            j = n >> 1;
+            kv = n & 1;
+          }
           const int t = 2 * j + kv, s = t & (kSlots - 1), u = t / kSlots;
           if (!mbar_wait_bounded(&bars->kv_empty[s], (u & 1) ^ 1, budget, abort_flag)) {
             record_timeout(p, bars);
@@ -397,14 +415,21 @@ __global__ void __launch_bounds__(Parts<QKF, PVF>::kThreads, 1)
                                   make_sdesc_rows16(sbase + L::kSfaOff + (i * kSfWords + w) * 512));
         }
       }
-      if (ok) ok = s_writable(0) && k_ready(0);
+      if (ok) ok = k_ready(0) && s_writable(0);
       if (ok) {
         tc_fence_after();
         bmm1(0);
       }
       for (int j = 0; j < nt && ok; ++j) {
         if (j + 1 < nt) {
-          ok = s_writable(j + 1) && k_ready(j + 1);
+          // kKAhead: K first. It is normally staged already, and testing it before the wait for the
+          // softmax keeps that test's latency (a barrier test costs as much as a wake-up) off the
+          // hand-over of S.
+          if constexpr (kKAhead) {
+            ok = k_ready(j + 1) && s_writable(j + 1);
+          } else {
+            ok = s_writable(j + 1) && k_ready(j + 1);
+          }
           if (!ok) break;
           tc_fence_after();
           bmm1(j + 1);
