@@ -61,25 +61,44 @@ __device__ __forceinline__ float quotient(float x, float scale, bool fast, float
   return (scale == 0.0f) ? 0.0f : __fdiv_rn(x, scale);
 }
 
+// quotient() of a lane's eight values by one block scale, two at a time on the packed pipes
+__device__ __forceinline__ void quotients8(float* q, float scale, bool fast, float rcp) {
+  if (fast) {
+    const float2 s2 = make_float2(scale, scale), r2 = make_float2(rcp, rcp);
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      const float2 v = div2_by_scale(make_float2(q[e], q[e + 1]), s2, r2);
+      q[e] = v.x;
+      q[e + 1] = v.y;
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) q[e] = (scale == 0.0f) ? 0.0f : __fdiv_rn(q[e], scale);
+  }
+}
+
 // INT8 codes without the conversion unit. Adding 1.5 * 2^23 to a float32 of magnitude <= 2^22
 // rounds it to an integer, half to even (the sum's unit in the last place is 1), and leaves that
 // integer n in the low mantissa bits: the sum's bits are 0x4B400000 + n. The quotient is clamped
-// to [-127, 127] first, which gives the same code as clamping the rounded value.
+// to [-127, 127] first, which gives the same code as clamping the rounded value. Two values at a
+// time: the addition runs on the packed float32 pipes (each lane rounds as the scalar add would).
 constexpr float kRoundInt = 12582912.0f;  // 1.5 * 2^23
-__device__ __forceinline__ uint32_t int8_round_bits(float q) {
-  return __float_as_uint(__fadd_rn(fminf(fmaxf(q, -127.0f), 127.0f), kRoundInt));
+__device__ __forceinline__ float2 int8_round2(float a, float b) {
+  return __fadd2_rn(make_float2(fminf(fmaxf(a, -127.0f), 127.0f), fminf(fmaxf(b, -127.0f), 127.0f)),
+                    make_float2(kRoundInt, kRoundInt));
 }
 
 // Four INT8 codes, `a` in the low byte (the low byte of the rounded sum is n's two's complement).
 __device__ __forceinline__ uint32_t int8_codes4(float a, float b, float c, float d) {
-  return __byte_perm(__byte_perm(int8_round_bits(a), int8_round_bits(b), 0x0040),
-                     __byte_perm(int8_round_bits(c), int8_round_bits(d), 0x0040), 0x5410);
+  const float2 ab = int8_round2(a, b), cd = int8_round2(c, d);
+  return __byte_perm(__byte_perm(__float_as_uint(ab.x), __float_as_uint(ab.y), 0x0040),
+                     __byte_perm(__float_as_uint(cd.x), __float_as_uint(cd.y), 0x0040), 0x5410);
 }
 
 // Two INT8 codes held exactly as fp16, `lo` in bits 0-15 (a zero code is +0).
 __device__ __forceinline__ uint32_t int8_code_f16x2(float lo, float hi) {
-  const __half2 h2 = __floats2half2_rn(__fsub_rn(__uint_as_float(int8_round_bits(lo)), kRoundInt),
-                                       __fsub_rn(__uint_as_float(int8_round_bits(hi)), kRoundInt));
+  const float2 n = __fadd2_rn(int8_round2(lo, hi), make_float2(-kRoundInt, -kRoundInt));
+  const __half2 h2 = __floats2half2_rn(n.x, n.y);
   return *reinterpret_cast<const uint32_t*>(&h2);
 }
 
@@ -289,7 +308,17 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const __nv_bfloat16* __res
       float vf[8];
       bf16x8_to_f32(raw[u], vf);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) vf[e] = quotient(vf[e], vs[e], fast[e], rcp[e]);
+      for (int e = 0; e < 8; e += 2) {
+        if (fast[e] && fast[e + 1]) {
+          const float2 v2 = div2_by_scale(make_float2(vf[e], vf[e + 1]), make_float2(vs[e], vs[e + 1]),
+                                          make_float2(rcp[e], rcp[e + 1]));
+          vf[e] = v2.x;
+          vf[e + 1] = v2.y;
+        } else {
+          vf[e] = quotient(vf[e], vs[e], fast[e], rcp[e]);
+          vf[e + 1] = quotient(vf[e + 1], vs[e + 1], fast[e + 1], rcp[e + 1]);
+        }
+      }
       uint2 w;
       w.x = e4m3x2(vf[0], vf[1]) | (e4m3x2(vf[2], vf[3]) << 16);
       w.y = e4m3x2(vf[4], vf[5]) | (e4m3x2(vf[6], vf[7]) << 16);
@@ -328,9 +357,14 @@ __global__ void __launch_bounds__(256) quant_tokens_kernel(const __nv_bfloat16* 
   }
   auto values = [&](const uint4& raw, float* out) {  // smoothed values of this lane's 8 channels of a row
     bf16x8_to_f32(raw, out);
+    if constexpr (SMOOTH) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e)
-      if constexpr (SMOOTH) out[e] = __fsub_rn(out[e], mu[e]);
+      for (int e = 0; e < 8; e += 2) {  // x - mu as x + (-mu): the same rounding
+        const float2 d = __fadd2_rn(make_float2(out[e], out[e + 1]), make_float2(-mu[e], -mu[e + 1]));
+        out[e] = d.x;
+        out[e + 1] = d.y;
+      }
+    }
   };
   auto row_offset = [&](int row) { return (((size_t)b * S + row) * H + h) * kHeadDim + cg * 8; };
   for (int t0 = 0; t0 < PER_WARP; t0 += NU) {
@@ -362,7 +396,7 @@ __global__ void __launch_bounds__(256) quant_tokens_kernel(const __nv_bfloat16* 
 #pragma unroll
       for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
       if constexpr (QB > 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
-      const float scale = __fdiv_rn(amax, QMAX);
+      const float scale = scale_of(amax, QMAX, 1.0f / QMAX);
       const bool fast = scale_in_fast_range(scale);
       const float rcp = fast ? __frcp_rn(scale) : 0.0f;
 #pragma unroll
@@ -372,8 +406,7 @@ __global__ void __launch_bounds__(256) quant_tokens_kernel(const __nv_bfloat16* 
         const size_t off = row_offset(row);
         float q[8];
         values(raw[n][it], q);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) q[e] = quotient(q[e], scale, fast, rcp);
+        quotients8(q, scale, fast, rcp);
         if constexpr (OUT == CODE_E4M3) {
           uint2 w;
           w.x = e4m3x2(q[0], q[1]) | (e4m3x2(q[2], q[3]) << 16);

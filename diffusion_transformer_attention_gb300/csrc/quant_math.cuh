@@ -24,4 +24,22 @@ __device__ __forceinline__ float div_by_scale(float x, float s, float r) {
   return __fmaf_rn(__fmaf_rn(-q1, s, x), r, q1);
 }
 
+// div_by_scale on two values at once, with the packed float32 pairs of the FMA pipes: each lane
+// takes the same IEEE steps (round-to-nearest products and fused multiply-adds, subnormals kept),
+// so each result equals div_by_scale's; the remainder x - s * q is formed as fma(q, -s, x).
+__device__ __forceinline__ float2 div2_by_scale(float2 x, float2 s, float2 r) {
+  const float2 ns = make_float2(-s.x, -s.y);
+  const float2 q0 = __fmul2_rn(x, r);
+  const float2 q1 = __ffma2_rn(__ffma2_rn(q0, ns, x), r, q0);
+  return __ffma2_rn(__ffma2_rn(q1, ns, x), r, q1);
+}
+
+// amax / qmax rounded to nearest even, for the block scales (qmax 127 or 448): div_by_scale with the
+// correctly rounded reciprocal of the constant, for amax in [2^-100, 2^120], where the products and
+// remainders neither underflow nor overflow; IEEE division outside that range (and for 0).
+__device__ __forceinline__ float scale_of(float amax, float qmax, float rcp_qmax) {
+  if (amax >= 0x1p-100f && amax <= 0x1p+120f) return div_by_scale(amax, qmax, rcp_qmax);
+  return __fdiv_rn(amax, qmax);
+}
+
 }  // namespace ditattn

@@ -1,6 +1,7 @@
 // Test probe (built by tests/test_gpu_division.py): compares the prepass's reciprocal-based
-// division with IEEE division (__fdiv_rn) bit for bit, for every quotient the quantizers can form
-// (|x / s| <= 448) that can change a code (|x / s| >= 2^-12).
+// division (scalar and packed) with IEEE division (__fdiv_rn) bit for bit, for every quotient the
+// quantizers can form (|x / s| <= 448) that can change a code (|x / s| >= 2^-12), and its block
+// scales amax / qmax for every float32 block max.
 #include <cuda_runtime.h>
 
 #include "../../diffusion_transformer_attention_gb300/csrc/quant_math.cuh"
@@ -17,8 +18,12 @@ __global__ void div_check_kernel(const float* xs, long long nx, const float* ss,
     // quotients the quantizers form (|x| <= absmax = s * QMAX, so |x / s| <= 448) that can change a code
     if (!(fabsf(ref) >= 0x1p-12f && fabsf(ref) <= 448.0f)) continue;
     ++nc;
-    const float q = ditattn::div_by_scale(x, s, __frcp_rn(s));
-    if (__float_as_uint(q) != __float_as_uint(ref)) {
+    const float r = __frcp_rn(s);
+    const float q = ditattn::div_by_scale(x, s, r);
+    // the packed form, with x and -x in its two lanes
+    const float2 q2 = ditattn::div2_by_scale(make_float2(x, -x), make_float2(s, s), make_float2(r, r));
+    if (__float_as_uint(q) != __float_as_uint(ref) || __float_as_uint(q2.x) != __float_as_uint(ref) ||
+        __float_as_uint(q2.y) != __float_as_uint(-ref)) {
       ++nb;
       const unsigned long long slot = atomicAdd(bad + 1, 1ull);  // bad[1]: samples taken so far
       if (slot < 8) {
@@ -31,6 +36,37 @@ __global__ void div_check_kernel(const float* xs, long long nx, const float* ss,
   }
   atomicAdd(bad, nb);
   atomicAdd(checked, nc);
+}
+
+// The block scales: scale_of(amax, qmax) against amax / qmax for qmax 127 and 448, over |x| for
+// every x (a block max is any non-negative float32: a bf16 value, or a smoothed K value).
+__global__ void scale_check_kernel(const float* xs, long long nx, unsigned long long* bad, unsigned long long* checked) {
+  unsigned long long nb = 0, nc = 0;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nx; i += (long long)gridDim.x * blockDim.x) {
+    const float a = fabsf(xs[i]);
+    if (!isfinite(a)) continue;
+    nc += 2;
+    if (__float_as_uint(ditattn::scale_of(a, 127.0f, 1.0f / 127.0f)) != __float_as_uint(__fdiv_rn(a, 127.0f))) ++nb;
+    if (__float_as_uint(ditattn::scale_of(a, 448.0f, 1.0f / 448.0f)) != __float_as_uint(__fdiv_rn(a, 448.0f))) ++nb;
+  }
+  atomicAdd(bad, nb);
+  atomicAdd(checked, nc);
+}
+
+// result_host[0] = mismatches, [1] = values checked.
+extern "C" int scale_check(const float* xs_host, long long nx, unsigned long long* result_host) {
+  float* xs = nullptr;
+  unsigned long long* res = nullptr;
+  if (cudaMalloc(&xs, nx * sizeof(float)) != cudaSuccess) return 1;
+  if (cudaMalloc(&res, 2 * sizeof(unsigned long long)) != cudaSuccess) return 1;
+  cudaMemcpy(xs, xs_host, nx * sizeof(float), cudaMemcpyHostToDevice);
+  cudaMemset(res, 0, 2 * sizeof(unsigned long long));
+  scale_check_kernel<<<152 * 8, 256>>>(xs, nx, res, res + 1);
+  const cudaError_t e = cudaDeviceSynchronize();
+  cudaMemcpy(result_host, res, 2 * sizeof(unsigned long long), cudaMemcpyDeviceToHost);
+  cudaFree(xs);
+  cudaFree(res);
+  return e == cudaSuccess ? 0 : 2;
 }
 
 // result_host[0] = mismatches, [2] = quotients checked; samples_host: up to 8 (x, s, q, ref) rows.

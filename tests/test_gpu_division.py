@@ -5,7 +5,10 @@ agree bit for bit on every quotient the quantizers can form (|x| <= absmax = s *
 bf16 values and a million random float32 values x, against about two thousand scales s spread
 over the range where the fast form is used, with the edge significands (all ones, powers of
 two) included. The codes are also checked end to end against the oracle by the prepass parity
-tests."""
+tests. The packed (two-lane) form of the same division is checked on the same quotients, and the
+block scales amax / 127 and amax / 448, which the quantizers form with the reciprocal of the constant
+inside a range and with IEEE division outside it, on every finite float32 amax of a broad sample.
+"""
 
 import ctypes
 import os
@@ -29,6 +32,7 @@ def _build(tmp_path):
     lib = ctypes.CDLL(so)
     lib.div_check.argtypes = [ctypes.c_void_p, ctypes.c_longlong, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                               ctypes.c_void_p]
+    lib.scale_check.argtypes = [ctypes.c_void_p, ctypes.c_longlong, ctypes.c_void_p]
     return lib
 
 
@@ -65,3 +69,20 @@ def test_reciprocal_division_equals_ieee_division(tmp_path):
     assert checked > 2 * 10 ** 8
     rows = [f"x={a!r} s={b!r} q={c!r} ieee={d!r}" for a, b, c, d in samples[:min(bad, 8)].tolist()]
     assert bad == 0, f"{bad} of {checked} quotients differ, e.g. " + "; ".join(rows)
+
+
+def test_block_scale_division_equals_ieee_division(tmp_path):
+    assert torch.cuda.is_available()
+    lib = _build(tmp_path)
+    bits = np.arange(65536, dtype=np.uint32) << 16  # every bf16 pattern
+    rng = np.random.default_rng(2)
+    rand = rng.integers(0, 1 << 32, 1 << 24, dtype=np.uint64).astype(np.uint32)  # any float32 bit pattern
+    edges = np.array([0x00000000, 0x00000001, 0x007FFFFF, 0x00800000, 0x0D800000, 0x0D7FFFFF, 0x7B800000,
+                      0x7B7FFFFF, 0x7F7FFFFF], np.uint32)  # zero, subnormals, the range ends (2^-100, 2^120)
+    xs = np.concatenate([bits, rand, edges]).view(np.float32)
+    xs = np.ascontiguousarray(xs[np.isfinite(xs)], dtype=np.float32)
+    res = np.zeros(2, np.uint64)
+    assert lib.scale_check(xs.ctypes.data, xs.size, res.ctypes.data) == 0
+    bad, checked = int(res[0]), int(res[1])
+    assert checked == 2 * xs.size
+    assert bad == 0, f"{bad} of {checked} block scales differ from IEEE division"
