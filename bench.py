@@ -628,7 +628,32 @@ def main():
     }
     if modes is not None:
         line["modes"] = modes
+        line["summary"] = summarize(line)
     print(json.dumps(line))
+
+
+def summarize(line):
+    """The numbers the targets are stated in, repeated at the end of the line so that a tail of the
+    log still shows every workload: fractions of each workload's peak (whole call; attention alone
+    where it differs), and the Skip-Softmax speedups over dense BF16 at the sweep point nearest 65%
+    skipped."""
+    m = line["modes"]
+
+    def at65(curve):
+        k = min(range(len(curve["skip"])), key=lambda i: abs(curve["skip"][i] - 0.65))
+        return {"skip": curve["skip"][k], "x": curve["x"][k]}
+
+    vid = m["video_skip_int8_75600"]
+    i8 = at65(vid["sage_int8_1_16_skip"])
+    i8["ceiling_x"] = vid["sage_int8_1_16_skip"]["ceiling_x"][vid["sage_int8_1_16_skip"]["skip"].index(i8["skip"])]
+    return {
+        "dit_dense_32k": line["roofline"]["frac"],
+        "dit_sage_int8_32k": [m["dit_sage_int8_32k"]["frac"], m["dit_sage_int8_32k"]["attn_frac"]],
+        "gqa_sage_fp8_16k": [m["gqa_sage_fp8_16k"]["frac"], m["gqa_sage_fp8_16k"]["attn_frac"]],
+        "video_skip_sage_int8": i8,
+        "video_skip_sage_fp8": at65(m["video_fp8_rate_bmm1"]["sage_fp8_1_16"]),
+        "video_skip_bf16": at65(vid["bf16_skip"]),
+    }
 
 
 if __name__ == "__main__":
