@@ -228,8 +228,11 @@ dit_status run_attention(const void* q, const void* k, const void* v, void* out,
   p.n_q_tiles = ceil_div(Sq, kTile);
   p.n_kv_tiles = ceil_div(Skv, kTile);
   p.c_scale = (float)(1.4426950408889634 / std::sqrt(128.0));  // softmax scale * log2(e)
-  const bool skip = (mode & DIT_MODE_SKIP) != 0;
-  p.log2_thr = (skip && factor > 0.0f) ? (float)std::log2((double)factor / (double)Skv) : -INFINITY;
+  // Skip-Softmax with factor 0 (the threshold 0, the setting of the steps where skipping is off) can skip
+  // nothing: it runs the kernel without the skip test, which gives the same output and LSE and writes
+  // zero skip counts.
+  const bool skip = (mode & DIT_MODE_SKIP) != 0 && factor > 0.0f;
+  p.log2_thr = skip ? (float)std::log2((double)factor / (double)Skv) : -INFINITY;
   p.q_scale = q_scale; p.q_block = q_block; p.nqb = ceil_div(Sq, q_block);
   p.k_scale = k_scale; p.k_block = k_block; p.nkb = ceil_div(Skv, k_block);
   p.v_scale = v_scale;

@@ -64,12 +64,14 @@ namespace {
 
 // Softmax warpgroups per Q tile and the launch shape they imply. Two (each thread holds 64 of a row's
 // 128 columns, the two halves exchange the row max through shared memory) for dense BF16 and SAGE
-// INT8; one (each thread holds the whole row) for the other recipes, all with an E4M3 P (SAGE FP8,
-// QK16PV8, MXFP8, NVFP4). Each measured faster for its recipes on GB300 (with one warpgroup SAGE FP8
-// ran 15% faster, dense 15% and SAGE INT8 2% slower).
-template <int QKF, int PVF>
+// INT8 without Skip-Softmax; one (each thread holds the whole row) for the other recipes, all with an
+// E4M3 P (SAGE FP8, QK16PV8, MXFP8, NVFP4, and SAGE INT8 with Skip-Softmax). Each measured faster for
+// its recipes on GB300 (with one warpgroup SAGE FP8 ran 15% faster, dense 15% slower, SAGE INT8 the
+// same without Skip-Softmax and slower only when that kernel had nothing to skip, which factor 0 no
+// longer sends to it).
+template <int QKF, int PVF, bool SKIP>
 struct Parts {
-  static constexpr int kNH = (PVF == PV_E4M3 && QKF != QK_F16) ? 1 : 2;
+  static constexpr int kNH = (PVF == PV_E4M3 && (QKF != QK_F16 || SKIP)) ? 1 : 2;
   static constexpr int kThreads = 128 + 256 * kNH;
   // launched at 65536 / kThreads registers (rounded down to a multiple of 8); warpgroup 0 (producer,
   // MMA issuers, scale stager) hands registers to the softmax warpgroups
@@ -151,7 +153,7 @@ __device__ __forceinline__ void record_timeout(const FmhaParams& p, Bars* bars) 
 // code is unaffected): the producer issues no copy, so nothing is in flight when the other roles'
 // bounded waits run out and they leave.
 template <int QKF, int PVF, int KB, bool SKIP, bool WITHHOLD = false>
-__global__ void __launch_bounds__(Parts<QKF, PVF>::kThreads, 1)
+__global__ void __launch_bounds__(Parts<QKF, PVF, SKIP>::kThreads, 1)
     fmha_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                     const FmhaParams p) {
@@ -197,7 +199,7 @@ __global__ void __launch_bounds__(Parts<QKF, PVF>::kThreads, 1)
   constexpr uint32_t kIdesc2 = (PVF == PV_BF16) ? make_idesc(1, 1, 0, 1, 128, 128) : make_idesc(0, 0, 0, 1, 128, 128);
 
   using L = SmemLayout<QKF, PVF>;
-  using P = Parts<QKF, PVF>;
+  using P = Parts<QKF, PVF, SKIP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + L::kBarOff);
@@ -1378,14 +1380,14 @@ cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
     cudaFuncAttributes fa;
     e = cudaFuncGetAttributes(&fa, fmha_fwd_kernel<QKF, PVF, KB, SKIP, WITHHOLD>);
     if (e != cudaSuccess) return e;
-    if (fa.numRegs != Parts<QKF, PVF>::kLaunchRegs) return cudaErrorInvalidKernelImage;
+    if (fa.numRegs != Parts<QKF, PVF, SKIP>::kLaunchRegs) return cudaErrorInvalidKernelImage;
     e = cudaFuncSetAttribute(fmha_fwd_kernel<QKF, PVF, KB, SKIP, WITHHOLD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SmemLayout<QKF, PVF>::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set[dev].store(true, std::memory_order_release);
   }
   const dim3 grid((p.Sq + 255) / 256, p.Hq, p.B);
-  fmha_fwd_kernel<QKF, PVF, KB, SKIP, WITHHOLD><<<grid, Parts<QKF, PVF>::kThreads, SmemLayout<QKF, PVF>::kSmemBytes, stream>>>(tq, tk, tv, to, p);
+  fmha_fwd_kernel<QKF, PVF, KB, SKIP, WITHHOLD><<<grid, Parts<QKF, PVF, SKIP>::kThreads, SmemLayout<QKF, PVF>::kSmemBytes, stream>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 
