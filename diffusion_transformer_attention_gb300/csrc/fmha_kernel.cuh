@@ -282,36 +282,34 @@ __global__ void __launch_bounds__(Parts<QKF, PVF, SKIP>::kThreads, 1)
       // reader of V_j's buffer), so a V buffer still in use never holds back the next K tile.
       // Otherwise K_j, V_j, K_{j+1}, ... Each slot receives its tiles in order either way.
       for (int n = 0; n <= 2 * nt && ok; ++n) {
-        {
-          int j, kv;
-          if constexpr (kKAhead) {
-            j = (n == 0) ? 0 : ((n & 1) ? (n + 1) >> 1 : (n >> 1) - 1);
-            kv = (n == 0) ? 0 : ((n & 1) ? 0 : 1);
-            if (kv == 0 && j >= nt) continue;  // no K_{j+1} after the last tile
-          } else {
-            if (n == 2 * nt) break;
-            j = n >> 1;
-            kv = n & 1;
-          }
-          const int t = 2 * j + kv, s = t & (kSlots - 1), u = t / kSlots;
-          if (!mbar_wait_bounded(&bars->kv_empty[s], (u & 1) ^ 1, budget, abort_flag)) {
-            record_timeout(p, bars);
-            ok = false;
-            break;
-          }
-          uint8_t* dst = smem + (kv ? L::kVOff + (s >> 1) * L::kVTile : L::kKOff + (s >> 1) * L::kKTile);
-          const CUtensorMap* map = kv ? &tm_v : &tm_k;
-          const int bytes = kv ? kVTileBytes : kQTileBytes;
-          const int eb = kv ? kPVBytes : kQKBytes;
-          mbar_arrive_expect_tx(&bars->kv_full[s], bytes);
-          if (eb == 2) {
-            tma_load_4d(dst, map, &bars->kv_full[s], 0, 128 * j, hkv, b, pol_kv);
-            tma_load_4d(dst + 16384, map, &bars->kv_full[s], 64, 128 * j, hkv, b, pol_kv);
-          } else {
-            tma_load_4d(dst, map, &bars->kv_full[s], 0, 128 * j, hkv, b, pol_kv);
-          }
-          ++issued[s];
+        int j, kv;
+        if constexpr (kKAhead) {
+          j = (n == 0) ? 0 : ((n & 1) ? (n + 1) >> 1 : (n >> 1) - 1);
+          kv = (n == 0) ? 0 : ((n & 1) ? 0 : 1);
+          if (kv == 0 && j >= nt) continue;  // no K_{j+1} after the last tile
+        } else {
+          if (n == 2 * nt) break;
+          j = n >> 1;
+          kv = n & 1;
         }
+        const int t = 2 * j + kv, s = t & (kSlots - 1), u = t / kSlots;
+        if (!mbar_wait_bounded(&bars->kv_empty[s], (u & 1) ^ 1, budget, abort_flag)) {
+          record_timeout(p, bars);
+          ok = false;
+          break;
+        }
+        uint8_t* dst = smem + (kv ? L::kVOff + (s >> 1) * L::kVTile : L::kKOff + (s >> 1) * L::kKTile);
+        const CUtensorMap* map = kv ? &tm_v : &tm_k;
+        const int bytes = kv ? kVTileBytes : kQTileBytes;
+        const int eb = kv ? kPVBytes : kQKBytes;
+        mbar_arrive_expect_tx(&bars->kv_full[s], bytes);
+        if (eb == 2) {
+          tma_load_4d(dst, map, &bars->kv_full[s], 0, 128 * j, hkv, b, pol_kv);
+          tma_load_4d(dst + 16384, map, &bars->kv_full[s], 64, 128 * j, hkv, b, pol_kv);
+        } else {
+          tma_load_4d(dst, map, &bars->kv_full[s], 0, 128 * j, hkv, b, pol_kv);
+        }
+        ++issued[s];
       }
       if (!ok) {
         // drain: wait (bounded) for every copy this thread started before shared memory goes away
