@@ -151,6 +151,10 @@ struct HostEvents {
 };
 HostEvents g_host_events[64];
 std::mutex g_host_mu;
+// Held by dit_attn_fwd_host while it queues a call's work: concurrent calls from several host threads
+// then queue one after the other. Reusing the events is safe once a call is queued, since each stream
+// wait binds to the record that precedes it at the time it is queued.
+std::mutex g_host_call_mu;
 
 HostEvents* host_events() {
   int dev = -1;
@@ -734,6 +738,7 @@ dit_status dit_attn_fwd_host(const void* q_host, const void* k_host, const void*
   if (ds != DIT_OK) return ds;
   HostEvents* ev = host_events();
   if (ev == nullptr) return DIT_E_CUDA;
+  std::lock_guard<std::mutex> call_lock(g_host_call_mu);
   cudaStream_t cs = static_cast<cudaStream_t>(compute_stream);
   cudaStream_t hs = static_cast<cudaStream_t>(h2d_stream);
   cudaStream_t ds2 = static_cast<cudaStream_t>(d2h_stream);

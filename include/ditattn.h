@@ -171,7 +171,9 @@ dit_status dit_attn_fwd_lse(const void* q, const void* k, const void* v, void* o
  * Consecutive groups' kernels alternate between compute_stream and a stream of the library's, so one
  * kernel's last partial wave overlaps the next one's first. The first call on a device creates that
  * stream and the library's events for this entry point (a one-time set-up; make it before any stream
- * capture). Calls must not be issued from several host threads at once.
+ * capture). Calls may come from several host threads: they share those events and that stream, so
+ * each call queues its work while holding a library lock, and calls queued at the same time run one
+ * after the other on the library's stream.
  */
 dit_status dit_attn_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* out_host, void* q,
                              void* k, void* v, void* out, int B, int Hq, int Hkv, int Sq, int Skv, int mode,

@@ -2,7 +2,7 @@
 kernels over groups of kv heads) writes exactly dit_attn_fwd's output, bit for bit, for any number
 of groups (equal ones, and the ramp of 1, 2, 4, ..., 1 kv heads), with the three streams distinct or the
 same, with page-locked or pageable host buffers (the first and last transfers by a copy kernel or by
-the copy engines), and with Skip-Softmax."""
+the copy engines), with Skip-Softmax, and from two host threads at once."""
 
 import pytest
 import torch
@@ -60,3 +60,40 @@ def test_pageable_buffers_take_the_copy_engines(pinned):
     # buffer is page-locked; pageable ones (either side) must give the same result through cudaMemcpy2D
     got, want = _run(workloads.Workload("h", 1, 24, 12, 200, 300, kind="koffset"), 5, pinned=pinned)
     assert torch.equal(got, want)
+
+
+def test_concurrent_calls_from_two_host_threads():
+    # the calls share the library's events and stream; each queues its work under a lock, so two
+    # threads calling at once (each with its own buffers and streams) both get dit_attn_fwd's output
+    import threading
+    w = workloads.Workload("h", 1, 8, 4, 384, 640, kind="koffset")
+    jobs = []
+    for t in range(2):
+        q, k, v = workloads.generate(w, seed=200 + t)
+        hq, hk, hv = (x.pin_memory() for x in (q, k, v))
+        hout = torch.full(q.shape, float("nan"), dtype=q.dtype).pin_memory()
+        dev = [torch.empty_like(x, device="cuda") for x in (q, k, v, q)]
+        streams = [torch.cuda.Stream() for _ in range(3)]
+        want = dit.dit_attn_fwd(q.cuda(), k.cuda(), v.cuda()).cpu()
+        jobs.append((hq, hk, hv, hout, dev, streams, want))
+    torch.cuda.synchronize()
+    errors = []
+
+    def work(job):
+        hq, hk, hv, hout, dev, (cs, h2d, d2h), _ = job
+        try:
+            for _ in range(20):
+                dit.dit_attn_fwd_host(hq, hk, hv, hout, *dev, chunks=4, stream=cs, h2d_stream=h2d, d2h_stream=d2h)
+            cs.synchronize()
+        except Exception as e:  # reported below, on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(job,)) for job in jobs]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    dit.dit_attn_check_errors()
+    for job in jobs:
+        assert torch.equal(job[3], job[6])
