@@ -26,10 +26,12 @@ QK_BF16, QK_INT8, QK_FP8_E4M3, QK_MXFP8, QK_NVFP4 = 0, 1, 2, 3, 4
 HEAD_DIM = 128
 TILE = 128
 STATUS_NAMES = {0: "DIT_OK", 1: "DIT_E_INVALID_ARG", 2: "DIT_E_UNSUPPORTED", 3: "DIT_E_CUDA", 4: "DIT_E_TIMEOUT",
-                5: "DIT_E_WORKSPACE"}
+                5: "DIT_E_WORKSPACE", 6: "DIT_E_BOUNDS"}
 QK_DTYPES = {"bf16": QK_BF16, "int8": QK_INT8, "fp8_e4m3": QK_FP8_E4M3, "mxfp8": QK_MXFP8, "nvfp4": QK_NVFP4}
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libditattn.so")
+# the in-tree build; DITATTN_LIBRARY may name another build of the same library (the bounds-checked one)
+LIB_PATH = os.environ.get("DITATTN_LIBRARY") or os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib",
+                                                             "libditattn.so")
 
 # Every symbol include/ditattn.h declares, with its ctypes signature.
 _c_int, _c_float, _c_size, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_void_p

@@ -1,9 +1,12 @@
 """Build libditattn.so (the C-ABI library) in-tree with nvcc for sm_103a.
 
-Usage: python -m diffusion_transformer_attention_gb300.build_lib [--verbose]
+Usage: python -m diffusion_transformer_attention_gb300.build_lib [--verbose] [--bounds-check]
 
 The translation units are compiled in parallel and linked with the static CUDA runtime, so the
-library loads on machines without a GPU (its calls then return DIT_E_UNSUPPORTED).
+library loads on machines without a GPU (its calls then return DIT_E_UNSUPPORTED). --bounds-check
+builds a debug variant into _lib_bounds/ instead: the attention kernels check their computed global
+and shared-memory indices and report one outside its buffer as DIT_E_BOUNDS (set DITATTN_LIBRARY to
+its path to load it).
 """
 
 from __future__ import annotations
@@ -32,10 +35,13 @@ def nvcc() -> str:
     return path
 
 
-def _compile(src: str, verbose: bool) -> str:
-    obj = os.path.join(OUT_DIR, os.path.splitext(src)[0] + ".o")
+BOUNDS_DIR = os.path.join(PKG, "_lib_bounds")
+
+
+def _compile(src: str, verbose: bool, out_dir: str = OUT_DIR, defines=()) -> str:
+    obj = os.path.join(out_dir, os.path.splitext(src)[0] + ".o")
     cmd = [nvcc(), *ARCH, "-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include"),
-           "-c", os.path.join(CSRC, src), "-o", obj]
+           *[f"-D{d}" for d in defines], "-c", os.path.join(CSRC, src), "-o", obj]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     res = subprocess.run(cmd, capture_output=True, text=True)
@@ -46,18 +52,21 @@ def _compile(src: str, verbose: bool) -> str:
     return obj
 
 
-def build(verbose: bool = False) -> str:
-    os.makedirs(OUT_DIR, exist_ok=True)
+def build(verbose: bool = False, bounds_check: bool = False) -> str:
+    out_dir = BOUNDS_DIR if bounds_check else OUT_DIR
+    lib = os.path.join(out_dir, "libditattn.so")
+    defines = ("DITATTN_BOUNDS_CHECK",) if bounds_check else ()
+    os.makedirs(out_dir, exist_ok=True)
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose), SOURCES))
-    tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, verbose, out_dir, defines), SOURCES))
+    tmp = lib + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(verbose="--verbose" in sys.argv))
+    print(build(verbose="--verbose" in sys.argv, bounds_check="--bounds-check" in sys.argv))

@@ -349,6 +349,7 @@ const char* dit_status_string(dit_status s) {
     case DIT_E_CUDA: return "CUDA error";
     case DIT_E_TIMEOUT: return "kernel wait timed out";
     case DIT_E_WORKSPACE: return "workspace missing or too small";
+    case DIT_E_BOUNDS: return "index outside its buffer (bounds-checked build)";
   }
   return "unknown status";
 }

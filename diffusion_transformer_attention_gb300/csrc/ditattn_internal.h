@@ -23,6 +23,7 @@ enum CodeOut { CODE_I8 = 0, CODE_I8_AS_F16 = 1, CODE_E4M3 = 2 };
 
 // Device error word codes (match dit_status).
 constexpr int kErrTimeout = 4;
+constexpr int kErrBounds = 6;  // DIT_E_BOUNDS: only a bounds-checked build records it
 
 struct FmhaParams {
   int B, Hq, Hkv, Sq, Skv;

@@ -143,6 +143,21 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= 512, "barrier block too large");
 
+// Bounds checks of computed indices, compiled only into a library built with DITATTN_BOUNDS_CHECK (a
+// debug build): an index outside its buffer records DIT_E_BOUNDS in the device error word (unless a
+// timeout is already recorded) and the caller skips that access. The default build compiles every
+// check to `true` and its arguments away.
+#ifdef DITATTN_BOUNDS_CHECK
+__device__ __forceinline__ bool index_ok(int* err, long long idx, long long n) {
+  if (idx >= 0 && idx < n) return true;
+  atomicCAS(err, 0, kErrBounds);
+  return false;
+}
+#define DIT_INDEX_OK(err, idx, n) ::ditattn::index_ok((err), (long long)(idx), (long long)(n))
+#else
+#define DIT_INDEX_OK(err, idx, n) true
+#endif
+
 __device__ __forceinline__ void record_timeout(const FmhaParams& p, Bars* bars) {
   atomicExch(p.err, kErrTimeout);
   *reinterpret_cast<volatile int*>(&bars->abort_flag) = 1;
@@ -497,7 +512,11 @@ __global__ void __launch_bounds__(Parts<QKF, PVF, SKIP>::kThreads, 1)
     if constexpr (kPV8) {
       const float* vs = p.v_scale + ((size_t)b * p.Hkv + hkv) * kHeadDim;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) s_vs[lane * 4 + e] = vs[lane * 4 + e];
+      for (int e = 0; e < 4; ++e)
+        s_vs[lane * 4 + e] = DIT_INDEX_OK(p.err, ((long long)b * p.Hkv + hkv) * kHeadDim + lane * 4 + e,
+                                          (long long)p.B * p.Hkv * kHeadDim)
+                                 ? vs[lane * 4 + e]
+                                 : 0.0f;
       mbar_arrive(&bars->vs_full);
     }
     if constexpr (kBS) {
@@ -508,8 +527,11 @@ __global__ void __launch_bounds__(Parts<QKF, PVF, SKIP>::kThreads, 1)
       // copy puts them in columns 0-3 of lane l of each lane quarter, where the MMA reads row 32c + l
       // from column c. Rows past the end get 0 (their codes are zero, as TMA fills them).
       constexpr int W = (int)kSfWords;
-      auto load_words = [&](const uint32_t* base, int row, int nrows, uint32_t* w) {
-        if (row < nrows) {
+      // base_words / all_words: the offset of `base` in its array and the array's size, in words
+      // (bounds-checked builds only)
+      auto load_words = [&](const uint32_t* base, long long base_words, long long all_words, int row, int nrows,
+                            uint32_t* w) {
+        if (row < nrows && DIT_INDEX_OK(p.err, base_words + (long long)row * W + (W - 1), all_words)) {
           if constexpr (W == 2) {
             const uint2 u = __ldg(reinterpret_cast<const uint2*>(base) + row);
             w[0] = u.x;
@@ -527,7 +549,9 @@ __global__ void __launch_bounds__(Parts<QKF, PVF, SKIP>::kThreads, 1)
       for (int t = 0; t < 2; ++t) {
         uint32_t w[4][W];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) load_words(qsf, q0 + 128 * t + 32 * c + lane, p.Sq, w[c]);
+        for (int c = 0; c < 4; ++c)
+          load_words(qsf, ((long long)b * p.Hq + hq) * p.Sq * W, (long long)p.B * p.Hq * p.Sq * W,
+                     q0 + 128 * t + 32 * c + lane, p.Sq, w[c]);
 #pragma unroll
         for (int ww = 0; ww < W; ++ww)
           *reinterpret_cast<uint4*>(smem + L::kSfaOff + (t * W + ww) * 512 + lane * 16) =
@@ -538,7 +562,9 @@ __global__ void __launch_bounds__(Parts<QKF, PVF, SKIP>::kThreads, 1)
       const uint32_t* ksf = reinterpret_cast<const uint32_t*>(p.k_sf) + ((size_t)b * p.Hkv + hkv) * p.Skv * W;
       auto load_tile = [&](int j, uint32_t (*w)[L::kSfWords]) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) load_words(ksf, 128 * j + 32 * c + lane, j < nt ? p.Skv : 0, w[c]);
+        for (int c = 0; c < 4; ++c)
+          load_words(ksf, ((long long)b * p.Hkv + hkv) * p.Skv * W, (long long)p.B * p.Hkv * p.Skv * W,
+                     128 * j + 32 * c + lane, j < nt ? p.Skv : 0, w[c]);
       };
       constexpr int kAhead = (W == 2) ? 2 : 4;
       uint32_t pre[kAhead][4][W];
@@ -577,7 +603,10 @@ __global__ void __launch_bounds__(Parts<QKF, PVF, SKIP>::kThreads, 1)
         for (int q = 0; q < 4; ++q) {
           const int g = lane * 4 + q;
           const int col = 128 * j + g * KB;
-          v[q] = (j < nt && g < 128 / KB && col < p.Skv) ? __ldg(ks + col / KB) : 0.0f;
+          v[q] = (j < nt && g < 128 / KB && col < p.Skv &&
+                  DIT_INDEX_OK(p.err, ((long long)b * p.Hkv + hkv) * p.nkb + col / KB, (long long)p.B * p.Hkv * p.nkb))
+                     ? __ldg(ks + col / KB)
+                     : 0.0f;
         }
       };
       constexpr int kAhead = 4;
@@ -623,7 +652,10 @@ __global__ void __launch_bounds__(Parts<QKF, PVF, SKIP>::kThreads, 1)
       float c = p.c_scale;
       if constexpr (kNV) c = c / (__ldg(p.q_gs) * __ldg(p.k_gs));  // BMM1 carries both tensor scales
       if constexpr (kQKScaled) {
-        const float qs = row_valid ? __ldg(p.q_scale + ((size_t)b * p.Hq + hq) * p.nqb + qrow / p.q_block) : 0.0f;
+        const float qs = (row_valid && DIT_INDEX_OK(p.err, ((long long)b * p.Hq + hq) * p.nqb + qrow / p.q_block,
+                                                    (long long)p.B * p.Hq * p.nqb))
+                             ? __ldg(p.q_scale + ((size_t)b * p.Hq + hq) * p.nqb + qrow / p.q_block)
+                             : 0.0f;
         c = qs * p.c_scale;
       }
       float m_ex = -INFINITY, m_ref = -INFINITY, l = 0.0f;
@@ -846,8 +878,9 @@ __global__ void __launch_bounds__(Parts<QKF, PVF, SKIP>::kThreads, 1)
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int ch = 4 * h + q;
-            *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) =
-                make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+            if (DIT_INDEX_OK(p.err, (prow - (smem + L::kPOff)) + ((ch ^ (r & 7)) << 4), L::kPBufs * 2 * 16384 - 15))
+              *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) =
+                  make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
           }
           fence_proxy_async_smem();  // visible to the tensor cores' reads
         }
@@ -908,7 +941,8 @@ __global__ void __launch_bounds__(Parts<QKF, PVF, SKIP>::kThreads, 1)
         // ln sum_j exp(s_j) = ln 2 * (m_ref + log2 l), with l relative to m_ref (and carrying P's 448
         // with E4M3 P); only the kept KV tiles contribute under Skip-Softmax, as to the output
         const float l_true = kPV8 ? l_row * (1.0f / 448.0f) : l_row;
-        p.lse[((size_t)b * p.Hq + hq) * p.Sq + qrow] = 0.69314718055994531f * (m_ref + log2f(l_true));
+        if (DIT_INDEX_OK(p.err, ((long long)b * p.Hq + hq) * p.Sq + qrow, (long long)p.B * p.Hq * p.Sq))
+          p.lse[((size_t)b * p.Hq + hq) * p.Sq + qrow] = 0.69314718055994531f * (m_ref + log2f(l_true));
       }
       if (ok) {
         ok = mbar_wait_bounded(&bars->o_full[i], 0, budget, abort_flag);
@@ -944,8 +978,9 @@ __global__ void __launch_bounds__(Parts<QKF, PVF, SKIP>::kThreads, 1)
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int ch = cc * 4 + q;
-            *reinterpret_cast<uint4*>(rowp + ((ch ^ (r & 7)) << 4)) =
-                make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+            if (DIT_INDEX_OK(p.err, (rowp - (smem + L::kQOff + i * 32768)) + ((ch ^ (r & 7)) << 4), 32768 - 15))
+              *reinterpret_cast<uint4*>(rowp + ((ch ^ (r & 7)) << 4)) =
+                  make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
           }
         }
         fence_proxy_async_smem();
@@ -958,7 +993,9 @@ __global__ void __launch_bounds__(Parts<QKF, PVF, SKIP>::kThreads, 1)
       }
       if (r == 0 && h == 0 && p.skip_counts != nullptr) {
         const int qt = 2 * blockIdx.x + i;
-        if (qt < p.n_q_tiles) p.skip_counts[((size_t)b * p.Hq + hq) * p.n_q_tiles + qt] = nskip;
+        if (qt < p.n_q_tiles && DIT_INDEX_OK(p.err, ((long long)b * p.Hq + hq) * p.n_q_tiles + qt,
+                                             (long long)p.B * p.Hq * p.n_q_tiles))
+          p.skip_counts[((size_t)b * p.Hq + hq) * p.n_q_tiles + qt] = nskip;
       }
     } else {
       // ------------------------------------------------------------ softmax warpgroups
@@ -982,7 +1019,10 @@ __global__ void __launch_bounds__(Parts<QKF, PVF, SKIP>::kThreads, 1)
       float c = p.c_scale;
       if constexpr (kNV) c = c / (__ldg(p.q_gs) * __ldg(p.k_gs));  // BMM1 carries both tensor scales
       if constexpr (kQKScaled) {
-        const float qs = row_valid ? __ldg(p.q_scale + ((size_t)b * p.Hq + hq) * p.nqb + qrow / p.q_block) : 0.0f;
+        const float qs = (row_valid && DIT_INDEX_OK(p.err, ((long long)b * p.Hq + hq) * p.nqb + qrow / p.q_block,
+                                                    (long long)p.B * p.Hq * p.nqb))
+                             ? __ldg(p.q_scale + ((size_t)b * p.Hq + hq) * p.nqb + qrow / p.q_block)
+                             : 0.0f;
         c = qs * p.c_scale;
       }
       float m_ex = -INFINITY, m_ref = -INFINITY, l = 0.0f;
@@ -1219,9 +1259,11 @@ __global__ void __launch_bounds__(Parts<QKF, PVF, SKIP>::kThreads, 1)
           for (int cq = 0; cq < NC / 16; ++cq) {
             const uint32_t ch = (uint32_t)((NC / 16) * h + cq);
             const float* x = s + 16 * cq;
-            *reinterpret_cast<uint4*>(p_row0 + (kDblP ? (n_pv & 1) * 16384 : 0) + ((ch ^ sw) << 4)) =
-                make_uint4(pack_e4m3x4(x[0], x[1], x[2], x[3]), pack_e4m3x4(x[4], x[5], x[6], x[7]),
-                           pack_e4m3x4(x[8], x[9], x[10], x[11]), pack_e4m3x4(x[12], x[13], x[14], x[15]));
+            if (DIT_INDEX_OK(p.err, (p_row0 - (smem + L::kPOff)) + (kDblP ? (n_pv & 1) * 16384 : 0) + ((ch ^ sw) << 4),
+                             L::kPBufs * 2 * 16384 - 15))
+              *reinterpret_cast<uint4*>(p_row0 + (kDblP ? (n_pv & 1) * 16384 : 0) + ((ch ^ sw) << 4)) =
+                  make_uint4(pack_e4m3x4(x[0], x[1], x[2], x[3]), pack_e4m3x4(x[4], x[5], x[6], x[7]),
+                             pack_e4m3x4(x[8], x[9], x[10], x[11]), pack_e4m3x4(x[12], x[13], x[14], x[15]));
           }
           fence_proxy_async_smem();  // visible to the tensor cores' reads
         }
@@ -1290,7 +1332,8 @@ __global__ void __launch_bounds__(Parts<QKF, PVF, SKIP>::kThreads, 1)
         // ln sum_j exp(s_j) = ln 2 * (m_ref + log2 l), with l relative to m_ref (and carrying P's 448
         // with E4M3 P); only the kept KV tiles contribute under Skip-Softmax, as to the output
         const float l_true = kPV8 ? l_row * (1.0f / 448.0f) : l_row;
-        p.lse[((size_t)b * p.Hq + hq) * p.Sq + qrow] = 0.69314718055994531f * (m_ref + log2f(l_true));
+        if (DIT_INDEX_OK(p.err, ((long long)b * p.Hq + hq) * p.Sq + qrow, (long long)p.B * p.Hq * p.Sq))
+          p.lse[((size_t)b * p.Hq + hq) * p.Sq + qrow] = 0.69314718055994531f * (m_ref + log2f(l_true));
       }
       if (ok) {
         ok = mbar_wait_bounded(&bars->o_full[i], 0, budget, abort_flag);
@@ -1330,7 +1373,8 @@ __global__ void __launch_bounds__(Parts<QKF, PVF, SKIP>::kThreads, 1)
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const uint32_t ch = (uint32_t)(((gc & 63) >> 3) + q);
-            sts128(rowp + ((ch ^ sw) << 4), w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+            if (DIT_INDEX_OK(p.err, (long long)(rowp - stage) + ((ch ^ sw) << 4), 32768 - 15))
+              sts128(rowp + ((ch ^ sw) << 4), w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
           }
         }
         fence_proxy_async_smem();
@@ -1348,7 +1392,9 @@ __global__ void __launch_bounds__(Parts<QKF, PVF, SKIP>::kThreads, 1)
       }
       if (r == 0 && h == 0 && p.skip_counts != nullptr) {
         const int qt = 2 * blockIdx.x + i;
-        if (qt < p.n_q_tiles) p.skip_counts[((size_t)b * p.Hq + hq) * p.n_q_tiles + qt] = nskip;
+        if (qt < p.n_q_tiles && DIT_INDEX_OK(p.err, ((long long)b * p.Hq + hq) * p.n_q_tiles + qt,
+                                             (long long)p.B * p.Hq * p.n_q_tiles))
+          p.skip_counts[((size_t)b * p.Hq + hq) * p.n_q_tiles + qt] = nskip;
       }
     }
   }

@@ -65,7 +65,10 @@ typedef enum dit_status {
   DIT_E_UNSUPPORTED = 2, /* no CUDA device, or the current device is not sm_103 */
   DIT_E_CUDA = 3,        /* a CUDA runtime/driver call or a kernel launch failed */
   DIT_E_TIMEOUT = 4,     /* a kernel gave up waiting (reported by dit_attn_check_errors) */
-  DIT_E_WORKSPACE = 5    /* workspace missing or smaller than the *_workspace_bytes query */
+  DIT_E_WORKSPACE = 5,   /* workspace missing or smaller than the *_workspace_bytes query */
+  DIT_E_BOUNDS = 6       /* a library built with device-side bounds checks (DITATTN_BOUNDS_CHECK) found
+                            a computed index outside its buffer and skipped that access (reported by
+                            dit_attn_check_errors); never returned by the default build */
 } dit_status;
 
 /* Mode bits (or-able): DIT_MODE_SAGE | DIT_MODE_SKIP is SAGE with Skip-Softmax.

@@ -48,8 +48,9 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_status_strings(lib):
     assert dit.dit_status_string(0) == "ok"
-    for s in range(6):
-        assert dit.dit_status_string(s)
+    for s in range(7):
+        assert dit.dit_status_string(s) and dit.dit_status_string(s) != "unknown status"
+    assert dit.dit_status_string(6).startswith("index outside its buffer")
     assert lib.dit_abi_version() == 4
 
 
