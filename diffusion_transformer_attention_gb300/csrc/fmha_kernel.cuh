@@ -1278,7 +1278,18 @@ __global__ void __launch_bounds__(Parts<QKF, PVF, SKIP>::kThreads, 1)
             }
           }
           const float2 a2 = make_float2(alpha, alpha);
-          if constexpr (NC == 128 || (kQKScaled && KB >= 16)) {
+          if constexpr (NC == 128 && kBS) {
+            // MXFP8 / NVFP4: the whole row in one round, S's registers being free by now (measured
+            // faster for them; slower for QK16PV8 and SAGE FP8, and SAGE FP8 with K blocks of 16 spills)
+            float2 o[64];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tmem_ld32(t_o + 32 * q, reinterpret_cast<float*>(o + 16 * q));
+            tmem_ld_wait();
+#pragma unroll
+            for (int k = 0; k < 64; ++k) o[k] = __fmul2_rn(o[k], a2);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tmem_st32(t_o + 32 * q, reinterpret_cast<const uint32_t*>(o + 16 * q));
+          } else if constexpr (NC == 128 || (kQKScaled && KB >= 16)) {
             // rounds of 64 columns with one wait each (measured faster with K blocks of 16; with finer
             // blocks and 64 columns per thread the rounds of 32 below are faster)
 #pragma unroll 1
