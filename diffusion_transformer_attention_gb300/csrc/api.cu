@@ -438,7 +438,7 @@ dit_status fwd_impl(const void* q, const void* k, const void* v, void* out, int 
   const int code_out = (qk_dtype == DIT_QK_INT8) ? CODE_I8_AS_F16 : CODE_E4M3;
   cudaError_t e = launch_kv_stats(k, v, B, Hkv, Skv, reinterpret_cast<double*>(ws + L.psum),
                                   reinterpret_cast<float*>(ws + L.pmax), k_mean, v_scale, st);
-  if (e == cudaSuccess) e = launch_quant_q(q, B, Hq, Sq, q_block, code_out, ws + L.q_codes, q_scale, st);
+  if (e == cudaSuccess) e = launch_quant_q(q, B, Hq, Sq, q_block, code_out, ws + L.q_codes, q_scale, st, true);
   if (e == cudaSuccess)
     e = launch_quant_kv(k, v, B, Hkv, Skv, k_block, code_out, k_mean, v_scale, ws + L.k_codes, k_scale,
                         ws + L.v_codes, st);
@@ -499,7 +499,7 @@ dit_status sage_quantize_qkv(const void* q, const void* k, const void* v, int B,
   const int code_out = (qk_dtype == DIT_QK_INT8) ? CODE_I8 : CODE_E4M3;
   cudaError_t e = launch_kv_stats(k, v, B, Hkv, Skv, reinterpret_cast<double*>(ws),
                                   reinterpret_cast<float*>(ws + align256(n * 8)), k_mean, v_scale, st);
-  if (e == cudaSuccess && Sq > 0) e = launch_quant_q(q, B, Hq, Sq, q_block, code_out, q_codes, q_scale, st);
+  if (e == cudaSuccess && Sq > 0) e = launch_quant_q(q, B, Hq, Sq, q_block, code_out, q_codes, q_scale, st, true);
   if (e == cudaSuccess)
     e = launch_quant_kv(k, v, B, Hkv, Skv, k_block, code_out, k_mean, v_scale, k_codes, k_scale, v_codes, st);
   return from_cuda(e);

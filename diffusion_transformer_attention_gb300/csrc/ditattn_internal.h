@@ -71,7 +71,11 @@ cudaError_t launch_fmha_nvfp4(bool skip, const CUtensorMap& tq, const CUtensorMa
 cudaError_t launch_fmha_mxfp8(bool skip, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const CUtensorMap& to, const FmhaParams& p, cudaStream_t stream);
 
-// Quantize-prepass launchers (prepass.cu).
+// Quantize-prepass launchers (prepass.cu). launch_kv_stats, then launch_quant_q with after_stats
+// set, then launch_quant_kv is the SAGE order: the Q quantizer then starts while the statistics are
+// combined, and the V quantizer while the K quantizer's last CTAs run (programmatic dependent launch);
+// each kernel in that chain still completes after the one before it, so an ordinary launch after
+// launch_quant_kv sees all of their results.
 cudaError_t launch_kv_stats(const void* k, const void* v, int B, int Hkv, int Skv, double* psum, float* pmax,
                             float* k_mean, float* v_scale, cudaStream_t stream);
 // V alone (QK16PV8): per-channel absmax scales, optionally reduced to one tensor-wide scale
@@ -81,7 +85,7 @@ cudaError_t launch_v_stats(const void* v, int B, int Hkv, int Skv, float* pmax, 
 cudaError_t launch_quant_v(const void* v, int B, int Hkv, int Skv, const float* v_scale, void* v_codes,
                            cudaStream_t stream);
 cudaError_t launch_quant_q(const void* q, int B, int Hq, int Sq, int q_block, int code_out, void* q_codes,
-                           float* q_scale, cudaStream_t stream);
+                           float* q_scale, cudaStream_t stream, bool after_stats = false);
 cudaError_t launch_quant_kv(const void* k, const void* v, int B, int Hkv, int Skv, int k_block, int code_out,
                             const float* k_mean, const float* v_scale, void* k_codes, float* k_scale, void* v_codes,
                             cudaStream_t stream);

@@ -92,7 +92,7 @@ dit_status sage_quantize_qkv_noalloc(const void* q, const void* k, const void* v
   const int code_out = (qk_dtype == DIT_QK_INT8) ? CODE_I8 : CODE_E4M3;
   cudaError_t e = launch_kv_stats(k, v, B, Hkv, Skv, reinterpret_cast<double*>(scratch),
                                   reinterpret_cast<float*>(scratch + sum_bytes), k_mean, v_scale, st);
-  if (e == cudaSuccess && Sq > 0) e = launch_quant_q(q, B, Hq, Sq, q_block, code_out, q_codes, q_scale, st);
+  if (e == cudaSuccess && Sq > 0) e = launch_quant_q(q, B, Hq, Sq, q_block, code_out, q_codes, q_scale, st, true);
   if (e == cudaSuccess)
     e = launch_quant_kv(k, v, B, Hkv, Skv, k_block, code_out, k_mean, v_scale, k_codes, k_scale, v_codes, st);
   if (e != cudaSuccess) {

@@ -39,6 +39,18 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   return r;
 }
 
+// Programmatic dependent launch. A kernel launched with the programmatic stream serialization
+// attribute may start once every CTA of the kernel before it in the stream has started or exited
+// and executed launch_dependents; griddepcontrol.wait then returns once that kernel has completed
+// and its writes are visible. Under an ordinary launch both are no-ops. The quantizers call
+// launch_dependents first and wait last: the next kernel may fill the SMs their last wave leaves
+// idle, and a quantizer still completes only after the kernel before it, so an ordinary launch
+// that follows the chain waits for all of it.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -62,12 +74,14 @@ __device__ __forceinline__ float quotient(float x, float scale, bool fast, float
 }
 
 // quotient() of a lane's eight values by one block scale, two at a time on the packed pipes
+// (ZERO_SIGN: see div2_by_scale; false only where the codes are INT8)
+template <bool ZERO_SIGN>
 __device__ __forceinline__ void quotients8(float* q, float scale, bool fast, float rcp) {
   if (fast) {
     const float2 s2 = make_float2(scale, scale), r2 = make_float2(rcp, rcp);
 #pragma unroll
     for (int e = 0; e < 8; e += 2) {
-      const float2 v = div2_by_scale(make_float2(q[e], q[e + 1]), s2, r2);
+      const float2 v = div2_by_scale<ZERO_SIGN>(make_float2(q[e], q[e + 1]), s2, r2);
       q[e] = v.x;
       q[e + 1] = v.y;
     }
@@ -103,21 +117,24 @@ __device__ __forceinline__ uint32_t int8_code_f16x2(float lo, float hi) {
 }
 
 // ------------------------------------------------------------------ K mean / V absmax
-// Exact float32 sums of K by exponent bin. A bf16 value whose float32 exponent field E lies in
-// a 10-wide window [lo, lo + 10) is M * 2^(E - 134) with M < 256, i.e. a multiple of
-// u = 2^(lo - 134) below 255 * 2^9 u; 128 such values sum to less than 2^24 u, so a float32
-// accumulator per window adds them without rounding. Five windows cover |x| in [2^-32, 2^18);
-// anything else that is not zero (including subnormals) is added in float64. GB300's float64 rate
-// is low, so this moves the per-element work to the float32 pipes; the float64 additions run only
-// in CTAs that meet such a value, in a second pass over their tokens.
-constexpr int kBinLo = 127 - 32, kBinWidth = 10, kBins = 5;
-constexpr int kStatsBatch = 8;  // token rows a lane loads before it adds them (loads in flight)
-
-// Offset of the exponent field from the first window: below kBins * kBinWidth inside the windows,
-// larger otherwise (zero and subnormals wrap around).
-__device__ __forceinline__ unsigned bin_offset(float x) {
-  return ((__float_as_uint(x) >> 23) & 0xFFu) - (unsigned)kBinLo;
+// Exact float32 sums of K by splitting each value over three levels. For a float32 r with
+// |r| <= 2^(k-6) and C = 1.5 * 2^k, r + C lies in [2^k, 2^(k+1)), where the unit in the last place
+// is g = 2^(k-23): (r + C) - C is exact (Sterbenz) and equals hi, r rounded to a multiple of g, and
+// r - hi (at most g/2 in magnitude, the low-order bits of r) is exact as well. A level's
+// accumulator adds 128 such hi values, multiples of g no larger than 2^17 g, so every partial sum
+// is a multiple of g of magnitude <= 2^24 g: float32 adds them without rounding. Level k takes the
+// remainder of the level before it (at most 2^(k-6) when k drops by 18 per level): with k = 24, 6,
+// -12 the levels' grids are 2^1, 2^-17 and 2^-35, and every bf16 value with |x| <= 2^18 whose
+// lowest set bit is at least 2^-35 (every such |x| >= 2^-28) is split with remainder 0. A CTA
+// that meets anything else (larger values, smaller bits, subnormals, Inf or NaN) sums its tokens
+// in float64 instead, in token order. GB300's float64 rate is low, so this keeps the per-element
+// work on the packed float32 pipes: four packed operations per level and channel pair.
+constexpr int kSplitLevels = 3;
+__device__ __forceinline__ constexpr float split_c(int i) {  // C = 1.5 * 2^k for k = 24, 6, -12
+  return i == 0 ? 0x1.8p+24f : (i == 1 ? 0x1.8p+6f : 0x1.8p-12f);
 }
+constexpr uint32_t kSplitMaxAbs = 0x48804880u;  // 2^18 in both bf16 halves
+constexpr int kStatsBatch = 8;  // token rows a lane loads before it adds them (loads in flight)
 
 __device__ __forceinline__ uint2 ld_stream_v2(const void* p) {
   uint2 r;
@@ -138,30 +155,46 @@ __device__ __forceinline__ void bf16x4_to_f32(const uint2& u, float* f) {
   f[3] = __uint_as_float(u.y & 0xFFFF0000u);
 }
 
+// Splits a pair of K values (one bf16x2 word) into the levels' accumulators; ORs the bits of the
+// final remainders into rem (zero while every value was split exactly, up to the sign of zero).
+__device__ __forceinline__ void split_add2(uint32_t word, float2 (&acc)[kSplitLevels], uint32_t& rem) {
+  const float2 m1 = make_float2(-1.0f, -1.0f);
+  float2 r = make_float2(__uint_as_float(word << 16), __uint_as_float(word & 0xFFFF0000u));
+#pragma unroll
+  for (int i = 0; i < kSplitLevels; ++i) {
+    const float2 c = make_float2(split_c(i), split_c(i)), nc = make_float2(-split_c(i), -split_c(i));
+    const float2 hi = __fadd2_rn(__fadd2_rn(r, c), nc);
+    r = __ffma2_rn(hi, m1, r);  // r - hi, exact
+    acc[i] = __fadd2_rn(acc[i], hi);
+  }
+  rem |= __float_as_uint(r.x) | __float_as_uint(r.y);
+}
+
 // Pass 1: each CTA reduces kStatsChunk tokens of one (batch, kv head): sums of K (WITH_K) and
 // float32 max |V| per channel. A warp reads whole 256-byte rows: lane l handles channels 4l..4l+3,
-// warp w tokens w + 8i (128 tokens: the bins above are exact for 128 values). Each lane's sum is
-// the exact sum of its in-window values (bins added smallest first in float64) plus the float64
-// sum, in token order, of the rest; the 8 warps' partial rows are then combined in a fixed order,
-// so the result is deterministic.
+// warp w tokens w + 8i (128 tokens: the split levels above are exact for 128 values). Each lane's
+// sum is the exact sum of its values (levels added smallest first in float64), or, in a CTA that
+// met a value the levels do not take, their float64 sum in token order; the 8 warps' partial rows
+// are then combined in a fixed order, so the result is deterministic.
 template <bool WITH_K>
 __global__ void __launch_bounds__(256) kv_stats_partial_kernel(const __nv_bfloat16* __restrict__ k,
                                                                const __nv_bfloat16* __restrict__ v, int Skv, int Hkv,
                                                                int nchunk, double* __restrict__ psum,
                                                                float* __restrict__ pmax) {
   constexpr int kWarps = 8, kTokens = kStatsChunk / kWarps;
-  static_assert(kTokens == 128, "128 tokens per lane: the exponent bins are exact for 128 values");
+  static_assert(kTokens == 128, "128 tokens per lane: the split levels are exact for 128 values");
   __shared__ double ssum[kWarps][kHeadDim];
   __shared__ float smax[kWarps][kHeadDim];
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   __nv_bfloat162 m2[2] = {u32_as_bf162(0u), u32_as_bf162(0u)};  // channel pairs (4l, 4l+1), (4l+2, 4l+3)
-  float acc[4][kBins];
+  __nv_bfloat162 km2 = u32_as_bf162(0u);                         // max |K| over both pairs
+  float2 acc[2][kSplitLevels];
 #pragma unroll
-  for (int e = 0; e < 4; ++e)
+  for (int p = 0; p < 2; ++p)
 #pragma unroll
-    for (int i = 0; i < kBins; ++i) acc[e][i] = 0.0f;
-  bool wide = false;  // a nonzero K value outside the windows
+    for (int i = 0; i < kSplitLevels; ++i) acc[p][i] = make_float2(0.0f, 0.0f);
+  uint32_t rem = 0u;
   const int j0 = chunk * kStatsChunk + w;
   const int jn = min(Skv, chunk * kStatsChunk + kStatsChunk);
   const size_t row0 = (((size_t)b * Skv + j0) * Hkv + h) * kHeadDim + lane * 4;
@@ -180,17 +213,9 @@ __global__ void __launch_bounds__(256) kv_stats_partial_kernel(const __nv_bfloat
 #pragma unroll
     for (int u = 0; u < kStatsBatch; ++u) {
       if constexpr (WITH_K) {
-        float kf[4];
-        bf16x4_to_f32(kr[u], kf);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float x = kf[e];
-          // window index d / 10 for d < 50, kBins (no accumulator) outside the windows
-          const unsigned bin = (min(bin_offset(x), (unsigned)(kBins * kBinWidth)) * 205u) >> 11;
-#pragma unroll
-          for (int i = 0; i < kBins; ++i) acc[e][i] += (bin == (unsigned)i) ? x : 0.0f;
-          wide |= (bin == (unsigned)kBins) && x != 0.0f;
-        }
+        split_add2(kr[u].x, acc[0], rem);
+        split_add2(kr[u].y, acc[1], rem);
+        km2 = __hmax2(km2, __hmax2(__habs2(u32_as_bf162(kr[u].x)), __habs2(u32_as_bf162(kr[u].y))));
       }
       // max |V| on bf16 pairs (exact: a max only selects)
       m2[0] = __hmax2(m2[0], __habs2(u32_as_bf162(vr[u].x)));
@@ -199,23 +224,36 @@ __global__ void __launch_bounds__(256) kv_stats_partial_kernel(const __nv_bfloat
   }
   const float m[4] = {__low2float(m2[0]), __high2float(m2[0]), __low2float(m2[1]), __high2float(m2[1])};
   double s[4] = {0.0, 0.0, 0.0, 0.0};
-  if (WITH_K && __syncthreads_or(wide)) {  // rare: add the out-of-window values in float64, in token order
-    for (int i = 0; i < kTokens && j0 + kWarps * i < jn; ++i) {
-      float kf[4];
-      bf16x4_to_f32(ld_stream_v2(k + row0 + (size_t)i * step), kf);
+  if constexpr (WITH_K) {
+    // __hmax2 passes over a NaN, whose remainder is NaN and so nonzero
+    uint32_t kmax;
+    memcpy(&kmax, &km2, sizeof(kmax));
+    const bool wide = (rem & 0x7FFFFFFFu) != 0u || (kmax & 0xFFFFu) > (kSplitMaxAbs & 0xFFFFu) ||
+                      (kmax >> 16) > (kSplitMaxAbs >> 16);
+    if (__syncthreads_or(wide)) {  // rare: this CTA sums its tokens in float64, in token order
+      for (int i = 0; i < kTokens && j0 + kWarps * i < jn; ++i) {
+        float kf[4];
+        bf16x4_to_f32(ld_stream_v2(k + row0 + (size_t)i * step), kf);
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (bin_offset(kf[e]) >= (unsigned)(kBins * kBinWidth) && kf[e] != 0.0f) s[e] += (double)kf[e];
+        for (int e = 0; e < 4; ++e) s[e] += (double)kf[e];
+      }
+    } else {
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        double tx = (double)acc[p][kSplitLevels - 1].x, ty = (double)acc[p][kSplitLevels - 1].y;
+#pragma unroll
+        for (int i = kSplitLevels - 2; i >= 0; --i) {
+          tx += (double)acc[p][i].x;
+          ty += (double)acc[p][i].y;
+        }
+        s[2 * p] = tx;
+        s[2 * p + 1] = ty;
+      }
     }
   }
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    if constexpr (WITH_K) {
-      double t = (double)acc[e][0];
-#pragma unroll
-      for (int i = 1; i < kBins; ++i) t += (double)acc[e][i];
-      ssum[w][lane * 4 + e] = t + s[e];
-    }
+    if constexpr (WITH_K) ssum[w][lane * 4 + e] = s[e];
     smax[w][lane * 4 + e] = m[e];
   }
   __syncthreads();
@@ -232,19 +270,36 @@ __global__ void __launch_bounds__(256) kv_stats_partial_kernel(const __nv_bfloat
   }
 }
 
-// Pass 2: combine the chunks of one (batch, kv head) in chunk order.
+// Pass 2: combine the chunks of one (batch, kv head) in chunk order, loading eight chunks' partials
+// before adding them (the order of the float64 additions is the chunk order all the same).
 template <bool WITH_K>
 __global__ void __launch_bounds__(128) kv_stats_final_kernel(const double* __restrict__ psum,
                                                              const float* __restrict__ pmax, int Skv, int Hkv,
                                                              int nchunk, float* __restrict__ k_mean,
                                                              float* __restrict__ v_scale) {
+  pdl_launch_dependents();  // the Q quantizer reads none of this kernel's inputs or outputs
+  pdl_wait();               // the partial sums
+  constexpr int kLoads = 8;
   const int h = blockIdx.x, b = blockIdx.y, c = threadIdx.x;
   const size_t base = ((size_t)b * Hkv + h) * nchunk * kHeadDim + c;
   double a = 0.0;
   float mx = 0.0f;
-  for (int i = 0; i < nchunk; ++i) {
-    if constexpr (WITH_K) a += psum[base + (size_t)i * kHeadDim];
-    mx = fmaxf(mx, pmax[base + (size_t)i * kHeadDim]);
+  for (int i0 = 0; i0 < nchunk; i0 += kLoads) {
+    double ps[kLoads];
+    float pm[kLoads];
+#pragma unroll
+    for (int u = 0; u < kLoads; ++u) {
+      const size_t o = base + (size_t)(i0 + u) * kHeadDim;
+      ps[u] = (WITH_K && i0 + u < nchunk) ? psum[o] : 0.0;
+      pm[u] = (i0 + u < nchunk) ? pmax[o] : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < kLoads; ++u) {
+      if (i0 + u < nchunk) {
+        if constexpr (WITH_K) a += ps[u];
+        mx = fmaxf(mx, pm[u]);
+      }
+    }
   }
   const size_t o = ((size_t)b * Hkv + h) * kHeadDim + c;
   if constexpr (WITH_K) k_mean[o] = __double2float_rn(__ddiv_rn(a, (double)Skv));
@@ -280,6 +335,7 @@ __global__ void __launch_bounds__(1024) v_scale_tensor_kernel(float* __restrict_
 __global__ void __launch_bounds__(256) quant_v_kernel(const __nv_bfloat16* __restrict__ v, int Hkv, int Skv,
                                                       const float* __restrict__ v_scale,
                                                       uint8_t* __restrict__ v_codes) {
+  pdl_launch_dependents();
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int cg = threadIdx.x & 15, tr = threadIdx.x >> 4;
   const float4* sp = reinterpret_cast<const float4*>(v_scale + ((size_t)b * Hkv + h) * kHeadDim + cg * 8);
@@ -325,6 +381,7 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const __nv_bfloat16* __res
       *reinterpret_cast<uint2*>(v_codes + row0 + (size_t)(i0 + u) * step) = w;
     }
   }
+  pdl_wait();  // complete only after the kernel before this one
 }
 
 // ------------------------------------------------------------------ token-block quantizer
@@ -345,6 +402,8 @@ __global__ void __launch_bounds__(256) quant_tokens_kernel(const __nv_bfloat16* 
   constexpr int NU = IT >= 8 ? 1 : 2;      // units loaded together
   constexpr float QMAX = (OUT == CODE_E4M3) ? 448.0f : 127.0f;
   static_assert(kQuantRows % 16 == 0 && PER_WARP % NU == 0, "whole blocks per CTA, whole batches per warp");
+  pdl_launch_dependents();
+  if constexpr (SMOOTH) pdl_wait();  // the mean comes from the kernel before
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int half = lane >> 4, cg = lane & 15;
@@ -406,7 +465,7 @@ __global__ void __launch_bounds__(256) quant_tokens_kernel(const __nv_bfloat16* 
         const size_t off = row_offset(row);
         float q[8];
         values(raw[n][it], q);
-        quotients8(q, scale, fast, rcp);
+        quotients8<OUT == CODE_E4M3>(q, scale, fast, rcp);
         if constexpr (OUT == CODE_E4M3) {
           uint2 w;
           w.x = e4m3x2(q[0], q[1]) | (e4m3x2(q[2], q[3]) << 16);
@@ -431,6 +490,7 @@ __global__ void __launch_bounds__(256) quant_tokens_kernel(const __nv_bfloat16* 
       }
     }
   }
+  pdl_wait();  // complete only after the kernel before this one
 }
 
 // ------------------------------------------------------------------ MXFP8 quantizer
@@ -590,26 +650,39 @@ int grid_for(long long work_items, int per_cta) {
   return (int)g;
 }
 
+// A launch without dynamic shared memory; pdl adds the programmatic stream serialization attribute
+// (see pdl_wait).
+template <typename... Params, typename... Args>
+cudaError_t launch(void (*kernel)(Params...), dim3 grid, int threads, cudaStream_t stream, bool pdl, Args... args) {
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cfg.attrs = &attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 template <int OUT, bool SMOOTH>
 cudaError_t launch_quant_tokens(const void* x, int B, int S, int H, int block, const float* mean, void* codes,
-                                float* scales, cudaStream_t stream) {
+                                float* scales, cudaStream_t stream, bool pdl) {
   const int nblk = (S + block - 1) / block;
   const dim3 grid((S + kQuantRows - 1) / kQuantRows, H, B);
   auto xb = static_cast<const __nv_bfloat16*>(x);
   switch (block) {
     case 1:
-      quant_tokens_kernel<1, OUT, SMOOTH><<<grid, 256, 0, stream>>>(xb, S, H, mean, codes, scales, nblk);
-      break;
+      return launch(quant_tokens_kernel<1, OUT, SMOOTH>, grid, 256, stream, pdl, xb, S, H, mean, codes, scales, nblk);
     case 4:
-      quant_tokens_kernel<4, OUT, SMOOTH><<<grid, 256, 0, stream>>>(xb, S, H, mean, codes, scales, nblk);
-      break;
+      return launch(quant_tokens_kernel<4, OUT, SMOOTH>, grid, 256, stream, pdl, xb, S, H, mean, codes, scales, nblk);
     case 16:
-      quant_tokens_kernel<16, OUT, SMOOTH><<<grid, 256, 0, stream>>>(xb, S, H, mean, codes, scales, nblk);
-      break;
-    default:
-      return cudaErrorInvalidValue;
+      return launch(quant_tokens_kernel<16, OUT, SMOOTH>, grid, 256, stream, pdl, xb, S, H, mean, codes, scales,
+                    nblk);
   }
-  return cudaGetLastError();
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -622,8 +695,8 @@ cudaError_t launch_kv_stats(const void* k, const void* v, int B, int Hkv, int Sk
                                                                           Hkv, nchunk, psum, pmax);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  kv_stats_final_kernel<true><<<dim3(Hkv, B), kHeadDim, 0, stream>>>(psum, pmax, Skv, Hkv, nchunk, k_mean, v_scale);
-  return cudaGetLastError();
+  return launch(kv_stats_final_kernel<true>, dim3(Hkv, B), kHeadDim, stream, true, (const double*)psum,
+                (const float*)pmax, Skv, Hkv, nchunk, k_mean, v_scale);
 }
 
 cudaError_t launch_v_stats(const void* v, int B, int Hkv, int Skv, float* pmax, float* v_scale, bool per_tensor,
@@ -641,22 +714,32 @@ cudaError_t launch_v_stats(const void* v, int B, int Hkv, int Skv, float* pmax, 
   return cudaGetLastError();
 }
 
+namespace {
+cudaError_t quant_v(const void* v, int B, int Hkv, int Skv, const float* v_scale, void* v_codes, cudaStream_t stream,
+                    bool pdl) {
+  return launch(quant_v_kernel, dim3((Skv + kQuantRows - 1) / kQuantRows, Hkv, B), 256, stream, pdl,
+                static_cast<const __nv_bfloat16*>(v), Hkv, Skv, v_scale, static_cast<uint8_t*>(v_codes));
+}
+}  // namespace
+
 cudaError_t launch_quant_v(const void* v, int B, int Hkv, int Skv, const float* v_scale, void* v_codes,
                            cudaStream_t stream) {
-  quant_v_kernel<<<dim3((Skv + kQuantRows - 1) / kQuantRows, Hkv, B), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(v), Hkv, Skv, v_scale, static_cast<uint8_t*>(v_codes));
-  return cudaGetLastError();
+  return quant_v(v, B, Hkv, Skv, v_scale, v_codes, stream, false);
 }
 
 cudaError_t launch_quant_q(const void* q, int B, int Hq, int Sq, int q_block, int code_out, void* q_codes,
-                           float* q_scale, cudaStream_t stream) {
+                           float* q_scale, cudaStream_t stream, bool after_stats) {
+  // after launch_kv_stats, Q (which reads none of the statistics) may overlap their final kernel
   switch (code_out) {
     case CODE_I8:
-      return launch_quant_tokens<CODE_I8, false>(q, B, Sq, Hq, q_block, nullptr, q_codes, q_scale, stream);
+      return launch_quant_tokens<CODE_I8, false>(q, B, Sq, Hq, q_block, nullptr, q_codes, q_scale, stream,
+                                                 after_stats);
     case CODE_I8_AS_F16:
-      return launch_quant_tokens<CODE_I8_AS_F16, false>(q, B, Sq, Hq, q_block, nullptr, q_codes, q_scale, stream);
+      return launch_quant_tokens<CODE_I8_AS_F16, false>(q, B, Sq, Hq, q_block, nullptr, q_codes, q_scale, stream,
+                                                        after_stats);
     case CODE_E4M3:
-      return launch_quant_tokens<CODE_E4M3, false>(q, B, Sq, Hq, q_block, nullptr, q_codes, q_scale, stream);
+      return launch_quant_tokens<CODE_E4M3, false>(q, B, Sq, Hq, q_block, nullptr, q_codes, q_scale, stream,
+                                                   after_stats);
   }
   return cudaErrorInvalidValue;
 }
@@ -665,19 +748,22 @@ cudaError_t launch_quant_kv(const void* k, const void* v, int B, int Hkv, int Sk
                             const float* k_mean, const float* v_scale, void* k_codes, float* k_scale, void* v_codes,
                             cudaStream_t stream) {
   cudaError_t e = cudaErrorInvalidValue;
+  // K by an ordinary launch (everything before it has completed); V, which reads only V and the V
+  // scales, may start while K's last CTAs run
   switch (code_out) {
     case CODE_I8:
-      e = launch_quant_tokens<CODE_I8, true>(k, B, Skv, Hkv, k_block, k_mean, k_codes, k_scale, stream);
+      e = launch_quant_tokens<CODE_I8, true>(k, B, Skv, Hkv, k_block, k_mean, k_codes, k_scale, stream, false);
       break;
     case CODE_I8_AS_F16:
-      e = launch_quant_tokens<CODE_I8_AS_F16, true>(k, B, Skv, Hkv, k_block, k_mean, k_codes, k_scale, stream);
+      e = launch_quant_tokens<CODE_I8_AS_F16, true>(k, B, Skv, Hkv, k_block, k_mean, k_codes, k_scale, stream,
+                                                    false);
       break;
     case CODE_E4M3:
-      e = launch_quant_tokens<CODE_E4M3, true>(k, B, Skv, Hkv, k_block, k_mean, k_codes, k_scale, stream);
+      e = launch_quant_tokens<CODE_E4M3, true>(k, B, Skv, Hkv, k_block, k_mean, k_codes, k_scale, stream, false);
       break;
   }
   if (e != cudaSuccess) return e;
-  return launch_quant_v(v, B, Hkv, Skv, v_scale, v_codes, stream);
+  return quant_v(v, B, Hkv, Skv, v_scale, v_codes, stream, true);
 }
 
 cudaError_t launch_mx_quant(const void* x, int B, int S, int H, void* codes, uint8_t* sf, cudaStream_t stream) {

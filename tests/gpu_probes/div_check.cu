@@ -1,7 +1,9 @@
 // Test probe (built by tests/test_gpu_division.py): compares the prepass's reciprocal-based
 // division (scalar and packed) with IEEE division (__fdiv_rn) bit for bit, for every quotient the
-// quantizers can form (|x / s| <= 448) that can change a code (|x / s| >= 2^-12), and its block
-// scales amax / qmax for every float32 block max.
+// quantizers can form (|x / s| <= 448) that can change a code (|x / s| >= 2^-12); for the smaller
+// ones, which encode to a signed zero, it checks the sign and that they stay below 2^-11. The
+// packed form without the sign of zero (INT8 codes only) is checked on the first range. It also
+// checks the block scales amax / qmax for every float32 block max.
 #include <cuda_runtime.h>
 
 #include "../../diffusion_transformer_attention_gb300/csrc/quant_math.cuh"
@@ -15,15 +17,25 @@ __global__ void div_check_kernel(const float* xs, long long nx, const float* ss,
     const float x = xs[i % nx], s = ss[i / nx];
     if (!ditattn::scale_in_fast_range(s)) continue;
     const float ref = __fdiv_rn(x, s);
-    // quotients the quantizers form (|x| <= absmax = s * QMAX, so |x / s| <= 448) that can change a code
-    if (!(fabsf(ref) >= 0x1p-12f && fabsf(ref) <= 448.0f)) continue;
+    if (!(fabsf(ref) <= 448.0f)) continue;  // quotients the quantizers form: |x| <= absmax = s * QMAX
     ++nc;
     const float r = __frcp_rn(s);
     const float q = ditattn::div_by_scale(x, s, r);
-    // the packed form, with x and -x in its two lanes
+    // the packed forms, with x and -x in their two lanes
     const float2 q2 = ditattn::div2_by_scale(make_float2(x, -x), make_float2(s, s), make_float2(r, r));
-    if (__float_as_uint(q) != __float_as_uint(ref) || __float_as_uint(q2.x) != __float_as_uint(ref) ||
-        __float_as_uint(q2.y) != __float_as_uint(-ref)) {
+    const float2 q3 = ditattn::div2_by_scale<false>(make_float2(x, -x), make_float2(s, s), make_float2(r, r));
+    bool ok;
+    if (fabsf(ref) >= 0x1p-12f) {  // can change a code: equal bit for bit
+      ok = __float_as_uint(q) == __float_as_uint(ref) && __float_as_uint(q2.x) == __float_as_uint(ref) &&
+           __float_as_uint(q2.y) == __float_as_uint(-ref) && __float_as_uint(q3.x) == __float_as_uint(ref) &&
+           __float_as_uint(q3.y) == __float_as_uint(-ref);
+    } else {  // a zero code: its sign, and a magnitude that encodes to zero
+      const bool neg = signbit(ref);
+      ok = (bool)signbit(q) == neg && (bool)signbit(q2.x) == neg && (bool)signbit(q2.y) == !neg &&
+           fabsf(q) < 0x1p-11f && fabsf(q2.x) < 0x1p-11f && fabsf(q2.y) < 0x1p-11f && fabsf(q3.x) < 0x1p-11f &&
+           fabsf(q3.y) < 0x1p-11f;
+    }
+    if (!ok) {
       ++nb;
       const unsigned long long slot = atomicAdd(bad + 1, 1ull);  // bad[1]: samples taken so far
       if (slot < 8) {

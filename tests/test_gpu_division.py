@@ -8,6 +8,8 @@ two) included. The codes are also checked end to end against the oracle by the p
 tests. The packed (two-lane) form of the same division is checked on the same quotients, and the
 block scales amax / 127 and amax / 448, which the quantizers form with the reciprocal of the constant
 inside a range and with IEEE division outside it, on every finite float32 amax of a broad sample.
+Smaller quotients (x = ±0 among them: the bf16 patterns include both) encode to a zero code whose
+sign E4M3 keeps, so for those the sign must match IEEE division's and the magnitude stay below 2^-11.
 """
 
 import ctypes

@@ -78,33 +78,50 @@ def test_prepass_is_deterministic():
 
 
 def _wide_range_k(Skv, seed=21):
-    """K (float32 values of bf16) whose channels leave the statistics pass's float32 exponent
-    windows [2^-32, 2^18): huge values among normal ones, tiny ones, bf16 subnormals, and values on
-    both sides of each window edge. Each channel's values span few enough bits that its float64
-    sum is exact."""
+    """K (float32 values of bf16) at and beyond the edges of the statistics pass's exact float32
+    split (|x| <= 2^18, lowest set bit >= 2^-35; a CTA of 1024 tokens that meets anything else sums
+    in float64). Head 0: huge values among normal ones and tiny ones. Head 1: bf16 subnormals,
+    values on both sides of the old 2^-32 edge and at 2^18. Head 2: only values the split takes,
+    at its edges, so every chunk stays on the float32 path. Head 3: one value just past each edge in
+    the first chunk only, so that chunk falls back and the rest do not. Each channel's values span
+    few enough bits that its float64 sum is exact. Channel 3 of head 2 is -0.0 throughout: its mean
+    is +0 and its smoothed values -0, whose E4M3 codes are 0x80."""
     rng = np.random.default_rng(seed)
-    k = rng.standard_normal((1, Skv, 2, 128)).astype(np.float32)
+    k = rng.standard_normal((1, Skv, 4, 128)).astype(np.float32)
     n = len(k[0, ::97, 0, 0])
-    k[0, ::97, 0, 0] = rng.choice([-1.0, 1.0], n) * 2.0 ** rng.uniform(18, 24, n)  # above the top window
+    k[0, ::97, 0, 0] = rng.choice([-1.0, 1.0], n) * 2.0 ** rng.uniform(18, 24, n)  # above the top level
     k[0, :, 0, 1] *= np.float32(2.0 ** -40)                                          # below the bottom one
     k[0, :, 1, 2] = rng.integers(-127, 128, Skv) * np.float32(2.0 ** -133)           # subnormal
-    k[0, :, 1, 3] = rng.choice([2.0 ** -32, -(2.0 ** -33), 1.5 * 2.0 ** -31], Skv)  # the bottom edge
-    k[0, :, 1, 4] = rng.choice([2.0 ** 18, -(2.0 ** 18 - 2.0 ** 10), 2.0 ** 17], Skv)  # the top edge
+    k[0, :, 1, 3] = rng.choice([2.0 ** -32, -(2.0 ** -33), 1.5 * 2.0 ** -31], Skv)
+    k[0, :, 1, 4] = rng.choice([2.0 ** 18, -(2.0 ** 18 - 2.0 ** 10), 2.0 ** 17], Skv)
     k[0, Skv // 2:, 1, 5] = 0.0
+    lo_in = (1.0 + 2.0 ** -7) * 2.0 ** -28                                           # lowest bit 2^-35
+    k[0, :, 2, 0] = rng.choice([2.0 ** 18, -(2.0 ** 18), 2.0 ** 17 + 2.0 ** 10], Skv)
+    k[0, :, 2, 1] = rng.choice([lo_in, -lo_in, 2.0 ** -35, 3.0 * 2.0 ** -35], Skv)
+    k[0, :, 2, 2] = rng.choice([2.0 ** 18, -1.0, 3.0 * 2.0 ** -10], Skv)              # all three levels
+    k[0, :, 2, 3] = -0.0
+    k[0, :, 3, 0] = rng.choice([2.0 ** 18, -2.5, 7.0], Skv)
+    k[0, :, 3, 1] = rng.choice([lo_in, -(2.0 ** -30)], Skv)
+    k[0, 5, 3, 0] = (1.0 + 2.0 ** -7) * 2.0 ** 18                                    # just above 2^18
+    k[0, 9, 3, 1] = (1.0 + 2.0 ** -7) * 2.0 ** -29                                   # lowest bit 2^-36
     return torch.from_numpy(k).bfloat16()
 
 
 @pytest.mark.parametrize("dtype", ["int8", "fp8_e4m3"])
 @pytest.mark.parametrize("Skv", [2053, 3000])
-def test_prepass_k_outside_the_exponent_windows(dtype, Skv):
+def test_prepass_k_at_and_outside_the_exact_split(dtype, Skv):
     rng = np.random.default_rng(22)
     k = _wide_range_k(Skv)
-    q = torch.from_numpy(rng.standard_normal((1, 200, 2, 128)).astype(np.float32)).bfloat16()
-    v = torch.from_numpy(rng.standard_normal((1, Skv, 2, 128)).astype(np.float32)).bfloat16()
+    qf = rng.standard_normal((1, 200, 4, 128)).astype(np.float32)
+    vf = rng.standard_normal((1, Skv, 4, 128)).astype(np.float32)
+    qf[0, ::3, 1, 5] = -0.0  # negative zeros: E4M3 codes 0x80, like IEEE -0 / scale
+    vf[0, ::7, 2, 3] = -0.0
+    q, v = torch.from_numpy(qf).bfloat16(), torch.from_numpy(vf).bfloat16()
     inp = dict(q=_np(q), k=_np(k), v=_np(v))
     want = sage_quant.sage_quantize(inp["q"], inp["k"], inp["v"], dtype, 1, 16)
-    for h, c in [(0, 0), (0, 1), (1, 2), (1, 3), (1, 4), (1, 5)]:  # the premise: one correct mean
-        assert np.float32(math.fsum(inp["k"][0, :, h, c].astype(np.float64)) / Skv) == want["k_mean"][0, h, c]
+    for h in range(4):  # the premise: one correct mean
+        for c in range(8):
+            assert np.float32(math.fsum(inp["k"][0, :, h, c].astype(np.float64)) / Skv) == want["k_mean"][0, h, c]
     got = dit.sage_quantize_qkv(*_gpu(q, k, v), qk_dtype=dtype, q_block=1, k_block=16)
     torch.cuda.synchronize()
     for name in ["k_mean", "v_scale", "q_scale", "k_scale"]:
