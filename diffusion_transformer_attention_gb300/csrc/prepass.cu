@@ -73,33 +73,39 @@ __device__ __forceinline__ float quotient(float x, float scale, bool fast, float
   return (scale == 0.0f) ? 0.0f : __fdiv_rn(x, scale);
 }
 
-// quotient() of a lane's eight values by one block scale, two at a time on the packed pipes
-// (ZERO_SIGN: see div2_by_scale; false only where the codes are INT8)
-template <bool ZERO_SIGN>
+// quotient() of a lane's eight values by one block scale, two at a time on the packed pipes. For
+// INT8 codes the sign of a zero quotient does not matter (div2_by_scale's ZERO_SIGN is off) and the
+// quotients are left in [-127.5, 127.5], where int8_round2 needs them: with the scale amax / 127
+// rounded to a normal float32 (every fast scale), |x / scale| <= 127 (1 + 2^-24) and its rounding
+// stays below 127.5; a subnormal scale (the IEEE path) can be far smaller than amax / 127, so there
+// the quotient is clamped to [-127, 127], which gives the same code as clamping the rounded value.
+template <bool INT8_CODES>
 __device__ __forceinline__ void quotients8(float* q, float scale, bool fast, float rcp) {
   if (fast) {
     const float2 s2 = make_float2(scale, scale), r2 = make_float2(rcp, rcp);
 #pragma unroll
     for (int e = 0; e < 8; e += 2) {
-      const float2 v = div2_by_scale<ZERO_SIGN>(make_float2(q[e], q[e + 1]), s2, r2);
+      const float2 v = div2_by_scale<!INT8_CODES>(make_float2(q[e], q[e + 1]), s2, r2);
       q[e] = v.x;
       q[e + 1] = v.y;
     }
   } else {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) q[e] = (scale == 0.0f) ? 0.0f : __fdiv_rn(q[e], scale);
+    for (int e = 0; e < 8; ++e) {
+      q[e] = (scale == 0.0f) ? 0.0f : __fdiv_rn(q[e], scale);
+      if constexpr (INT8_CODES) q[e] = fminf(fmaxf(q[e], -127.0f), 127.0f);
+    }
   }
 }
 
 // INT8 codes without the conversion unit. Adding 1.5 * 2^23 to a float32 of magnitude <= 2^22
 // rounds it to an integer, half to even (the sum's unit in the last place is 1), and leaves that
-// integer n in the low mantissa bits: the sum's bits are 0x4B400000 + n. The quotient is clamped
-// to [-127, 127] first, which gives the same code as clamping the rounded value. Two values at a
+// integer n in the low mantissa bits: the sum's bits are 0x4B400000 + n. The quotients come from
+// quotients8<true>, within [-127.5, 127.5), so n is in [-127, 127] without a clamp. Two values at a
 // time: the addition runs on the packed float32 pipes (each lane rounds as the scalar add would).
 constexpr float kRoundInt = 12582912.0f;  // 1.5 * 2^23
 __device__ __forceinline__ float2 int8_round2(float a, float b) {
-  return __fadd2_rn(make_float2(fminf(fmaxf(a, -127.0f), 127.0f), fminf(fmaxf(b, -127.0f), 127.0f)),
-                    make_float2(kRoundInt, kRoundInt));
+  return __fadd2_rn(make_float2(a, b), make_float2(kRoundInt, kRoundInt));
 }
 
 // Four INT8 codes, `a` in the low byte (the low byte of the rounded sum is n's two's complement).
@@ -465,7 +471,7 @@ __global__ void __launch_bounds__(256) quant_tokens_kernel(const __nv_bfloat16* 
         const size_t off = row_offset(row);
         float q[8];
         values(raw[n][it], q);
-        quotients8<OUT == CODE_E4M3>(q, scale, fast, rcp);
+        quotients8<OUT != CODE_E4M3>(q, scale, fast, rcp);
         if constexpr (OUT == CODE_E4M3) {
           uint2 w;
           w.x = e4m3x2(q[0], q[1]) | (e4m3x2(q[2], q[3]) << 16);
