@@ -42,10 +42,11 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
 // Programmatic dependent launch. A kernel launched with the programmatic stream serialization
 // attribute may start once every CTA of the kernel before it in the stream has started or exited
 // and executed launch_dependents; griddepcontrol.wait then returns once that kernel has completed
-// and its writes are visible. Under an ordinary launch both are no-ops. The quantizers call
-// launch_dependents first and wait last: the next kernel may fill the SMs their last wave leaves
-// idle, and a quantizer still completes only after the kernel before it, so an ordinary launch
-// that follows the chain waits for all of it.
+// and its writes are visible. Under an ordinary launch both are no-ops. The statistics kernels and
+// the quantizers call launch_dependents first; a kernel that reads the one before it waits first,
+// and a quantizer waits last: the next kernel may fill the SMs a last wave leaves idle, and each
+// kernel still completes only after the kernel before it, so an ordinary launch that follows the
+// chain waits for all of it.
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
@@ -191,6 +192,9 @@ __global__ void __launch_bounds__(256) kv_stats_partial_kernel(const __nv_bfloat
   static_assert(kTokens == 128, "128 tokens per lane: the split levels are exact for 128 values");
   __shared__ double ssum[kWarps][kHeadDim];
   __shared__ float smax[kWarps][kHeadDim];
+  // The final kernel (which waits for this one) and the Q quantizer behind it may take the SMs this
+  // grid's last wave leaves idle.
+  pdl_launch_dependents();
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   __nv_bfloat162 m2[2] = {u32_as_bf162(0u), u32_as_bf162(0u)};  // channel pairs (4l, 4l+1), (4l+2, 4l+3)
