@@ -10,9 +10,10 @@
 //     in float64, rounded once to float32; smoothed K = float32(K) - mean (float32 subtract);
 //   * scale = absmax / QMAX (QMAX 127 or 448) and code = f(x / scale), both IEEE float32
 //     divisions (true division, round to nearest); INT8 rounds half to even and clamps to
-//     +-127; E4M3 rounds to nearest even and saturates; an all-zero block has scale 0 and
-//     zero codes. The quotients x / scale are computed from the scale's correctly rounded
-//     reciprocal with one remainder correction (quant_math.cuh), which gives the same codes.
+//     +-127; E4M3 rounds to nearest even and saturates, and a quotient of -0 gives 0x80; an
+//     all-zero block has scale 0 and zero codes. The quotients x / scale are computed from the
+//     scale's correctly rounded reciprocal with two remainder corrections (quant_math.cuh),
+//     which gives the same codes.
 //
 // Access pattern: a row of one head is 128 bf16 = 256 contiguous bytes. The quantizers read it with
 // 16 lanes and 16-byte vector loads (a warp covers two rows per instruction) and write codes with

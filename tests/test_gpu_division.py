@@ -1,4 +1,4 @@
-"""The prepass divides by a block scale with a reciprocal and one remainder correction
+"""The prepass divides by a block scale with a reciprocal and two remainder corrections
 (Markstein's division theorem) instead of IEEE division. This checks, on the GPU, that the two
 agree bit for bit on every quotient the quantizers can form (|x| <= absmax = s * QMAX, so
 |x / s| <= 448) that can change a code (|x / s| >= 2^-12), for all finite
