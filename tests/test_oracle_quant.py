@@ -80,6 +80,32 @@ def test_zero_block_gives_zero_scale_and_codes(dtype):
     assert np.all(formats.code_values(codes[:, 4:], dtype) == 0.0)
 
 
+def test_negative_zero_keeps_its_sign_in_e4m3_codes():
+    """IEEE division keeps the sign of zero (-0 / s = -0 for s > 0) and E4M3 encodes -0 as 0x80
+    (the format has both zeros); INT8 has one zero. A K channel of -0 has mean +0 (the float64
+    sum of -0 values starting from +0) and smoothed values -0 - 0 = -0."""
+    rng = np.random.default_rng(9)
+    x = _bf16_values(rng, (1, 8, 1, 128))
+    x[0, :, 0, 3] = -0.0
+    x[0, 2, 0, 7] = 0.0
+    codes, scales = sage_quant.quantize_token_blocks(x, 4, "fp8_e4m3")
+    assert np.all(scales > 0)
+    assert np.all(codes[0, :, 0, 3] == 0x80) and codes[0, 2, 0, 7] == 0x00
+    i8, _ = sage_quant.quantize_token_blocks(x, 4, "int8")
+    assert np.all(i8[0, :, 0, 3] == 0)
+    vc, vs = sage_quant.quantize_v_per_channel(x)
+    assert vs[0, 0, 3] == 0.0 and np.all(vc[0, :, 0, 3] == 0x00)  # a zero channel: scale 0, codes +0
+    v = x.copy()
+    v[0, 0, 0, 3] = 1.0
+    vc, vs = sage_quant.quantize_v_per_channel(v)
+    assert vs[0, 0, 3] > 0 and np.all(vc[0, 1:, 0, 3] == 0x80)
+    k = x.copy()
+    k[0, :, 0, 5] = -0.0
+    out = sage_quant.sage_quantize(x, k, v, "fp8_e4m3", 1, 4)
+    assert out["k_mean"][0, 0, 5] == 0.0 and not np.signbit(out["k_mean"][0, 0, 5])
+    assert np.all(out["k_codes"][0, :, 0, 5] == 0x80)
+
+
 def _brute_force_block_quant(x, block, dtype):
     """Per-block loops written out element by element (independent of the vectorised path)."""
     B, S, H, D = x.shape
