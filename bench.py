@@ -145,12 +145,16 @@ class ClockSampler:
 
     def summary(self):
         if self.nvml is not None:
-            load = [r for r in self.rows if r[1] > 300] or self.rows  # samples under load
+            # Every NVML sample falls inside the sampled region, which only launches kernels and waits
+            # for them, so all count as under load. (NVML's power reading is a moving average that
+            # trails a short burst: filtering on it dropped most samples of a sub-second region.)
+            load = self.rows
             if not load:
                 return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no samples"], "source": "nvml"}
             reasons = sorted({name for _, _, bits in load for bit, name in self.REASONS.items() if bits & bit})
             return {"sm_mhz": statistics.median(r[0] for r in load), "sm_max_mhz": self.max_mhz,
-                    "reasons": reasons, "samples": len(load), "source": "nvml, 10 ms"}
+                    "reasons": reasons, "samples": len(load), "power_w_max": max(r[1] for r in load),
+                    "source": "nvml, 10 ms"}
         if self.proc is None or self.file is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         rows = []
