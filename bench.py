@@ -152,9 +152,10 @@ class ClockSampler:
             if not load:
                 return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no samples"], "source": "nvml"}
             reasons = sorted({name for _, _, bits in load for bit, name in self.REASONS.items() if bits & bit})
-            return {"sm_mhz": statistics.median(r[0] for r in load), "sm_max_mhz": self.max_mhz,
-                    "reasons": reasons, "samples": len(load), "power_w_max": max(r[1] for r in load),
-                    "source": "nvml, 10 ms"}
+            # the mean of evenly spaced samples is the region's time-averaged clock (cycles / time)
+            return {"sm_mhz": statistics.median(r[0] for r in load), "sm_mhz_mean": round(statistics.fmean(
+                r[0] for r in load), 1), "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(load),
+                "source": "nvml, 10 ms"}
         if self.proc is None or self.file is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         rows = []
@@ -614,7 +615,7 @@ def main():
         # (M128 N128 K16 in 64 clocks = 8192 FLOP per clock per SM): a clock-independent duty estimate,
         # since the measured cuBLAS peak ran at a lower, power-capped clock
         "tensor_duty_at_clock": (round(kernel_tflops * 1e12 / (8192.0 * props.multi_processor_count *
-                                                             clocks["sm_mhz"] * 1e6), 3)
+                                                             clocks.get("sm_mhz_mean", clocks["sm_mhz"]) * 1e6), 3)
                                  if clocks.get("sm_mhz") else None),
         "roofline": {"bound": "tensor", "achieved": round(kernel_tflops, 1), "peak": peak16, "unit": "TFLOP/s",
                      "frac": round(kernel_tflops / peak16, 3), "traffic": traffic,
