@@ -36,6 +36,14 @@ def test_truncating_int8_is_caught(monkeypatch):
     _fails(TF.test_int8_half_even_and_clamp)
 
 
+def test_quotient_losing_the_sign_of_zero_is_caught(monkeypatch):
+    # -0 + 0 = +0: a quotient formed through a sum with a positive zero encodes -0 as 0x00
+    good = sage_quant._codes_from_quotient
+    monkeypatch.setattr(sage_quant, "_codes_from_quotient",
+                        lambda quot, dtype: good(np.asarray(quot, np.float32) + np.float32(0.0), dtype))
+    _fails(TQ.test_negative_zero_keeps_its_sign_in_e4m3_codes)
+
+
 def test_missing_k_smoothing_is_caught(monkeypatch):
     monkeypatch.setattr(sage_quant, "smooth_k", lambda k, mean: np.asarray(k, np.float32))
     _fails(TQ.test_smoothed_k_has_zero_channel_mean)
