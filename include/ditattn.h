@@ -202,7 +202,9 @@ size_t sage_quantize_workspace_bytes(int B, int Hkv, int Skv);
  *   k_mean     device float [B, Hkv, 128]               = mean of K over all Skv tokens
  *   workspace  device scratch of sage_quantize_workspace_bytes(B, Hkv, Skv) bytes
  * QMAX is 127 for INT8 and 448 for E4M3; a block or channel whose absmax is 0 gets scale 0 and
- * zero codes. Results are bit-for-bit deterministic.
+ * zero codes (+0). Otherwise codes are those of the IEEE float32 quotient x / scale, so an E4M3
+ * code of a -0 input (or of a negative quotient that rounds to zero) is 0x80. Results are
+ * bit-for-bit deterministic.
  */
 dit_status sage_quantize_qkv(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int Sq, int Skv,
                              int qk_dtype, int q_block, int k_block, void* q_codes, void* k_codes, void* v_codes,
