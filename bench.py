@@ -480,7 +480,8 @@ def run_modes(dit, steps, warmup, world, stream, peak16, hbm_gbs, cpu: bool):
     short = (0.0, 2.0, 50.0, 3200.0)
     res["video_fp8_rate_bmm1"] = {"f": list(short)}
     res["video_fp8_rate_bmm1"].update({
-        label: skip_sweep(dit, q, k, v, out, counts, w, short, s, wu, world, stream, dense_ms, mode=sk, dt=dt, qb=qb, kb=kb)
+        label: skip_sweep(dit, q, k, v, out, counts, w, short, s, wu, world, stream, dense_ms, mode=sk, dt=dt, qb=qb,
+                          kb=kb)
         for label, dt, qb, kb in [("sage_fp8_1_16", "fp8_e4m3", 1, 16), ("mxfp8", "mxfp8", 0, 0),
                                   ("nvfp4", "nvfp4", 0, 0)]})
     curve = skip_sweep(dit, q, k, v, out, counts, w, w.factors, s, wu, world, stream, dense_ms, mode=sk,
