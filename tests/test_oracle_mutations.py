@@ -10,6 +10,7 @@ from oracle import formats, sage_quant
 
 from . import test_oracle_attention as TA
 from . import test_oracle_formats as TF
+from . import test_oracle_lse as TLSE
 from . import test_oracle_quant as TQ
 from . import test_oracle_sage_lossless as TL
 
@@ -42,6 +43,48 @@ def test_quotient_losing_the_sign_of_zero_is_caught(monkeypatch):
     monkeypatch.setattr(sage_quant, "_codes_from_quotient",
                         lambda quot, dtype: good(np.asarray(quot, np.float32) + np.float32(0.0), dtype))
     _fails(TQ.test_negative_zero_keeps_its_sign_in_e4m3_codes)
+
+
+def test_k_mean_over_s_minus_one_is_caught(monkeypatch):
+    def biased(k):
+        k = np.asarray(k, np.float32)
+        return (k.astype(np.float64).sum(axis=1) / (k.shape[1] - 1)).astype(np.float32)
+    monkeypatch.setattr(sage_quant, "k_channel_mean", biased)
+    _fails(TQ.test_k_mean_constant_channel_is_exact)
+
+
+def test_lse_in_base_two_is_caught(monkeypatch):
+    good = att.dense_lse
+    monkeypatch.setattr(att, "dense_lse", lambda q, k, rows=None: good(q, k, rows) / np.log(2.0))
+    _fails(TLSE.test_tiled_lse_equals_logsumexp_of_brute_force_logits, 128)
+
+
+def test_block_absmax_over_all_heads_is_caught(monkeypatch):
+    good = sage_quant.quantize_token_blocks
+
+    def all_heads(x, block, qk_dtype):
+        # one scale per token block shared by every head: the head axis taken into the block max
+        x = np.asarray(x, np.float32)
+        _, scales = good(x, block, qk_dtype)
+        scales = np.broadcast_to(scales.max(axis=1, keepdims=True), scales.shape).copy()
+        row_scale = np.repeat(scales, block, axis=2)[:, :, :x.shape[1]].transpose(0, 2, 1)[:, :, :, None]
+        with np.errstate(divide="ignore", invalid="ignore"):
+            quot = np.where(row_scale == 0, np.float32(0), (x / row_scale).astype(np.float32))
+        return sage_quant._codes_from_quotient(quot, qk_dtype), scales
+    monkeypatch.setattr(sage_quant, "quantize_token_blocks", all_heads)
+    _fails(TQ.test_block_quant_matches_brute_force, "int8", 4)
+
+
+def test_smoothed_q_is_caught(monkeypatch):
+    good = sage_quant.sage_quantize
+
+    def q_smoothed(q, k, v, qk_dtype, q_block, k_block, k_mean=None):
+        out = good(q, k, v, qk_dtype, q_block, k_block, k_mean)
+        qs = sage_quant.smooth_k(q, out["k_mean"])  # Hq == Hkv in the pin
+        out["q_codes"], out["q_scale"] = sage_quant.quantize_token_blocks(qs, q_block, qk_dtype)
+        return out
+    monkeypatch.setattr(sage_quant, "sage_quantize", q_smoothed)
+    _fails(TQ.test_q_is_not_smoothed, "int8")
 
 
 def test_missing_k_smoothing_is_caught(monkeypatch):

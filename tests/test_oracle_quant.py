@@ -80,6 +80,22 @@ def test_zero_block_gives_zero_scale_and_codes(dtype):
     assert np.all(formats.code_values(codes[:, 4:], dtype) == 0.0)
 
 
+@pytest.mark.parametrize("dtype", ["int8", "fp8_e4m3"])
+def test_q_is_not_smoothed(dtype):
+    """Reading 2: only K is smoothed. Q constant within each token (a different constant per token)
+    has full-scale codes in every block of one token, whatever K's channel means are; Q minus K's
+    mean would not be constant and would not reach +QMAX everywhere."""
+    rng = np.random.default_rng(8)
+    q = np.repeat(np.linspace(0.5, 3.0, 12, dtype=np.float32)[None, :, None, None], 128, axis=3)
+    q = np.repeat(q, 2, axis=2)
+    k = _bf16_values(rng, (1, 20, 2, 128), mean=5.0)
+    k += np.float32(2.0) * np.arange(128, dtype=np.float32)[None, None, None, :] / 128
+    v = _bf16_values(rng, (1, 20, 2, 128))
+    out = sage_quant.sage_quantize(q, k, v, dtype, 1, 4)
+    assert np.all(np.abs(out["k_mean"]) > 1.0)
+    assert np.all(formats.code_values(out["q_codes"], dtype) == QMAX[dtype])
+
+
 def test_negative_zero_keeps_its_sign_in_e4m3_codes():
     """IEEE division keeps the sign of zero (-0 / s = -0 for s > 0) and E4M3 encodes -0 as 0x80
     (the format has both zeros); INT8 has one zero. A K channel of -0 has mean +0 (the float64
