@@ -283,3 +283,25 @@ def test_sage_q_scale_of_the_previous_row_is_caught(monkeypatch):
     good = att.sage_scores
     monkeypatch.setattr(att, "sage_scores", lambda qc, kc, qs, ks, dt: good(qc, kc, np.roll(qs, 1), ks, dt))
     _fails(TL._compare, "int8", 4, 4, None)
+
+
+def test_code_dots_in_float32_are_caught(monkeypatch):
+    # float32 accumulation: exact for INT8 codes (sums below 2^22) but not for E4M3 products
+    monkeypatch.setattr(att, "code_dots", lambda qc, kc, dt: (formats.code_values(qc, dt).astype(np.float32) @
+                                                              formats.code_values(kc, dt).astype(np.float32).T
+                                                              ).astype(np.float64))
+    _fails(TA.test_code_dot_products_match_triple_loop)
+
+
+def test_wrong_e2m1_value_is_caught(monkeypatch):
+    table = np.array(formats.E2M1_VALUES, dtype=np.float64)
+    table[7] = 5.0  # the largest magnitude taken as 5 instead of 6
+    monkeypatch.setattr(formats, "E2M1_VALUES", table)
+    _fails(TN.test_e2m1_values_from_bit_fields)
+
+
+def test_mx_decode_with_the_wrong_bias_is_caught(monkeypatch):
+    good = mx_quant.mx_decode
+    monkeypatch.setattr(mx_quant, "mx_decode", lambda codes, sf: good(codes, sf) * 2.0)  # bias 126 in decode only
+    _fails(TM.test_round_trip_error_is_within_e4m3_rounding)
+
