@@ -305,3 +305,20 @@ def test_mx_decode_with_the_wrong_bias_is_caught(monkeypatch):
     monkeypatch.setattr(mx_quant, "mx_decode", lambda codes, sf: good(codes, sf) * 2.0)  # bias 126 in decode only
     _fails(TM.test_round_trip_error_is_within_e4m3_rounding)
 
+
+def test_nvfp4_scores_with_the_neighbouring_block_scale_are_caught(monkeypatch):
+    good = nvfp4_quant.nvfp4_scores
+    monkeypatch.setattr(nvfp4_quant, "nvfp4_scores", lambda qc, qsf, qs, kc, ksf, ks:
+                        good(qc, qsf, qs, kc, np.roll(np.asarray(ksf), 1, axis=-1), ks))
+    _fails(TN.test_scores_equal_the_product_of_dequantized_operands)
+
+
+def test_swapped_nibbles_on_unpacking_are_caught(monkeypatch):
+    good = formats.unpack_nibbles
+
+    def swapped(p):
+        out = good(p)
+        return np.stack([out[..., 1::2], out[..., 0::2]], axis=-1).reshape(out.shape)
+    monkeypatch.setattr(formats, "unpack_nibbles", swapped)
+    _fails(TN.test_nibble_packing_order)
+
